@@ -1,0 +1,194 @@
+"""fp64 CPU oracle for the fused scaled-dot-product attention forward pass.
+
+TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` are the only callers.  Nothing here is used
+by, or shares code with, the CUDA path in ``scaled_dot_product_09_gb300``.
+
+The arithmetic lives in ``sdpa_oracle.c`` (plain C, fp64, OpenMP over rows);
+this module compiles it on first use with gcc and wraps it with ctypes.  Its
+inputs are float64 numpy arrays converted exactly from the half-precision
+tensors by the caller.
+
+Definition followed (per slice): S = scale*Q.K^T + bias, P = softmax_rows(S),
+O = P.V -- "视觉大模型训练和推理加速" section 一 (attention map from query and
+key with softmax, weighting the values) and "Accelerated Diffusers with
+PyTorch 2.0" section 加速 Transformer 块 (all SDPA backends compute the same
+function; the native C++ one is the high-precision path).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sdpa_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libsdpa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+BIAS_NONE, BIAS_SWIN, BIAS_SAM = 0, 1, 2
+
+
+class _Bias(ctypes.Structure):
+    _fields_ = [
+        ("kind", ctypes.c_int),
+        ("table", ctypes.c_void_p),
+        ("win", ctypes.c_int),
+        ("grid_h", ctypes.c_int),
+        ("grid_w", ctypes.c_int),
+        ("shift", ctypes.c_int),
+        ("rel_h", ctypes.c_void_p),
+        ("rel_w", ctypes.c_void_p),
+        ("s_h", ctypes.c_int),
+        ("s_w", ctypes.c_int),
+    ]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library (gcc, -O2, OpenMP) if stale."""
+    with _lock:
+        fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+        if fresh and not force:
+            return _LIB_PATH
+        os.makedirs(_OUT_DIR, exist_ok=True)
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+        return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = build()
+    lib = ctypes.CDLL(path)
+    dp = ctypes.c_void_p
+    i = ctypes.c_int
+    lib.oracle_swin_index.argtypes = [i, i, i, i, i]
+    lib.oracle_swin_index.restype = i
+    lib.oracle_swin_mask.argtypes = [i, i, i, i, i, i, i]
+    lib.oracle_swin_mask.restype = ctypes.c_double
+    lib.oracle_bias_matrix.argtypes = [dp, i, i, i, i, i, ctypes.POINTER(_Bias), dp]
+    lib.oracle_bias_matrix.restype = i
+    lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, i, i, i, i, i, ctypes.c_double,
+                                    ctypes.POINTER(_Bias), i]
+    lib.oracle_attn_fwd.restype = i
+    lib.oracle_attn_rows.argtypes = [dp, dp, dp, dp, i, i, i, i, i, ctypes.c_double,
+                                     ctypes.POINTER(_Bias), dp, ctypes.c_int64, i]
+    lib.oracle_attn_rows.restype = i
+    lib.oracle_attn_probs.argtypes = [dp, dp, dp, i, i, i, i, i, ctypes.c_double,
+                                      ctypes.POINTER(_Bias), i, dp, dp]
+    lib.oracle_attn_probs.restype = i
+    _lib = lib
+    return lib
+
+
+def _f64(a):
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    return a
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+class Bias:
+    """Bias description in fp64.  kind: 'none' | 'swin' | 'sam'.
+
+    swin: table [(2M-1)^2, H], win=M, grid_h, grid_w, shift.
+    sam:  rel_h [2*s_h-1, d], rel_w [2*s_w-1, d], s_h, s_w.
+    """
+
+    def __init__(self, kind="none", table=None, win=0, grid_h=0, grid_w=0, shift=0,
+                 rel_h=None, rel_w=None, s_h=0, s_w=0):
+        self.kind = kind
+        self.table = None if table is None else _f64(table)
+        self.rel_h = None if rel_h is None else _f64(rel_h)
+        self.rel_w = None if rel_w is None else _f64(rel_w)
+        self.win, self.grid_h, self.grid_w, self.shift = win, grid_h, grid_w, shift
+        self.s_h, self.s_w = s_h, s_w
+
+    def _c(self):
+        k = {"none": BIAS_NONE, "swin": BIAS_SWIN, "sam": BIAS_SAM}[self.kind]
+        return _Bias(k, _ptr(self.table), self.win, self.grid_h, self.grid_w, self.shift,
+                     _ptr(self.rel_h), _ptr(self.rel_w), self.s_h, self.s_w)
+
+
+def _shape(q, k):
+    BH, Nq, d = q.shape
+    assert k.shape[0] == BH and k.shape[2] == d
+    return BH, Nq, k.shape[1], d
+
+
+def attn_fwd(q, k, v, H, scale, bias: Bias | None = None, nthreads: int = 0):
+    """O for every row.  q [BH, Nq, d], k/v [BH, Nk, d] (any float dtype,
+    converted to fp64).  Returns (out [BH, Nq, d] float64, threads used)."""
+    lib = _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    BH, Nq, Nk, d = _shape(q, k)
+    out = np.empty((BH, Nq, d), dtype=np.float64)
+    b = (bias or Bias())._c()
+    used = lib.oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), BH, H, Nq, Nk, d,
+                               float(scale), ctypes.byref(b), int(nthreads))
+    if used < 0:
+        raise ValueError("oracle_attn_fwd: invalid arguments")
+    return out, used
+
+
+def attn_rows(q, k, v, H, scale, row_ids, bias: Bias | None = None, nthreads: int = 0):
+    """O for selected rows only; row_ids[t] = slice*Nq + i.  Returns
+    (out [n, d] float64, threads used)."""
+    lib = _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    BH, Nq, Nk, d = _shape(q, k)
+    ids = np.ascontiguousarray(row_ids, dtype=np.int64)
+    out = np.empty((ids.size, d), dtype=np.float64)
+    b = (bias or Bias())._c()
+    used = lib.oracle_attn_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(out), BH, H, Nq, Nk, d,
+                                float(scale), ctypes.byref(b), _ptr(ids), ids.size, int(nthreads))
+    if used < 0:
+        raise ValueError("oracle_attn_rows: invalid arguments")
+    return out, used
+
+
+def attn_probs(q, k, v, H, scale, slice_index, bias: Bias | None = None):
+    """(P [Nq, Nk], O [Nq, d]) of one slice, fp64."""
+    lib = _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    BH, Nq, Nk, d = _shape(q, k)
+    probs = np.empty((Nq, Nk), dtype=np.float64)
+    out = np.empty((Nq, d), dtype=np.float64)
+    b = (bias or Bias())._c()
+    rc = lib.oracle_attn_probs(_ptr(q), _ptr(k), _ptr(v), BH, H, Nq, Nk, d, float(scale),
+                               ctypes.byref(b), int(slice_index), _ptr(probs), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_attn_probs: invalid arguments")
+    return probs, out
+
+
+def bias_matrix(q, H, slice_index, Nk, bias: Bias):
+    """The bias of one slice as an explicit Nq x Nk matrix (fp64)."""
+    lib = _load()
+    q = _f64(q)
+    BH, Nq, d = q.shape
+    out = np.empty((Nq, Nk), dtype=np.float64)
+    b = bias._c()
+    rc = lib.oracle_bias_matrix(_ptr(q), H, int(slice_index), Nq, Nk, d, ctypes.byref(b), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_bias_matrix: invalid arguments")
+    return out
+
+
+def swin_index(M, ri, ci, rj, cj) -> int:
+    return _load().oracle_swin_index(M, ri, ci, rj, cj)
+
+
+def swin_mask(M, grid_h, grid_w, shift, window, ti, tj) -> float:
+    return _load().oracle_swin_mask(M, grid_h, grid_w, shift, window, ti, tj)

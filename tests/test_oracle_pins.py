@@ -1,0 +1,371 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+None of these compares the oracle with a retyped copy of itself: each pin is
+a hand-enumerated fixture, a closed form, an invariant, a brute-force
+geometric characterisation, or an independent library routine
+(torch's CPU scaled_dot_product_attention, the pages' "native C++"
+backend -- "Accelerated Diffusers with PyTorch 2.0", section 加速 Transformer 块).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from scaled_dot_product_09_gb300.workloads import WORKLOADS, make_inputs
+
+
+def _rand(shape, seed, scale=1.0):
+    g = np.random.default_rng(seed)
+    return g.standard_normal(shape) * scale
+
+
+def _read_golden(path):
+    rows = []
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            rows.append(line.split())
+    return rows
+
+
+# ------------------------------------------------------------------ softmax --
+
+@pytest.mark.parametrize("kind", ["none", "swin", "sam"])
+def test_p1_rows_sum_to_one(kind):
+    """P1: every probability row sums to 1 (softmax definition)."""
+    H, d = 2, 8
+    if kind == "swin":
+        M = 3
+        N = M * M
+        bias = oracle.Bias("swin", table=_rand(((2 * M - 1) ** 2, H), 7, 0.5), win=M,
+                           grid_h=6, grid_w=6, shift=1)
+        BH = 4 * H
+    elif kind == "sam":
+        sh, sw = 3, 4
+        N = sh * sw
+        bias = oracle.Bias("sam", rel_h=_rand((2 * sh - 1, d), 8, 0.3),
+                           rel_w=_rand((2 * sw - 1, d), 9, 0.3), s_h=sh, s_w=sw)
+        BH = 2 * H
+    else:
+        N, bias, BH = 13, None, 2 * H
+    q, k, v = (_rand((BH, N, d), s) for s in (1, 2, 3))
+    for s in range(BH):
+        P, _ = oracle.attn_probs(q, k, v, H, 0.37, s, bias)
+        assert np.all(P >= 0)
+        np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+
+
+def test_p2_uniform_scores_give_mean_of_v():
+    """P2: Q = 0 makes every score equal, so O is the column mean of V."""
+    BH, H, N, d = 3, 3, 17, 8
+    q = np.zeros((BH, N, d))
+    k, v = _rand((BH, N, d), 4), _rand((BH, N, d), 5)
+    out, _ = oracle.attn_fwd(q, k, v, H, 0.25)
+    want = np.broadcast_to(v.mean(axis=1, keepdims=True), out.shape)
+    np.testing.assert_allclose(out, want, rtol=0, atol=1e-14)
+
+
+def test_single_key_returns_that_value():
+    """Nk = 1: the only key gets probability 1, O = V[0] exactly."""
+    q, k, v = _rand((2, 5, 8), 1), _rand((2, 1, 8), 2), _rand((2, 1, 8), 3)
+    out, _ = oracle.attn_fwd(q, k, v, 1, 1.0)
+    np.testing.assert_array_equal(out, np.broadcast_to(v, out.shape))
+
+
+def test_large_scores_are_stable_and_pick_the_argmax():
+    """A key whose score dominates by >> 40 gets all the weight; no overflow."""
+    d = 4
+    q = np.array([[[1.0, 0, 0, 0]]])
+    k = np.array([[[1000.0, 0, 0, 0], [900.0, 0, 0, 0], [-1000.0, 0, 0, 0]]])
+    v = np.array([[[1.0, 2, 3, 4], [5.0, 6, 7, 8], [9.0, 9, 9, 9]]])
+    out, _ = oracle.attn_fwd(q, k, v, 1, 1.0)
+    np.testing.assert_array_equal(out[0, 0], v[0, 0])
+
+
+def test_p9_matches_torch_sdpa_fp64():
+    """P9: no-bias attention equals torch's CPU SDPA math backend in fp64."""
+    B, H, Nq, Nk, d = 2, 3, 19, 23, 16
+    q, k, v = _rand((B * H, Nq, d), 1), _rand((B * H, Nk, d), 2), _rand((B * H, Nk, d), 3)
+    scale = 1 / math.sqrt(d)
+    out, _ = oracle.attn_fwd(q, k, v, H, scale)
+    t = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v), scale=scale)
+    np.testing.assert_allclose(out, t.numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("kind", ["swin", "sam"])
+def test_p9_biased_matches_torch_sdpa_with_explicit_mask(kind):
+    """The attention half of the biased path equals torch SDPA given the
+    oracle's explicit bias matrix as an additive float mask."""
+    H, d = 2, 8
+    if kind == "swin":
+        M = 3
+        N = M * M
+        bias = oracle.Bias("swin", table=_rand(((2 * M - 1) ** 2, H), 7), win=M,
+                           grid_h=6, grid_w=9, shift=1)
+        BH = 6 * H
+    else:
+        sh, sw = 3, 5
+        N = sh * sw
+        bias = oracle.Bias("sam", rel_h=_rand((2 * sh - 1, d), 8), rel_w=_rand((2 * sw - 1, d), 9),
+                           s_h=sh, s_w=sw)
+        BH = 2 * H
+    q, k, v = (_rand((BH, N, d), s) for s in (1, 2, 3))
+    out, _ = oracle.attn_fwd(q, k, v, H, 0.3, bias)
+    for s in range(BH):
+        Bm = oracle.bias_matrix(q, H, s, N, bias)
+        t = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[s:s + 1]), torch.from_numpy(k[s:s + 1]),
+            torch.from_numpy(v[s:s + 1]), attn_mask=torch.from_numpy(Bm)[None], scale=0.3)
+        np.testing.assert_allclose(out[s], t[0].numpy(), rtol=0, atol=1e-12)
+
+
+def test_rows_entry_equals_full_entry():
+    BH, H, N, d = 4, 2, 11, 8
+    q, k, v = (_rand((BH, N, d), s) for s in (1, 2, 3))
+    full, _ = oracle.attn_fwd(q, k, v, H, 0.5)
+    ids = np.array([0, 5, 12, 43, 21])
+    rows, _ = oracle.attn_rows(q, k, v, H, 0.5, ids)
+    np.testing.assert_array_equal(rows, full.reshape(-1, d)[ids])
+
+
+# --------------------------------------------------------------------- Swin --
+
+def test_p5_swin_index_2x2_golden(golden_dir):
+    """P5: the hand-enumerated index matrix of one 2x2 window."""
+    want = np.array(_read_golden(os.path.join(golden_dir, "swin_index_M2.txt")), dtype=int)
+    got = np.array([[oracle.swin_index(2, i // 2, i % 2, j // 2, j % 2) for j in range(4)]
+                    for i in range(4)])
+    np.testing.assert_array_equal(got, want)
+
+
+def test_p4_swin_index_invariants():
+    """P4: idx(i,i) = 2M(M-1) (84 for M=7); idx(i,j)+idx(j,i) = 2*idx(i,i);
+    range [0, (2M-1)^2); for a fixed query all keys get distinct indices."""
+    M = 7
+    N = M * M
+    idx = np.array([[oracle.swin_index(M, i // M, i % M, j // M, j % M) for j in range(N)]
+                    for i in range(N)])
+    assert np.all(np.diag(idx) == 84)
+    assert np.all(idx + idx.T == 168)
+    assert idx.min() == 0 and idx.max() == 168
+    for i in range(N):
+        assert len(set(idx[i])) == N
+
+
+def _brute_force_allowed(G_h, G_w, M, s):
+    """Geometric characterisation of the shifted-window mask, independent of
+    the strip rule: roll the map of original coordinates by -s (torch.roll),
+    partition into windows, and allow a pair iff the two tokens were within
+    one window size of each other in the ORIGINAL image (a pair that wrapped
+    around the border is > G-M apart)."""
+    ys, xs = torch.meshgrid(torch.arange(G_h), torch.arange(G_w), indexing="ij")
+    ys = torch.roll(ys, shifts=(-s, -s), dims=(0, 1))
+    xs = torch.roll(xs, shifts=(-s, -s), dims=(0, 1))
+    res = []
+    for wr in range(G_h // M):
+        for wc in range(G_w // M):
+            oy = ys[wr * M:(wr + 1) * M, wc * M:(wc + 1) * M].reshape(-1)
+            ox = xs[wr * M:(wr + 1) * M, wc * M:(wc + 1) * M].reshape(-1)
+            near = ((oy[:, None] - oy[None, :]).abs() < M) & ((ox[:, None] - ox[None, :]).abs() < M)
+            res.append(near.numpy())
+    return res
+
+
+@pytest.mark.parametrize("geom", [(56, 56, 7, 3), (4, 4, 2, 1), (14, 21, 7, 3), (12, 8, 4, 2)])
+def test_p3_swin_mask_matches_geometric_brute_force(geom):
+    G_h, G_w, M, s = geom
+    allowed = _brute_force_allowed(G_h, G_w, M, s)
+    for w, want in enumerate(allowed):
+        got = np.array([[oracle.swin_mask(M, G_h, G_w, s, w, i, j) for j in range(M * M)]
+                        for i in range(M * M)])
+        assert set(np.unique(got)) <= {0.0, -100.0}
+        np.testing.assert_array_equal(got == 0.0, want)
+
+
+def test_p3_swin_mask_counts_golden(golden_dir):
+    """P3: allowed pair counts per window and per image (hand-enumerated)."""
+    rows = _read_golden(os.path.join(golden_dir, "swin_mask_counts.txt"))
+    cache = {}
+    for gh, gw, M, s, w, cnt in rows:
+        gh, gw, M, s, cnt = int(gh), int(gw), int(M), int(s), int(cnt)
+        key = (gh, gw, M, s)
+        if key not in cache:
+            nW = (gh // M) * (gw // M)
+            cache[key] = [sum(oracle.swin_mask(M, gh, gw, s, win, i, j) == 0.0
+                              for i in range(M * M) for j in range(M * M)) for win in range(nW)]
+        counts = cache[key]
+        if w == "total":
+            assert sum(counts) == cnt
+        else:
+            assert counts[int(w)] == cnt
+
+
+def test_swin_no_shift_means_no_mask():
+    for w in range(16):
+        for i in range(0, 49, 5):
+            for j in range(0, 49, 3):
+                assert oracle.swin_mask(7, 28, 28, 0, w, i, j) == 0.0
+
+
+def test_swin_bias_is_table_gather_plus_mask():
+    """bias = table[idx, h] + mask, read back through an integer-valued table
+    (value = index + 256*h, exact in fp64/fp32)."""
+    M, H = 2, 3
+    table = np.array([[r + 256.0 * h for h in range(H)] for r in range((2 * M - 1) ** 2)])
+    b = oracle.Bias("swin", table=table, win=M, grid_h=4, grid_w=4, shift=1)
+    q = np.zeros((4 * H, M * M, 4))
+    golden = np.array([[4, 3, 1, 0], [5, 4, 2, 1], [7, 6, 4, 3], [8, 7, 5, 4]])
+    for s in range(4 * H):
+        w, h = (s // H) % 4, s % H
+        Bm = oracle.bias_matrix(q, H, s, M * M, b)
+        mask = np.array([[oracle.swin_mask(M, 4, 4, 1, w, i, j) for j in range(4)] for i in range(4)])
+        np.testing.assert_array_equal(Bm, golden + 256.0 * h + mask)
+
+
+def test_swin_2x2_window_softmax_brute_force():
+    """Q = K = 0 leaves only the bias; with V = I the output row is the
+    softmax of the bias row, computed here by hand with math.exp over the
+    golden index matrix and table value 0.1*index."""
+    M, H = 2, 1
+    table = np.arange(9, dtype=float)[:, None] * 0.1
+    b = oracle.Bias("swin", table=table, win=M, grid_h=2, grid_w=2, shift=0)
+    q = np.zeros((1, 4, 4))
+    k = np.zeros((1, 4, 4))
+    v = np.eye(4)[None]
+    out, _ = oracle.attn_fwd(q, k, v, H, 1.0, b)
+    golden = [[4, 3, 1, 0], [5, 4, 2, 1], [7, 6, 4, 3], [8, 7, 5, 4]]
+    for i in range(4):
+        e = [math.exp(0.1 * golden[i][j]) for j in range(4)]
+        want = [x / sum(e) for x in e]
+        np.testing.assert_allclose(out[0, i], want, rtol=0, atol=1e-15)
+
+
+def test_swin_mask_is_finite_minus_100():
+    """Masked pairs keep a weight of about e^-100 (finite mask), not 0."""
+    M, H = 2, 1
+    b = oracle.Bias("swin", table=np.zeros((9, 1)), win=M, grid_h=4, grid_w=4, shift=1)
+    q = np.zeros((4, 4, 4))
+    P, _ = oracle.attn_probs(q, q, np.ones((4, 4, 4)), H, 1.0, 3, b)
+    # window 3: four singleton regions -> diagonal weight 1/(1+3e^-100)
+    off = P[~np.eye(4, dtype=bool)]
+    assert np.all(off > 0)
+    np.testing.assert_allclose(off, math.exp(-100) / (1 + 3 * math.exp(-100)), rtol=1e-12)
+
+
+def test_p7_swin_table_column_shift_invariance():
+    """P7: adding a constant to one head's whole table column shifts every
+    score row of that head by the same amount; O is unchanged."""
+    M, H, d = 3, 2, 8
+    table = _rand(((2 * M - 1) ** 2, H), 3)
+    b1 = oracle.Bias("swin", table=table, win=M, grid_h=6, grid_w=6, shift=1)
+    t2 = table.copy()
+    t2[:, 1] += 5.0
+    b2 = oracle.Bias("swin", table=t2, win=M, grid_h=6, grid_w=6, shift=1)
+    q, k, v = (_rand((4 * H, M * M, d), s) for s in (1, 2, 3))
+    o1, _ = oracle.attn_fwd(q, k, v, H, 0.4, b1)
+    o2, _ = oracle.attn_fwd(q, k, v, H, 0.4, b2)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------------- SAM --
+
+@pytest.mark.parametrize("grid", [(2, 2), (3, 5), (5, 3), (14, 14)])
+def test_p6_p8_sam_relpos_closed_form(grid):
+    """P6/P8: with R_h[r] = r*u and R_w[r] = r*w the decomposed term is
+    (qh-kh+S_h-1)*(Q.u) + (qw-kw+S_w-1)*(Q.w) for tokens i=(qh,qw), j=(kh,kw).
+    Non-square grids catch a swapped height/width; the sign of the offsets
+    and the S-1 shift are fixed by the closed form."""
+    sh, sw = grid
+    d = 6
+    u, w = _rand(d, 11), _rand(d, 12)
+    Rh = np.arange(2 * sh - 1)[:, None] * u[None]
+    Rw = np.arange(2 * sw - 1)[:, None] * w[None]
+    b = oracle.Bias("sam", rel_h=Rh, rel_w=Rw, s_h=sh, s_w=sw)
+    N = sh * sw
+    q = _rand((1, N, d), 13)
+    Bm = oracle.bias_matrix(q, 1, 0, N, b)
+    for i in range(N):
+        qh, qw = divmod(i, sw)
+        for j in range(N):
+            kh, kw = divmod(j, sw)
+            want = (qh - kh + sh - 1) * (q[0, i] @ u) + (qw - kw + sw - 1) * (q[0, i] @ w)
+            assert abs(Bm[i, j] - want) < 1e-12 * (1 + abs(want))
+
+
+def test_p8_sam_integer_tables_exact():
+    """P8: integer-valued tables and Q = 128*e0 + e1 give the exact index
+    pair 128*(qh-kh+S_h-1) + (qw-kw+S_w-1), the fixture of the bit-exact
+    kernel test."""
+    sh, sw, d = 3, 4, 16
+    Rh = np.zeros((2 * sh - 1, d))
+    Rh[:, 0] = np.arange(2 * sh - 1)
+    Rw = np.zeros((2 * sw - 1, d))
+    Rw[:, 1] = np.arange(2 * sw - 1)
+    N = sh * sw
+    q = np.zeros((1, N, d))
+    q[..., 0] = 128.0
+    q[..., 1] = 1.0
+    b = oracle.Bias("sam", rel_h=Rh, rel_w=Rw, s_h=sh, s_w=sw)
+    Bm = oracle.bias_matrix(q, 1, 0, N, b)
+    for i in range(N):
+        for j in range(N):
+            want = 128 * (i // sw - j // sw + sh - 1) + (i % sw - j % sw + sw - 1)
+            assert Bm[i, j] == want
+
+
+def test_p7_sam_constant_table_shift_invariance():
+    """P7: adding the same vector c to every row of R_h adds Q_i.c to the
+    whole score row i; the softmax output is unchanged."""
+    sh, sw, d = 3, 4, 8
+    Rh, Rw = _rand((2 * sh - 1, d), 1), _rand((2 * sw - 1, d), 2)
+    c = _rand(d, 3)
+    q, k, v = (_rand((2, sh * sw, d), s) for s in (4, 5, 6))
+    o1, _ = oracle.attn_fwd(q, k, v, 1, 0.5, oracle.Bias("sam", rel_h=Rh, rel_w=Rw, s_h=sh, s_w=sw))
+    o2, _ = oracle.attn_fwd(q, k, v, 1, 0.5,
+                            oracle.Bias("sam", rel_h=Rh + c, rel_w=Rw, s_h=sh, s_w=sw))
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+
+
+def test_sam_bias_uses_unscaled_q():
+    """The decomposed term does not depend on the softmax scale: zero K makes
+    the scores bias-only, and changing scale must leave O unchanged."""
+    sh, sw, d = 2, 3, 4
+    Rh, Rw = _rand((2 * sh - 1, d), 1), _rand((2 * sw - 1, d), 2)
+    b = oracle.Bias("sam", rel_h=Rh, rel_w=Rw, s_h=sh, s_w=sw)
+    q, v = _rand((1, 6, d), 3), _rand((1, 6, d), 4)
+    k = np.zeros_like(q)
+    o1, _ = oracle.attn_fwd(q, k, v, 1, 0.1, b)
+    o2, _ = oracle.attn_fwd(q, k, v, 1, 7.0, b)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-14)
+
+
+# --------------------------------------------------------------- arguments --
+
+def test_oracle_rejects_bad_shapes():
+    q = np.zeros((2, 9, 4))
+    with pytest.raises(ValueError):
+        oracle.attn_fwd(q, q, q, 3, 1.0)  # BH not a multiple of H
+    with pytest.raises(ValueError):
+        oracle.attn_fwd(q, q, q, 1, 1.0, oracle.Bias("swin", table=np.zeros((25, 1)), win=2,
+                                                     grid_h=4, grid_w=4))  # N != M*M
+    with pytest.raises(ValueError):
+        oracle.attn_fwd(q, q, q, 1, 1.0, oracle.Bias("sam", rel_h=np.zeros((3, 4)),
+                                                     rel_w=np.zeros((3, 4)), s_h=2, s_w=2))
+
+
+def test_workload_inputs_are_seeded_and_shaped():
+    w = WORKLOADS["toy"]
+    a, b = make_inputs(w), make_inputs(w)
+    assert torch.equal(a.q, b.q) and a.q.shape == (1, 2, 64, 32) and a.q.dtype == torch.bfloat16
+    sw = WORKLOADS["swin_t_stage1"].with_(B=64)
+    i = make_inputs(sw)
+    assert i.table.shape == (169, 3) and i.table.dtype == torch.float32
+    sm = WORKLOADS["sam_vith_window"].with_(B=2)
+    i = make_inputs(sm)
+    assert i.rel_h.shape == (27, 80) and i.rel_h.dtype == torch.bfloat16
