@@ -1,0 +1,419 @@
+"""Benchmark of the fused SDPA forward on one GB300 (or N replicas).
+
+Default workload: Swin-T stage-1 shifted-window attention (32 images x 64
+windows of 7x7 tokens, 3 heads, d=32, fp16, relative-position bias and
+shift-3 mask).  One step = one attn_fwd over that whole batch with the
+inputs resident in HBM.  The metric is attention forward TFLOP/s counted as
+4*B*H*Nq*Nk*d with the true head dim.
+
+Timing: the K timed steps run as CUDA-graph replays of back-to-back
+launches on one stream, bracketed by CUDA events, after W warm-up steps;
+input sets rotate so their total exceeds 3x the L2 size (no L2 reuse
+between consecutive steps).  SM clocks are sampled with nvidia-smi during
+the timed region.  ``e2e`` repeats the measurement through the same C-ABI
+call with pinned host buffers: each step copies Q, K, V host->device, runs
+the kernel and copies O device->host, all inside the timed region.
+
+``--impl reference`` times the fp64 CPU oracle (test infrastructure, as it
+stands) on the host cores on a bounded sample of the same workload.
+
+Multi-GPU: the path has no exchange step; with torchrun each rank runs an
+independent replica of the workload (weak scaling) and rank 0 reports the
+aggregate over the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from scaled_dot_product_09_gb300.workloads import WORKLOADS, Workload, make_inputs  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+GRAPH_CHUNK = 100
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def _bound(w: Workload) -> str:
+    # arithmetic intensity vs the machine balance (~300 flop/B for bf16 on GB300)
+    return "tensor" if w.flops / w.io_bytes > 300 else "hbm"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except Exception:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _gpu_bias(w, inp, dev):
+    import scaled_dot_product_09_gb300 as sdpa
+    if w.bias == "swin":
+        return sdpa.SwinBias(inp.table.to(dev), w.win, w.grid_h, w.grid_w, w.shift)
+    if w.bias == "sam":
+        return sdpa.SamBias(inp.rel_h.to(dev), inp.rel_w.to(dev), w.s_h, w.s_w)
+    return None
+
+
+class DeviceSets:
+    """Rotating input sets resident in HBM, totalling > 3x L2."""
+
+    def __init__(self, w: Workload, inp, dev):
+        per = w.io_bytes
+        self.n = max(2, math.ceil(3 * L2_BYTES / per) + 1)
+        self.q = [inp.q.to(dev) for _ in range(self.n)]
+        self.k = [inp.k.to(dev) for _ in range(self.n)]
+        self.v = [inp.v.to(dev) for _ in range(self.n)]
+        self.o = [torch.empty_like(self.q[0]) for _ in range(self.n)]
+        self.bias = _gpu_bias(w, inp, dev)
+
+
+def _time_device(w: Workload, sets: DeviceSets, steps: int, warmup: int, stream):
+    """Returns (total seconds of the K timed steps, number of launches)."""
+    import scaled_dot_product_09_gb300 as sdpa
+
+    def step(i):
+        j = i % sets.n
+        sdpa.attn_fwd(sets.q[j], sets.k[j], sets.v[j], out=sets.o[j], scale=w.scale,
+                      bias=sets.bias, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):
+            step(i)
+    torch.cuda.synchronize()
+    chunk = min(GRAPH_CHUNK, max(1, steps))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(chunk):
+            step(i)
+    torch.cuda.synchronize()
+    full, rest = divmod(steps, chunk)
+    rest_graph = None
+    if rest:
+        rest_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(rest_graph, stream=stream):
+            for i in range(rest):
+                step(i)
+    with torch.cuda.stream(stream):
+        graph.replay()  # one warm replay of the captured sequence
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            graph.replay()
+        if rest_graph is not None:
+            rest_graph.replay()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3, steps
+
+
+def _time_e2e(w: Workload, inp, steps: int, warmup: int, stream, dev):
+    """Pinned host buffers; per step: H2D of q,k,v, kernel, D2H of O."""
+    import scaled_dot_product_09_gb300 as sdpa
+    hq, hk, hv = (x.pin_memory() for x in (inp.q, inp.k, inp.v))
+    ho = torch.empty_like(hq).pin_memory()
+    dq, dk, dv = (torch.empty_like(x, device=dev) for x in (hq, hk, hv))
+    do = torch.empty_like(dq)
+    bias = _gpu_bias(w, inp, dev)
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        sdpa.attn_fwd(dq, dk, dv, out=do, scale=w.scale, bias=bias, stream=stream)
+        ho.copy_(do, non_blocking=True)
+
+    n = max(1, min(steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(n):
+            step()
+        end.record(stream)
+    end.synchronize()
+    sec = start.elapsed_time(end) / 1e3 / n
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size()
+    return sec, h2d, d2h
+
+
+def _suite(stream, dev, peaks, names):
+    """Quick device-only numbers for the other workloads (same method)."""
+    out = {}
+    for name in names:
+        w = WORKLOADS[name]
+        inp = make_inputs(w)
+        sets = DeviceSets(w, inp, dev)
+        steps = max(20, min(2000, int(0.3 / max(w.flops / 1e15, 1e-6))))
+        sec, _ = _time_device(w, sets, steps, 3, stream)
+        t = sec / steps
+        tf = w.flops / t / 1e12
+        gbs = w.io_bytes / t / 1e9
+        bound = _bound(w)
+        frac = tf / peaks["bf16_tflops"] if bound == "tensor" else gbs / peaks["hbm_gbs"]
+        out[name] = {"us_per_step": round(t * 1e6, 2), "tflops": round(tf, 2), "gbs": round(gbs, 1),
+                     "bound": bound, "frac": round(frac, 4)}
+        del sets
+        torch.cuda.empty_cache()
+    return out
+
+
+def _oracle_sample(w: Workload, inp, budget_s: float, nthreads: int = 0):
+    """Time the oracle on whole slices until ~budget_s; returns
+    (TFLOP/s, seconds, slices, threads)."""
+    import oracle
+    BH = w.B * w.H
+    q = inp.q.double().reshape(BH, w.Nq, w.d).numpy()
+    k = inp.k.double().reshape(BH, w.Nk, w.d).numpy()
+    v = inp.v.double().reshape(BH, w.Nk, w.d).numpy()
+    if w.bias == "swin":
+        b = oracle.Bias("swin", table=inp.table.double().numpy(), win=w.win, grid_h=w.grid_h,
+                        grid_w=w.grid_w, shift=w.shift)
+    elif w.bias == "sam":
+        b = oracle.Bias("sam", rel_h=inp.rel_h.double().numpy(), rel_w=inp.rel_w.double().numpy(),
+                        s_h=w.s_h, s_w=w.s_w)
+    else:
+        b = None
+    # calibrate on a few rows, then size the sample to the budget
+    probe_rows = min(w.Nq, 64)
+    t0 = time.perf_counter()
+    _, used = oracle.attn_rows(q, k, v, w.H, w.scale, list(range(probe_rows)), b, nthreads)
+    per_row = max((time.perf_counter() - t0) / probe_rows, 1e-9)
+    rows = int(min(BH * w.Nq, max(w.Nq, budget_s / per_row)))
+    ids = list(range(rows))
+    t0 = time.perf_counter()
+    _, used = oracle.attn_rows(q, k, v, w.H, w.scale, ids, b, nthreads)
+    sec = time.perf_counter() - t0
+    flops = 4.0 * rows * w.Nk * w.d
+    return flops / sec / 1e12, sec, rows, used
+
+
+def run_reference(args, w: Workload, world, rank):
+    if rank != 0:
+        return 0
+    inp = make_inputs(w)
+    steps, warmup = args.steps, args.warmup
+    per_step_budget = max(0.05, min(5.0, 60.0 / max(1, steps + warmup)))
+    for _ in range(warmup):
+        _oracle_sample(w, inp, per_step_budget)
+    rates, secs, rows_total, used = [], 0.0, 0, 0
+    for _ in range(steps):
+        tf, sec, rows, used = _oracle_sample(w, inp, per_step_budget)
+        rates.append(tf)
+        secs += sec
+        rows_total += rows
+    value = (4.0 * rows_total * w.Nk * w.d) / secs / 1e12
+    line = {
+        "impl": "reference", "metric": args.metric, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": warmup,
+        "ms_per_step": secs / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "bias": w.bias, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
+                         "sample": f"{rows_total // steps} of {w.B * w.H * w.Nq} query rows per step "
+                                   "(whole rows, fp64 oracle, OpenMP over rows)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="swin_t_stage1", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-suite", action="store_true", help="skip the other workloads' numbers")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    args = ap.parse_args(argv)
+    args.metric = "attention fwd TFLOP/s (4*B*H*Nq*Nk*d)"
+    world, rank, local = _dist()
+    w = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        return run_reference(args, w, world, rank)
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import scaled_dot_product_09_gb300 as sdpa
+    sdpa.load_library()
+    peaks = _peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    # CPU baseline first (host only), before any GPU timing.
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        inp_cpu = make_inputs(w)
+        tf, sec, rows, used = _oracle_sample(w, inp_cpu, 15.0)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
+               "sample": f"{rows} of {w.B * w.H * w.Nq} query rows ({sec:.1f} s, fp64, OpenMP over rows)"}
+
+    inp = make_inputs(w)
+    sets = DeviceSets(w, inp, dev)
+    n_sets = sets.n
+    _barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    sec, launches = _time_device(w, sets, args.steps, args.warmup, stream)
+    clocks = sampler.stop()
+    torch.cuda.synchronize()
+    _barrier(world)
+    sec = _max_over_ranks(sec, world, dev)
+
+    t_step = sec / args.steps
+    value = world * w.flops / t_step / 1e12
+    bound = _bound(w)
+    if bound == "hbm":
+        achieved = w.io_bytes / t_step / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": peaks["source"], "bytes_per_launch": w.io_bytes}
+    else:
+        achieved = w.flops / t_step / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "peak_source": peaks["source"], "flops_per_launch": w.flops}
+
+    e2e_sec, h2d, d2h = _time_e2e(w, inp, args.steps, args.warmup, stream, dev)
+    e2e_sec = _max_over_ranks(e2e_sec, world, dev)
+    suite = None
+    if rank == 0 and not args.no_suite:
+        del sets
+        torch.cuda.empty_cache()
+        suite = _suite(stream, dev, peaks, [n for n in ("sam_vith_window", "sam_vith_global",
+                                                        "sd_unet_self", "sd_unet_cross") if n != w.name])
+    if rank == 0:
+        line = {
+            "metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                       "bias": w.bias, "global_batch": w.B * world, "parallelism": f"replicas{world}",
+                       "l2": f"{n_sets} rotating input sets, {n_sets * w.io_bytes / 2**20:.0f} MiB > 3x L2",
+                       "launch": f"CUDA graph of {GRAPH_CHUNK} back-to-back attn_fwd launches"},
+            "roofline": roof,
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "e2e": {"value": world * w.flops / e2e_sec / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "cpu_baseline": cpu,
+        }
+        if suite is not None:
+            line["suite"] = suite
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

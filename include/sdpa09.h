@@ -1,0 +1,153 @@
+/*
+ * sdpa09.h -- C ABI of the GB300 (sm_103a) fused scaled-dot-product
+ * attention forward library, libsdpa09.so.
+ *
+ * The operation (per batch-head slice):
+ *
+ *     O = softmax(scale * Q . K^T + bias) . V
+ *
+ * "视觉大模型训练和推理加速" (NVIDIA Swin talk), section 一 Swin Transformer简介:
+ * attention takes query, key and value; query and key with a softmax give
+ * the attention map that weights the values; multi-head attention repeats
+ * this per head.  "Accelerated Diffusers with PyTorch 2.0", section 加速
+ * Transformer 块: the scaled-dot-product-attention function takes
+ * (query, key, value) and every backend computes the same result.  The
+ * bias kinds are described at attn_bias_kind.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensors are device pointers owned by the caller.  The library
+ *    never allocates per call, never copies host<->device and never
+ *    synchronises the stream ("PyTorch团队重写「分割一切」模型，比原始实现快8倍",
+ *    section on the bf16 baseline: an index operation whose host-side
+ *    coordinates forced a copy and a blocking cudaStreamSynchronize was the
+ *    first bottleneck removed).  Bias arguments are read from the host
+ *    struct at call time and passed by value to the kernel.
+ *  - Layout: Q and O are [B][H][Nq][d], K and V are [B][H][Nk][d], all
+ *    contiguous with d innermost, in the dtype given (bf16 or fp16).  Each
+ *    pointer must be 16-byte aligned and d a multiple of 8 (the row pitch
+ *    must be a multiple of 16 bytes for the tensor-memory-access engine).
+ *  - Work runs on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream).  The call returns once the kernel is enqueued.
+ *  - Return value 0 on success, a negative ATTN_ERR_* code otherwise;
+ *    attn_last_error() then describes the failure.  No exception or abort
+ *    crosses the ABI.  Arguments are validated before any CUDA call.
+ */
+#ifndef SDPA09_H
+#define SDPA09_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SDPA09_ABI_VERSION 1
+
+typedef enum {
+    ATTN_BF16 = 0, /* bfloat16 Q/K/V/O ("model.to(torch.bfloat16)" in the SAM rewrite) */
+    ATTN_FP16 = 1  /* float16 Q/K/V/O (torch.cuda.amp in the Swin talk, fp16 diffusers) */
+} attn_dtype;
+
+/* Bias added to scale * Q.K^T before the softmax.
+ *
+ * ATTN_BIAS_NONE: no bias -- the diffusion UNet self- and cross-attention
+ *   of "Accelerated Diffusers with PyTorch 2.0", section 在 diffusers 中使用缩放点积注意力机制.
+ *
+ * ATTN_BIAS_SWIN: Swin window attention with relative position bias and the
+ *   shifted-window mask ("视觉大模型训练和推理加速", section 一: window
+ *   attention, window shift, relative position bias).  Each slice is one
+ *   M x M window (Nq = Nk = M*M, tokens row-major in the window); the
+ *   batch index b counts windows, b = image * nW + w with window w
+ *   row-major over the (grid_h/M) x (grid_w/M) window grid.  For query
+ *   token (ri,ci) and key token (rj,cj) of head h the bias is
+ *       table[((ri-rj+M-1)*(2M-1) + (ci-cj+M-1)) * H + h]
+ *   plus -100 when, after a cyclic shift by `shift`, the two tokens lie in
+ *   different regions (strips [0,G-M), [G-M,G-shift), [G-shift,G) along
+ *   each axis); shift = 0 means no mask.  The cyclic shift and window
+ *   partition themselves happen before this call.
+ *
+ * ATTN_BIAS_SAM_RELPOS: SAM image-encoder decomposed relative position
+ *   ("Accelerating Generative AI (part 1), Segment Anything", section
+ *   Bfloat16 半精度: the encoder indexes rel_pos_resized with q_coords /
+ *   k_coords).  Tokens are row-major on a q_h x q_w grid; for query
+ *   i = (qh,qw) and key j = (kh,kw)
+ *       bias = Q_i . R_h[qh-kh+q_h-1] + Q_i . R_w[qw-kw+q_w-1]
+ *   with the unscaled Q.  This version requires q_h == k_h, q_w == k_w.
+ */
+typedef enum {
+    ATTN_BIAS_NONE = 0,
+    ATTN_BIAS_SWIN = 1,
+    ATTN_BIAS_SAM_RELPOS = 2
+} attn_bias_kind;
+
+typedef struct {
+    const float* table; /* device, [(2*win-1)^2][H] row-major fp32 */
+    int win;            /* M, window side in tokens (7 for Swin-T) */
+    int grid_h, grid_w; /* tokens per image side, multiples of win (56, 56) */
+    int shift;          /* cyclic shift, 0 <= shift < win; 0 = no mask */
+} attn_swin_args;
+
+typedef struct {
+    const void* rel_h;  /* device, [2*q_h-1][d], same dtype as Q */
+    const void* rel_w;  /* device, [2*q_w-1][d], same dtype as Q */
+    int q_h, q_w;       /* query grid; Nq = q_h * q_w */
+    int k_h, k_w;       /* key grid; must equal the query grid */
+} attn_sam_args;
+
+enum {
+    ATTN_OK = 0,
+    ATTN_ERR_ARG = -1,            /* null/misaligned pointer, bad size, bad bias args */
+    ATTN_ERR_UNSUPPORTED = -2,    /* valid but not implemented (e.g. d > 128, SAM q grid != k grid) */
+    ATTN_ERR_CUDA = -3,           /* a CUDA runtime/driver call or the launch failed */
+    ATTN_ERR_DEVICE_TIMEOUT = -4  /* a kernel wait ran out of time (attn_device_status) */
+};
+
+/* attn_fwd -- the fused forward pass O = softmax(scale*Q.K^T + bias).V.
+ *
+ *  q, k, v    device inputs, layout above; not modified.
+ *  out        device output [B][H][Nq][d]; fully overwritten; must not
+ *             alias q, k or v.
+ *  B, H       batch (or window count) and heads, >= 1.
+ *  Nq, Nk     query and key lengths, >= 1 (Nk <= 2^20).
+ *  d          head dim: a multiple of 8, 8 <= d <= 128.
+ *  scale      multiplies Q.K^T only (usually 1/sqrt(d)).
+ *  dtype      element type of q, k, v, out (and SAM tables).
+ *  bias_kind  see attn_bias_kind; bias_args points to attn_swin_args or
+ *             attn_sam_args (host memory, read during the call), or NULL
+ *             for ATTN_BIAS_NONE.
+ *  stream     cudaStream_t to enqueue on.
+ *
+ * Accumulation is fp32 (scores, softmax, P.V); P is rounded to the input
+ * dtype before the second product; O is rounded to nearest even.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int H, int Nq,
+             int Nk, int d, float scale, attn_dtype dtype, attn_bias_kind bias_kind,
+             const void* bias_args, void* stream);
+
+/* attn_debug_bias -- test hook for the in-kernel bias builders.
+ *
+ * Runs the same kernel as attn_fwd with the same arguments but, instead
+ * of O, writes the bias value the builder adds to each score (in natural
+ * units, before the softmax; masked-out key padding excluded) to
+ * bias_out [B][H][Nq][Nk] fp32 (device).  Meant for small shapes.
+ */
+int attn_debug_bias(const void* q, const void* k, const void* v, float* bias_out, int B, int H,
+                    int Nq, int Nk, int d, float scale, attn_dtype dtype,
+                    attn_bias_kind bias_kind, const void* bias_args, void* stream);
+
+/* attn_device_status -- synchronises `stream`, then reads and clears the
+ * library's device status word.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT
+ * when some kernel wait ran out of time since the last call (the kernel
+ * then stopped early and its output is invalid), or ATTN_ERR_CUDA. */
+int attn_device_status(void* stream);
+
+/* attn_last_error -- text of the last failure on the calling thread
+ * (empty string when none).  The pointer stays valid until the next call
+ * on the same thread. */
+const char* attn_last_error(void);
+
+/* attn_abi_version -- SDPA09_ABI_VERSION of the built library. */
+int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SDPA09_H */

@@ -1,0 +1,186 @@
+"""GB300 (sm_103a) fused scaled-dot-product attention forward.
+
+Thin Python binding over the C ABI of ``libsdpa09.so`` (declared in
+``include/sdpa09.h``): it only marshals torch tensors into pointers and
+sizes.  Every step of the computation runs in the library's CUDA kernels;
+there is no CPU or PyTorch fallback -- a missing or unbuildable library
+raises.
+
+    O = softmax(scale * Q.K^T + bias) . V
+
+with bias one of: none (diffusion UNet self/cross attention), Swin's
+relative-position table plus shifted-window mask, or SAM's decomposed
+relative position ("视觉大模型训练和推理加速" section 一; "Accelerated
+Diffusers with PyTorch 2.0" section 加速 Transformer 块; SAM rewrite,
+section Bfloat16 半精度).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = ["attn_fwd", "attn_debug_bias", "attn_device_status", "SwinBias", "SamBias",
+           "load_library", "AttnError", "ATTN_OK", "ATTN_ERR_ARG", "ATTN_ERR_UNSUPPORTED",
+           "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT", "HEADER_SYMBOLS"]
+
+ATTN_OK, ATTN_ERR_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = 0, -1, -2, -3, -4
+ATTN_BF16, ATTN_FP16 = 0, 1
+ATTN_BIAS_NONE, ATTN_BIAS_SWIN, ATTN_BIAS_SAM_RELPOS = 0, 1, 2
+
+# Every extern "C" function include/sdpa09.h declares.
+HEADER_SYMBOLS = ("attn_fwd", "attn_debug_bias", "attn_device_status", "attn_last_error",
+                  "attn_abi_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"sdpa09 error {code}: {msg}")
+        self.code = code
+
+
+class _SwinArgs(ctypes.Structure):
+    _fields_ = [("table", ctypes.c_void_p), ("win", ctypes.c_int), ("grid_h", ctypes.c_int),
+                ("grid_w", ctypes.c_int), ("shift", ctypes.c_int)]
+
+
+class _SamArgs(ctypes.Structure):
+    _fields_ = [("rel_h", ctypes.c_void_p), ("rel_w", ctypes.c_void_p), ("q_h", ctypes.c_int),
+                ("q_w", ctypes.c_int), ("k_h", ctypes.c_int), ("k_w", ctypes.c_int)]
+
+
+class SwinBias:
+    """Swin relative-position bias + shifted-window mask.
+    table: device fp32 [(2*win-1)^2, H]; grid_h/grid_w: tokens per image side."""
+
+    def __init__(self, table, win, grid_h, grid_w, shift):
+        self.table, self.win, self.grid_h, self.grid_w, self.shift = table, win, grid_h, grid_w, shift
+
+    def _c(self):
+        return _SwinArgs(_ptr(self.table), self.win, self.grid_h, self.grid_w, self.shift)
+
+
+class SamBias:
+    """SAM decomposed relative position.  rel_h [2*q_h-1, d], rel_w [2*q_w-1, d]
+    on the device in the Q dtype; query grid == key grid."""
+
+    def __init__(self, rel_h, rel_w, q_h, q_w, k_h=None, k_w=None):
+        self.rel_h, self.rel_w, self.q_h, self.q_w = rel_h, rel_w, q_h, q_w
+        self.k_h = q_h if k_h is None else k_h
+        self.k_w = q_w if k_w is None else k_w
+
+    def _c(self):
+        return _SamArgs(_ptr(self.rel_h), _ptr(self.rel_w), self.q_h, self.q_w, self.k_h, self.k_w)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def load_library(build: bool = True):
+    """Load libsdpa09.so (building it first when missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        from . import _build
+        path = _build.build() if build else _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libsdpa09.so not found at {path}; run the build first")
+        lib = ctypes.CDLL(path)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp]
+        lib.attn_fwd.restype = i
+        lib.attn_debug_bias.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp]
+        lib.attn_debug_bias.restype = i
+        lib.attn_device_status.argtypes = [vp]
+        lib.attn_device_status.restype = i
+        lib.attn_last_error.argtypes = []
+        lib.attn_last_error.restype = ctypes.c_char_p
+        lib.attn_abi_version.argtypes = []
+        lib.attn_abi_version.restype = i
+        _lib = lib
+        return lib
+
+
+def _check(lib, rc):
+    if rc != ATTN_OK:
+        raise AttnError(rc, lib.attn_last_error().decode(errors="replace"))
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float16:
+        return ATTN_FP16
+    raise AttnError(ATTN_ERR_ARG, f"unsupported dtype {t.dtype}")
+
+
+def _bias_args(bias):
+    if bias is None:
+        return ATTN_BIAS_NONE, None, None
+    c = bias._c()
+    kind = ATTN_BIAS_SWIN if isinstance(bias, SwinBias) else ATTN_BIAS_SAM_RELPOS
+    return kind, c, ctypes.byref(c)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _shape(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise AttnError(ATTN_ERR_ARG, "q, k, v must be [B, H, N, d]")
+    B, H, Nq, d = q.shape
+    if k.shape[:2] != (B, H) or v.shape != k.shape or k.shape[3] != d:
+        raise AttnError(ATTN_ERR_ARG, "k, v must be [B, H, Nk, d] matching q")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise AttnError(ATTN_ERR_ARG, "tensors must be contiguous")
+    return B, H, Nq, k.shape[2], d
+
+
+def attn_fwd(q, k, v, out=None, scale=None, bias=None, stream=None):
+    """O = softmax(scale*Q.K^T + bias).V on the GPU.  q [B,H,Nq,d], k/v
+    [B,H,Nk,d] contiguous bf16/fp16 CUDA tensors; returns out [B,H,Nq,d]."""
+    import torch
+    lib = load_library()
+    B, H, Nq, Nk, d = _shape(q, k, v)
+    if out is None:
+        out = torch.empty_like(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kind, _keep, args = _bias_args(bias)
+    rc = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Nq, Nk, d, scale,
+                      _dtype_code(q), kind, args, _stream_ptr(stream))
+    _check(lib, rc)
+    return out
+
+
+def attn_debug_bias(q, k, v, scale=None, bias=None, stream=None):
+    """The bias the in-kernel builder adds, as fp32 [B,H,Nq,Nk] (test hook)."""
+    import torch
+    lib = load_library()
+    B, H, Nq, Nk, d = _shape(q, k, v)
+    dbg = torch.zeros((B, H, Nq, Nk), dtype=torch.float32, device=q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kind, _keep, args = _bias_args(bias)
+    rc = lib.attn_debug_bias(_ptr(q), _ptr(k), _ptr(v), _ptr(dbg), B, H, Nq, Nk, d, scale,
+                             _dtype_code(q), kind, args, _stream_ptr(stream))
+    _check(lib, rc)
+    return dbg
+
+
+def attn_device_status(stream=None):
+    """Synchronise the stream and return the library's device status code."""
+    lib = load_library()
+    return lib.attn_device_status(_stream_ptr(stream))

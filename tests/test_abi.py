@@ -1,0 +1,111 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+symbol include/sdpa09.h declares, and rejects bad arguments before making
+any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import scaled_dot_product_09_gb300 as sdpa
+from scaled_dot_product_09_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdpa09.h")
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced by argument checks
+
+
+def _header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return sdpa.load_library()
+
+
+def test_header_symbols_match_binding():
+    assert _header_functions() == sorted(sdpa.HEADER_SYMBOLS)
+
+
+def test_library_exports_every_header_symbol(lib):
+    for name in _header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_targets_sm103a_only():
+    assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_abi_version(lib):
+    assert lib.attn_abi_version() == 1
+
+
+def _call(lib, q=FAKE, k=FAKE + 4096, v=FAKE + 8192, out=FAKE + 1 << 20, B=1, H=1, Nq=64, Nk=64,
+          d=32, scale=0.125, dtype=0, kind=0, args=None):
+    return lib.attn_fwd(q, k, v, out, B, H, Nq, Nk, d, scale, dtype, kind, args, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), sdpa.ATTN_ERR_ARG),
+    (dict(out=None), sdpa.ATTN_ERR_ARG),
+    (dict(q=FAKE + 8), sdpa.ATTN_ERR_ARG),       # misaligned
+    (dict(B=0), sdpa.ATTN_ERR_ARG),
+    (dict(Nq=0), sdpa.ATTN_ERR_ARG),
+    (dict(Nk=-3), sdpa.ATTN_ERR_ARG),
+    (dict(d=36), sdpa.ATTN_ERR_ARG),             # not a multiple of 8
+    (dict(d=0), sdpa.ATTN_ERR_ARG),
+    (dict(d=256), sdpa.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=7), sdpa.ATTN_ERR_ARG),
+    (dict(kind=9), sdpa.ATTN_ERR_ARG),
+    (dict(scale=float("nan")), sdpa.ATTN_ERR_ARG),
+    (dict(out=FAKE), sdpa.ATTN_ERR_ARG),         # aliases q
+])
+def test_bad_arguments_rejected_before_cuda(lib, kw, code):
+    assert _call(lib, **kw) == code
+    assert lib.attn_last_error().decode()
+
+
+def test_swin_argument_checks(lib):
+    a = sdpa._SwinArgs(FAKE, 7, 56, 56, 3)
+    # Nq != win*win
+    assert _call(lib, Nq=50, Nk=50, kind=1, args=ctypes.byref(a)) == sdpa.ATTN_ERR_ARG
+    # missing struct / table
+    assert _call(lib, Nq=49, Nk=49, kind=1, args=None) == sdpa.ATTN_ERR_ARG
+    bad = sdpa._SwinArgs(None, 7, 56, 56, 3)
+    assert _call(lib, Nq=49, Nk=49, kind=1, args=ctypes.byref(bad)) == sdpa.ATTN_ERR_ARG
+    # shift out of range, grid not a multiple of win, B not whole images
+    for s in (sdpa._SwinArgs(FAKE, 7, 56, 56, 7), sdpa._SwinArgs(FAKE, 7, 50, 56, 3)):
+        assert _call(lib, B=64, Nq=49, Nk=49, kind=1, args=ctypes.byref(s)) == sdpa.ATTN_ERR_ARG
+    assert _call(lib, B=63, Nq=49, Nk=49, kind=1, args=ctypes.byref(a)) == sdpa.ATTN_ERR_ARG
+    # windows above 128 tokens
+    big = sdpa._SwinArgs(FAKE, 12, 24, 24, 0)
+    assert _call(lib, B=4, Nq=144, Nk=144, kind=1, args=ctypes.byref(big)) == sdpa.ATTN_ERR_UNSUPPORTED
+
+
+def test_sam_argument_checks(lib):
+    ok = sdpa._SamArgs(FAKE, FAKE, 8, 8, 8, 8)
+    assert _call(lib, Nq=65, Nk=65, kind=2, args=ctypes.byref(ok)) == sdpa.ATTN_ERR_ARG
+    diff = sdpa._SamArgs(FAKE, FAKE, 8, 8, 4, 4)
+    assert _call(lib, Nq=64, Nk=16, kind=2, args=ctypes.byref(diff)) == sdpa.ATTN_ERR_UNSUPPORTED
+    none = sdpa._SamArgs(None, FAKE, 8, 8, 8, 8)
+    assert _call(lib, Nq=64, Nk=64, kind=2, args=ctypes.byref(none)) == sdpa.ATTN_ERR_ARG
+    huge = sdpa._SamArgs(FAKE, FAKE, 100, 100, 100, 100)
+    assert _call(lib, Nq=10000, Nk=10000, kind=2, args=ctypes.byref(huge)) == sdpa.ATTN_ERR_UNSUPPORTED
+
+
+def test_debug_bias_rejects_null_output(lib):
+    assert lib.attn_debug_bias(FAKE, FAKE, FAKE, None, 1, 1, 64, 64, 32, 0.1, 0, 0, None, None) \
+        == sdpa.ATTN_ERR_ARG
+
+
+def test_binding_rejects_bad_tensors():
+    import torch
+    q = torch.zeros(1, 2, 8, 32, dtype=torch.bfloat16)
+    with pytest.raises(sdpa.AttnError):
+        sdpa.attn_fwd(q, q[:, :1], q)
+    with pytest.raises(sdpa.AttnError):
+        sdpa.attn_fwd(q.float(), q.float(), q.float())

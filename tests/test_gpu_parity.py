@@ -1,0 +1,171 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64
+oracle on the same seeded inputs.  Tolerance: max |err| <= 2e-2 and mean
+|err| <= 2e-3 on the bf16/fp16 outputs; bias indexing bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scaled_dot_product_09_gb300 as sdpa
+from scaled_dot_product_09_gb300.workloads import WORKLOADS, Workload, make_inputs
+
+from gpu_util import (compare, flat64, full_parity, gpu_bias, oracle_bias, require_gpu, run_gpu,
+                      sampled_parity)
+
+pytestmark = pytest.mark.gpu
+
+W = WORKLOADS
+
+
+# ----------------------------------------------------- workloads, reduced --
+
+def test_toy_full():
+    full_parity(W["toy"])
+
+
+def test_swin_reduced_full():
+    # 2 images x 64 windows x 3 heads
+    full_parity(W["swin_t_stage1"].with_(B=2 * 64))
+
+
+def test_swin_ragged_tail():
+    # one 21x21 image: 9 windows x 3 heads = 27 slices -> last tile holds one window
+    full_parity(W["swin_t_stage1"].with_(B=9, grid_h=21, grid_w=21, seed=11))
+
+
+def test_swin_no_shift():
+    full_parity(W["swin_t_stage1"].with_(B=64, shift=0, seed=12))
+
+
+def test_sam_window_reduced_full():
+    full_parity(W["sam_vith_window"].with_(B=3))
+
+
+def test_sam_global_reduced_grid():
+    # 16x16 grid: 256 tokens, two query and two key tiles
+    full_parity(W["sam_vith_global"].with_(B=1, H=3, Nq=256, Nk=256, s_h=16, s_w=16, seed=21))
+
+
+def test_sam_global_nonsquare_ragged():
+    # 12x20 grid: 240 tokens, ragged last tiles, height != width
+    full_parity(W["sam_vith_global"].with_(B=1, H=2, Nq=240, Nk=240, s_h=12, s_w=20, seed=22))
+
+
+def test_sd_self_reduced_ragged():
+    full_parity(W["sd_unet_self"].with_(B=1, H=2, Nq=1000, Nk=1000, seed=31))
+
+
+def test_sd_cross_reduced():
+    full_parity(W["sd_unet_cross"].with_(B=2, H=3, Nq=700))
+
+
+# ------------------------------------------------------ workloads, full size --
+
+@pytest.mark.parametrize("name", ["swin_t_stage1", "sam_vith_window", "sam_vith_global",
+                                  "sd_unet_self", "sd_unet_cross"])
+def test_full_size_sampled(name):
+    sampled_parity(W[name])
+
+
+# ------------------------------------------------------------- edge shapes --
+
+@pytest.mark.parametrize("d", [8, 16, 24, 40, 56, 64, 80, 96, 112, 128])
+def test_head_dims(d):
+    w = Workload("edge_d", B=1, H=2, Nq=150, Nk=200, d=d, dtype="bf16", bias="none", seed=40 + d)
+    full_parity(w)
+
+
+@pytest.mark.parametrize("nq,nk", [(1, 1), (1, 300), (300, 1), (128, 128), (129, 129),
+                                   (64, 64), (7, 9), (33, 100), (200, 50)])
+def test_lengths(nq, nk):
+    w = Workload("edge_n", B=2, H=3, Nq=nq, Nk=nk, d=32, dtype="fp16", bias="none", seed=nq * 7 + nk)
+    full_parity(w)
+
+
+def test_single_slice():
+    full_parity(Workload("bh1", B=1, H=1, Nq=77, Nk=333, d=40, dtype="fp16", bias="none", seed=5))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_dtypes(dtype):
+    full_parity(Workload("dt", B=2, H=2, Nq=256, Nk=256, d=64, dtype=dtype, bias="none", seed=9))
+
+
+def test_large_scores_stay_finite():
+    """Scores of a few hundred: the online softmax must rescale, not overflow."""
+    w = Workload("big", B=1, H=1, Nq=256, Nk=512, d=64, dtype="bf16", bias="none", seed=3)
+    inp = make_inputs(w)
+    inp.q = (inp.q.float() * 4).to(torch.bfloat16)
+    got = run_gpu(w, inp, scale=1.0)
+    want, _ = oracle.attn_fwd(flat64(inp.q), flat64(inp.k), flat64(inp.v), 1, 1.0)
+    compare(flat64(got), want, what="large scores")
+
+
+def test_output_not_aliasing_and_repeatable():
+    w = W["toy"]
+    inp = make_inputs(w)
+    a = run_gpu(w, inp)
+    b = run_gpu(w, inp)
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------- bias bit-exactness --
+
+def test_swin_bias_indexing_bit_exact():
+    """table[r, h] = r + 256*h is exact in fp32: the in-kernel gather must
+    return index + 256*h (+ -100 across regions) exactly."""
+    require_gpu()
+    w = W["swin_t_stage1"].with_(B=64)
+    M, H = w.win, w.H
+    table = torch.tensor([[r + 256.0 * h for h in range(H)] for r in range((2 * M - 1) ** 2)])
+    inp = make_inputs(w)
+    inp.table = table
+    q, k, v = (x.cuda() for x in (inp.q, inp.k, inp.v))
+    got = sdpa.attn_debug_bias(q, k, v, scale=w.scale, bias=gpu_bias(w, inp)).cpu().double()
+    b = oracle_bias(w, inp)
+    for s in range(0, w.B * H, 7):
+        want = oracle.bias_matrix(flat64(inp.q), H, s, w.Nk, b)
+        np.testing.assert_array_equal(got.reshape(-1, w.Nq, w.Nk)[s].numpy(), want)
+
+
+def test_sam_bias_indexing_bit_exact():
+    """Integer tables R_h[r,0] = r, R_w[r,1] = r and Q = 128*e0 + e1 make
+    the decomposed term 128*(qh-kh+S_h-1) + (qw-kw+S_w-1), exact in bf16
+    operands with fp32 accumulation."""
+    require_gpu()
+    w = W["sam_vith_global"].with_(B=1, H=2, Nq=240, Nk=240, s_h=12, s_w=20)
+    inp = make_inputs(w)
+    Rh = torch.zeros(2 * w.s_h - 1, w.d)
+    Rh[:, 0] = torch.arange(2 * w.s_h - 1)
+    Rw = torch.zeros(2 * w.s_w - 1, w.d)
+    Rw[:, 1] = torch.arange(2 * w.s_w - 1)
+    inp.rel_h, inp.rel_w = Rh.to(torch.bfloat16), Rw.to(torch.bfloat16)
+    qq = torch.zeros_like(inp.q, dtype=torch.float32)
+    qq[..., 0], qq[..., 1] = 128.0, 1.0
+    inp.q = qq.to(torch.bfloat16)
+    q, k, v = (x.cuda() for x in (inp.q, inp.k, inp.v))
+    got = sdpa.attn_debug_bias(q, k, v, scale=w.scale, bias=gpu_bias(w, inp)).cpu().double()
+    b = oracle_bias(w, inp)
+    for s in range(w.B * w.H):
+        want = oracle.bias_matrix(flat64(inp.q), w.H, s, w.Nk, b)
+        np.testing.assert_array_equal(got.reshape(-1, w.Nq, w.Nk)[s].numpy(), want)
+
+
+def test_sam_window_bias_indexing_bit_exact():
+    require_gpu()
+    w = W["sam_vith_window"].with_(B=2, H=2)
+    inp = make_inputs(w)
+    Rh = torch.zeros(2 * w.s_h - 1, w.d)
+    Rh[:, 0] = torch.arange(2 * w.s_h - 1)
+    Rw = torch.zeros(2 * w.s_w - 1, w.d)
+    Rw[:, 1] = torch.arange(2 * w.s_w - 1)
+    inp.rel_h, inp.rel_w = Rh.to(torch.bfloat16), Rw.to(torch.bfloat16)
+    qq = torch.zeros_like(inp.q, dtype=torch.float32)
+    qq[..., 0], qq[..., 1] = 128.0, 1.0
+    inp.q = qq.to(torch.bfloat16)
+    q, k, v = (x.cuda() for x in (inp.q, inp.k, inp.v))
+    got = sdpa.attn_debug_bias(q, k, v, scale=w.scale, bias=gpu_bias(w, inp)).cpu().double()
+    b = oracle_bias(w, inp)
+    for s in range(w.B * w.H):
+        want = oracle.bias_matrix(flat64(inp.q), w.H, s, w.Nk, b)
+        np.testing.assert_array_equal(got.reshape(-1, w.Nq, w.Nk)[s].numpy(), want)
