@@ -1,0 +1,6 @@
+// Instantiates the attention kernels for head dims padded to 80, bias kind "sam".
+#include "attn_launch.cuh"
+
+namespace sdpa09 {
+SDPA09_INSTANTIATE(80, kBiasSam, launch_attn_sam)
+}  // namespace sdpa09

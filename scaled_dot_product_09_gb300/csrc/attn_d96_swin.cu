@@ -1,0 +1,6 @@
+// Instantiates the attention kernels for head dims padded to 96, bias kind "swin".
+#include "attn_launch.cuh"
+
+namespace sdpa09 {
+SDPA09_INSTANTIATE(96, kBiasSwin, launch_attn_swin)
+}  // namespace sdpa09

@@ -2,34 +2,49 @@
 // GB300 (sm_103a): O = softmax(scale * Q.K^T + bias) . V.
 //
 // Method: "视觉大模型训练和推理加速" section 一 (attention map from query and
-// key through a softmax, weighting the values) computed the memory-efficient
+// key through a softmax, weighting the values), computed the memory-efficient
 // way the SAM and diffusers pages describe ("PyTorch团队重写「分割一切」模型，
 // 比原始实现快8倍", section SDPA: scaled_dot_product_attention; "Accelerated
 // Diffusers with PyTorch 2.0", section 加速 Transformer 块): the score matrix
 // never leaves the chip; an online softmax (running max and sum) carries the
 // row statistics across key tiles.
 //
-// One CTA owns one 128-row query tile.  Eight warps, specialised:
-//   warp 0      TMA producer: Q once, then a ring of K/V stages.
-//   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma.
-//   warps 2-3   bias helpers (SAM relative-position prologue).
-//   warps 4-7   softmax: thread t owns query row t = TMEM lane t.  They
-//               read S from TMEM, add scale and bias, keep the running max
-//               and sum, write P (16-bit) back into TMEM over S, rescale O
-//               when the max grows by more than 2^8, and run the epilogue.
-// Tensor memory (512 columns): S double buffer at columns [0,128) and
-// [128,256) (P aliases the first 64 columns of its S buffer), O at
-// [256, 256+DPAD).
-// Shared memory holds Q, K and V in the 32-byte-swizzled K-major layout the
-// TMA writes: DPAD/16 column blocks of 128 rows x 32 bytes.  S = Q.K^T is an
-// SS MMA with both operands K-major; O += P.V is a TS MMA with P from TMEM
-// and V read MN-major from shared memory.
+// Persistent kernel, one CTA per SM, twelve warps (three warpgroups):
+//   warps 0-3   softmax slot A: thread t owns query row t of tile A (TMEM lane t)
+//   warps 4-7   softmax slot B: the same for tile B
+//   warp 8      TMA producer
+//   warp 9      tensor-memory allocator; lane 0 issues every tcgen05.mma
+//   warps 10-11 idle
+// While one slot runs its softmax the tensor core works on the other slot's
+// products.  After setup the softmax warpgroups grow to kSoftmaxRegs registers
+// and the control warpgroup shrinks to kControlRegs; the split adds up exactly
+// to the launch allocation.
 //
-// Two tilings:
-//   long   : one slice per CTA, 128 query rows, key loop over 128-key tiles.
-//   packed : g whole slices per CTA (g*Nq <= 128, g*Nk <= 128), one key
-//            tile, block-diagonal validity (window attention with short
-//            windows: Swin's 49-token windows, two per tile).
+// Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A [256,384),
+// O_B [384,512).  P (16-bit) overwrites the first 64 columns of its S buffer
+// and feeds the P.V MMA straight from TMEM.
+//
+// Shared-memory operand tiles are 32-byte-swizzled K-major blocks (16-column
+// blocks of R rows x 32 bytes) as the TMA writes them.  S = Q.K^T: both
+// operands K-major.  O += P.V: V read MN-major.
+//
+// Job modes:
+//   shared   : a job is 256 query rows of one slice (A = first 128, B = next
+//              128); both slots consume the same K/V ring (long sequences,
+//              SAM windows of 196 tokens).  With the SAM bias each job first
+//              passes the rel-pos tables R_w, R_h through the ring; the tensor
+//              core forms G_w = Q.R_w^T and G_h = Q.R_h^T, from which every
+//              row gathers its decomposed relative terms.
+//   separate : a job is two packed tiles; a tile holds 128/SL whole slices,
+//              one per SL-row slot (short windows: two 49-token Swin windows
+//              in 64-row slots), and brings its own Q, K and V.  A warp's
+//              rows all lie in one slot, so it only reads that slot's SL key
+//              columns.  The Swin bias is added by the tensor core: with Qone
+//              the one-hot code of each row's window token, Qone.E_h^T adds
+//              the per-head relative-position block E_h[t_q][t_k] =
+//              table[idx(t_q,t_k), h] / scale and Qone.M^T the shifted-window
+//              mask block of the window's kind (interior, last row, last
+//              column, corner), both built once per CTA in shared memory.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -39,18 +54,26 @@
 
 namespace sdpa09 {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 208;
+constexpr int kControlRegs = 88;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs == kThreads * kLaunchRegs,
+              "register split must add up to the launch allocation");
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
-constexpr int kSoftmaxWarp0 = 4;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
-constexpr int kTmemO = 256;
+constexpr int kMaxStages = 8;
+constexpr int kSamMaxSide = 64;  // rel-pos grids up to 64 x 64
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before O is rescaled
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may reach 2^8 before O is rescaled
 
 enum BiasKind { kBiasNone = 0, kBiasSwin = 1, kBiasSam = 2 };
+enum JobMode { kModeShared = 0, kModeSeparate = 1 };
 
-// Error codes left in the device status word.
+// Codes left in the device status word when a bounded wait runs out.
 enum DevStatus {
     kStatusOk = 0,
     kStatusWaitQ = 1,
@@ -60,83 +83,209 @@ enum DevStatus {
     kStatusWaitP = 5,
     kStatusWaitO = 6,
     kStatusWaitEmpty = 7,
-    kStatusWaitFinal = 8,
+    kStatusWaitG = 8,
 };
 
 struct AttnParams {
-    void* out;         // [BH][Nq][d]
-    float* dbg;        // debug bias [BH][Nq][Nk] or null
-    int* status;       // device status word
+    void* out;        // [BH][Nq][d]
+    float* dbg;       // debug bias [BH][Nq][Nk] or null
+    int* status;      // device status word
     int BH, H, Nq, Nk, d;
-    int g;             // slices per tile (packed) or 1 (long)
-    int packed;        // 1 = packed tiling
-    int n_q_tiles;     // query tiles per slice (long)
-    int n_kv_tiles;    // key tiles (long) or 1 (packed)
-    int kv_cols;       // N of the S MMA (multiple of 16)
-    int box_rows_q;    // rows per Q TMA box
-    int box_rows_kv;   // rows per K/V TMA box
-    float scale_log2;  // scale * log2(e)
+    int n_jobs;       // jobs of the grid-stride loop
+    int n_kv;         // key tiles per job (shared mode)
+    int kv_w;         // keys advanced per key tile (shared mode)
+    int kv_cols;      // N of the S MMA, multiple of 16, <= 128
+    int q_jobs;       // 256-row jobs per slice (shared mode)
+    int g;            // slices per packed tile (separate mode)
+    int nst;          // ring stages
+    int nq;           // Q buffers per slot (shared mode): 1 or 2
+    int box_q, box_kv;
+    uint32_t off_q, off_ring, off_extra;  // shared-memory offsets (bytes)
+    uint32_t ring_stage_bytes;
+    float scale;
+    float scale_log2;
     int is_bf16;
     // Swin
     const float* table;  // [(2M-1)^2][H]
-    int win, grid_h, grid_w, shift, n_w, n_ww;
+    int win, grid_h, grid_w, shift, n_w, n_ww, n_wh;
     // SAM
-    const void* rel_h;   // [2*s_h-1][d]
-    const void* rel_w;   // [2*s_w-1][d]
-    const void* q;       // Q again, read by the SAM prologue
-    int s_h, s_w;
+    int s_h, s_w, n_rh, n_rw;
 };
+
+// Shared memory after the ring ("extra"):
+//   Swin (separate mode, slot SL): Qone [128 rows][SL] then H + 3 bias blocks
+//        [SL][SL] (per-head tables, then last-column / last-row / corner
+//        masks), all 16-bit K-major 32B-swizzled
+//   SAM : rel_h [2 slots][s_h][128] fp32, then for generic grids rel_w
+//        [2][s_w][128] and a key table [Nk]
+__host__ __device__ constexpr uint32_t swin_extra_bytes(int sl, int H) {
+    return (uint32_t)(128 * sl * 2 + (H + 3) * sl * sl * 2);
+}
+__host__ __device__ constexpr uint32_t sam_extra_floats(bool generic, int s_h, int s_w, int nk) {
+    return 2u * (uint32_t)s_h * kBlockM + (generic ? 2u * (uint32_t)s_w * kBlockM + (uint32_t)nk : 0u);
+}
 
 template <int DPAD>
-struct KernelCfg {
-    static constexpr int kAtoms = DPAD / 16;                 // 16-element column blocks
-    static constexpr int kTileBytes = kAtoms * kBlockM * 32; // 128 rows x DPAD x 2 B
-    static constexpr int kStages = DPAD <= 64 ? 4 : (DPAD <= 96 ? 3 : 2);
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kTileBytes;
-    static constexpr int kOffV = kOffK + kStages * kTileBytes;
-    static constexpr int kOffExtra = kOffV + kStages * kTileBytes;  // bias scratch
+struct Tile {
+    static constexpr int kAtoms = DPAD / 16;
+    static constexpr int kBytes = kAtoms * kBlockM * 32;  // 128 rows x DPAD x 2 B
     static_assert(DPAD % 16 == 0 && DPAD >= 16 && DPAD <= 128, "head dim block");
 };
-
-// Bias scratch in shared memory (after the tiles).
-//   Swin: table for the heads present [(2M-1)^2 * H] (log2 units unless
-//         debugging), then per-column info for the key tile [128].
-//   SAM : per-row relative terms [128][s_h + s_w + 1] fp32 (natural units),
-//         then (kh, kw) of every key [Nk].
-__host__ __device__ constexpr int swin_extra_bytes(int table_len) {
-    return (table_len + kBlockN) * 4;
-}
-__host__ __device__ constexpr int sam_extra_bytes(int s_h, int s_w, int n_keys) {
-    return (kBlockM * (s_h + s_w + 1) + n_keys) * 4;
-}
 
 __device__ __forceinline__ int swin_strip(int pos, int G, int M, int s) {
     return pos < G - M ? 0 : (pos < G - s ? 1 : 2);
 }
 
-__device__ __forceinline__ float to_float(const void* base, size_t idx, int is_bf16) {
-    if (is_bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
-    return __half2float(reinterpret_cast<const __half*>(base)[idx]);
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
-template <int DPAD, int BIAS, bool DBG>
+// Byte offset of element (row, k) in a K-major 32B-swizzled block of `rows`
+// rows: 16-column blocks of rows x 32 bytes; inside a 32-byte row the two
+// 16-byte halves swap on rows 4-7 of every 8 (the TMA/MMA 32B swizzle).
+__device__ __forceinline__ uint32_t kmajor_offset(int rows, int row, int k) {
+    return (uint32_t)((k >> 4) * rows * 32 + row * 32 + ((((k >> 3) & 1) ^ ((row >> 2) & 1)) << 4) +
+                      (k & 7) * 2);
+}
+
+__device__ __forceinline__ uint16_t to_half_bits(float v, bool bf16) {
+    return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
+}
+
+// Barrel shift of a 128-entry register row: afterwards v[u] = v_in[u + sh]
+// for every u with u + sh < 128 (0 <= sh < 128).  Unrolled selects keep the
+// row in registers.
+__device__ __forceinline__ void shift_down(float (&v)[128], int sh) {
+#pragma unroll
+    for (int b = 0; b < 7; ++b) {
+        const int step = 1 << b;
+        const bool on = (sh >> b) & 1;
+#pragma unroll
+        for (int u = 0; u + step < 128; ++u) v[u] = on ? v[u + step] : v[u];
+    }
+}
+
+// Load N (multiple of 16, <= 128) consecutive TMEM columns of this lane.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[N]) {
+    static_assert(N % 16 == 0 && N <= 128, "columns");
+    if constexpr (N == 128) {
+        tmem_ld128(taddr, v);
+    } else {
+        if constexpr (N >= 64) {
+            uint32_t t[64];
+            tmem_ld64(taddr, t);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) v[i] = t[i];
+        }
+        if constexpr (N % 64 >= 32) {
+            uint32_t t[32];
+            tmem_ld32(taddr + (N / 64) * 64, t);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[(N / 64) * 64 + i] = t[i];
+        }
+        if constexpr (N % 32 == 16) {
+            uint32_t t[16];
+            tmem_ld16(taddr + (N / 32) * 32, t);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[(N / 32) * 32 + i] = t[i];
+        }
+    }
+}
+
+// Max of N floats with independent partial maxima (short dependency chains).
+template <int N>
+__device__ __forceinline__ float row_max(const float* x) {
+    static_assert(N % 16 == 0, "row_max");
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = fmaxf(x[2 * i], x[2 * i + 1]);
+#pragma unroll
+    for (int c = 16; c < N; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m[i] = max3f(m[i], x[c + 2 * i], x[c + 2 * i + 1]);
+    return fmaxf(fmaxf(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5])), fmaxf(m[6], m[7]));
+}
+
+// p = 2^(x*sc + off) for N columns (x = -inf gives 0), packed to 16-bit pairs;
+// returns the fp32 sum of the p values.
+template <int N>
+__device__ __forceinline__ float exp_pack(const float* x, float sc, float off, bool bf16, uint32_t* pk) {
+    const float2 sc2 = make_float2(sc, sc), off2 = make_float2(off, off);
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    if (bf16) {
+#pragma unroll
+        for (int c = 0; c < N; c += 2) {
+            const float2 a = __ffma2_rn(make_float2(x[c], x[c + 1]), sc2, off2);
+            const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+            acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(p0, p1));
+            pk[c / 2] = pack_bf16(p0, p1);
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < N; c += 2) {
+            const float2 a = __ffma2_rn(make_float2(x[c], x[c + 1]), sc2, off2);
+            const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+            acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(p0, p1));
+            pk[c / 2] = pack_f16(p0, p1);
+        }
+    }
+    const float2 s = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+    return s.x + s.y;
+}
+
+// S = Q.K^T for one 128-row tile (both operands K-major, 32B swizzle).
+template <int DPAD>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr,
+                                         uint32_t idesc) {
+#pragma unroll
+    for (int ks = 0; ks < Tile<DPAD>::kAtoms; ++ks) {
+        const uint64_t da = make_sdesc(q_addr + ks * kBlockM * 32, 16, 256, kSwizzle32B);
+        const uint64_t db = make_sdesc(k_addr + ks * kBlockN * 32, 16, 256, kSwizzle32B);
+        mma_ss(d_tmem, da, db, idesc, ks > 0 ? 1u : 0u);
+    }
+}
+
+// D[:, 0:SL] (+)= Qone . E^T with Qone [128][SL] and E [SL][SL] K-major.
+__device__ __forceinline__ void issue_bias(uint32_t d_tmem, uint32_t qone, uint32_t blk, int sl,
+                                          uint32_t idesc, uint32_t acc0) {
+    for (int ks = 0; ks < sl / 16; ++ks) {
+        const uint64_t da = make_sdesc(qone + ks * kBlockM * 32, 16, 256, kSwizzle32B);
+        const uint64_t db = make_sdesc(blk + ks * sl * 32, 16, 256, kSwizzle32B);
+        mma_ss(d_tmem, da, db, idesc, (ks > 0 || acc0) ? 1u : 0u);
+    }
+}
+
+// O (+)= P.V: P from TMEM (two 16-bit values per column), V MN-major.
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_addr,
+                                         uint32_t idesc, int kv_steps, bool accumulate) {
+    for (int ks = 0; ks < kv_steps; ++ks) {
+        const uint64_t db = make_sdesc(v_addr + ks * 512, kBlockN * 32, 256, kSwizzle32B);
+        mma_ts(o_tmem, p_tmem + ks * 8, db, idesc, (accumulate || ks > 0) ? 1u : 0u);
+    }
+}
+
+template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-    using Cfg = KernelCfg<DPAD>;
-    constexpr int NST = Cfg::kStages;
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rh,
+                    const __grid_constant__ CUtensorMap tm_rw, const AttnParams p) {
+    using T = Tile<DPAD>;
+    static_assert(MODE == kModeShared || (SL == 32 || SL == 64 || SL == 128), "slot size");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char* sQ = smem + Cfg::kOffQ;
-    unsigned char* sK = smem + Cfg::kOffK;
-    unsigned char* sV = smem + Cfg::kOffV;
-    float* sExtra = reinterpret_cast<float*>(smem + Cfg::kOffExtra);
+    unsigned char* sQ = smem + p.off_q;        // shared mode: [slot][buffer] Q tiles
+    unsigned char* sRing = smem + p.off_ring;  // ring stages
+    unsigned char* sExtraB = smem + p.off_extra;
+    float* sExtra = reinterpret_cast<float*>(sExtraB);
 
-    __shared__ uint64_t bar_q, bar_o, bar_o_final, bar_mma_final;
-    __shared__ uint64_t bar_k[NST], bar_v[NST], bar_empty[NST];
-    __shared__ uint64_t bar_s[2], bar_p[2];
+    __shared__ uint64_t bar_q_full[2][2], bar_q_empty[2][2];
+    __shared__ uint64_t bar_full_k[kMaxStages], bar_full_v[kMaxStages], bar_empty[kMaxStages];
+    __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2], bar_g[2], bar_gdone[2], bar_oempty[2];
+    __shared__ uint64_t bar_final;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
 
@@ -144,365 +293,634 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     volatile int* abort_flag = &abort_sh;
+    const int nst = p.nst;
+    const bool bf = p.is_bf16 != 0;
 
-    // ------------------------------------------------------------ tile --
-    const int tile = blockIdx.x;
-    int slice0, q_row0, rows_valid;
-    if (p.packed) {
-        slice0 = tile * p.g;
-        q_row0 = 0;
-        const int ns = min(p.g, p.BH - slice0);
-        rows_valid = ns * p.Nq;
-    } else {
-        slice0 = tile / p.n_q_tiles;
-        q_row0 = (tile % p.n_q_tiles) * kBlockM;
-        rows_valid = min(kBlockM, p.Nq - q_row0);
-    }
-    const int n_kv = p.n_kv_tiles;
-
-    // ------------------------------------------------------------ setup --
     if (tid == 0) {
         abort_sh = 0;
-        mbar_init(&bar_q, 1);
-        mbar_init(&bar_o, 1);
-        mbar_init(&bar_o_final, 1);
-        mbar_init(&bar_mma_final, 1);
-        for (int i = 0; i < NST; ++i) {
-            mbar_init(&bar_k[i], 1);
-            mbar_init(&bar_v[i], 1);
+        for (int x = 0; x < 2; ++x) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&bar_q_full[x][b], 1);
+                mbar_init(&bar_q_empty[x][b], 1);
+            }
+            mbar_init(&bar_s[x], 1);
+            mbar_init(&bar_p[x], kBlockM);
+            mbar_init(&bar_o[x], 1);
+            mbar_init(&bar_g[x], 1);
+            mbar_init(&bar_gdone[x], kBlockM);
+            mbar_init(&bar_oempty[x], kBlockM);
+        }
+        for (int i = 0; i < kMaxStages; ++i) {
+            mbar_init(&bar_full_k[i], 1);
+            mbar_init(&bar_full_v[i], 1);
             mbar_init(&bar_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar_s[i], 1);
-            mbar_init(&bar_p[i], kBlockM);
-        }
+        mbar_init(&bar_final, 1);
         fence_mbar_init();
+    }
+    if (warp == kProducerWarp && lane == 0) {
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
+        if constexpr (BIAS == kBiasSam) {
+            prefetch_tensormap(&tm_rh);
+            prefetch_tensormap(&tm_rw);
+        }
     }
-    if (p.packed) {
-        // Boxes shorter than 128 rows leave the tail rows of each block
-        // untouched; zero them once so the MMAs read finite values there.
-        const int total = Cfg::kOffExtra / 16;
-        uint4 z = make_uint4(0, 0, 0, 0);
-        for (int i = tid; i < total; i += kThreads) reinterpret_cast<uint4*>(smem)[i] = z;
-        fence_proxy_async_smem();
+    if constexpr (MODE == kModeSeparate) {
+        // Slot rows past the slice length are never written by the TMA; they
+        // must read as zero in the MMAs.
+        const int total = (int)((p.off_extra - p.off_ring) / 16);
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < total; i += kThreads) reinterpret_cast<uint4*>(sRing)[i] = z;
     }
-    if (warp == 1) {
+    if constexpr (BIAS == kBiasSwin) {
+        // Qone [128][SL]: row r has a single 1 at column r mod SL.
+        // Blocks [SL][SL] (row = key token j, column = query token t):
+        //   h < H        : table[idx(t, j), h] / scale      (natural units when debugging)
+        //   H + kind - 1 : -100 / scale where t and j fall in different regions
+        //                  of a window on the last column (kind 1), last row
+        //                  (kind 2) or both (kind 3)
+        const int M = p.win, N = p.Nk;
+        const float f = DBG ? 1.0f : 1.0f / p.scale;
+        uint16_t* qone = reinterpret_cast<uint16_t*>(sExtraB);
+        const uint16_t one = to_half_bits(1.0f, bf);
+        for (int i = tid; i < kBlockM * SL; i += kThreads) {
+            const int r = i / SL, t = i % SL;
+            qone[kmajor_offset(kBlockM, r, t) / 2] = (t == r % SL) ? one : (uint16_t)0;
+        }
+        const int nblk = p.H + 3;
+        uint16_t* blocks = reinterpret_cast<uint16_t*>(sExtraB + kBlockM * SL * 2);
+        const int yb = (p.n_wh - 1) * M, xb = (p.n_ww - 1) * M;  // last window row / column origin
+        for (int i = tid; i < nblk * SL * SL; i += kThreads) {
+            const int b = i / (SL * SL), j = (i / SL) % SL, t = i % SL;
+            float v = 0.f;
+            if (j < N && t < N) {
+                const int rt = t / M, ct = t % M, rj = j / M, cj = j % M;
+                if (b < p.H) {
+                    const int idx = (rt - rj + M - 1) * (2 * M - 1) + (ct - cj + M - 1);
+                    v = p.table[idx * p.H + b] * f;
+                } else if (p.shift) {
+                    const int kind = b - p.H + 1;
+                    bool same = true;
+                    if (kind & 1) same = same && swin_strip(xb + ct, p.grid_w, M, p.shift) == swin_strip(xb + cj, p.grid_w, M, p.shift);
+                    if (kind & 2) same = same && swin_strip(yb + rt, p.grid_h, M, p.shift) == swin_strip(yb + rj, p.grid_h, M, p.shift);
+                    v = same ? 0.f : -100.0f * f;
+                }
+            }
+            blocks[(b * SL * SL * 2 + kmajor_offset(SL, j, t)) / 2] = to_half_bits(v, bf);
+        }
+    }
+    if constexpr (MODE == kModeSeparate) fence_proxy_async_smem();
+    if constexpr (BIAS == kBiasSam && SW == 0) {
+        // key table for generic grids: (s_h-1-kh) | (s_w-1-kw) << 16
+        int* kt = reinterpret_cast<int*>(sExtra + 2 * (p.s_h + p.s_w) * kBlockM);
+        for (int k = tid; k < p.Nk; k += kThreads) {
+            const int kh = k / p.s_w, kw = k % p.s_w;
+            kt[k] = (p.s_h - 1 - kh) | ((p.s_w - 1 - kw) << 16);
+        }
+    }
+    if (warp == kMmaWarp) {
         tmem_alloc(&tmem_base_sh, kTmemCols);
         tmem_relinquish();
-    }
-    // Bias tables into shared memory.
-    if constexpr (BIAS == kBiasSwin) {
-        const int tl = (2 * p.win - 1) * (2 * p.win - 1);
-        const float f = DBG ? 1.0f : kLog2e;
-        // stored head-major: [h][idx]
-        for (int i = tid; i < tl * p.H; i += kThreads) {
-            const int idx = i / p.H, h = i % p.H;
-            sExtra[h * tl + idx] = p.table[i] * f;
-        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
+    const int job0 = blockIdx.x, job_step = gridDim.x;
 
-    const int q_atom_bytes = p.box_rows_q * 32;
-    const int kv_atom_bytes = p.box_rows_kv * 32;
-
-    if (warp == 0) {
-        // ====================================================== producer ==
+    if (warp >= 8) {
+      regs_dec<kControlRegs>();
+      if (warp == kProducerWarp) {
+        // =========================================================== producer
         if (lane == 0) {
-            int z_q = slice0;
-            mbar_arrive_expect_tx(&bar_q, Cfg::kAtoms * q_atom_bytes);
-            for (int a = 0; a < Cfg::kAtoms; ++a) {
-                if (p.packed)
-                    tma_load_2d(sQ + a * kBlockM * 32, &tm_q, &bar_q, a * 16, slice0 * p.Nq);
-                else
-                    tma_load_3d(sQ + a * kBlockM * 32, &tm_q, &bar_q, a * 16, q_row0, z_q);
-            }
-            int issued = 0;
-            for (int j = 0; j < n_kv; ++j) {
-                const int st = j % NST;
-                if (j >= NST) {
-                    if (!mbar_wait(&bar_empty[st], ((j / NST) + 1) & 1, abort_flag, kStatusWaitEmpty)) break;
-                }
-                unsigned char* dk = sK + st * Cfg::kTileBytes;
-                unsigned char* dv = sV + st * Cfg::kTileBytes;
-                mbar_arrive_expect_tx(&bar_k[st], Cfg::kAtoms * kv_atom_bytes);
-                for (int a = 0; a < Cfg::kAtoms; ++a) {
-                    if (p.packed)
-                        tma_load_2d(dk + a * kBlockN * 32, &tm_k, &bar_k[st], a * 16, slice0 * p.Nk);
-                    else
-                        tma_load_3d(dk + a * kBlockN * 32, &tm_k, &bar_k[st], a * 16, j * kBlockN, slice0);
-                }
-                mbar_arrive_expect_tx(&bar_v[st], Cfg::kAtoms * kv_atom_bytes);
-                for (int a = 0; a < Cfg::kAtoms; ++a) {
-                    if (p.packed)
-                        tma_load_2d(dv + a * kBlockN * 32, &tm_v, &bar_v[st], a * 16, slice0 * p.Nk);
-                    else
-                        tma_load_3d(dv + a * kBlockN * 32, &tm_v, &bar_v[st], a * 16, j * kBlockN, slice0);
-                }
-                issued = j + 1;
-            }
-            if (*abort_flag) {
-                // Let copies still in flight land before the CTA retires.
-                mbar_wait(&bar_q, 0, nullptr, 0);
-                for (int j = max(0, issued - NST); j < issued; ++j) {
-                    const int st = j % NST;
-                    mbar_wait(&bar_k[st], (j / NST) & 1, nullptr, 0);
-                    mbar_wait(&bar_v[st], (j / NST) & 1, nullptr, 0);
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ========================================================= MMA ==
-        if (lane == 0) {
-            const bool bf = p.is_bf16 != 0;
-            const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, p.kv_cols, false);
-            const uint32_t idesc_o = make_idesc_f16(bf, kBlockM, DPAD, true);
-            const int kv_steps = p.kv_cols / 16;
-            bool ok = mbar_wait(&bar_q, 0, abort_flag, kStatusWaitQ);
-            auto issue_s = [&](int j) -> bool {
-                const int st = j % NST;
-                if (!mbar_wait(&bar_k[st], (j / NST) & 1, abort_flag, kStatusWaitK)) return false;
-                tc_fence_after();
-                const uint32_t qa = smem_u32(sQ);
-                const uint32_t ka = smem_u32(sK + st * Cfg::kTileBytes);
-                const uint32_t d_tmem = tmem + (j & 1) * kBlockN;
-#pragma unroll
-                for (int ks = 0; ks < Cfg::kAtoms; ++ks) {
-                    const uint64_t da = make_sdesc(qa + ks * kBlockM * 32, 16, 256, kSwizzle32B);
-                    const uint64_t db = make_sdesc(ka + ks * kBlockN * 32, 16, 256, kSwizzle32B);
-                    mma_ss(d_tmem, da, db, idesc_s, ks > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar_s[j & 1]);
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv) {
-                    if (!issue_s(j + 1)) break;
-                }
-                if (!mbar_wait(&bar_p[j & 1], (j >> 1) & 1, abort_flag, kStatusWaitP)) break;
-                const int st = j % NST;
-                if (!mbar_wait(&bar_v[st], (j / NST) & 1, abort_flag, kStatusWaitV)) break;
-                tc_fence_after();
-                const uint32_t va = smem_u32(sV + st * Cfg::kTileBytes);
-                const uint32_t p_tmem = tmem + (j & 1) * kBlockN;
-                for (int ks = 0; ks < kv_steps; ++ks) {
-                    // V: MN-major, 32-byte swizzle; 16 keys = 512 bytes per step,
-                    // column blocks of 16 dims are kBlockN*32 bytes apart.
-                    const uint64_t db = make_sdesc(va + ks * 512, kBlockN * 32, 256, kSwizzle32B);
-                    mma_ts(tmem + kTmemO, p_tmem + ks * 8, db, idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
-                }
-                mma_commit(&bar_empty[st]);
-                mma_commit(&bar_o);
-                if (j == n_kv - 1) mma_commit(&bar_o_final);
-            }
-            // Every MMA this thread issued has retired before TMEM is freed.
-            mma_commit(&bar_mma_final);
-            mbar_wait(&bar_mma_final, 0, nullptr, 0);
-        }
-    } else if (warp >= kSoftmaxWarp0) {
-        // ===================================================== softmax ==
-        const int r = tid - kSoftmaxWarp0 * 32;              // row in tile == TMEM lane
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const bool row_ok = r < rows_valid;
-        int my_slice, my_tok, my_sl;
-        if (p.packed) {
-            my_sl = r / p.Nq;
-            my_slice = slice0 + my_sl;
-            my_tok = r - my_sl * p.Nq;
-        } else {
-            my_sl = 0;
-            my_slice = slice0;
-            my_tok = q_row0 + r;
-        }
-        // ---- bias row setup
-        const float* swin_tab = nullptr;
-        int swin_row_base = 0, swin_lab = 0;
-        int* col_info = nullptr;
-        float mask_val = DBG ? -100.0f : -100.0f * kLog2e;
-        if constexpr (BIAS == kBiasSwin) {
-            const int M = p.win, tl = (2 * M - 1) * (2 * M - 1);
-            col_info = reinterpret_cast<int*>(sExtra + tl * p.H);
-            const int h = my_slice % p.H;
-            swin_tab = sExtra + h * tl;
-            const int ri = my_tok / M, ci = my_tok % M;
-            swin_row_base = (ri + M - 1) * (2 * M - 1) + (ci + M - 1);
-            const int w = (my_slice / p.H) % p.n_w;
-            const int y = (w / p.n_ww) * M + ri, x = (w % p.n_ww) * M + ci;
-            swin_lab = p.shift ? swin_strip(y, p.grid_h, M, p.shift) * 3 + swin_strip(x, p.grid_w, M, p.shift) : 0;
-            // column info of the (single) key tile: key offset, region, slice
-            {
-                const int c = r;
-                const int sl = c / p.Nk;
-                const int slice = slice0 + sl;
-                const int t = c - sl * p.Nk;
-                const int rj = t / M, cj = t % M;
-                const int wk = (slice / p.H) % p.n_w;
-                const int yk = (wk / p.n_ww) * M + rj, xk = (wk % p.n_ww) * M + cj;
-                const int lab = p.shift ? swin_strip(yk, p.grid_h, M, p.shift) * 3 + swin_strip(xk, p.grid_w, M, p.shift) : 0;
-                const int valid = (sl < p.g) ? 1 : 0;
-                col_info[c] = (rj * (2 * M - 1) + cj) | (lab << 16) | ((valid ? sl : 255) << 20);
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-        }
-        float* sam_rel = nullptr;
-        int* sam_col = nullptr;
-        int sam_qh = 0, sam_qw = 0;
-        if constexpr (BIAS == kBiasSam) {
-            const int sh = p.s_h, sw = p.s_w, rs = sh + sw + 1;
-            sam_rel = sExtra + r * rs;
-            sam_col = reinterpret_cast<int*>(sExtra + kBlockM * rs);
-            // (kh, kw) of every key, shared by all rows
-            for (int key = r; key < p.Nk; key += kBlockM) sam_col[key] = (key / sw) | ((key % sw) << 16);
-            sam_qh = my_tok / sw;
-            sam_qw = my_tok % sw;
-            if (row_ok) {
-                // rel_h[kh] = Q_i . R_h[qh-kh+sh-1], rel_w[kw] = Q_i . R_w[qw-kw+sw-1]
-                const size_t qoff = ((size_t)my_slice * p.Nq + my_tok) * p.d;
-                float qv[DPAD];
-#pragma unroll
-                for (int c = 0; c < DPAD; ++c) qv[c] = c < p.d ? to_float(p.q, qoff + c, p.is_bf16) : 0.f;
-                for (int kh = 0; kh < sh; ++kh) {
-                    const size_t ro = (size_t)(sam_qh - kh + sh - 1) * p.d;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int c = 0; c < DPAD; ++c) acc += c < p.d ? qv[c] * to_float(p.rel_h, ro + c, p.is_bf16) : 0.f;
-                    sam_rel[kh] = acc;
-                }
-                for (int kw = 0; kw < sw; ++kw) {
-                    const size_t ro = (size_t)(sam_qw - kw + sw - 1) * p.d;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int c = 0; c < DPAD; ++c) acc += c < p.d ? qv[c] * to_float(p.rel_w, ro + c, p.is_bf16) : 0.f;
-                    sam_rel[sh + kw] = acc;
-                }
-            } else {
-                for (int t = 0; t < sh + sw; ++t) sam_rel[t] = 0.f;
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-        }
-
-        float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            __syncwarp();
-            if (!mbar_wait(&bar_s[j & 1], (j >> 1) & 1, abort_flag, kStatusWaitS)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t s_tmem = tmem + lane_base + (j & 1) * kBlockN;
-            float x[kBlockN];
-#pragma unroll
-            for (int c0 = 0; c0 < kBlockN; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(s_tmem + c0, v);
-#pragma unroll
-                for (int t = 0; t < 32; ++t) x[c0 + t] = __uint_as_float(v[t]);
-            }
-            const int key0 = j * kBlockN;
-            float m_tile = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kBlockN; ++c) {
-                bool valid;
-                float b = 0.f;
-                if (p.packed) {
-                    valid = c < p.kv_cols;
+            const uint32_t q_tx = (uint32_t)T::kAtoms * (uint32_t)p.box_q * 32u;
+            const uint32_t kv_tx = (uint32_t)T::kAtoms * (uint32_t)p.box_kv * 32u;
+            int ring = 0;  // stage uses issued
+            bool ok = true;
+            int ju = 0;
+            for (int job = job0; ok && job < p.n_jobs; job += job_step, ++ju) {
+                if constexpr (MODE == kModeShared) {
+                    const int slice = job / p.q_jobs;
+                    const int q0 = (job % p.q_jobs) * 2 * kBlockM;
+                    const int qb = ju % p.nq;
+                    for (int x = 0; x < 2; ++x) {
+                        if (ju >= p.nq &&
+                            !mbar_wait(&bar_q_empty[x][qb], ((ju / p.nq) + 1) & 1, abort_flag, kStatusWaitEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        unsigned char* dq = sQ + (x * p.nq + qb) * T::kBytes;
+                        mbar_arrive_expect_tx(&bar_q_full[x][qb], q_tx);
+                        for (int a = 0; a < T::kAtoms; ++a)
+                            tma_load_3d(dq + a * kBlockM * 32, &tm_q, &bar_q_full[x][qb], a * 16, q0 + x * kBlockM, slice);
+                    }
+                    const int n_uses = p.n_kv + (BIAS == kBiasSam ? 1 : 0);
+                    for (int u = 0; ok && u < n_uses; ++u) {
+                        const int st = ring % nst;
+                        if (ring >= nst &&
+                            !mbar_wait(&bar_empty[st], ((ring / nst) + 1) & 1, abort_flag, kStatusWaitEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        ++ring;
+                        unsigned char* dk = sRing + st * p.ring_stage_bytes;
+                        unsigned char* dv = dk + T::kBytes;
+                        if (BIAS == kBiasSam && u == 0) {
+                            // rel-pos tables: R_w in the K slot, R_h in the V slot
+                            const uint32_t r_tx = (uint32_t)T::kAtoms * kBlockN * 32u;
+                            mbar_arrive_expect_tx(&bar_full_k[st], r_tx);
+                            for (int a = 0; a < T::kAtoms; ++a)
+                                tma_load_2d(dk + a * kBlockN * 32, &tm_rw, &bar_full_k[st], a * 16, 0);
+                            mbar_arrive_expect_tx(&bar_full_v[st], r_tx);
+                            for (int a = 0; a < T::kAtoms; ++a)
+                                tma_load_2d(dv + a * kBlockN * 32, &tm_rh, &bar_full_v[st], a * 16, 0);
+                        } else {
+                            const int j = u - (BIAS == kBiasSam ? 1 : 0);
+                            mbar_arrive_expect_tx(&bar_full_k[st], kv_tx);
+                            for (int a = 0; a < T::kAtoms; ++a)
+                                tma_load_3d(dk + a * kBlockN * 32, &tm_k, &bar_full_k[st], a * 16, j * p.kv_w, slice);
+                            mbar_arrive_expect_tx(&bar_full_v[st], kv_tx);
+                            for (int a = 0; a < T::kAtoms; ++a)
+                                tma_load_3d(dv + a * kBlockN * 32, &tm_v, &bar_full_v[st], a * 16, j * p.kv_w, slice);
+                        }
+                    }
                 } else {
-                    valid = key0 + c < p.Nk;
-                }
-                if constexpr (BIAS == kBiasSwin) {
-                    const int info = col_info[c];
-                    valid = valid && ((info >> 20) == my_sl);
-                    const int idx = swin_row_base - (info & 0xFFFF);
-                    b = valid ? swin_tab[idx] + ((((info >> 16) & 15) == swin_lab) ? 0.f : mask_val) : 0.f;
-                } else if constexpr (BIAS == kBiasSam) {
-                    const int ci = sam_col[min(key0 + c, p.Nk - 1)];
-                    b = valid ? (sam_rel[ci & 0xFFFF] + sam_rel[p.s_h + (ci >> 16)]) : 0.f;
-                } else {
-                    if (p.packed) valid = valid && (c / p.Nk == my_sl);
-                }
-                if constexpr (DBG) {
-                    if (valid && row_ok) {
-                        const int key = p.packed ? (c - my_sl * p.Nk) : (key0 + c);
-                        p.dbg[((size_t)my_slice * p.Nq + my_tok) * p.Nk + key] = b;
+                    for (int x = 0; x < 2; ++x) {
+                        const int st = ring % nst;
+                        if (ring >= nst &&
+                            !mbar_wait(&bar_empty[st], ((ring / nst) + 1) & 1, abort_flag, kStatusWaitEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        ++ring;
+                        const int tile = 2 * job + x;
+                        unsigned char* dq = sRing + st * p.ring_stage_bytes;
+                        unsigned char* dk = dq + T::kBytes;
+                        unsigned char* dv = dk + T::kBytes;
+                        mbar_arrive_expect_tx(&bar_full_k[st], (uint32_t)p.g * (q_tx + 2 * kv_tx));
+                        for (int sl = 0; sl < p.g; ++sl) {
+                            const int slice = tile * p.g + sl;
+                            for (int a = 0; a < T::kAtoms; ++a) {
+                                const int so = a * kBlockM * 32 + sl * SL * 32;
+                                tma_load_2d(dq + so, &tm_q, &bar_full_k[st], a * 16, slice * p.Nq);
+                                tma_load_2d(dk + so, &tm_k, &bar_full_k[st], a * 16, slice * p.Nk);
+                                tma_load_2d(dv + so, &tm_v, &bar_full_k[st], a * 16, slice * p.Nk);
+                            }
+                        }
                     }
                 }
-                float xv;
-                if constexpr (BIAS == kBiasSam) {
-                    xv = fmaf(x[c], p.scale_log2, b * kLog2e);
-                } else if constexpr (BIAS == kBiasSwin && DBG) {
-                    xv = fmaf(x[c], p.scale_log2, b * kLog2e);
-                } else {
-                    xv = fmaf(x[c], p.scale_log2, b);
-                }
-                x[c] = valid ? xv : -INFINITY;
-                m_tile = fmaxf(m_tile, x[c]);
             }
-            const float m_new = fmaxf(m_run, m_tile);
-            const bool need = m_new > m_run + kRescaleThreshold;
-            const bool warp_need = __any_sync(0xffffffffu, need && j > 0);
-            if (warp_need) {
-                // O must hold P_{j-1}.V_{j-1} before it is rescaled.
-                if (!mbar_wait(&bar_o, (j - 1) & 1, abort_flag, kStatusWaitO)) { ok = false; break; }
-                tc_fence_after();
-                const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
-#pragma unroll
-                for (int c0 = 0; c0 < DPAD; c0 += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tmem + lane_base + kTmemO + c0, v);
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
-                    tmem_st16(tmem + lane_base + kTmemO + c0, v);
+            if (*abort_flag) {
+                // let copies still in flight land before the CTA retires
+                for (int u = (ring > nst ? ring - nst : 0); u < ring; ++u) {
+                    const int st = u % nst;
+                    mbar_wait(&bar_full_k[st], (u / nst) & 1, nullptr, 0);
+                    if (MODE == kModeShared) mbar_wait(&bar_full_v[st], (u / nst) & 1, nullptr, 0);
                 }
             }
-            if (need) {
-                l_run *= ex2_approx(m_run - m_new);
-                m_run = m_new;
-            }
-            const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-            float lsum = 0.f;
-            uint32_t pk[kBlockN / 2];
-#pragma unroll
-            for (int c = 0; c < kBlockN; c += 2) {
-                const float p0 = ex2_approx(x[c] - m_use);
-                const float p1 = ex2_approx(x[c + 1] - m_use);
-                lsum += p0 + p1;
-                pk[c / 2] = p.is_bf16 ? pack_bf16(p0, p1) : pack_f16(p0, p1);
-            }
-            l_run += lsum;
-#pragma unroll
-            for (int c0 = 0; c0 < kBlockN / 2; c0 += 16) {
-                uint32_t v[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) v[t] = pk[c0 + t];
-                tmem_st16(s_tmem + c0, v);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&bar_p[j & 1]);
         }
-        // ---------------------------------------------------- epilogue --
-        if (ok && mbar_wait(&bar_o_final, 0, abort_flag, kStatusWaitO)) {
+      } else if (warp == kMmaWarp) {
+        // ================================================================ MMA
+        if (lane == 0) {
+            const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, p.kv_cols, false);
+            const uint32_t idesc_o = make_idesc_f16(bf, kBlockM, DPAD, true);
+            const uint32_t idesc_b = make_idesc_f16(bf, kBlockM, MODE == kModeSeparate ? SL : 16, false);
+            const int kv_steps = p.kv_cols / 16;
+            uint32_t tS[2], tO[2];
+            tS[0] = tmem;
+            tS[1] = tmem + 128;
+            tO[0] = tmem + 256;
+            tO[1] = tmem + 384;
+            int ring = 0;  // stage uses consumed
+            int cnt_p[2] = {0, 0};
+            int ju = 0;
+            bool ok = true;
+            const uint32_t qone = smem_u32(sExtraB);
+            const uint32_t blocks = qone + kBlockM * SL * 2;
+            // S of packed tile `tile` (separate mode) into S_x, with the Swin bias
+            auto issue_sep_scores = [&](int x, int tile, uint32_t qa) {
+                if (!DBG || BIAS != kBiasSwin) issue_qk<DPAD>(tS[x], qa, qa + T::kBytes, idesc_s);
+                if constexpr (BIAS == kBiasSwin) {
+                    for (int sl = 0; sl < p.g; ++sl) {
+                        const int slice = tile * p.g + sl;
+                        if (slice >= p.BH) break;
+                        const int h = slice % p.H;
+                        const int w = (slice / p.H) % p.n_w;
+                        const int kind = p.shift ? ((((w % p.n_ww) == p.n_ww - 1) ? 1 : 0) |
+                                                    (((w / p.n_ww) == p.n_wh - 1) ? 2 : 0))
+                                                 : 0;
+                        const uint32_t d = tS[x] + sl * SL;
+                        issue_bias(d, qone, blocks + h * SL * SL * 2, SL, idesc_b, DBG ? 0u : 1u);
+                        if (kind) issue_bias(d, qone, blocks + (p.H + kind - 1) * SL * SL * 2, SL, idesc_b, 1u);
+                    }
+                }
+            };
+            for (int job = job0; ok && job < p.n_jobs; job += job_step, ++ju) {
+                if constexpr (MODE == kModeShared) {
+                    const int qb = ju % p.nq;
+                    uint32_t qa[2];
+                    qa[0] = smem_u32(sQ + (0 * p.nq + qb) * T::kBytes);
+                    qa[1] = smem_u32(sQ + (1 * p.nq + qb) * T::kBytes);
+                    for (int x = 0; x < 2 && ok; ++x)
+                        ok = mbar_wait(&bar_q_full[x][qb], (ju / p.nq) & 1, abort_flag, kStatusWaitQ);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if constexpr (BIAS == kBiasSam) {
+                        const int st = ring % nst;
+                        if (!mbar_wait(&bar_full_k[st], (ring / nst) & 1, abort_flag, kStatusWaitK) ||
+                            !mbar_wait(&bar_full_v[st], (ring / nst) & 1, abort_flag, kStatusWaitV)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t rw = smem_u32(sRing + st * p.ring_stage_bytes);
+                        const uint32_t rh = rw + T::kBytes;
+                        const uint32_t id_w = make_idesc_f16(bf, kBlockM, p.n_rw, false);
+                        const uint32_t id_h = make_idesc_f16(bf, kBlockM, p.n_rh, false);
+                        for (int x = 0; x < 2; ++x) {
+                            // G_h rewrites O_x: the previous job's epilogue must be done with it
+                            if (ju > 0 && !mbar_wait(&bar_oempty[x], (ju - 1) & 1, abort_flag, kStatusWaitO)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_qk<DPAD>(tS[x], qa[x], rw, id_w);
+                            issue_qk<DPAD>(tO[x], qa[x], rh, id_h);
+                            mma_commit(&bar_g[x]);
+                        }
+                        if (!ok) break;
+                        mma_commit(&bar_empty[st]);
+                        ++ring;
+                    }
+                    const int n = p.n_kv;
+                    {
+                        const int st = ring % nst;
+                        if (!mbar_wait(&bar_full_k[st], (ring / nst) & 1, abort_flag, kStatusWaitK)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t ka = smem_u32(sRing + st * p.ring_stage_bytes);
+                        for (int x = 0; x < 2; ++x) {
+                            if (BIAS == kBiasSam) {
+                                // S_x rewrites the G_w values the slot is still gathering
+                                if (!mbar_wait(&bar_gdone[x], ju & 1, abort_flag, kStatusWaitG)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                            }
+                            issue_qk<DPAD>(tS[x], qa[x], ka, idesc_s);
+                            mma_commit(&bar_s[x]);
+                        }
+                        if (!ok) break;
+                    }
+                    for (int j = 0; j < n && ok; ++j) {
+                        const int use = ring + j;
+                        const int st = use % nst;
+                        const uint32_t va = smem_u32(sRing + st * p.ring_stage_bytes + T::kBytes);
+                        const int st1 = (use + 1) % nst;
+                        const uint32_t ka1 = smem_u32(sRing + st1 * p.ring_stage_bytes);
+                        for (int x = 0; x < 2; ++x) {
+                            if (!mbar_wait(&bar_p[x], cnt_p[x] & 1, abort_flag, kStatusWaitP)) { ok = false; break; }
+                            ++cnt_p[x];
+                            if (x == 0 && !mbar_wait(&bar_full_v[st], (use / nst) & 1, abort_flag, kStatusWaitV)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_pv(tO[x], tS[x], va, idesc_o, kv_steps, j > 0);
+                            if (j == n - 1) mma_commit(&bar_o[x]);
+                            if (x == 1) {
+                                mma_commit(&bar_empty[st]);
+                                if (j == n - 1) {
+                                    mma_commit(&bar_q_empty[0][qb]);
+                                    mma_commit(&bar_q_empty[1][qb]);
+                                }
+                            }
+                            if (j + 1 < n) {
+                                if (x == 0 && !mbar_wait(&bar_full_k[st1], ((use + 1) / nst) & 1, abort_flag, kStatusWaitK)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                issue_qk<DPAD>(tS[x], qa[x], ka1, idesc_s);
+                                mma_commit(&bar_s[x]);
+                            }
+                        }
+                    }
+                    ring += n;
+                } else {
+                    // separate mode: ring uses `ring` (tile 2*job, slot A) and `ring+1` (slot B)
+                    if (ju == 0) {
+                        for (int x = 0; x < 2 && ok; ++x) {
+                            const int st = (ring + x) % nst;
+                            if (!mbar_wait(&bar_full_k[st], ((ring + x) / nst) & 1, abort_flag, kStatusWaitK)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_sep_scores(x, 2 * job + x, smem_u32(sRing + st * p.ring_stage_bytes));
+                            mma_commit(&bar_s[x]);
+                        }
+                    }
+                    const int next = job + job_step;
+                    for (int x = 0; x < 2 && ok; ++x) {
+                        const int st = (ring + x) % nst;
+                        const uint32_t qa = smem_u32(sRing + st * p.ring_stage_bytes);
+                        if (!mbar_wait(&bar_p[x], cnt_p[x] & 1, abort_flag, kStatusWaitP)) { ok = false; break; }
+                        ++cnt_p[x];
+                        tc_fence_after();
+                        issue_pv(tO[x], tS[x], qa + 2 * T::kBytes, idesc_o, kv_steps, false);
+                        mma_commit(&bar_empty[st]);
+                        mma_commit(&bar_o[x]);
+                        if (next < p.n_jobs) {
+                            const int use2 = ring + 2 + x;
+                            const int st2 = use2 % nst;
+                            if (!mbar_wait(&bar_full_k[st2], (use2 / nst) & 1, abort_flag, kStatusWaitK)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_sep_scores(x, 2 * next + x, smem_u32(sRing + st2 * p.ring_stage_bytes));
+                            mma_commit(&bar_s[x]);
+                        }
+                    }
+                    ring += 2;
+                }
+            }
+            // every MMA issued has retired before tensor memory is released
+            mma_commit(&bar_final);
+            mbar_wait(&bar_final, 0, nullptr, 0);
+        }
+      }
+    } else {
+        regs_inc<kSoftmaxRegs>();
+        // ============================================================ softmax
+        const int x = warp >> 2;                // slot A or B
+        const int r = tid & 127;                // row in tile == TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + (uint32_t)(x * 128);
+        const uint32_t tO = tmem + lane_base + 256u + (uint32_t)(x * 128);
+        int cnt_s = 0, ju = 0;
+        bool ok = true;
+        const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
+        float* sam_rh = nullptr;
+        float* sam_rw = nullptr;
+        const int* sam_kt = nullptr;
+        if constexpr (BIAS == kBiasSam) {
+            sam_rh = sExtra + x * (p.s_h * kBlockM);
+            sam_rw = sExtra + 2 * p.s_h * kBlockM + x * (p.s_w * kBlockM);
+            sam_kt = reinterpret_cast<const int*>(sExtra + 2 * (p.s_h + p.s_w) * kBlockM);
+        }
+
+        for (int job = job0; ok && job < p.n_jobs; job += job_step, ++ju) {
+            // ------------------------------------------------- row of this job
+            int my_slice, my_tok, my_sl = 0;
+            bool row_ok;
+            if constexpr (MODE == kModeShared) {
+                my_slice = job / p.q_jobs;
+                my_tok = (job % p.q_jobs) * 2 * kBlockM + x * kBlockM + r;
+                row_ok = my_tok < p.Nq;
+            } else {
+                const int tile = 2 * job + x;
+                my_sl = r / SL;
+                my_slice = tile * p.g + my_sl;
+                my_tok = r - my_sl * SL;
+                row_ok = (my_tok < p.Nq) && (my_sl < p.g) && (my_slice < p.BH);
+            }
+            float l_run = 0.f;
+
+            if constexpr (MODE == kModeSeparate) {
+                // ---------------------------- one key tile: own slot's SL columns
+                __syncwarp();
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[x], cnt_s & 1, abort_flag, kStatusWaitS))) { ok = false; break; }
+                ++cnt_s;
+                tc_fence_after();
+                float xs[SL];
+                {
+                    uint32_t v[SL];
+                    tmem_ld_cols<SL>(tS + my_sl * SL, v);
+#pragma unroll
+                    for (int t = 0; t < SL; ++t) xs[t] = __uint_as_float(v[t]);
+                }
+                const int nk = p.Nk;
+                if constexpr (DBG) {
+                    // the scores hold only the bias when debugging (no Q.K^T)
+                    if (row_ok) {
+                        float* dst = p.dbg + ((size_t)my_slice * p.Nq + my_tok) * p.Nk;
+#pragma unroll
+                        for (int c = 0; c < SL; ++c)
+                            if (c < nk) dst[c] = (BIAS == kBiasSwin) ? xs[c] : 0.f;
+                    }
+                }
+                // keys past the slice length: -inf (16-column chunks, uniform branches)
+#pragma unroll
+                for (int c0 = 0; c0 < SL; c0 += 16) {
+                    if (c0 + 16 > nk) {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t)
+                            if (c0 + t >= nk) xs[c0 + t] = -INFINITY;
+                    }
+                }
+                const float m = row_max<SL>(xs) * p.scale_log2;
+                const float m_use = (m == -INFINITY) ? 0.f : m;
+                uint32_t pk[64];
+#pragma unroll
+                for (int t = 0; t < 64; ++t) pk[t] = 0u;  // other slots' keys: probability 0
+                uint32_t own[SL / 2];
+                l_run = exp_pack<SL>(xs, p.scale_log2, -m_use, bf, own);
+#pragma unroll
+                for (int s = 0; s < 128 / SL; ++s)
+                    if (s == my_sl)
+#pragma unroll
+                        for (int t = 0; t < SL / 2; ++t) pk[s * (SL / 2) + t] = own[t];
+                tmem_st64(tS, pk);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bar_p[x]);
+            } else {
+                // ------------------------------------------------- bias row setup
+                float sam_rw_reg[SW > 0 ? SW : 1];
+                if constexpr (BIAS == kBiasSam) {
+                    const int qh = my_tok / p.s_w, qw = my_tok % p.s_w;
+                    __syncwarp();
+                    if (!__all_sync(0xffffffffu, mbar_wait(&bar_g[x], ju & 1, abort_flag, kStatusWaitG))) { ok = false; break; }
+                    tc_fence_after();
+                    const float f = DBG ? 1.0f : kLog2e;
+                    float gv[128];
+                    // G_w row: rel_w for key column kw is G_w[qw + s_w - 1 - kw]
+                    {
+                        uint32_t v[128];
+                        tmem_ld128(tS, v);
+#pragma unroll
+                        for (int t = 0; t < 128; ++t) gv[t] = __uint_as_float(v[t]) * f;
+                    }
+                    shift_down(gv, qw);
+                    if constexpr (SW > 0) {
+#pragma unroll
+                        for (int kw = 0; kw < SW; ++kw) sam_rw_reg[kw] = gv[SW - 1 - kw];
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < kSamMaxSide; ++u)
+                            if (u < p.s_w) sam_rw[u * kBlockM + r] = gv[u];
+                    }
+                    // G_h row: rel_h for key row kh is G_h[qh + s_h - 1 - kh]
+                    {
+                        uint32_t v[128];
+                        tmem_ld128(tO, v);
+#pragma unroll
+                        for (int t = 0; t < 128; ++t) gv[t] = __uint_as_float(v[t]) * f;
+                    }
+                    shift_down(gv, qh);
+#pragma unroll
+                    for (int u = 0; u < kSamMaxSide; ++u)
+                        if (u < p.s_h) sam_rh[u * kBlockM + r] = gv[u];
+                    tc_fence_before();
+                    mbar_arrive(&bar_gdone[x]);
+                }
+
+                // ------------------------------------------------------ key tiles
+                float m_run = -INFINITY;
+                for (int j = 0; j < p.n_kv; ++j) {
+                    __syncwarp();
+                    if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[x], cnt_s & 1, abort_flag, kStatusWaitS))) { ok = false; break; }
+                    ++cnt_s;
+                    tc_fence_after();
+                    float xs[128];
+                    {
+                        uint32_t v[128];
+                        tmem_ld128(tS, v);
+#pragma unroll
+                        for (int t = 0; t < 128; ++t) xs[t] = __uint_as_float(v[t]);
+                    }
+                    const int key0 = j * p.kv_w;
+                    const int hi = min(p.kv_w, p.Nk - key0);  // valid key columns [0, hi)
+                    float m_tile;  // log2 units
+                    float sc;      // multiplier applied to xs in the exponent
+                    if (BIAS == kBiasNone && !DBG) {
+                        // no bias: max on raw scores, p = 2^(s*scale*log2e - m)
+                        if (hi < 128) {
+#pragma unroll
+                            for (int c0 = 0; c0 < 128; c0 += 16)
+                                if (c0 + 16 > hi)
+#pragma unroll
+                                    for (int t = 0; t < 16; ++t)
+                                        if (c0 + t >= hi) xs[c0 + t] = -INFINITY;
+                        }
+                        m_tile = row_max<128>(xs) * p.scale_log2;
+                        sc = p.scale_log2;
+                    } else {
+                        constexpr int kRows = (BIAS == kBiasSam && SW > 0) ? (128 + (SW > 0 ? SW : 1) - 1) / (SW > 0 ? SW : 1) : 1;
+                        float rh_tile[kRows];
+                        if constexpr (BIAS == kBiasSam && SW > 0) {
+                            // key rows of this tile; the tile starts at a multiple of SW
+                            const int kh0 = key0 / SW;
+#pragma unroll
+                            for (int rr = 0; rr < kRows; ++rr) {
+                                const int kh = min(kh0 + rr, p.s_h - 1);
+                                rh_tile[rr] = sam_rh[(p.s_h - 1 - kh) * kBlockM + r];
+                            }
+                        }
+#pragma unroll
+                        for (int c = 0; c < 128; c += 2) {
+                            float b0 = 0.f, b1 = 0.f;
+                            if constexpr (BIAS == kBiasSam) {
+                                if constexpr (SW > 0) {
+                                    b0 = rh_tile[c / SW] + sam_rw_reg[c % SW];
+                                    b1 = rh_tile[(c + 1) / SW] + sam_rw_reg[(c + 1) % SW];
+                                } else {
+                                    const int k0 = sam_kt[min(key0 + c, p.Nk - 1)];
+                                    const int k1 = sam_kt[min(key0 + c + 1, p.Nk - 1)];
+                                    b0 = sam_rh[(k0 & 0xFFFF) * kBlockM + r] + sam_rw[(k0 >> 16) * kBlockM + r];
+                                    b1 = sam_rh[(k1 & 0xFFFF) * kBlockM + r] + sam_rw[(k1 >> 16) * kBlockM + r];
+                                }
+                            }
+                            if constexpr (DBG) {
+                                if (row_ok) {
+                                    float* dst = p.dbg + ((size_t)my_slice * p.Nq + my_tok) * p.Nk + key0;
+                                    if (c < hi) dst[c] = b0;
+                                    if (c + 1 < hi) dst[c + 1] = b1;
+                                }
+                            }
+                            float2 bv = make_float2(b0, b1);
+                            if constexpr (DBG) bv = __fmul2_rn(bv, make_float2(kLog2e, kLog2e));
+                            const float2 y = __ffma2_rn(make_float2(xs[c], xs[c + 1]), scale2, bv);
+                            xs[c] = y.x;
+                            xs[c + 1] = y.y;
+                        }
+                        if (hi < 128) {
+#pragma unroll
+                            for (int c0 = 0; c0 < 128; c0 += 16)
+                                if (c0 + 16 > hi)
+#pragma unroll
+                                    for (int t = 0; t < 16; ++t)
+                                        if (c0 + t >= hi) xs[c0 + t] = -INFINITY;
+                        }
+                        m_tile = row_max<128>(xs);
+                        sc = 1.0f;
+                    }
+                    const float m_new = fmaxf(m_run, m_tile);
+                    const bool need = m_new > m_run + kRescaleThreshold;
+                    if (__any_sync(0xffffffffu, need && j > 0)) {
+                        // O holds the earlier tiles' P.V, complete: this score tile
+                        // was committed after it
+                        const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+                        uint32_t v[DPAD];
+                        tmem_ld_cols<DPAD>(tO, v);
+#pragma unroll
+                        for (int t = 0; t < DPAD; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
+#pragma unroll
+                        for (int c0 = 0; c0 < DPAD; c0 += 16) {
+                            uint32_t w16[16];
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) w16[t] = v[c0 + t];
+                            tmem_st16(tO + c0, w16);
+                        }
+                    }
+                    if (need) {
+                        l_run *= ex2_approx(m_run - m_new);
+                        m_run = m_new;
+                    }
+                    const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                    uint32_t pk[64];
+                    l_run += exp_pack<128>(xs, sc, -m_use, bf, pk);
+                    tmem_st64(tS, pk);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(&bar_p[x]);
+                }
+                if (!ok) break;
+            }
+
+            // -------------------------------------------------------- epilogue
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_o[x], ju & 1, abort_flag, kStatusWaitO))) { ok = false; break; }
             tc_fence_after();
             const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
             uint32_t o[DPAD / 2];
+            {
+                uint32_t v[DPAD];
+                tmem_ld_cols<DPAD>(tO, v);
+                if (bf) {
 #pragma unroll
-            for (int c0 = 0; c0 < DPAD; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem + lane_base + kTmemO + c0, v);
+                    for (int t = 0; t < DPAD; t += 2)
+                        o[t / 2] = pack_bf16(__uint_as_float(v[t]) * inv_l, __uint_as_float(v[t + 1]) * inv_l);
+                } else {
 #pragma unroll
-                for (int t = 0; t < 16; t += 2) {
-                    const float a = __uint_as_float(v[t]) * inv_l;
-                    const float b = __uint_as_float(v[t + 1]) * inv_l;
-                    o[(c0 + t) / 2] = p.is_bf16 ? pack_bf16(a, b) : pack_f16(a, b);
+                    for (int t = 0; t < DPAD; t += 2)
+                        o[t / 2] = pack_f16(__uint_as_float(v[t]) * inv_l, __uint_as_float(v[t + 1]) * inv_l);
                 }
+            }
+            if constexpr (BIAS == kBiasSam) {
+                tc_fence_before();
+                mbar_arrive(&bar_oempty[x]);
             }
             if (row_ok && !DBG) {
                 uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(p.out) +
-                                                      (((size_t)my_slice * p.Nq + my_tok) * p.d) * 2);
+                                                      ((size_t)my_slice * p.Nq + my_tok) * (size_t)p.d * 2);
 #pragma unroll
                 for (int c = 0; c < DPAD / 8; ++c)
                     if (c * 8 < p.d) dst[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
@@ -510,10 +928,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // ------------------------------------------------------------ teardown --
+    // ============================================================== teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);

@@ -1,44 +1,83 @@
-// attn_launch.cuh -- per-head-dim launcher of the attention kernel.  Each
-// attn_d<DPAD>.cu translation unit instantiates one head-dim block so the
-// build compiles them in parallel.
+// attn_launch.cuh -- launchers of the attention kernel instantiations.  Each
+// attn_d<DPAD>_<bias>.cu translation unit instantiates one (head-dim block,
+// bias kind) pair so the build compiles them in parallel.
 #pragma once
 #include <cuda_runtime.h>
 #include "attn_fwd_kernel.cuh"
 
 namespace sdpa09 {
 
-// Launches attn_fwd_kernel<DPAD, bias, dbg>.  Returns the cudaError_t of
-// the attribute call or the launch.
-template <int DPAD>
-cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const AttnParams& p, int bias, bool dbg, int grid, size_t smem,
-                        cudaStream_t stream);
+struct LaunchArgs {
+    const CUtensorMap* tq;
+    const CUtensorMap* tk;
+    const CUtensorMap* tv;
+    const CUtensorMap* trh;
+    const CUtensorMap* trw;
+    const AttnParams* p;
+    int mode;   // kModeShared / kModeSeparate
+    int sw;     // SAM grid-width specialisation (0 = generic)
+    int sl;     // slot rows in separate mode (32, 64, 128)
+    bool dbg;
+    int grid;
+    size_t smem;
+    cudaStream_t stream;
+};
 
-#define SDPA09_DEFINE_LAUNCH(DPAD)                                                              \
-    template <int BIAS, bool DBG>                                                               \
-    static cudaError_t launch_attn_##DPAD##_impl(const CUtensorMap& tq, const CUtensorMap& tk,  \
-                                                 const CUtensorMap& tv, const AttnParams& p,    \
-                                                 int grid, size_t smem, cudaStream_t stream) {  \
-        auto kern = attn_fwd_kernel<DPAD, BIAS, DBG>;                                           \
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                             (int)smem);                                        \
-        if (e != cudaSuccess) return e;                                                         \
-        kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);                                  \
-        return cudaGetLastError();                                                              \
-    }                                                                                           \
-    template <>                                                                                 \
-    cudaError_t launch_attn<DPAD>(const CUtensorMap& tq, const CUtensorMap& tk,                 \
-                                  const CUtensorMap& tv, const AttnParams& p, int bias,         \
-                                  bool dbg, int grid, size_t smem, cudaStream_t stream) {       \
-        switch (bias * 2 + (dbg ? 1 : 0)) {                                                     \
-            case 0: return launch_attn_##DPAD##_impl<kBiasNone, false>(tq, tk, tv, p, grid, smem, stream); \
-            case 1: return launch_attn_##DPAD##_impl<kBiasNone, true>(tq, tk, tv, p, grid, smem, stream);  \
-            case 2: return launch_attn_##DPAD##_impl<kBiasSwin, false>(tq, tk, tv, p, grid, smem, stream); \
-            case 3: return launch_attn_##DPAD##_impl<kBiasSwin, true>(tq, tk, tv, p, grid, smem, stream);  \
-            case 4: return launch_attn_##DPAD##_impl<kBiasSam, false>(tq, tk, tv, p, grid, smem, stream);  \
-            case 5: return launch_attn_##DPAD##_impl<kBiasSam, true>(tq, tk, tv, p, grid, smem, stream);   \
-            default: return cudaErrorInvalidValue;                                              \
-        }                                                                                       \
+template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG>
+cudaError_t launch_one(const LaunchArgs& a) {
+    auto kern = attn_fwd_kernel<DPAD, BIAS, MODE, SW, SL, DBG>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a.smem);
+    if (e != cudaSuccess) return e;
+    kern<<<a.grid, kThreads, a.smem, a.stream>>>(*a.tq, *a.tk, *a.tv, *a.trh, *a.trw, *a.p);
+    return cudaGetLastError();
+}
+
+template <int DPAD, int BIAS, int MODE, int SW, int SL>
+cudaError_t launch_dbg(const LaunchArgs& a) {
+    return a.dbg ? launch_one<DPAD, BIAS, MODE, SW, SL, true>(a)
+                 : launch_one<DPAD, BIAS, MODE, SW, SL, false>(a);
+}
+
+// Defined in the per-(DPAD, bias) translation units.
+template <int DPAD, int BIAS>
+cudaError_t launch_attn(const LaunchArgs& a);
+
+// The packed (separate) tiling keeps three tiles per ring stage; it is built
+// for head dims up to 64 only.
+template <int DPAD>
+cudaError_t launch_attn_none(const LaunchArgs& a) {
+    if (a.mode == kModeShared) return launch_dbg<DPAD, kBiasNone, kModeShared, 0, 0>(a);
+    if constexpr (DPAD <= 64) {
+        if (a.sl == 32) return launch_dbg<DPAD, kBiasNone, kModeSeparate, 0, 32>(a);
+        if (a.sl == 64) return launch_dbg<DPAD, kBiasNone, kModeSeparate, 0, 64>(a);
     }
+    return cudaErrorInvalidValue;
+}
+
+template <int DPAD>
+cudaError_t launch_attn_swin(const LaunchArgs& a) {
+    if constexpr (DPAD <= 64) {
+        if (a.mode == kModeSeparate) {
+            if (a.sl == 32) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 32>(a);
+            if (a.sl == 64) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 64>(a);
+            if (a.sl == 128) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 128>(a);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int DPAD>
+cudaError_t launch_attn_sam(const LaunchArgs& a) {
+    if (a.mode != kModeShared) return cudaErrorInvalidValue;
+    switch (a.sw) {
+        case 64: return launch_dbg<DPAD, kBiasSam, kModeShared, 64, 0>(a);
+        case 14: return launch_dbg<DPAD, kBiasSam, kModeShared, 14, 0>(a);
+        default: return launch_dbg<DPAD, kBiasSam, kModeShared, 0, 0>(a);
+    }
+}
+
+#define SDPA09_INSTANTIATE(DPAD, BIAS, FN) \
+    template <>                            \
+    cudaError_t launch_attn<DPAD, BIAS>(const LaunchArgs& a) { return FN<DPAD>(a); }
 
 }  // namespace sdpa09

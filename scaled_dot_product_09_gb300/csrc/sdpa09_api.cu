@@ -106,28 +106,41 @@ int dpad_for(int d) {
     return r;
 }
 
-size_t tiles_bytes(int dpad) {
-    const int stages = dpad <= 64 ? 4 : (dpad <= 96 ? 3 : 2);
-    return (size_t)(dpad / 16) * kBlockM * 32 * (1 + 2 * stages);
-}
-
-cudaError_t dispatch(int dpad, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     const AttnParams& p, int bias, bool dbg, int grid, size_t smem,
-                     cudaStream_t st) {
-    switch (dpad) {
-        case 32: return launch_attn<32>(tq, tk, tv, p, bias, dbg, grid, smem, st);
-        case 48: return launch_attn<48>(tq, tk, tv, p, bias, dbg, grid, smem, st);
-        case 64: return launch_attn<64>(tq, tk, tv, p, bias, dbg, grid, smem, st);
-        case 80: return launch_attn<80>(tq, tk, tv, p, bias, dbg, grid, smem, st);
-        case 96: return launch_attn<96>(tq, tk, tv, p, bias, dbg, grid, smem, st);
-        case 128: return launch_attn<128>(tq, tk, tv, p, bias, dbg, grid, smem, st);
+template <int DPAD>
+cudaError_t dispatch_bias(int bias, const LaunchArgs& a) {
+    switch (bias) {
+        case kBiasNone: return launch_attn<DPAD, kBiasNone>(a);
+        case kBiasSwin: return launch_attn<DPAD, kBiasSwin>(a);
+        case kBiasSam: return launch_attn<DPAD, kBiasSam>(a);
         default: return cudaErrorInvalidValue;
     }
 }
 
-constexpr size_t kMaxSmem = 227 * 1024;
-constexpr int kMaxSwinTable = 4096;  // floats of (2M-1)^2 * H kept in shared memory
-constexpr int kMaxSamKeys = 4096;
+cudaError_t dispatch(int dpad, int bias, const LaunchArgs& a) {
+    switch (dpad) {
+        case 32: return dispatch_bias<32>(bias, a);
+        case 48: return dispatch_bias<48>(bias, a);
+        case 64: return dispatch_bias<64>(bias, a);
+        case 80: return dispatch_bias<80>(bias, a);
+        case 96: return dispatch_bias<96>(bias, a);
+        case 128: return dispatch_bias<128>(bias, a);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    static int cache[64] = {0};
+    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+// Dynamic shared memory left for the kernel's buffers after the 1 KB
+// alignment pad and its static barriers.
+constexpr size_t kSmemBudget = 227 * 1024 - 1024 - 1024;
 
 int run(const void* q, const void* k, const void* v, void* out, float* dbg, int B, int H, int Nq,
         int Nk, int d, float scale, attn_dtype dtype, attn_bias_kind bias_kind,
@@ -159,12 +172,15 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
     p.Nq = Nq;
     p.Nk = Nk;
     p.d = d;
+    p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.is_bf16 = dtype == ATTN_BF16;
-    p.q = q;
     const int dpad = dpad_for(d);
+    const size_t tile_bytes = (size_t)(dpad / 16) * kBlockM * 32;
     size_t extra = 0;
-    int bias = kBiasNone;
+    int bias = kBiasNone, sw_spec = 0;
+    const void* rel_h = nullptr;
+    const void* rel_w = nullptr;
 
     if (bias_kind == ATTN_BIAS_SWIN) {
         const attn_swin_args* a = static_cast<const attn_swin_args*>(bias_args);
@@ -177,8 +193,7 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         if (a->shift < 0 || a->shift >= M) return fail(ATTN_ERR_ARG, "shift must lie in [0, win)");
         const int nW = (a->grid_h / M) * (a->grid_w / M);
         if (B % nW) return fail(ATTN_ERR_ARG, "B (windows) must be a multiple of the windows per image");
-        const int tl = (2 * M - 1) * (2 * M - 1);
-        if (tl * H > kMaxSwinTable) return fail(ATTN_ERR_UNSUPPORTED, "Swin table larger than %d floats", kMaxSwinTable);
+        if (dpad > 64) return fail(ATTN_ERR_UNSUPPORTED, "SWIN with d > 64 is not supported");
         p.table = a->table;
         p.win = M;
         p.grid_h = a->grid_h;
@@ -186,7 +201,7 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         p.shift = a->shift;
         p.n_w = nW;
         p.n_ww = a->grid_w / M;
-        extra = swin_extra_bytes(tl * H);
+        p.n_wh = a->grid_h / M;
         bias = kBiasSwin;
     } else if (bias_kind == ATTN_BIAS_SAM_RELPOS) {
         const attn_sam_args* a = static_cast<const attn_sam_args*>(bias_args);
@@ -195,65 +210,121 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         if (a->q_h != a->k_h || a->q_w != a->k_w)
             return fail(ATTN_ERR_UNSUPPORTED, "SAM with different query and key grids");
         if (a->q_h * a->q_w != Nq || Nk != Nq) return fail(ATTN_ERR_ARG, "SAM needs Nq == Nk == q_h*q_w");
-        if (a->q_h + a->q_w > kBlockM || Nk > kMaxSamKeys)
-            return fail(ATTN_ERR_UNSUPPORTED, "SAM grid too large (q_h+q_w <= 128, N <= 4096)");
-        p.rel_h = a->rel_h;
-        p.rel_w = a->rel_w;
+        if (a->q_h > kSamMaxSide || a->q_w > kSamMaxSide)
+            return fail(ATTN_ERR_UNSUPPORTED, "SAM grid sides above %d", kSamMaxSide);
+        if (!aligned16(a->rel_h) || !aligned16(a->rel_w)) return fail(ATTN_ERR_ARG, "rel_h/rel_w must be 16-byte aligned");
+        rel_h = a->rel_h;
+        rel_w = a->rel_w;
         p.s_h = a->q_h;
         p.s_w = a->q_w;
-        extra = sam_extra_bytes(a->q_h, a->q_w, Nk);
+        p.n_rh = (2 * a->q_h - 1 + 15) / 16 * 16;
+        p.n_rw = (2 * a->q_w - 1 + 15) / 16 * 16;
+        sw_spec = (a->q_w == 64 || a->q_w == 14) ? a->q_w : 0;
+        extra = (size_t)sam_extra_floats(sw_spec == 0, a->q_h, a->q_w, Nk) * 4;
         bias = kBiasSam;
     } else if (bias_kind != ATTN_BIAS_NONE) {
         return fail(ATTN_ERR_ARG, "unknown bias kind %d", (int)bias_kind);
     }
 
-    // Tiling.
-    int g = std::min(kBlockM / Nq, kBlockN / Nk);
-    const bool packed = bias == kBiasSwin || (bias == kBiasNone && g >= 2);
-    if (bias == kBiasSwin) g = std::max(g, 1);
-    int grid;
-    if (packed) {
-        p.packed = 1;
-        p.g = g;
-        p.n_q_tiles = 1;
-        p.n_kv_tiles = 1;
-        p.kv_cols = (g * Nk + 15) / 16 * 16;
-        p.box_rows_q = g * Nq;
-        p.box_rows_kv = g * Nk;
-        grid = (int)((BH + g - 1) / g);
-    } else {
-        p.packed = 0;
-        p.g = 1;
-        p.n_q_tiles = (Nq + kBlockM - 1) / kBlockM;
-        p.n_kv_tiles = (Nk + kBlockN - 1) / kBlockN;
+    // ---- job layout
+    const int nmax = std::max(Nq, Nk);
+    const int sl = nmax <= 32 ? 32 : (nmax <= 64 ? 64 : 128);
+    const bool separate = bias == kBiasSwin || (bias == kBiasNone && sl <= 64 && dpad <= 64);
+    int mode;
+    if (separate) {
+        mode = kModeSeparate;
+        p.g = kBlockM / sl;
+        const int64_t n_tiles = (BH + p.g - 1) / p.g;
+        p.n_jobs = (int)((n_tiles + 1) / 2);
+        p.n_kv = 1;
+        p.kv_w = kBlockN;
         p.kv_cols = kBlockN;
-        p.box_rows_q = kBlockM;
-        p.box_rows_kv = kBlockN;
-        const int64_t nt = BH * p.n_q_tiles;
-        if (nt > 0x7fffffff) return fail(ATTN_ERR_UNSUPPORTED, "too many tiles");
-        grid = (int)nt;
+        p.box_q = Nq;
+        p.box_kv = Nk;
+        p.nq = 0;
+        if (bias == kBiasSwin) extra = swin_extra_bytes(sl, H);
+        p.ring_stage_bytes = (uint32_t)(3 * tile_bytes);
+        const size_t avail = kSmemBudget > extra ? kSmemBudget - extra : 0;
+        p.nst = (int)std::min<size_t>(kMaxStages, avail / p.ring_stage_bytes);
+        if (p.nst < 2) return fail(ATTN_ERR_UNSUPPORTED, "shared memory too small for the packed tiling (H=%d)", H);
+        p.off_q = 0;
+        p.off_ring = 0;
+        p.off_extra = (uint32_t)(p.nst * p.ring_stage_bytes);
+    } else {
+        mode = kModeShared;
+        p.g = 1;
+        p.kv_w = (bias == kBiasSam && sw_spec) ? (kBlockN / sw_spec) * sw_spec : kBlockN;
+        p.kv_cols = (p.kv_w + 15) / 16 * 16;
+        p.n_kv = (Nk + p.kv_w - 1) / p.kv_w;
+        p.q_jobs = (Nq + 2 * kBlockM - 1) / (2 * kBlockM);
+        const int64_t nj = BH * p.q_jobs;
+        if (nj > 0x7fffffff) return fail(ATTN_ERR_UNSUPPORTED, "too many jobs");
+        p.n_jobs = (int)nj;
+        p.box_q = kBlockM;
+        p.box_kv = p.kv_cols;
+        p.ring_stage_bytes = (uint32_t)(2 * tile_bytes);
+        // prefer >= 3 K/V stages, then double-buffered Q
+        int nq = 0, nst = 0;
+        const int tries[4][2] = {{2, 3}, {1, 3}, {2, 2}, {1, 2}};
+        for (auto& t : tries) {
+            const size_t fixed = 2 * (size_t)t[0] * tile_bytes + extra;
+            if (fixed >= kSmemBudget) continue;
+            const int s = (int)std::min<size_t>(kMaxStages, (kSmemBudget - fixed) / p.ring_stage_bytes);
+            if (s >= t[1]) {
+                nq = t[0];
+                nst = s;
+                break;
+            }
+        }
+        if (!nst) return fail(ATTN_ERR_UNSUPPORTED, "shared memory too small for d=%d with this bias", d);
+        p.nq = nq;
+        p.nst = nst;
+        p.off_q = 0;
+        p.off_ring = (uint32_t)(2 * nq * tile_bytes);
+        p.off_extra = (uint32_t)(p.off_ring + nst * p.ring_stage_bytes);
     }
-    const size_t smem = tiles_bytes(dpad) + extra + 1024;
-    if (smem > kMaxSmem)
-        return fail(ATTN_ERR_UNSUPPORTED, "shared memory %zu B exceeds the per-CTA limit", smem);
+    const size_t smem = p.off_extra + extra + 1024;
+    const int nsm = sm_count();
+    if (nsm <= 0) return fail(ATTN_ERR_CUDA, "no CUDA device");
+    const int grid = std::min(p.n_jobs, nsm);
 
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, trh, trw;
     const bool bf = p.is_bf16 != 0;
     int rc;
-    if (packed) {
-        if ((rc = encode_map(&tq, q, bf, d, BH * Nq, 0, p.box_rows_q))) return rc;
-        if ((rc = encode_map(&tk, k, bf, d, BH * Nk, 0, p.box_rows_kv))) return rc;
-        if ((rc = encode_map(&tv, v, bf, d, BH * Nk, 0, p.box_rows_kv))) return rc;
+    if (separate) {
+        if ((rc = encode_map(&tq, q, bf, d, BH * Nq, 0, p.box_q))) return rc;
+        if ((rc = encode_map(&tk, k, bf, d, BH * Nk, 0, p.box_kv))) return rc;
+        if ((rc = encode_map(&tv, v, bf, d, BH * Nk, 0, p.box_kv))) return rc;
     } else {
-        if ((rc = encode_map(&tq, q, bf, d, Nq, BH, kBlockM))) return rc;
-        if ((rc = encode_map(&tk, k, bf, d, Nk, BH, kBlockN))) return rc;
-        if ((rc = encode_map(&tv, v, bf, d, Nk, BH, kBlockN))) return rc;
+        if ((rc = encode_map(&tq, q, bf, d, Nq, BH, p.box_q))) return rc;
+        if ((rc = encode_map(&tk, k, bf, d, Nk, BH, p.box_kv))) return rc;
+        if ((rc = encode_map(&tv, v, bf, d, Nk, BH, p.box_kv))) return rc;
+    }
+    if (bias == kBiasSam) {
+        if ((rc = encode_map(&trh, rel_h, bf, d, 2 * p.s_h - 1, 0, kBlockN))) return rc;
+        if ((rc = encode_map(&trw, rel_w, bf, d, 2 * p.s_w - 1, 0, kBlockN))) return rc;
+    } else {
+        trh = tq;
+        trw = tq;
     }
     p.status = status_ptr();
     if (!p.status) return fail(ATTN_ERR_CUDA, "no CUDA device / status word unavailable");
 
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = dispatch(dpad, tq, tk, tv, p, bias, dbg != nullptr, grid, smem, st);
+    LaunchArgs la;
+    la.tq = &tq;
+    la.tk = &tk;
+    la.tv = &tv;
+    la.trh = &trh;
+    la.trw = &trw;
+    la.p = &p;
+    la.mode = mode;
+    la.sw = sw_spec;
+    la.sl = sl;
+    la.dbg = dbg != nullptr;
+    la.grid = grid;
+    la.smem = smem;
+    la.stream = static_cast<cudaStream_t>(stream);
+    cudaError_t e = dispatch(dpad, bias, la);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     static const bool debug_env = getenv("SDPA09_DEBUG") && getenv("SDPA09_DEBUG")[0] == '1';
     if (debug_env) return attn_device_status(stream);
