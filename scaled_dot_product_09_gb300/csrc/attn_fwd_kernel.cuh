@@ -100,6 +100,8 @@ struct AttnParams {
     int nst;          // ring stages
     int nq;           // Q buffers per slot (shared mode): 1 or 2
     int box_q, box_kv;
+    int full_atoms;   // 16-column blocks fully inside d
+    int part;         // 1 when d is not a multiple of 16 (one partial block)
     uint32_t off_q, off_ring, off_extra;  // shared-memory offsets (bytes)
     uint32_t ring_stage_bytes;
     float scale;
@@ -124,6 +126,15 @@ __host__ __device__ constexpr uint32_t swin_extra_bytes(int sl, int H) {
 __host__ __device__ constexpr uint32_t sam_extra_floats(bool generic, int s_h, int s_w, int nk) {
     return 2u * (uint32_t)s_h * kBlockM + (generic ? 2u * (uint32_t)s_w * kBlockM + (uint32_t)nk : 0u);
 }
+
+// TMA descriptors.  Data maps view a [slices][rows][d] tensor as
+// (16 elements, row, slice, column block) so that one copy brings every full
+// 16-column block of a tile, landing as [block][row][16] (the 32B-swizzled
+// K-major layout); the *p maps cover a last partial block when d is not a
+// multiple of 16.  Rel-pos maps view [rows][d] as (16, row, block).
+struct TmaMaps {
+    CUtensorMap q, k, v, qp, kp, vp, rh, rw, rhp, rwp;
+};
 
 template <int DPAD>
 struct Tile {
@@ -236,6 +247,13 @@ __device__ __forceinline__ float exp_pack(const float* x, float sc, float off, b
     return s.x + s.y;
 }
 
+// One arrival per warp once every lane is done (the barriers that the
+// softmax warps signal count four arrivals, one per warp of the slot).
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // S = Q.K^T for one 128-row tile (both operands K-major, 32B swizzle).
 template <int DPAD>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr,
@@ -269,9 +287,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
 
 template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rh,
-                    const __grid_constant__ CUtensorMap tm_rw, const AttnParams p) {
+    attn_fwd_kernel(const __grid_constant__ TmaMaps tm, const AttnParams p) {
     using T = Tile<DPAD>;
     static_assert(MODE == kModeShared || (SL == 32 || SL == 64 || SL == 128), "slot size");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -304,11 +320,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_init(&bar_q_empty[x][b], 1);
             }
             mbar_init(&bar_s[x], 1);
-            mbar_init(&bar_p[x], kBlockM);
+            mbar_init(&bar_p[x], 4);
             mbar_init(&bar_o[x], 1);
             mbar_init(&bar_g[x], 1);
-            mbar_init(&bar_gdone[x], kBlockM);
-            mbar_init(&bar_oempty[x], kBlockM);
+            mbar_init(&bar_gdone[x], 4);
+            mbar_init(&bar_oempty[x], 4);
         }
         for (int i = 0; i < kMaxStages; ++i) {
             mbar_init(&bar_full_k[i], 1);
@@ -319,12 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == kProducerWarp && lane == 0) {
-        prefetch_tensormap(&tm_q);
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm.q);
+        prefetch_tensormap(&tm.k);
+        prefetch_tensormap(&tm.v);
         if constexpr (BIAS == kBiasSam) {
-            prefetch_tensormap(&tm_rh);
-            prefetch_tensormap(&tm_rw);
+            prefetch_tensormap(&tm.rh);
+            prefetch_tensormap(&tm.rw);
         }
     }
     if constexpr (MODE == kModeSeparate) {
@@ -413,8 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         unsigned char* dq = sQ + (x * p.nq + qb) * T::kBytes;
                         mbar_arrive_expect_tx(&bar_q_full[x][qb], q_tx);
-                        for (int a = 0; a < T::kAtoms; ++a)
-                            tma_load_3d(dq + a * kBlockM * 32, &tm_q, &bar_q_full[x][qb], a * 16, q0 + x * kBlockM, slice);
+                        tma_load_4d(dq, &tm.q, &bar_q_full[x][qb], 0, q0 + x * kBlockM, slice, 0);
+                        if (p.part) tma_load_3d(dq + p.full_atoms * kBlockM * 32, &tm.qp, &bar_q_full[x][qb], 0, q0 + x * kBlockM, slice);
                     }
                     const int n_uses = p.n_kv + (BIAS == kBiasSam ? 1 : 0);
                     for (int u = 0; ok && u < n_uses; ++u) {
@@ -431,19 +447,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // rel-pos tables: R_w in the K slot, R_h in the V slot
                             const uint32_t r_tx = (uint32_t)T::kAtoms * kBlockN * 32u;
                             mbar_arrive_expect_tx(&bar_full_k[st], r_tx);
-                            for (int a = 0; a < T::kAtoms; ++a)
-                                tma_load_2d(dk + a * kBlockN * 32, &tm_rw, &bar_full_k[st], a * 16, 0);
+                            tma_load_3d(dk, &tm.rw, &bar_full_k[st], 0, 0, 0);
+                            if (p.part) tma_load_2d(dk + p.full_atoms * kBlockN * 32, &tm.rwp, &bar_full_k[st], 0, 0);
                             mbar_arrive_expect_tx(&bar_full_v[st], r_tx);
-                            for (int a = 0; a < T::kAtoms; ++a)
-                                tma_load_2d(dv + a * kBlockN * 32, &tm_rh, &bar_full_v[st], a * 16, 0);
+                            tma_load_3d(dv, &tm.rh, &bar_full_v[st], 0, 0, 0);
+                            if (p.part) tma_load_2d(dv + p.full_atoms * kBlockN * 32, &tm.rhp, &bar_full_v[st], 0, 0);
                         } else {
                             const int j = u - (BIAS == kBiasSam ? 1 : 0);
                             mbar_arrive_expect_tx(&bar_full_k[st], kv_tx);
-                            for (int a = 0; a < T::kAtoms; ++a)
-                                tma_load_3d(dk + a * kBlockN * 32, &tm_k, &bar_full_k[st], a * 16, j * p.kv_w, slice);
+                            tma_load_4d(dk, &tm.k, &bar_full_k[st], 0, j * p.kv_w, slice, 0);
+                            if (p.part) tma_load_3d(dk + p.full_atoms * kBlockN * 32, &tm.kp, &bar_full_k[st], 0, j * p.kv_w, slice);
                             mbar_arrive_expect_tx(&bar_full_v[st], kv_tx);
-                            for (int a = 0; a < T::kAtoms; ++a)
-                                tma_load_3d(dv + a * kBlockN * 32, &tm_v, &bar_full_v[st], a * 16, j * p.kv_w, slice);
+                            tma_load_4d(dv, &tm.v, &bar_full_v[st], 0, j * p.kv_w, slice, 0);
+                            if (p.part) tma_load_3d(dv + p.full_atoms * kBlockN * 32, &tm.vp, &bar_full_v[st], 0, j * p.kv_w, slice);
                         }
                     }
                 } else {
@@ -459,15 +475,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         unsigned char* dq = sRing + st * p.ring_stage_bytes;
                         unsigned char* dk = dq + T::kBytes;
                         unsigned char* dv = dk + T::kBytes;
-                        mbar_arrive_expect_tx(&bar_full_k[st], (uint32_t)p.g * (q_tx + 2 * kv_tx));
-                        for (int sl = 0; sl < p.g; ++sl) {
-                            const int slice = tile * p.g + sl;
-                            for (int a = 0; a < T::kAtoms; ++a) {
-                                const int so = a * kBlockM * 32 + sl * SL * 32;
-                                tma_load_2d(dq + so, &tm_q, &bar_full_k[st], a * 16, slice * p.Nq);
-                                tma_load_2d(dk + so, &tm_k, &bar_full_k[st], a * 16, slice * p.Nk);
-                                tma_load_2d(dv + so, &tm_v, &bar_full_k[st], a * 16, slice * p.Nk);
-                            }
+                        // one copy per operand: g slices of SL rows (rows past
+                        // the slice length read as zero), all column blocks
+                        mbar_arrive_expect_tx(&bar_full_k[st], 3u * T::kBytes);
+                        const int s0 = tile * p.g;
+                        tma_load_4d(dq, &tm.q, &bar_full_k[st], 0, 0, s0, 0);
+                        tma_load_4d(dk, &tm.k, &bar_full_k[st], 0, 0, s0, 0);
+                        tma_load_4d(dv, &tm.v, &bar_full_k[st], 0, 0, s0, 0);
+                        if (p.part) {
+                            const int po = p.full_atoms * kBlockM * 32;
+                            tma_load_3d(dq + po, &tm.qp, &bar_full_k[st], 0, 0, s0);
+                            tma_load_3d(dk + po, &tm.kp, &bar_full_k[st], 0, 0, s0);
+                            tma_load_3d(dv + po, &tm.vp, &bar_full_k[st], 0, 0, s0);
                         }
                     }
                 }
@@ -740,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st64(tS, pk);
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&bar_p[x]);
+                warp_arrive(&bar_p[x]);
             } else {
                 // ------------------------------------------------- bias row setup
                 float sam_rw_reg[SW > 0 ? SW : 1];
@@ -779,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int u = 0; u < kSamMaxSide; ++u)
                         if (u < p.s_h) sam_rh[u * kBlockM + r] = gv[u];
                     tc_fence_before();
-                    mbar_arrive(&bar_gdone[x]);
+                    warp_arrive(&bar_gdone[x]);
                 }
 
                 // ------------------------------------------------------ key tiles
@@ -890,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st64(tS, pk);
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(&bar_p[x]);
+                    warp_arrive(&bar_p[x]);
                 }
                 if (!ok) break;
             }
@@ -916,7 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if constexpr (BIAS == kBiasSam) {
                 tc_fence_before();
-                mbar_arrive(&bar_oempty[x]);
+                warp_arrive(&bar_oempty[x]);
             }
             if (row_ok && !DBG) {
                 uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(p.out) +

@@ -8,11 +8,7 @@
 namespace sdpa09 {
 
 struct LaunchArgs {
-    const CUtensorMap* tq;
-    const CUtensorMap* tk;
-    const CUtensorMap* tv;
-    const CUtensorMap* trh;
-    const CUtensorMap* trw;
+    const TmaMaps* tm;
     const AttnParams* p;
     int mode;   // kModeShared / kModeSeparate
     int sw;     // SAM grid-width specialisation (0 = generic)
@@ -28,7 +24,7 @@ cudaError_t launch_one(const LaunchArgs& a) {
     auto kern = attn_fwd_kernel<DPAD, BIAS, MODE, SW, SL, DBG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a.smem);
     if (e != cudaSuccess) return e;
-    kern<<<a.grid, kThreads, a.smem, a.stream>>>(*a.tq, *a.tk, *a.tv, *a.trh, *a.trw, *a.p);
+    kern<<<a.grid, kThreads, a.smem, a.stream>>>(*a.tm, *a.p);
     return cudaGetLastError();
 }
 

@@ -73,22 +73,80 @@ int* status_ptr() {
     return ptrs[dev];
 }
 
-// Rank-2 or rank-3 tiled map over a [outer][rows][d] half tensor with a
-// box of 16 elements x box_rows rows, 32-byte swizzle.
-int encode_map(CUtensorMap* m, const void* base, bool bf16, int d, int64_t rows, int64_t outer,
-               int box_rows) {
+// Generic tiled map with 32-byte swizzle over 16-bit elements.
+int encode(CUtensorMap* m, const void* base, bool bf16, int rank, const uint64_t* dims,
+           const uint64_t* strides_bytes, const uint32_t* box) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
     const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)outer};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
-    cuuint32_t box[3] = {16, (cuuint32_t)box_rows, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    const cuuint32_t rank = outer > 0 ? 3 : 2;
-    CUresult r = enc(m, dt, rank, const_cast<void*>(base), dims, strides, box, es,
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) gs[i] = strides_bytes[i];
+    }
+    CUresult r = enc(m, dt, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return ATTN_OK;
+}
+
+// Maps of a [slices][rows][d] tensor (slices = 0: a plain [rows][d] table).
+// The full map is (16 elements, row, slice, column block) with a box of
+// (16, box_rows, box_slices, atoms - part): one copy lands every 16-column
+// block of the tile as [block][row][16]; blocks and rows past the data are
+// zero-filled.  When d is not a multiple of 16 the partial map covers the
+// last block: (d mod 16 elements, row, slice), box (16, box_rows, box_slices).
+int encode_operand(CUtensorMap* full, CUtensorMap* partial, const void* base, bool bf16, int d,
+                   int64_t rows, int64_t slices, int atoms, int box_rows, int box_slices) {
+    const int fa = d / 16, rem = d % 16;
+    const int part = (fa > 0 && rem) ? 1 : 0;
+    const bool table = slices == 0;
+    const uint64_t row_b = (uint64_t)d * 2, slice_b = (uint64_t)rows * d * 2;
+    {
+        uint64_t dims[4], str[3];
+        uint32_t box[4];
+        int rk = 0;
+        dims[rk] = fa > 0 ? 16 : (uint64_t)d;
+        box[rk++] = 16;
+        dims[rk] = (uint64_t)rows;
+        box[rk++] = (uint32_t)box_rows;
+        if (!table) {
+            dims[rk] = (uint64_t)slices;
+            box[rk++] = (uint32_t)box_slices;
+        }
+        dims[rk] = (uint64_t)(fa > 0 ? fa : 1);
+        box[rk++] = (uint32_t)(atoms - part);
+        int si = 0;
+        str[si++] = row_b;
+        if (!table) str[si++] = slice_b;
+        str[si++] = 32;
+        int rc = encode(full, base, bf16, rk, dims, str, box);
+        if (rc) return rc;
+    }
+    if (part) {
+        uint64_t dims[3], str[2];
+        uint32_t box[3];
+        int rk = 0;
+        dims[rk] = (uint64_t)rem;
+        box[rk++] = 16;
+        dims[rk] = (uint64_t)rows;
+        box[rk++] = (uint32_t)box_rows;
+        if (!table) {
+            dims[rk] = (uint64_t)slices;
+            box[rk++] = (uint32_t)box_slices;
+        }
+        str[0] = row_b;
+        str[1] = slice_b;
+        const void* pb = static_cast<const unsigned char*>(base) + fa * 32;
+        int rc = encode(partial, pb, bf16, rk, dims, str, box);
+        if (rc) return rc;
+    } else {
+        *partial = *full;
+    }
     return ATTN_OK;
 }
 
@@ -239,8 +297,8 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         p.n_kv = 1;
         p.kv_w = kBlockN;
         p.kv_cols = kBlockN;
-        p.box_q = Nq;
-        p.box_kv = Nk;
+        p.box_q = sl;
+        p.box_kv = sl;
         p.nq = 0;
         if (bias == kBiasSwin) extra = swin_extra_bytes(sl, H);
         p.ring_stage_bytes = (uint32_t)(3 * tile_bytes);
@@ -261,7 +319,7 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         if (nj > 0x7fffffff) return fail(ATTN_ERR_UNSUPPORTED, "too many jobs");
         p.n_jobs = (int)nj;
         p.box_q = kBlockM;
-        p.box_kv = p.kv_cols;
+        p.box_kv = kBlockN;
         p.ring_stage_bytes = (uint32_t)(2 * tile_bytes);
         // prefer >= 3 K/V stages, then double-buffered Q
         int nq = 0, nst = 0;
@@ -288,34 +346,32 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
     if (nsm <= 0) return fail(ATTN_ERR_CUDA, "no CUDA device");
     const int grid = std::min(p.n_jobs, nsm);
 
-    CUtensorMap tq, tk, tv, trh, trw;
+    TmaMaps tm;
     const bool bf = p.is_bf16 != 0;
+    const int atoms = dpad / 16;
+    p.full_atoms = d / 16;
+    p.part = (d / 16 > 0 && d % 16) ? 1 : 0;
     int rc;
     if (separate) {
-        if ((rc = encode_map(&tq, q, bf, d, BH * Nq, 0, p.box_q))) return rc;
-        if ((rc = encode_map(&tk, k, bf, d, BH * Nk, 0, p.box_kv))) return rc;
-        if ((rc = encode_map(&tv, v, bf, d, BH * Nk, 0, p.box_kv))) return rc;
+        if ((rc = encode_operand(&tm.q, &tm.qp, q, bf, d, Nq, BH, atoms, sl, p.g))) return rc;
+        if ((rc = encode_operand(&tm.k, &tm.kp, k, bf, d, Nk, BH, atoms, sl, p.g))) return rc;
+        if ((rc = encode_operand(&tm.v, &tm.vp, v, bf, d, Nk, BH, atoms, sl, p.g))) return rc;
     } else {
-        if ((rc = encode_map(&tq, q, bf, d, Nq, BH, p.box_q))) return rc;
-        if ((rc = encode_map(&tk, k, bf, d, Nk, BH, p.box_kv))) return rc;
-        if ((rc = encode_map(&tv, v, bf, d, Nk, BH, p.box_kv))) return rc;
+        if ((rc = encode_operand(&tm.q, &tm.qp, q, bf, d, Nq, BH, atoms, kBlockM, 1))) return rc;
+        if ((rc = encode_operand(&tm.k, &tm.kp, k, bf, d, Nk, BH, atoms, kBlockN, 1))) return rc;
+        if ((rc = encode_operand(&tm.v, &tm.vp, v, bf, d, Nk, BH, atoms, kBlockN, 1))) return rc;
     }
     if (bias == kBiasSam) {
-        if ((rc = encode_map(&trh, rel_h, bf, d, 2 * p.s_h - 1, 0, kBlockN))) return rc;
-        if ((rc = encode_map(&trw, rel_w, bf, d, 2 * p.s_w - 1, 0, kBlockN))) return rc;
+        if ((rc = encode_operand(&tm.rh, &tm.rhp, rel_h, bf, d, 2 * p.s_h - 1, 0, atoms, kBlockN, 1))) return rc;
+        if ((rc = encode_operand(&tm.rw, &tm.rwp, rel_w, bf, d, 2 * p.s_w - 1, 0, atoms, kBlockN, 1))) return rc;
     } else {
-        trh = tq;
-        trw = tq;
+        tm.rh = tm.rhp = tm.rw = tm.rwp = tm.q;
     }
     p.status = status_ptr();
     if (!p.status) return fail(ATTN_ERR_CUDA, "no CUDA device / status word unavailable");
 
     LaunchArgs la;
-    la.tq = &tq;
-    la.tk = &tk;
-    la.tv = &tv;
-    la.trh = &trh;
-    la.trw = &trw;
+    la.tm = &tm;
     la.p = &p;
     la.mode = mode;
     la.sw = sw_spec;

@@ -70,13 +70,21 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: every legal wait is mi
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           int code) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
+    // try_wait suspends in hardware for a while; the abort word and the
+    // clock are looked at only every 64 / 1024 unsuccessful tries so a wait
+    // wakes promptly once its phase completes.
+    uint64_t t0 = 0;
+    for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (abort && *abort) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            if (abort && code) atomicCAS((int*)abort, 0, code);
-            return false;
+        if ((n & 63) == 0 && abort && *abort) return false;
+        if ((n & 1023) == 0) {
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitNs) {
+                if (abort && code) atomicCAS((int*)abort, 0, code);
+                return false;
+            }
         }
     }
 }
@@ -97,6 +105,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z, int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
         : "memory");
 }
 
