@@ -254,35 +254,41 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-// S = Q.K^T for one 128-row tile (both operands K-major, 32B swizzle).
+// Shared-memory descriptor of a 32B-swizzled operand block at `addr`
+// (K-major: 8-row groups 256 B apart).  Moving along a block only changes the
+// start-address field (bits 0-13, in 16-byte units), so the issue loops add
+// offsets to one precomputed descriptor instead of rebuilding it per MMA:
+// the single issuing thread is latency-bound on that scalar work.
+__device__ __forceinline__ uint64_t kdesc(uint32_t addr) { return make_sdesc(addr, 16, 256, kSwizzle32B); }
+// MN-major (V): 16-column blocks kBlockN*32 bytes apart, 8-key groups 256 B apart.
+__device__ __forceinline__ uint64_t vdesc(uint32_t addr) { return make_sdesc(addr, kBlockN * 32, 256, kSwizzle32B); }
+
+// S = Q.K^T for one 128-row tile: one MMA per 16-column block of d.
 template <int DPAD>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr,
-                                         uint32_t idesc) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t kd, uint32_t idesc) {
 #pragma unroll
-    for (int ks = 0; ks < Tile<DPAD>::kAtoms; ++ks) {
-        const uint64_t da = make_sdesc(q_addr + ks * kBlockM * 32, 16, 256, kSwizzle32B);
-        const uint64_t db = make_sdesc(k_addr + ks * kBlockN * 32, 16, 256, kSwizzle32B);
-        mma_ss(d_tmem, da, db, idesc, ks > 0 ? 1u : 0u);
-    }
+    for (int ks = 0; ks < Tile<DPAD>::kAtoms; ++ks)
+        mma_ss(d_tmem, qd + (uint64_t)(ks * (kBlockM * 32 / 16)), kd + (uint64_t)(ks * (kBlockN * 32 / 16)),
+               idesc, ks > 0 ? 1u : 0u);
 }
 
 // D[:, 0:SL] (+)= Qone . E^T with Qone [128][SL] and E [SL][SL] K-major.
-__device__ __forceinline__ void issue_bias(uint32_t d_tmem, uint32_t qone, uint32_t blk, int sl,
-                                          uint32_t idesc, uint32_t acc0) {
-    for (int ks = 0; ks < sl / 16; ++ks) {
-        const uint64_t da = make_sdesc(qone + ks * kBlockM * 32, 16, 256, kSwizzle32B);
-        const uint64_t db = make_sdesc(blk + ks * sl * 32, 16, 256, kSwizzle32B);
-        mma_ss(d_tmem, da, db, idesc, (ks > 0 || acc0) ? 1u : 0u);
-    }
+template <int SL>
+__device__ __forceinline__ void issue_bias(uint32_t d_tmem, uint64_t qone_d, uint64_t blk_d, uint32_t idesc,
+                                          uint32_t acc0) {
+#pragma unroll
+    for (int ks = 0; ks < SL / 16; ++ks)
+        mma_ss(d_tmem, qone_d + (uint64_t)(ks * (kBlockM * 32 / 16)), blk_d + (uint64_t)(ks * (SL * 32 / 16)),
+               idesc, (ks > 0 || acc0) ? 1u : 0u);
 }
 
-// O (+)= P.V: P from TMEM (two 16-bit values per column), V MN-major.
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_addr,
-                                         uint32_t idesc, int kv_steps, bool accumulate) {
-    for (int ks = 0; ks < kv_steps; ++ks) {
-        const uint64_t db = make_sdesc(v_addr + ks * 512, kBlockN * 32, 256, kSwizzle32B);
-        mma_ts(o_tmem, p_tmem + ks * 8, db, idesc, (accumulate || ks > 0) ? 1u : 0u);
-    }
+// O (+)= P.V over 128 keys: P from TMEM (two 16-bit values per column),
+// V MN-major; 16 keys (512 bytes of V) per MMA.
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vd, uint32_t idesc,
+                                         uint32_t accumulate) {
+#pragma unroll
+    for (int ks = 0; ks < kBlockN / 16; ++ks)
+        mma_ts(o_tmem, p_tmem + ks * 8, vd + (uint64_t)(ks * (512 / 16)), idesc, (accumulate || ks > 0) ? 1u : 0u);
 }
 
 template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG>
@@ -503,24 +509,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (warp == kMmaWarp) {
         // ================================================================ MMA
         if (lane == 0) {
+            // Slots are handled with explicit slot-0 / slot-1 code so every
+            // TMEM address and phase stays in a register.
             const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, p.kv_cols, false);
             const uint32_t idesc_o = make_idesc_f16(bf, kBlockM, DPAD, true);
             const uint32_t idesc_b = make_idesc_f16(bf, kBlockM, MODE == kModeSeparate ? SL : 16, false);
-            const int kv_steps = p.kv_cols / 16;
-            uint32_t tS[2], tO[2];
-            tS[0] = tmem;
-            tS[1] = tmem + 128;
-            tO[0] = tmem + 256;
-            tO[1] = tmem + 384;
+            const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
             int ring = 0;  // stage uses consumed
-            int cnt_p[2] = {0, 0};
+            uint32_t ph_p0 = 0, ph_p1 = 0;
             int ju = 0;
             bool ok = true;
-            const uint32_t qone = smem_u32(sExtraB);
-            const uint32_t blocks = qone + kBlockM * SL * 2;
-            // S of packed tile `tile` (separate mode) into S_x, with the Swin bias
-            auto issue_sep_scores = [&](int x, int tile, uint32_t qa) {
-                if (!DBG || BIAS != kBiasSwin) issue_qk<DPAD>(tS[x], qa, qa + T::kBytes, idesc_s);
+            const uint64_t qone_d = kdesc(smem_u32(sExtraB));
+            const uint32_t blocks = smem_u32(sExtraB) + kBlockM * SL * 2;
+            auto waitb = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
+                if (!mbar_wait(bar, parity, abort_flag, code)) return false;
+                tc_fence_after();
+                return true;
+            };
+            // S of packed tile `tile` (separate mode) into the S buffer dS, with the Swin bias
+            auto sep_scores = [&](uint32_t dS, int tile, uint32_t qa) {
+                if (!DBG || BIAS != kBiasSwin) issue_qk<DPAD>(dS, kdesc(qa), kdesc(qa + T::kBytes), idesc_s);
                 if constexpr (BIAS == kBiasSwin) {
                     for (int sl = 0; sl < p.g; ++sl) {
                         const int slice = tile * p.g + sl;
@@ -530,142 +538,129 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int kind = p.shift ? ((((w % p.n_ww) == p.n_ww - 1) ? 1 : 0) |
                                                     (((w / p.n_ww) == p.n_wh - 1) ? 2 : 0))
                                                  : 0;
-                        const uint32_t d = tS[x] + sl * SL;
-                        issue_bias(d, qone, blocks + h * SL * SL * 2, SL, idesc_b, DBG ? 0u : 1u);
-                        if (kind) issue_bias(d, qone, blocks + (p.H + kind - 1) * SL * SL * 2, SL, idesc_b, 1u);
+                        const uint32_t d = dS + sl * SL;
+                        issue_bias<SL>(d, qone_d, kdesc(blocks + h * SL * SL * 2), idesc_b, DBG ? 0u : 1u);
+                        if (kind) issue_bias<SL>(d, qone_d, kdesc(blocks + (p.H + kind - 1) * SL * SL * 2), idesc_b, 1u);
                     }
                 }
             };
             for (int job = job0; ok && job < p.n_jobs; job += job_step, ++ju) {
                 if constexpr (MODE == kModeShared) {
                     const int qb = ju % p.nq;
-                    uint32_t qa[2];
-                    qa[0] = smem_u32(sQ + (0 * p.nq + qb) * T::kBytes);
-                    qa[1] = smem_u32(sQ + (1 * p.nq + qb) * T::kBytes);
-                    for (int x = 0; x < 2 && ok; ++x)
-                        ok = mbar_wait(&bar_q_full[x][qb], (ju / p.nq) & 1, abort_flag, kStatusWaitQ);
-                    if (!ok) break;
-                    tc_fence_after();
+                    const uint64_t qa0 = kdesc(smem_u32(sQ + (0 * p.nq + qb) * T::kBytes));
+                    const uint64_t qa1 = kdesc(smem_u32(sQ + (1 * p.nq + qb) * T::kBytes));
+                    const uint32_t qpar = (ju / p.nq) & 1;
+                    if (!waitb(&bar_q_full[0][qb], qpar, kStatusWaitQ) || !waitb(&bar_q_full[1][qb], qpar, kStatusWaitQ)) {
+                        ok = false;
+                        break;
+                    }
                     if constexpr (BIAS == kBiasSam) {
                         const int st = ring % nst;
-                        if (!mbar_wait(&bar_full_k[st], (ring / nst) & 1, abort_flag, kStatusWaitK) ||
-                            !mbar_wait(&bar_full_v[st], (ring / nst) & 1, abort_flag, kStatusWaitV)) {
+                        const uint32_t par = (ring / nst) & 1;
+                        if (!waitb(&bar_full_k[st], par, kStatusWaitK) || !waitb(&bar_full_v[st], par, kStatusWaitV)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-                        const uint32_t rw = smem_u32(sRing + st * p.ring_stage_bytes);
-                        const uint32_t rh = rw + T::kBytes;
+                        const uint64_t rw = kdesc(smem_u32(sRing + st * p.ring_stage_bytes));
+                        const uint64_t rh = kdesc(smem_u32(sRing + st * p.ring_stage_bytes + T::kBytes));
                         const uint32_t id_w = make_idesc_f16(bf, kBlockM, p.n_rw, false);
                         const uint32_t id_h = make_idesc_f16(bf, kBlockM, p.n_rh, false);
-                        for (int x = 0; x < 2; ++x) {
-                            // G_h rewrites O_x: the previous job's epilogue must be done with it
-                            if (ju > 0 && !mbar_wait(&bar_oempty[x], (ju - 1) & 1, abort_flag, kStatusWaitO)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            issue_qk<DPAD>(tS[x], qa[x], rw, id_w);
-                            issue_qk<DPAD>(tO[x], qa[x], rh, id_h);
-                            mma_commit(&bar_g[x]);
-                        }
-                        if (!ok) break;
+                        // G_h rewrites O_x: the previous job's epilogue must be done with it
+                        if (ju > 0 && !waitb(&bar_oempty[0], (ju - 1) & 1, kStatusWaitO)) { ok = false; break; }
+                        issue_qk<DPAD>(tS0, qa0, rw, id_w);
+                        issue_qk<DPAD>(tO0, qa0, rh, id_h);
+                        mma_commit(&bar_g[0]);
+                        if (ju > 0 && !waitb(&bar_oempty[1], (ju - 1) & 1, kStatusWaitO)) { ok = false; break; }
+                        issue_qk<DPAD>(tS1, qa1, rw, id_w);
+                        issue_qk<DPAD>(tO1, qa1, rh, id_h);
+                        mma_commit(&bar_g[1]);
                         mma_commit(&bar_empty[st]);
                         ++ring;
                     }
                     const int n = p.n_kv;
                     {
                         const int st = ring % nst;
-                        if (!mbar_wait(&bar_full_k[st], (ring / nst) & 1, abort_flag, kStatusWaitK)) {
+                        if (!waitb(&bar_full_k[st], (ring / nst) & 1, kStatusWaitK)) { ok = false; break; }
+                        const uint64_t ka = kdesc(smem_u32(sRing + st * p.ring_stage_bytes));
+                        // with the SAM bias, S_x rewrites the G_w values slot x is still gathering
+                        if (BIAS == kBiasSam && !waitb(&bar_gdone[0], ju & 1, kStatusWaitG)) { ok = false; break; }
+                        issue_qk<DPAD>(tS0, qa0, ka, idesc_s);
+                        mma_commit(&bar_s[0]);
+                        if (BIAS == kBiasSam && !waitb(&bar_gdone[1], ju & 1, kStatusWaitG)) { ok = false; break; }
+                        issue_qk<DPAD>(tS1, qa1, ka, idesc_s);
+                        mma_commit(&bar_s[1]);
+                    }
+                    for (int j = 0; j < n; ++j) {
+                        const int use = ring + j;
+                        const int st = use % nst;
+                        const uint64_t va = vdesc(smem_u32(sRing + st * p.ring_stage_bytes + T::kBytes));
+                        const int st1 = (use + 1) % nst;
+                        const uint64_t ka1 = kdesc(smem_u32(sRing + st1 * p.ring_stage_bytes));
+                        const bool last = j == n - 1;
+                        // slot A: O_A += P_A.V_j, then S_A for the next key tile
+                        if (!waitb(&bar_p[0], ph_p0, kStatusWaitP) || !waitb(&bar_full_v[st], (use / nst) & 1, kStatusWaitV)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-                        const uint32_t ka = smem_u32(sRing + st * p.ring_stage_bytes);
-                        for (int x = 0; x < 2; ++x) {
-                            if (BIAS == kBiasSam) {
-                                // S_x rewrites the G_w values the slot is still gathering
-                                if (!mbar_wait(&bar_gdone[x], ju & 1, abort_flag, kStatusWaitG)) {
-                                    ok = false;
-                                    break;
-                                }
-                                tc_fence_after();
-                            }
-                            issue_qk<DPAD>(tS[x], qa[x], ka, idesc_s);
-                            mma_commit(&bar_s[x]);
+                        ph_p0 ^= 1;
+                        issue_pv(tO0, tS0, va, idesc_o, j > 0 ? 1u : 0u);
+                        if (last) mma_commit(&bar_o[0]);
+                        if (!last) {
+                            if (!waitb(&bar_full_k[st1], ((use + 1) / nst) & 1, kStatusWaitK)) { ok = false; break; }
+                            issue_qk<DPAD>(tS0, qa0, ka1, idesc_s);
+                            mma_commit(&bar_s[0]);
                         }
-                        if (!ok) break;
-                    }
-                    for (int j = 0; j < n && ok; ++j) {
-                        const int use = ring + j;
-                        const int st = use % nst;
-                        const uint32_t va = smem_u32(sRing + st * p.ring_stage_bytes + T::kBytes);
-                        const int st1 = (use + 1) % nst;
-                        const uint32_t ka1 = smem_u32(sRing + st1 * p.ring_stage_bytes);
-                        for (int x = 0; x < 2; ++x) {
-                            if (!mbar_wait(&bar_p[x], cnt_p[x] & 1, abort_flag, kStatusWaitP)) { ok = false; break; }
-                            ++cnt_p[x];
-                            if (x == 0 && !mbar_wait(&bar_full_v[st], (use / nst) & 1, abort_flag, kStatusWaitV)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            issue_pv(tO[x], tS[x], va, idesc_o, kv_steps, j > 0);
-                            if (j == n - 1) mma_commit(&bar_o[x]);
-                            if (x == 1) {
-                                mma_commit(&bar_empty[st]);
-                                if (j == n - 1) {
-                                    mma_commit(&bar_q_empty[0][qb]);
-                                    mma_commit(&bar_q_empty[1][qb]);
-                                }
-                            }
-                            if (j + 1 < n) {
-                                if (x == 0 && !mbar_wait(&bar_full_k[st1], ((use + 1) / nst) & 1, abort_flag, kStatusWaitK)) {
-                                    ok = false;
-                                    break;
-                                }
-                                tc_fence_after();
-                                issue_qk<DPAD>(tS[x], qa[x], ka1, idesc_s);
-                                mma_commit(&bar_s[x]);
-                            }
+                        // slot B
+                        if (!waitb(&bar_p[1], ph_p1, kStatusWaitP)) { ok = false; break; }
+                        ph_p1 ^= 1;
+                        issue_pv(tO1, tS1, va, idesc_o, j > 0 ? 1u : 0u);
+                        mma_commit(&bar_empty[st]);
+                        if (last) {
+                            mma_commit(&bar_o[1]);
+                            mma_commit(&bar_q_empty[0][qb]);
+                            mma_commit(&bar_q_empty[1][qb]);
+                        } else {
+                            issue_qk<DPAD>(tS1, qa1, ka1, idesc_s);
+                            mma_commit(&bar_s[1]);
                         }
                     }
                     ring += n;
                 } else {
                     // separate mode: ring uses `ring` (tile 2*job, slot A) and `ring+1` (slot B)
+                    const int st0 = ring % nst, st1 = (ring + 1) % nst;
+                    const uint32_t qa0 = smem_u32(sRing + st0 * p.ring_stage_bytes);
+                    const uint32_t qa1 = smem_u32(sRing + st1 * p.ring_stage_bytes);
                     if (ju == 0) {
-                        for (int x = 0; x < 2 && ok; ++x) {
-                            const int st = (ring + x) % nst;
-                            if (!mbar_wait(&bar_full_k[st], ((ring + x) / nst) & 1, abort_flag, kStatusWaitK)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            issue_sep_scores(x, 2 * job + x, smem_u32(sRing + st * p.ring_stage_bytes));
-                            mma_commit(&bar_s[x]);
-                        }
+                        if (!waitb(&bar_full_k[st0], (ring / nst) & 1, kStatusWaitK)) { ok = false; break; }
+                        sep_scores(tS0, 2 * job, qa0);
+                        mma_commit(&bar_s[0]);
+                        if (!waitb(&bar_full_k[st1], ((ring + 1) / nst) & 1, kStatusWaitK)) { ok = false; break; }
+                        sep_scores(tS1, 2 * job + 1, qa1);
+                        mma_commit(&bar_s[1]);
                     }
                     const int next = job + job_step;
-                    for (int x = 0; x < 2 && ok; ++x) {
-                        const int st = (ring + x) % nst;
-                        const uint32_t qa = smem_u32(sRing + st * p.ring_stage_bytes);
-                        if (!mbar_wait(&bar_p[x], cnt_p[x] & 1, abort_flag, kStatusWaitP)) { ok = false; break; }
-                        ++cnt_p[x];
-                        tc_fence_after();
-                        issue_pv(tO[x], tS[x], qa + 2 * T::kBytes, idesc_o, kv_steps, false);
-                        mma_commit(&bar_empty[st]);
-                        mma_commit(&bar_o[x]);
-                        if (next < p.n_jobs) {
-                            const int use2 = ring + 2 + x;
-                            const int st2 = use2 % nst;
-                            if (!mbar_wait(&bar_full_k[st2], (use2 / nst) & 1, abort_flag, kStatusWaitK)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            issue_sep_scores(x, 2 * next + x, smem_u32(sRing + st2 * p.ring_stage_bytes));
-                            mma_commit(&bar_s[x]);
-                        }
+                    const int u2 = ring + 2, u3 = ring + 3;
+                    const uint32_t qn0 = smem_u32(sRing + (u2 % nst) * p.ring_stage_bytes);
+                    const uint32_t qn1 = smem_u32(sRing + (u3 % nst) * p.ring_stage_bytes);
+                    if (!waitb(&bar_p[0], ph_p0, kStatusWaitP)) { ok = false; break; }
+                    ph_p0 ^= 1;
+                    issue_pv(tO0, tS0, vdesc(qa0 + 2 * T::kBytes), idesc_o, 0u);
+                    mma_commit(&bar_empty[st0]);
+                    mma_commit(&bar_o[0]);
+                    if (next < p.n_jobs) {
+                        if (!waitb(&bar_full_k[u2 % nst], (u2 / nst) & 1, kStatusWaitK)) { ok = false; break; }
+                        sep_scores(tS0, 2 * next, qn0);
+                        mma_commit(&bar_s[0]);
+                    }
+                    if (!waitb(&bar_p[1], ph_p1, kStatusWaitP)) { ok = false; break; }
+                    ph_p1 ^= 1;
+                    issue_pv(tO1, tS1, vdesc(qa1 + 2 * T::kBytes), idesc_o, 0u);
+                    mma_commit(&bar_empty[st1]);
+                    mma_commit(&bar_o[1]);
+                    if (next < p.n_jobs) {
+                        if (!waitb(&bar_full_k[u3 % nst], (u3 / nst) & 1, kStatusWaitK)) { ok = false; break; }
+                        sep_scores(tS1, 2 * next + 1, qn1);
+                        mma_commit(&bar_s[1]);
                     }
                     ring += 2;
                 }

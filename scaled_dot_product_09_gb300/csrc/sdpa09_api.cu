@@ -312,7 +312,7 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         mode = kModeShared;
         p.g = 1;
         p.kv_w = (bias == kBiasSam && sw_spec) ? (kBlockN / sw_spec) * sw_spec : kBlockN;
-        p.kv_cols = (p.kv_w + 15) / 16 * 16;
+        p.kv_cols = kBlockN;  // the key tile always spans 128 columns; keys past kv_w are masked
         p.n_kv = (Nk + p.kv_w - 1) / p.kv_w;
         p.q_jobs = (Nq + 2 * kBlockM - 1) / (2 * kBlockM);
         const int64_t nj = BH * p.q_jobs;
