@@ -110,6 +110,7 @@ struct AttnParams {
     // Swin
     const float* table;  // [(2M-1)^2][H]
     int win, grid_h, grid_w, shift, n_w, n_ww, n_wh;
+    uint32_t fd_h[2], fd_w[2], fd_ww[2];  // magic/shift pairs dividing by H, n_w, n_ww
     // SAM
     int s_h, s_w, n_rh, n_rw;
 };
@@ -142,6 +143,14 @@ struct Tile {
     static constexpr int kBytes = kAtoms * kBlockM * 32;  // 128 rows x DPAD x 2 B
     static_assert(DPAD % 16 == 0 && DPAD >= 16 && DPAD <= 128, "head dim block");
 };
+
+// Unsigned division by a divisor fixed at launch: q = (umulhi(n, m) + n) >> s
+// with the magic number m and shift s the host derives (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994);
+// valid for n < 2^31.
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const uint32_t (&fd)[2]) {
+    return (__umulhi(n, fd[0]) + n) >> fd[1];
+}
 
 __device__ __forceinline__ int swin_strip(int pos, int G, int M, int s) {
     return pos < G - M ? 0 : (pos < G - s ? 1 : 2);
@@ -296,6 +305,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ TmaMaps tm, const AttnParams p) {
     using T = Tile<DPAD>;
     static_assert(MODE == kModeShared || (SL == 32 || SL == 64 || SL == 128), "slot size");
+    // Head dims up to 64 leave room in tensor memory for separate P buffers:
+    // S_A [0,128) S_B [128,256) P_A [256,320) P_B [320,384) O_A [384,448)
+    // O_B [448,512).  The next score tile of a slot is then issued as soon as
+    // its softmax has read the current one, overlapping Q.K^T with the
+    // softmax.  Larger head dims keep P over the first half of S.
+    constexpr bool kSepP = DPAD <= 64 && BIAS != kBiasSam;
+    static_assert(MODE == kModeShared || kSepP, "the packed tiling uses separate P buffers");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -307,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint64_t bar_q_full[2][2], bar_q_empty[2][2];
     __shared__ uint64_t bar_full_k[kMaxStages], bar_full_v[kMaxStages], bar_empty[kMaxStages];
     __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2], bar_g[2], bar_gdone[2], bar_oempty[2];
+    __shared__ uint64_t bar_sfree[2], bar_pvd[2];
     __shared__ uint64_t bar_final;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -331,6 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar_g[x], 1);
             mbar_init(&bar_gdone[x], 4);
             mbar_init(&bar_oempty[x], 4);
+            mbar_init(&bar_sfree[x], 4);
+            mbar_init(&bar_pvd[x], 1);
         }
         for (int i = 0; i < kMaxStages; ++i) {
             mbar_init(&bar_full_k[i], 1);
@@ -511,12 +530,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // Slots are handled with explicit slot-0 / slot-1 code so every
             // TMEM address and phase stays in a register.
-            const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, p.kv_cols, false);
+            const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, kBlockN, false);
             const uint32_t idesc_o = make_idesc_f16(bf, kBlockM, DPAD, true);
             const uint32_t idesc_b = make_idesc_f16(bf, kBlockM, MODE == kModeSeparate ? SL : 16, false);
-            const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+            const uint32_t tS0 = tmem, tS1 = tmem + 128;
+            const uint32_t tP0 = kSepP ? tmem + 256 : tS0, tP1 = kSepP ? tmem + 320 : tS1;
+            const uint32_t tO0 = tmem + (kSepP ? 384 : 256), tO1 = tmem + (kSepP ? 448 : 384);
             int ring = 0;  // stage uses consumed
             uint32_t ph_p0 = 0, ph_p1 = 0;
+            int s_cnt0 = 0, s_cnt1 = 0;  // score tiles issued per slot
             int ju = 0;
             bool ok = true;
             const uint64_t qone_d = kdesc(smem_u32(sExtraB));
@@ -526,18 +548,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 return true;
             };
+            // Before a slot's next score tile overwrites S_x: its softmax must
+            // have read the previous one (separate P buffers only).
+            auto s_free = [&](int x) -> bool {
+                const int c = x ? s_cnt1 : s_cnt0;
+                if (!kSepP || c == 0) return true;
+                return waitb(&bar_sfree[x], (c - 1) & 1, kStatusWaitS);
+            };
             // S of packed tile `tile` (separate mode) into the S buffer dS, with the Swin bias
             auto sep_scores = [&](uint32_t dS, int tile, uint32_t qa) {
                 if (!DBG || BIAS != kBiasSwin) issue_qk<DPAD>(dS, kdesc(qa), kdesc(qa + T::kBytes), idesc_s);
                 if constexpr (BIAS == kBiasSwin) {
                     for (int sl = 0; sl < p.g; ++sl) {
-                        const int slice = tile * p.g + sl;
-                        if (slice >= p.BH) break;
-                        const int h = slice % p.H;
-                        const int w = (slice / p.H) % p.n_w;
-                        const int kind = p.shift ? ((((w % p.n_ww) == p.n_ww - 1) ? 1 : 0) |
-                                                    (((w / p.n_ww) == p.n_wh - 1) ? 2 : 0))
-                                                 : 0;
+                        const uint32_t slice = (uint32_t)(tile * p.g + sl);
+                        if ((int)slice >= p.BH) break;
+                        const uint32_t bimg = fast_div(slice, p.fd_h);
+                        const uint32_t h = slice - bimg * (uint32_t)p.H;
+                        const uint32_t w = bimg - fast_div(bimg, p.fd_w) * (uint32_t)p.n_w;
+                        const uint32_t wr = fast_div(w, p.fd_ww);
+                        const uint32_t wc = w - wr * (uint32_t)p.n_ww;
+                        const int kind = p.shift ? (((int)wc == p.n_ww - 1 ? 1 : 0) | ((int)wr == p.n_wh - 1 ? 2 : 0)) : 0;
                         const uint32_t d = dS + sl * SL;
                         issue_bias<SL>(d, qone_d, kdesc(blocks + h * SL * SL * 2), idesc_b, DBG ? 0u : 1u);
                         if (kind) issue_bias<SL>(d, qone_d, kdesc(blocks + (p.H + kind - 1) * SL * SL * 2), idesc_b, 1u);
@@ -579,16 +609,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int n = p.n_kv;
                     {
+                        // first score tiles of the job
                         const int st = ring % nst;
                         if (!waitb(&bar_full_k[st], (ring / nst) & 1, kStatusWaitK)) { ok = false; break; }
                         const uint64_t ka = kdesc(smem_u32(sRing + st * p.ring_stage_bytes));
                         // with the SAM bias, S_x rewrites the G_w values slot x is still gathering
                         if (BIAS == kBiasSam && !waitb(&bar_gdone[0], ju & 1, kStatusWaitG)) { ok = false; break; }
+                        if (!s_free(0)) { ok = false; break; }
                         issue_qk<DPAD>(tS0, qa0, ka, idesc_s);
                         mma_commit(&bar_s[0]);
+                        ++s_cnt0;
                         if (BIAS == kBiasSam && !waitb(&bar_gdone[1], ju & 1, kStatusWaitG)) { ok = false; break; }
+                        if (!s_free(1)) { ok = false; break; }
                         issue_qk<DPAD>(tS1, qa1, ka, idesc_s);
                         mma_commit(&bar_s[1]);
+                        ++s_cnt1;
                     }
                     for (int j = 0; j < n; ++j) {
                         const int use = ring + j;
@@ -597,15 +632,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int st1 = (use + 1) % nst;
                         const uint64_t ka1 = kdesc(smem_u32(sRing + st1 * p.ring_stage_bytes));
                         const bool last = j == n - 1;
-                        // slot A: O_A += P_A.V_j, then S_A for the next key tile
+                        if (kSepP && !last) {
+                            // next score tiles first: they overlap this tile's softmax
+                            if (!waitb(&bar_full_k[st1], ((use + 1) / nst) & 1, kStatusWaitK) || !s_free(0)) { ok = false; break; }
+                            issue_qk<DPAD>(tS0, qa0, ka1, idesc_s);
+                            mma_commit(&bar_s[0]);
+                            ++s_cnt0;
+                            if (!s_free(1)) { ok = false; break; }
+                            issue_qk<DPAD>(tS1, qa1, ka1, idesc_s);
+                            mma_commit(&bar_s[1]);
+                            ++s_cnt1;
+                        }
+                        // slot A: O_A += P_A.V_j
                         if (!waitb(&bar_p[0], ph_p0, kStatusWaitP) || !waitb(&bar_full_v[st], (use / nst) & 1, kStatusWaitV)) {
                             ok = false;
                             break;
                         }
                         ph_p0 ^= 1;
-                        issue_pv(tO0, tS0, va, idesc_o, j > 0 ? 1u : 0u);
-                        if (last) mma_commit(&bar_o[0]);
-                        if (!last) {
+                        issue_pv(tO0, tP0, va, idesc_o, j > 0 ? 1u : 0u);
+                        if (last) {
+                            mma_commit(&bar_o[0]);
+                        } else if (kSepP) {
+                            mma_commit(&bar_pvd[0]);
+                        }
+                        if (!kSepP && !last) {
                             if (!waitb(&bar_full_k[st1], ((use + 1) / nst) & 1, kStatusWaitK)) { ok = false; break; }
                             issue_qk<DPAD>(tS0, qa0, ka1, idesc_s);
                             mma_commit(&bar_s[0]);
@@ -613,13 +663,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // slot B
                         if (!waitb(&bar_p[1], ph_p1, kStatusWaitP)) { ok = false; break; }
                         ph_p1 ^= 1;
-                        issue_pv(tO1, tS1, va, idesc_o, j > 0 ? 1u : 0u);
-                        mma_commit(&bar_empty[st]);
+                        issue_pv(tO1, tP1, va, idesc_o, j > 0 ? 1u : 0u);
                         if (last) {
                             mma_commit(&bar_o[1]);
+                        } else if (kSepP) {
+                            mma_commit(&bar_pvd[1]);
+                        }
+                        mma_commit(&bar_empty[st]);
+                        if (last) {
                             mma_commit(&bar_q_empty[0][qb]);
                             mma_commit(&bar_q_empty[1][qb]);
-                        } else {
+                        } else if (!kSepP) {
                             issue_qk<DPAD>(tS1, qa1, ka1, idesc_s);
                             mma_commit(&bar_s[1]);
                         }
@@ -634,34 +688,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!waitb(&bar_full_k[st0], (ring / nst) & 1, kStatusWaitK)) { ok = false; break; }
                         sep_scores(tS0, 2 * job, qa0);
                         mma_commit(&bar_s[0]);
+                        ++s_cnt0;
                         if (!waitb(&bar_full_k[st1], ((ring + 1) / nst) & 1, kStatusWaitK)) { ok = false; break; }
                         sep_scores(tS1, 2 * job + 1, qa1);
                         mma_commit(&bar_s[1]);
+                        ++s_cnt1;
                     }
                     const int next = job + job_step;
-                    const int u2 = ring + 2, u3 = ring + 3;
-                    const uint32_t qn0 = smem_u32(sRing + (u2 % nst) * p.ring_stage_bytes);
-                    const uint32_t qn1 = smem_u32(sRing + (u3 % nst) * p.ring_stage_bytes);
+                    if (next < p.n_jobs) {
+                        // next tiles' scores first: they overlap this tile's softmax
+                        const int u2 = ring + 2, u3 = ring + 3;
+                        if (!waitb(&bar_full_k[u2 % nst], (u2 / nst) & 1, kStatusWaitK) || !s_free(0)) { ok = false; break; }
+                        sep_scores(tS0, 2 * next, smem_u32(sRing + (u2 % nst) * p.ring_stage_bytes));
+                        mma_commit(&bar_s[0]);
+                        ++s_cnt0;
+                        if (!waitb(&bar_full_k[u3 % nst], (u3 / nst) & 1, kStatusWaitK) || !s_free(1)) { ok = false; break; }
+                        sep_scores(tS1, 2 * next + 1, smem_u32(sRing + (u3 % nst) * p.ring_stage_bytes));
+                        mma_commit(&bar_s[1]);
+                        ++s_cnt1;
+                    }
                     if (!waitb(&bar_p[0], ph_p0, kStatusWaitP)) { ok = false; break; }
                     ph_p0 ^= 1;
-                    issue_pv(tO0, tS0, vdesc(qa0 + 2 * T::kBytes), idesc_o, 0u);
+                    issue_pv(tO0, tP0, vdesc(qa0 + 2 * T::kBytes), idesc_o, 0u);
                     mma_commit(&bar_empty[st0]);
                     mma_commit(&bar_o[0]);
-                    if (next < p.n_jobs) {
-                        if (!waitb(&bar_full_k[u2 % nst], (u2 / nst) & 1, kStatusWaitK)) { ok = false; break; }
-                        sep_scores(tS0, 2 * next, qn0);
-                        mma_commit(&bar_s[0]);
-                    }
                     if (!waitb(&bar_p[1], ph_p1, kStatusWaitP)) { ok = false; break; }
                     ph_p1 ^= 1;
-                    issue_pv(tO1, tS1, vdesc(qa1 + 2 * T::kBytes), idesc_o, 0u);
+                    issue_pv(tO1, tP1, vdesc(qa1 + 2 * T::kBytes), idesc_o, 0u);
                     mma_commit(&bar_empty[st1]);
                     mma_commit(&bar_o[1]);
-                    if (next < p.n_jobs) {
-                        if (!waitb(&bar_full_k[u3 % nst], (u3 / nst) & 1, kStatusWaitK)) { ok = false; break; }
-                        sep_scores(tS1, 2 * next + 1, qn1);
-                        mma_commit(&bar_s[1]);
-                    }
                     ring += 2;
                 }
             }
@@ -677,7 +732,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = tid & 127;                // row in tile == TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + (uint32_t)(x * 128);
-        const uint32_t tO = tmem + lane_base + 256u + (uint32_t)(x * 128);
+        const uint32_t tP = kSepP ? tmem + lane_base + 256u + (uint32_t)(x * 64) : tS;
+        const uint32_t tO = tmem + lane_base + (kSepP ? 384u + (uint32_t)(x * 64) : 256u + (uint32_t)(x * 128));
+        int pvd_cnt = 0;  // P.V completions of this slot awaited (separate P buffers)
         int cnt_s = 0, ju = 0;
         bool ok = true;
         const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
@@ -720,6 +777,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int t = 0; t < SL; ++t) xs[t] = __uint_as_float(v[t]);
                 }
+                // S_x may now be overwritten by the next tile's scores
+                tc_fence_before();
+                warp_arrive(&bar_sfree[x]);
                 const int nk = p.Nk;
                 if constexpr (DBG) {
                     // the scores hold only the bias when debugging (no Q.K^T)
@@ -751,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (s == my_sl)
 #pragma unroll
                         for (int t = 0; t < SL / 2; ++t) pk[s * (SL / 2) + t] = own[t];
-                tmem_st64(tS, pk);
+                tmem_st64(tP, pk);
                 tmem_st_wait();
                 tc_fence_before();
                 warp_arrive(&bar_p[x]);
@@ -809,6 +869,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld128(tS, v);
 #pragma unroll
                         for (int t = 0; t < 128; ++t) xs[t] = __uint_as_float(v[t]);
+                    }
+                    if constexpr (kSepP) {
+                        // S_x may now be overwritten by the next tile's scores
+                        tc_fence_before();
+                        warp_arrive(&bar_sfree[x]);
                     }
                     const int key0 = j * p.kv_w;
                     const int hi = min(p.kv_w, p.Nk - key0);  // valid key columns [0, hi)
@@ -876,11 +941,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m_tile = row_max<128>(xs);
                         sc = 1.0f;
                     }
+                    if (kSepP && j > 0) {
+                        // P_x and O_x are rewritten below: the previous P.V must be done
+                        __syncwarp();
+                        if (!__all_sync(0xffffffffu, mbar_wait(&bar_pvd[x], pvd_cnt & 1, abort_flag, kStatusWaitO))) { ok = false; break; }
+                        ++pvd_cnt;
+                        tc_fence_after();
+                    }
                     const float m_new = fmaxf(m_run, m_tile);
                     const bool need = m_new > m_run + kRescaleThreshold;
                     if (__any_sync(0xffffffffu, need && j > 0)) {
-                        // O holds the earlier tiles' P.V, complete: this score tile
-                        // was committed after it
+                        // O holds the earlier tiles' P.V, complete (with a shared P/S
+                        // buffer this score tile was committed after it)
                         const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
                         uint32_t v[DPAD];
                         tmem_ld_cols<DPAD>(tO, v);
@@ -901,7 +973,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
                     uint32_t pk[64];
                     l_run += exp_pack<128>(xs, sc, -m_use, bf, pk);
-                    tmem_st64(tS, pk);
+                    tmem_st64(tP, pk);
                     tmem_st_wait();
                     tc_fence_before();
                     warp_arrive(&bar_p[x]);

@@ -150,6 +150,15 @@ int encode_operand(CUtensorMap* full, CUtensorMap* partial, const void* base, bo
     return ATTN_OK;
 }
 
+// Magic number and shift for fast_div (unsigned division by an invariant d,
+// Granlund and Montgomery 1994): l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1.
+void fast_div_params(uint32_t d, uint32_t out[2]) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    out[0] = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << l) - d)) / d + 1);
+    out[1] = l;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -260,6 +269,9 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         p.n_w = nW;
         p.n_ww = a->grid_w / M;
         p.n_wh = a->grid_h / M;
+        fast_div_params((uint32_t)H, p.fd_h);
+        fast_div_params((uint32_t)nW, p.fd_w);
+        fast_div_params((uint32_t)p.n_ww, p.fd_ww);
         bias = kBiasSwin;
     } else if (bias_kind == ATTN_BIAS_SAM_RELPOS) {
         const attn_sam_args* a = static_cast<const attn_sam_args*>(bias_args);
