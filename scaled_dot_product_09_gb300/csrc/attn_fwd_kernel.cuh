@@ -13,8 +13,9 @@
 //   warps 0-3   softmax slot A: thread t owns query row t of tile A (TMEM lane t)
 //   warps 4-7   softmax slot B: the same for tile B
 //   warp 8      TMA producer
-//   warp 9      tensor-memory allocator; lane 0 issues every tcgen05.mma
-//   warps 10-11 idle
+//   warp 9      tensor-memory allocator; lane 0 issues slot A's tcgen05.mma
+//   warp 10     lane 0 issues slot B's tcgen05.mma
+//   warp 11     idle
 // While one slot runs its softmax the tensor core works on the other slot's
 // products.  After setup the softmax warpgroups grow to kSoftmaxRegs registers
 // and the control warpgroup shrinks to kControlRegs; the split adds up exactly
@@ -354,9 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kMaxStages; ++i) {
             mbar_init(&bar_full_k[i], 1);
             mbar_init(&bar_full_v[i], 1);
-            mbar_init(&bar_empty[i], 1);
+            mbar_init(&bar_empty[i], MODE == kModeShared ? 2 : 1);
         }
-        mbar_init(&bar_final, 1);
+        mbar_init(&bar_final, 2);
         fence_mbar_init();
     }
     if (warp == kProducerWarp && lane == 0) {
@@ -525,20 +526,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-      } else if (warp == kMmaWarp) {
+      } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
         // ================================================================ MMA
+        // One issuing thread per slot (warp 9: slot A, warp 10: slot B):
+        // tcgen05.commit tracks the MMAs of the issuing thread, so each slot's
+        // products run on their own schedule; a shared K/V stage is released
+        // after both threads have committed their last use of it.
         if (lane == 0) {
-            // Slots are handled with explicit slot-0 / slot-1 code so every
-            // TMEM address and phase stays in a register.
+            const int x = warp - kMmaWarp;
             const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, kBlockN, false);
             const uint32_t idesc_o = make_idesc_f16(bf, kBlockM, DPAD, true);
             const uint32_t idesc_b = make_idesc_f16(bf, kBlockM, MODE == kModeSeparate ? SL : 16, false);
-            const uint32_t tS0 = tmem, tS1 = tmem + 128;
-            const uint32_t tP0 = kSepP ? tmem + 256 : tS0, tP1 = kSepP ? tmem + 320 : tS1;
-            const uint32_t tO0 = tmem + (kSepP ? 384 : 256), tO1 = tmem + (kSepP ? 448 : 384);
+            const uint32_t tSx = tmem + 128u * x;
+            const uint32_t tPx = kSepP ? tmem + 256u + 64u * x : tSx;
+            const uint32_t tOx = tmem + (kSepP ? 384u + 64u * x : 256u + 128u * x);
+            uint64_t* const bs = &bar_s[x];
+            uint64_t* const bp = &bar_p[x];
+            uint64_t* const bo = &bar_o[x];
+            uint64_t* const bsf = &bar_sfree[x];
+            uint64_t* const bpv = &bar_pvd[x];
             int ring = 0;  // stage uses consumed
-            uint32_t ph_p0 = 0, ph_p1 = 0;
-            int s_cnt0 = 0, s_cnt1 = 0;  // score tiles issued per slot
+            uint32_t ph_p = 0;
+            int s_cnt = 0;  // score tiles issued
             int ju = 0;
             bool ok = true;
             const uint64_t qone_d = kdesc(smem_u32(sExtraB));
@@ -548,16 +557,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 return true;
             };
-            // Before a slot's next score tile overwrites S_x: its softmax must
-            // have read the previous one (separate P buffers only).
-            auto s_free = [&](int x) -> bool {
-                const int c = x ? s_cnt1 : s_cnt0;
-                if (!kSepP || c == 0) return true;
-                return waitb(&bar_sfree[x], (c - 1) & 1, kStatusWaitS);
+            // Before the next score tile overwrites S_x its softmax must have
+            // read the previous one (separate P buffers only).
+            auto s_free = [&]() -> bool {
+                if (!kSepP || s_cnt == 0) return true;
+                return waitb(bsf, (s_cnt - 1) & 1, kStatusWaitS);
             };
-            // S of packed tile `tile` (separate mode) into the S buffer dS, with the Swin bias
-            auto sep_scores = [&](uint32_t dS, int tile, uint32_t qa) {
-                if (!DBG || BIAS != kBiasSwin) issue_qk<DPAD>(dS, kdesc(qa), kdesc(qa + T::kBytes), idesc_s);
+            // S of packed tile `tile` (separate mode), with the Swin bias
+            auto sep_scores = [&](int tile, uint32_t qa) {
+                if (!DBG || BIAS != kBiasSwin) issue_qk<DPAD>(tSx, kdesc(qa), kdesc(qa + T::kBytes), idesc_s);
                 if constexpr (BIAS == kBiasSwin) {
                     for (int sl = 0; sl < p.g; ++sl) {
                         const uint32_t slice = (uint32_t)(tile * p.g + sl);
@@ -568,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t wr = fast_div(w, p.fd_ww);
                         const uint32_t wc = w - wr * (uint32_t)p.n_ww;
                         const int kind = p.shift ? (((int)wc == p.n_ww - 1 ? 1 : 0) | ((int)wr == p.n_wh - 1 ? 2 : 0)) : 0;
-                        const uint32_t d = dS + sl * SL;
+                        const uint32_t d = tSx + sl * SL;
                         issue_bias<SL>(d, qone_d, kdesc(blocks + h * SL * SL * 2), idesc_b, DBG ? 0u : 1u);
                         if (kind) issue_bias<SL>(d, qone_d, kdesc(blocks + (p.H + kind - 1) * SL * SL * 2), idesc_b, 1u);
                     }
@@ -577,13 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int job = job0; ok && job < p.n_jobs; job += job_step, ++ju) {
                 if constexpr (MODE == kModeShared) {
                     const int qb = ju % p.nq;
-                    const uint64_t qa0 = kdesc(smem_u32(sQ + (0 * p.nq + qb) * T::kBytes));
-                    const uint64_t qa1 = kdesc(smem_u32(sQ + (1 * p.nq + qb) * T::kBytes));
-                    const uint32_t qpar = (ju / p.nq) & 1;
-                    if (!waitb(&bar_q_full[0][qb], qpar, kStatusWaitQ) || !waitb(&bar_q_full[1][qb], qpar, kStatusWaitQ)) {
-                        ok = false;
-                        break;
-                    }
+                    const uint64_t qa = kdesc(smem_u32(sQ + (x * p.nq + qb) * T::kBytes));
+                    if (!waitb(&bar_q_full[x][qb], (ju / p.nq) & 1, kStatusWaitQ)) { ok = false; break; }
                     if constexpr (BIAS == kBiasSam) {
                         const int st = ring % nst;
                         const uint32_t par = (ring / nst) & 1;
@@ -591,132 +594,86 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
-                        const uint64_t rw = kdesc(smem_u32(sRing + st * p.ring_stage_bytes));
-                        const uint64_t rh = kdesc(smem_u32(sRing + st * p.ring_stage_bytes + T::kBytes));
-                        const uint32_t id_w = make_idesc_f16(bf, kBlockM, p.n_rw, false);
-                        const uint32_t id_h = make_idesc_f16(bf, kBlockM, p.n_rh, false);
                         // G_h rewrites O_x: the previous job's epilogue must be done with it
-                        if (ju > 0 && !waitb(&bar_oempty[0], (ju - 1) & 1, kStatusWaitO)) { ok = false; break; }
-                        issue_qk<DPAD>(tS0, qa0, rw, id_w);
-                        issue_qk<DPAD>(tO0, qa0, rh, id_h);
-                        mma_commit(&bar_g[0]);
-                        if (ju > 0 && !waitb(&bar_oempty[1], (ju - 1) & 1, kStatusWaitO)) { ok = false; break; }
-                        issue_qk<DPAD>(tS1, qa1, rw, id_w);
-                        issue_qk<DPAD>(tO1, qa1, rh, id_h);
-                        mma_commit(&bar_g[1]);
+                        if (ju > 0 && !waitb(&bar_oempty[x], (ju - 1) & 1, kStatusWaitO)) { ok = false; break; }
+                        issue_qk<DPAD>(tSx, qa, kdesc(smem_u32(sRing + st * p.ring_stage_bytes)),
+                                       make_idesc_f16(bf, kBlockM, p.n_rw, false));
+                        issue_qk<DPAD>(tOx, qa, kdesc(smem_u32(sRing + st * p.ring_stage_bytes + T::kBytes)),
+                                       make_idesc_f16(bf, kBlockM, p.n_rh, false));
+                        mma_commit(&bar_g[x]);
                         mma_commit(&bar_empty[st]);
                         ++ring;
                     }
                     const int n = p.n_kv;
                     {
-                        // first score tiles of the job
                         const int st = ring % nst;
                         if (!waitb(&bar_full_k[st], (ring / nst) & 1, kStatusWaitK)) { ok = false; break; }
-                        const uint64_t ka = kdesc(smem_u32(sRing + st * p.ring_stage_bytes));
-                        // with the SAM bias, S_x rewrites the G_w values slot x is still gathering
-                        if (BIAS == kBiasSam && !waitb(&bar_gdone[0], ju & 1, kStatusWaitG)) { ok = false; break; }
-                        if (!s_free(0)) { ok = false; break; }
-                        issue_qk<DPAD>(tS0, qa0, ka, idesc_s);
-                        mma_commit(&bar_s[0]);
-                        ++s_cnt0;
-                        if (BIAS == kBiasSam && !waitb(&bar_gdone[1], ju & 1, kStatusWaitG)) { ok = false; break; }
-                        if (!s_free(1)) { ok = false; break; }
-                        issue_qk<DPAD>(tS1, qa1, ka, idesc_s);
-                        mma_commit(&bar_s[1]);
-                        ++s_cnt1;
+                        // with the SAM bias S_x rewrites the G_w values the slot is still gathering
+                        if (BIAS == kBiasSam && !waitb(&bar_gdone[x], ju & 1, kStatusWaitG)) { ok = false; break; }
+                        if (!s_free()) { ok = false; break; }
+                        issue_qk<DPAD>(tSx, qa, kdesc(smem_u32(sRing + st * p.ring_stage_bytes)), idesc_s);
+                        mma_commit(bs);
+                        ++s_cnt;
                     }
                     for (int j = 0; j < n; ++j) {
                         const int use = ring + j;
                         const int st = use % nst;
-                        const uint64_t va = vdesc(smem_u32(sRing + st * p.ring_stage_bytes + T::kBytes));
                         const int st1 = (use + 1) % nst;
                         const uint64_t ka1 = kdesc(smem_u32(sRing + st1 * p.ring_stage_bytes));
                         const bool last = j == n - 1;
                         if (kSepP && !last) {
-                            // next score tiles first: they overlap this tile's softmax
-                            if (!waitb(&bar_full_k[st1], ((use + 1) / nst) & 1, kStatusWaitK) || !s_free(0)) { ok = false; break; }
-                            issue_qk<DPAD>(tS0, qa0, ka1, idesc_s);
-                            mma_commit(&bar_s[0]);
-                            ++s_cnt0;
-                            if (!s_free(1)) { ok = false; break; }
-                            issue_qk<DPAD>(tS1, qa1, ka1, idesc_s);
-                            mma_commit(&bar_s[1]);
-                            ++s_cnt1;
+                            // next score tile first: it overlaps this tile's softmax
+                            if (!waitb(&bar_full_k[st1], ((use + 1) / nst) & 1, kStatusWaitK) || !s_free()) { ok = false; break; }
+                            issue_qk<DPAD>(tSx, qa, ka1, idesc_s);
+                            mma_commit(bs);
+                            ++s_cnt;
                         }
-                        // slot A: O_A += P_A.V_j
-                        if (!waitb(&bar_p[0], ph_p0, kStatusWaitP) || !waitb(&bar_full_v[st], (use / nst) & 1, kStatusWaitV)) {
+                        if (!waitb(bp, ph_p, kStatusWaitP) || !waitb(&bar_full_v[st], (use / nst) & 1, kStatusWaitV)) {
                             ok = false;
                             break;
                         }
-                        ph_p0 ^= 1;
-                        issue_pv(tO0, tP0, va, idesc_o, j > 0 ? 1u : 0u);
+                        ph_p ^= 1;
+                        issue_pv(tOx, tPx, vdesc(smem_u32(sRing + st * p.ring_stage_bytes + T::kBytes)), idesc_o,
+                                 j > 0 ? 1u : 0u);
                         if (last) {
-                            mma_commit(&bar_o[0]);
+                            mma_commit(bo);
+                            mma_commit(&bar_q_empty[x][qb]);
                         } else if (kSepP) {
-                            mma_commit(&bar_pvd[0]);
-                        }
-                        if (!kSepP && !last) {
-                            if (!waitb(&bar_full_k[st1], ((use + 1) / nst) & 1, kStatusWaitK)) { ok = false; break; }
-                            issue_qk<DPAD>(tS0, qa0, ka1, idesc_s);
-                            mma_commit(&bar_s[0]);
-                        }
-                        // slot B
-                        if (!waitb(&bar_p[1], ph_p1, kStatusWaitP)) { ok = false; break; }
-                        ph_p1 ^= 1;
-                        issue_pv(tO1, tP1, va, idesc_o, j > 0 ? 1u : 0u);
-                        if (last) {
-                            mma_commit(&bar_o[1]);
-                        } else if (kSepP) {
-                            mma_commit(&bar_pvd[1]);
+                            mma_commit(bpv);
                         }
                         mma_commit(&bar_empty[st]);
-                        if (last) {
-                            mma_commit(&bar_q_empty[0][qb]);
-                            mma_commit(&bar_q_empty[1][qb]);
-                        } else if (!kSepP) {
-                            issue_qk<DPAD>(tS1, qa1, ka1, idesc_s);
-                            mma_commit(&bar_s[1]);
+                        if (!kSepP && !last) {
+                            if (!waitb(&bar_full_k[st1], ((use + 1) / nst) & 1, kStatusWaitK)) { ok = false; break; }
+                            issue_qk<DPAD>(tSx, qa, ka1, idesc_s);
+                            mma_commit(bs);
+                            ++s_cnt;
                         }
                     }
                     ring += n;
                 } else {
-                    // separate mode: ring uses `ring` (tile 2*job, slot A) and `ring+1` (slot B)
-                    const int st0 = ring % nst, st1 = (ring + 1) % nst;
-                    const uint32_t qa0 = smem_u32(sRing + st0 * p.ring_stage_bytes);
-                    const uint32_t qa1 = smem_u32(sRing + st1 * p.ring_stage_bytes);
+                    // separate mode: this slot's tile of the job is ring use `ring + x`
+                    const int u = ring + x;
+                    const uint32_t qa = smem_u32(sRing + (u % nst) * p.ring_stage_bytes);
                     if (ju == 0) {
-                        if (!waitb(&bar_full_k[st0], (ring / nst) & 1, kStatusWaitK)) { ok = false; break; }
-                        sep_scores(tS0, 2 * job, qa0);
-                        mma_commit(&bar_s[0]);
-                        ++s_cnt0;
-                        if (!waitb(&bar_full_k[st1], ((ring + 1) / nst) & 1, kStatusWaitK)) { ok = false; break; }
-                        sep_scores(tS1, 2 * job + 1, qa1);
-                        mma_commit(&bar_s[1]);
-                        ++s_cnt1;
+                        if (!waitb(&bar_full_k[u % nst], (u / nst) & 1, kStatusWaitK)) { ok = false; break; }
+                        sep_scores(2 * job + x, qa);
+                        mma_commit(bs);
+                        ++s_cnt;
                     }
                     const int next = job + job_step;
                     if (next < p.n_jobs) {
-                        // next tiles' scores first: they overlap this tile's softmax
-                        const int u2 = ring + 2, u3 = ring + 3;
-                        if (!waitb(&bar_full_k[u2 % nst], (u2 / nst) & 1, kStatusWaitK) || !s_free(0)) { ok = false; break; }
-                        sep_scores(tS0, 2 * next, smem_u32(sRing + (u2 % nst) * p.ring_stage_bytes));
-                        mma_commit(&bar_s[0]);
-                        ++s_cnt0;
-                        if (!waitb(&bar_full_k[u3 % nst], (u3 / nst) & 1, kStatusWaitK) || !s_free(1)) { ok = false; break; }
-                        sep_scores(tS1, 2 * next + 1, smem_u32(sRing + (u3 % nst) * p.ring_stage_bytes));
-                        mma_commit(&bar_s[1]);
-                        ++s_cnt1;
+                        // next tile's scores first: they overlap this tile's softmax
+                        const int u2 = u + 2;
+                        if (!waitb(&bar_full_k[u2 % nst], (u2 / nst) & 1, kStatusWaitK) || !s_free()) { ok = false; break; }
+                        sep_scores(2 * next + x, smem_u32(sRing + (u2 % nst) * p.ring_stage_bytes));
+                        mma_commit(bs);
+                        ++s_cnt;
                     }
-                    if (!waitb(&bar_p[0], ph_p0, kStatusWaitP)) { ok = false; break; }
-                    ph_p0 ^= 1;
-                    issue_pv(tO0, tP0, vdesc(qa0 + 2 * T::kBytes), idesc_o, 0u);
-                    mma_commit(&bar_empty[st0]);
-                    mma_commit(&bar_o[0]);
-                    if (!waitb(&bar_p[1], ph_p1, kStatusWaitP)) { ok = false; break; }
-                    ph_p1 ^= 1;
-                    issue_pv(tO1, tP1, vdesc(qa1 + 2 * T::kBytes), idesc_o, 0u);
-                    mma_commit(&bar_empty[st1]);
-                    mma_commit(&bar_o[1]);
+                    if (!waitb(bp, ph_p, kStatusWaitP)) { ok = false; break; }
+                    ph_p ^= 1;
+                    issue_pv(tOx, tPx, vdesc(qa + 2 * T::kBytes), idesc_o, 0u);
+                    mma_commit(&bar_empty[u % nst]);
+                    mma_commit(bo);
                     ring += 2;
                 }
             }
@@ -941,16 +898,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m_tile = row_max<128>(xs);
                         sc = 1.0f;
                     }
-                    if (kSepP && j > 0) {
-                        // P_x and O_x are rewritten below: the previous P.V must be done
+                    // With separate P buffers the previous P.V may still be running:
+                    // it must be done before O is rescaled or P_x rewritten.
+                    bool pv_waited = !(kSepP && j > 0);
+                    auto wait_pv = [&]() -> bool {
+                        if (pv_waited) return true;
+                        pv_waited = true;
                         __syncwarp();
-                        if (!__all_sync(0xffffffffu, mbar_wait(&bar_pvd[x], pvd_cnt & 1, abort_flag, kStatusWaitO))) { ok = false; break; }
+                        if (!__all_sync(0xffffffffu, mbar_wait(&bar_pvd[x], pvd_cnt & 1, abort_flag, kStatusWaitO))) return false;
                         ++pvd_cnt;
                         tc_fence_after();
-                    }
+                        return true;
+                    };
                     const float m_new = fmaxf(m_run, m_tile);
                     const bool need = m_new > m_run + kRescaleThreshold;
-                    if (__any_sync(0xffffffffu, need && j > 0)) {
+                    const bool any_rescale = __any_sync(0xffffffffu, need && j > 0);
+                    if (any_rescale && !wait_pv()) { ok = false; break; }
+                    if (any_rescale) {
                         // O holds the earlier tiles' P.V, complete (with a shared P/S
                         // buffer this score tile was committed after it)
                         const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
@@ -973,6 +937,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
                     uint32_t pk[64];
                     l_run += exp_pack<128>(xs, sc, -m_use, bf, pk);
+                    if (!wait_pv()) { ok = false; break; }
                     tmem_st64(tP, pk);
                     tmem_st_wait();
                     tc_fence_before();
