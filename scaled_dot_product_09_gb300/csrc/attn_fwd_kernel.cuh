@@ -175,6 +175,38 @@ __device__ __forceinline__ uint16_t to_half_bits(float v, bool bf16) {
     return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
 }
 
+// Eight consecutive K-elements of a K-major row, rounded to the operand type,
+// as one 16-byte shared-memory store.
+__device__ __forceinline__ void store_half8(unsigned char* dst, const float* v, bool bf16) {
+    uint32_t w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        w[u] = (uint32_t)to_half_bits(v[2 * u], bf16) | ((uint32_t)to_half_bits(v[2 * u + 1], bf16) << 16);
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Eight columns t0..t0+7 of row j (a key token) of a Swin table block:
+// column t holds table[idx(t, j), h] * f, idx the relative-position index
+// ("视觉大模型训练和推理加速" section 一, relative position bias):
+// (dr + M - 1)(2M - 1) + (dc + M - 1) with dr, dc the row / column offsets of
+// query token t from key token j, i.e. pos(t) - pos(j) + (M - 1)(2M) with
+// pos(t) = r_t (2M - 1) + c_t. tok[] holds pos in its low 16 bits. The eight
+// gathers are issued together; out-of-window entries are zeroed afterwards.
+__device__ __forceinline__ void swin_table_group(unsigned char* dst, const float* tab, const int* tok, int t0,
+                                                 int pos_j, bool key_ok, int h, int H, int M, int N, float f,
+                                                 bool bf16) {
+    const int c0 = 2 * M * (M - 1) - pos_j;
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int idx = (key_ok && t0 + u < N) ? (tok[t0 + u] & 0xFFFF) + c0 : 0;
+        v[u] = tab[idx * H + h];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = (key_ok && t0 + u < N) ? v[u] * f : 0.f;
+    store_half8(dst, v, bf16);
+}
+
 // Barrel shift of a 128-entry register row: afterwards v[u] = v_in[u + sh]
 // for every u with u + sh < 128 (0 <= sh < 128).  Unrolled selects keep the
 // row in registers.
@@ -314,8 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kSepP = DPAD <= 64 && BIAS != kBiasSam;
     static_assert(MODE == kModeShared || kSepP, "the packed tiling uses separate P buffers");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char* smem =
-        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1 KB-aligned base, formed by offsetting the array itself so that the
+    // compiler keeps every derived access in the shared state space
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* sQ = smem + p.off_q;        // shared mode: [slot][buffer] Q tiles
     unsigned char* sRing = smem + p.off_ring;  // ring stages
     unsigned char* sExtraB = smem + p.off_extra;
@@ -328,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint64_t bar_final;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
+    __shared__ int s_tok[128];  // Swin: per-token position and region labels
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -369,13 +403,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&tm.rw);
         }
     }
-    if constexpr (MODE == kModeSeparate) {
-        // Slot rows past the slice length are never written by the TMA; they
-        // must read as zero in the MMAs.
-        const int total = (int)((p.off_extra - p.off_ring) / 16);
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int i = tid; i < total; i += kThreads) reinterpret_cast<uint4*>(sRing)[i] = z;
-    }
     if constexpr (BIAS == kBiasSwin) {
         // Qone [128][SL]: row r has a single 1 at column r mod SL.
         // Blocks [SL][SL] (row = key token j, column = query token t):
@@ -383,34 +410,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         //   H + kind - 1 : -100 / scale where t and j fall in different regions
         //                  of a window on the last column (kind 1), last row
         //                  (kind 2) or both (kind 3)
-        const int M = p.win, N = p.Nk;
+        // Slot rows past the slice length need no clearing: the TMA box covers
+        // them and fills them with zeros.
+        const int M = p.win, N = p.Nk, T = 2 * M - 1;
         const float f = DBG ? 1.0f : 1.0f / p.scale;
-        uint16_t* qone = reinterpret_cast<uint16_t*>(sExtraB);
-        const uint16_t one = to_half_bits(1.0f, bf);
-        for (int i = tid; i < kBlockM * SL; i += kThreads) {
-            const int r = i / SL, t = i % SL;
-            qone[kmajor_offset(kBlockM, r, t) / 2] = (t == r % SL) ? one : (uint16_t)0;
-        }
+        unsigned char* qone_b = sExtraB;
+        unsigned char* blocks_b = sExtraB + kBlockM * SL * 2;
+        // the table goes through shared memory (the Qone area, built last) when
+        // it fits, so each thread's gathers are shared-memory loads
+        const int ntab = T * T * p.H;
+        const bool tab_smem = ntab * 4 <= kBlockM * SL * 2;
+        float* stab = reinterpret_cast<float*>(qone_b);
+        if (tab_smem)
+            for (int i = tid; i < ntab; i += kThreads) stab[i] = p.table[i];
+        __syncthreads();
+        const float* tab = tab_smem ? stab : p.table;
         const int nblk = p.H + 3;
-        uint16_t* blocks = reinterpret_cast<uint16_t*>(sExtraB + kBlockM * SL * 2);
+        // per query/key token: pos = r (2M - 1) + c, region labels of the
+        // token in a window on the last column (bits 16-17) and last row
+        // (bits 18-19)
         const int yb = (p.n_wh - 1) * M, xb = (p.n_ww - 1) * M;  // last window row / column origin
-        for (int i = tid; i < nblk * SL * SL; i += kThreads) {
-            const int b = i / (SL * SL), j = (i / SL) % SL, t = i % SL;
-            float v = 0.f;
-            if (j < N && t < N) {
-                const int rt = t / M, ct = t % M, rj = j / M, cj = j % M;
-                if (b < p.H) {
-                    const int idx = (rt - rj + M - 1) * (2 * M - 1) + (ct - cj + M - 1);
-                    v = p.table[idx * p.H + b] * f;
-                } else if (p.shift) {
-                    const int kind = b - p.H + 1;
-                    bool same = true;
-                    if (kind & 1) same = same && swin_strip(xb + ct, p.grid_w, M, p.shift) == swin_strip(xb + cj, p.grid_w, M, p.shift);
-                    if (kind & 2) same = same && swin_strip(yb + rt, p.grid_h, M, p.shift) == swin_strip(yb + rj, p.grid_h, M, p.shift);
-                    v = same ? 0.f : -100.0f * f;
+        for (int t = tid; t < SL; t += kThreads) {
+            const int rt = t / M, ct = t - (t / M) * M;
+            const int lab = swin_strip(xb + ct, p.grid_w, M, p.shift) | (swin_strip(yb + rt, p.grid_h, M, p.shift) << 2);
+            s_tok[t] = (rt * T + ct) | (lab << 16);
+        }
+        __syncthreads();
+        // one work item = 8 columns of one row (key token j) of one block
+        for (int w = tid; w < nblk * SL * (SL / 8); w += kThreads) {
+            const int j = w % SL, g = (w / SL) % (SL / 8), b = w / (SL * (SL / 8));
+            const int t0 = g * 8;
+            const bool key_ok = j < N;
+            const int tj = s_tok[j];
+            unsigned char* dst = blocks_b + b * SL * SL * 2 + kmajor_offset(SL, j, t0);
+            if (b < p.H) {
+                if (tab_smem) swin_table_group(dst, stab, s_tok, t0, tj & 0xFFFF, key_ok, b, p.H, M, N, f, bf);
+                else swin_table_group(dst, p.table, s_tok, t0, tj & 0xFFFF, key_ok, b, p.H, M, N, f, bf);
+            } else {
+                // mask blocks 1..3: -100 where t and j carry different region
+                // labels along the axes the window kind cuts
+                const int kind = b - p.H + 1;
+                const int sel = ((kind & 1) ? 0x3 : 0) | ((kind & 2) ? 0xC : 0);
+                const float mv = -100.0f * f;
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const bool diff = ((((s_tok[t0 + u] ^ tj) >> 16) & sel) != 0);
+                    v[u] = (key_ok && t0 + u < N && p.shift && diff) ? mv : 0.f;
                 }
+                store_half8(dst, v, bf);
             }
-            blocks[(b * SL * SL * 2 + kmajor_offset(SL, j, t)) / 2] = to_half_bits(v, bf);
+        }
+        __syncthreads();  // the table's area becomes Qone
+        const uint32_t one = to_half_bits(1.0f, bf);
+        for (int c = tid; c < kBlockM * SL / 8; c += kThreads) {
+            const int r = c / (SL / 8), t0 = (c - r * (SL / 8)) * 8;
+            const int e = (r % SL) - t0;  // position of the 1 in this chunk, if any
+            uint32_t pk[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                pk[u] = (e == 2 * u ? one : 0u) | (e == 2 * u + 1 ? one << 16 : 0u);
+            *reinterpret_cast<uint4*>(qone_b + kmajor_offset(kBlockM, r, t0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
     }
     if constexpr (MODE == kModeSeparate) fence_proxy_async_smem();
