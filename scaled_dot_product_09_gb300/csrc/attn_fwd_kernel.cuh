@@ -112,16 +112,24 @@ struct AttnParams {
     const float* table;  // [(2M-1)^2][H]
     int win, grid_h, grid_w, shift, n_w, n_ww, n_wh;
     uint32_t fd_h[2], fd_w[2], fd_ww[2];  // magic/shift pairs dividing by H, n_w, n_ww
+    int swin_rows;  // 1: bias rows in shared memory, added by the softmax; 0: added by MMAs
     // SAM
     int s_h, s_w, n_rh, n_rw;
 };
 
 // Shared memory after the ring ("extra"):
-//   Swin (separate mode, slot SL): Qone [128 rows][SL] then H + 3 bias blocks
+//   Swin (separate mode, slot SL), rows variant: per head an fp32 bias matrix
+//        [SL query tokens][SL key tokens] (16-byte chunks of a row XOR-swizzled
+//        by the row's low 3 bits), then region-difference bits
+//        [3 window kinds][SL query tokens][SL / 32 words]
+//   Swin, MMA variant: Qone [128 rows][SL] then H + 3 bias blocks
 //        [SL][SL] (per-head tables, then last-column / last-row / corner
 //        masks), all 16-bit K-major 32B-swizzled
 //   SAM : rel_h [2 slots][s_h][128] fp32, then for generic grids rel_w
 //        [2][s_w][128] and a key table [Nk]
+__host__ __device__ constexpr uint32_t swin_rows_extra_bytes(int sl, int H) {
+    return (uint32_t)(H * sl * sl * 4 + 3 * sl * (sl / 32) * 4);
+}
 __host__ __device__ constexpr uint32_t swin_extra_bytes(int sl, int H) {
     return (uint32_t)(128 * sl * 2 + (H + 3) * sl * sl * 2);
 }
@@ -151,6 +159,20 @@ struct Tile {
 // valid for n < 2^31.
 __device__ __forceinline__ uint32_t fast_div(uint32_t n, const uint32_t (&fd)[2]) {
     return (__umulhi(n, fd[0]) + n) >> fd[1];
+}
+
+// Head and window kind (0 interior, 1 last window column, 2 last window row,
+// 3 corner; 0 for every window without a shift) of a Swin slice: slices run
+// head-fastest over windows numbered row-major within each image.
+__device__ __forceinline__ void swin_slice_info(uint32_t slice, int H, int n_w, int n_ww, int n_wh, int shift,
+                                                const uint32_t (&fd_h)[2], const uint32_t (&fd_w)[2],
+                                                const uint32_t (&fd_ww)[2], int& h, int& kind) {
+    const uint32_t bimg = fast_div(slice, fd_h);
+    h = (int)(slice - bimg * (uint32_t)H);
+    const uint32_t w = bimg - fast_div(bimg, fd_w) * (uint32_t)n_w;
+    const uint32_t wr = fast_div(w, fd_ww);
+    const uint32_t wc = w - wr * (uint32_t)n_ww;
+    kind = shift ? (((int)wc == n_ww - 1 ? 1 : 0) | ((int)wr == n_wh - 1 ? 2 : 0)) : 0;
 }
 
 __device__ __forceinline__ int swin_strip(int pos, int G, int M, int s) {
@@ -218,6 +240,52 @@ __device__ __forceinline__ void shift_down(float (&v)[128], int sh) {
 #pragma unroll
         for (int u = 0; u + step < 128; ++u) v[u] = on ? v[u + step] : v[u];
     }
+}
+
+// xs[c] = xs[c] * scale_log2 + bias row c (+ -100 log2(e) where the region
+// bit of column c is set, MASK), the row read as float4 chunks XOR-swizzled by
+// swz. With DBG the bias is in natural units and also written to dbg_row.
+template <int SL, bool MASK, bool DBG>
+__device__ __forceinline__ void swin_add_bias_row(float (&xs)[SL], const unsigned char* rowp, int swz,
+                                                  const uint32_t* mrow, float scale_log2, float* dbg_row, int nk) {
+    const float mneg = DBG ? -100.0f : -100.0f * kLog2e;
+    const float2 s2 = make_float2(scale_log2, scale_log2);
+#pragma unroll
+    for (int wd = 0; wd < SL / 32; ++wd) {
+        const uint32_t mb = MASK ? mrow[wd] : 0u;
+#pragma unroll
+        for (int q = wd * 8; q < wd * 8 + 8; ++q) {
+            const float4 b4 = *reinterpret_cast<const float4*>(rowp + ((q ^ swz) << 4));
+            float b[4] = {b4.x, b4.y, b4.z, b4.w};
+            if constexpr (MASK) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if ((mb >> (4 * (q - wd * 8) + e)) & 1u) b[e] += mneg;
+            }
+            if constexpr (DBG) {
+                if (dbg_row) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (4 * q + e < nk) dbg_row[4 * q + e] = b[e];
+                }
+            }
+            const float2 y0 = __ffma2_rn(make_float2(xs[4 * q], xs[4 * q + 1]), s2, make_float2(b[0], b[1]));
+            const float2 y1 = __ffma2_rn(make_float2(xs[4 * q + 2], xs[4 * q + 3]), s2, make_float2(b[2], b[3]));
+            xs[4 * q] = y0.x;
+            xs[4 * q + 1] = y0.y;
+            xs[4 * q + 2] = y1.x;
+            xs[4 * q + 3] = y1.y;
+        }
+    }
+}
+
+// Store N (16, 32 or 64) consecutive TMEM columns of this lane.
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[N]) {
+    static_assert(N == 16 || N == 32 || N == 64, "columns");
+    if constexpr (N == 16) tmem_st16(taddr, v);
+    else if constexpr (N == 32) tmem_st32(taddr, v);
+    else tmem_st64(taddr, v);
 }
 
 // Load N (multiple of 16, <= 128) consecutive TMEM columns of this lane.
@@ -344,6 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // its softmax has read the current one, overlapping Q.K^T with the
     // softmax.  Larger head dims keep P over the first half of S.
     constexpr bool kSepP = DPAD <= 64 && BIAS != kBiasSam;
+    // Packed tiling with head dims up to 32 and slots up to 64 rows: two O
+    // buffers per slot (O_x holds 64 columns), so a tile's output is written
+    // while the next tile's P.V runs.
+    constexpr bool kDblO = MODE == kModeSeparate && DPAD <= 32 && SL <= 64;
     static_assert(MODE == kModeShared || kSepP, "the packed tiling uses separate P buffers");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1 KB-aligned base, formed by offsetting the array itself so that the
@@ -403,7 +475,58 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&tm.rw);
         }
     }
-    if constexpr (BIAS == kBiasSwin) {
+    if (BIAS == kBiasSwin && SL <= 64 && p.swin_rows) {
+        // Per head h: row i (query token), column j (key token) holds
+        // table[idx(i, j), h] in log2 units (natural units when debugging);
+        // idx is the relative-position index ("视觉大模型训练和推理加速"
+        // section 一, relative position bias), pos(i) - pos(j) + 2M(M - 1)
+        // with pos(t) = r_t (2M - 1) + c_t. Then, per window kind k = 1..3,
+        // bit j of row i is set when i and j fall in different regions of the
+        // shifted window (cut by the last column (k = 1), the last row (k = 2)
+        // or both (k = 3)): those pairs get -100 more.
+        const int M = p.win, N = p.Nk, T = 2 * M - 1;
+        const float fl = DBG ? 1.0f : kLog2e;
+        const int yb = (p.n_wh - 1) * M, xb = (p.n_ww - 1) * M;  // last window row / column origin
+        for (int t = tid; t < SL; t += kThreads) {
+            const int rt = t / M, ct = t - (t / M) * M;
+            const int lab = swin_strip(xb + ct, p.grid_w, M, p.shift) | (swin_strip(yb + rt, p.grid_h, M, p.shift) << 2);
+            s_tok[t] = (rt * T + ct) | (lab << 16);
+        }
+        // the table passes through the (not yet loaded) ring
+        float* stab = reinterpret_cast<float*>(smem + p.off_ring);
+        for (int i = tid; i < T * T * p.H; i += kThreads) stab[i] = p.table[i];
+        __syncthreads();
+        const int c0 = 2 * M * (M - 1);
+        for (int w = tid; w < p.H * SL * (SL / 4); w += kThreads) {
+            const int q = w % (SL / 4), i = (w / (SL / 4)) % SL, h = w / (SL * (SL / 4));
+            const int pi = s_tok[i] & 0xFFFF;
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = 4 * q + e;
+                const bool ok = i < N && j < N;
+                const int idx = ok ? pi - (s_tok[j] & 0xFFFF) + c0 : 0;
+                v[e] = stab[idx * p.H + h];
+                v[e] = ok ? v[e] * fl : 0.f;
+            }
+            *reinterpret_cast<float4*>(sExtraB + (h * SL + i) * SL * 4 + ((q ^ (i & 7)) << 4)) =
+                make_float4(v[0], v[1], v[2], v[3]);
+        }
+        uint32_t* mbits = reinterpret_cast<uint32_t*>(sExtraB + p.H * SL * SL * 4);
+        for (int w = tid; w < 3 * SL * (SL / 32); w += kThreads) {
+            const int wd = w % (SL / 32), i = (w / (SL / 32)) % SL, kind = w / (SL * (SL / 32)) + 1;
+            const int sel = ((kind & 1) ? 0x3 : 0) | ((kind & 2) ? 0xC : 0);
+            const int li = s_tok[i] >> 16;
+            uint32_t bits = 0;
+            if (i < N && p.shift) {
+                for (int e = 0; e < 32; ++e) {
+                    const int j = wd * 32 + e;
+                    if (j < N && (((s_tok[j] >> 16) ^ li) & sel)) bits |= 1u << e;
+                }
+            }
+            mbits[w] = bits;
+        }
+    } else if constexpr (BIAS == kBiasSwin) {
         // Qone [128][SL]: row r has a single 1 at column r mod SL.
         // Blocks [SL][SL] (row = key token j, column = query token t):
         //   h < H        : table[idx(t, j), h] / scale      (natural units when debugging)
@@ -625,17 +748,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // S of packed tile `tile` (separate mode), with the Swin bias
             auto sep_scores = [&](int tile, uint32_t qa) {
-                if (!DBG || BIAS != kBiasSwin) issue_qk<DPAD>(tSx, kdesc(qa), kdesc(qa + T::kBytes), idesc_s);
-                if constexpr (BIAS == kBiasSwin) {
+                if (!DBG || BIAS != kBiasSwin || (SL <= 64 && p.swin_rows))
+                    issue_qk<DPAD>(tSx, kdesc(qa), kdesc(qa + T::kBytes), idesc_s);
+                if (BIAS == kBiasSwin && !(SL <= 64 && p.swin_rows)) {
                     for (int sl = 0; sl < p.g; ++sl) {
                         const uint32_t slice = (uint32_t)(tile * p.g + sl);
                         if ((int)slice >= p.BH) break;
-                        const uint32_t bimg = fast_div(slice, p.fd_h);
-                        const uint32_t h = slice - bimg * (uint32_t)p.H;
-                        const uint32_t w = bimg - fast_div(bimg, p.fd_w) * (uint32_t)p.n_w;
-                        const uint32_t wr = fast_div(w, p.fd_ww);
-                        const uint32_t wc = w - wr * (uint32_t)p.n_ww;
-                        const int kind = p.shift ? (((int)wc == p.n_ww - 1 ? 1 : 0) | ((int)wr == p.n_wh - 1 ? 2 : 0)) : 0;
+                        int h, kind;
+                        swin_slice_info(slice, p.H, p.n_w, p.n_ww, p.n_wh, p.shift, p.fd_h, p.fd_w, p.fd_ww, h, kind);
                         const uint32_t d = tSx + sl * SL;
                         issue_bias<SL>(d, qone_d, kdesc(blocks + h * SL * SL * 2), idesc_b, DBG ? 0u : 1u);
                         if (kind) issue_bias<SL>(d, qone_d, kdesc(blocks + (p.H + kind - 1) * SL * SL * 2), idesc_b, 1u);
@@ -731,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (!waitb(bp, ph_p, kStatusWaitP)) { ok = false; break; }
                     ph_p ^= 1;
-                    issue_pv(tOx, tPx, vdesc(qa + 2 * T::kBytes), idesc_o, 0u);
+                    issue_pv(tOx + (kDblO ? (uint32_t)((ju & 1) * DPAD) : 0u), tPx, vdesc(qa + 2 * T::kBytes), idesc_o, 0u);
                     mma_commit(&bar_empty[u % nst]);
                     mma_commit(bo);
                     ring += 2;
@@ -763,6 +883,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             sam_rw = sExtra + 2 * p.s_h * kBlockM + x * (p.s_w * kBlockM);
             sam_kt = reinterpret_cast<const int*>(sExtra + 2 * (p.s_h + p.s_w) * kBlockM);
         }
+
+        // O / l rounded to the output type and stored (row-per-thread, 16 bytes at a time)
+        auto epilogue = [&](uint32_t tObuf, float l, int slice, int tok, bool rok) {
+            const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+            uint32_t o[DPAD / 2];
+            {
+                uint32_t v[DPAD];
+                tmem_ld_cols<DPAD>(tObuf, v);
+                if (bf) {
+#pragma unroll
+                    for (int t = 0; t < DPAD; t += 2)
+                        o[t / 2] = pack_bf16(__uint_as_float(v[t]) * inv_l, __uint_as_float(v[t + 1]) * inv_l);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < DPAD; t += 2)
+                        o[t / 2] = pack_f16(__uint_as_float(v[t]) * inv_l, __uint_as_float(v[t + 1]) * inv_l);
+                }
+            }
+            if constexpr (BIAS == kBiasSam) {
+                // O_x is free for the next job's G_h
+                tc_fence_before();
+                warp_arrive(&bar_oempty[x]);
+            }
+            if (rok && !DBG) {
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(p.out) +
+                                                      ((size_t)slice * p.Nq + tok) * (size_t)p.d * 2);
+#pragma unroll
+                for (int c = 0; c < DPAD / 8; ++c)
+                    if (c * 8 < p.d) dst[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            }
+        };
+        // the previous job's row (pipelined epilogue)
+        float pv_l = 0.f;
+        int pv_slice = 0, pv_tok = 0;
+        bool pv_ok = false;
 
         for (int job = job0; ok && job < p.n_jobs; job += job_step, ++ju) {
             // ------------------------------------------------- row of this job
@@ -798,7 +953,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 warp_arrive(&bar_sfree[x]);
                 const int nk = p.Nk;
-                if constexpr (DBG) {
+                float sc = p.scale_log2;  // multiplier of xs in the exponent
+                if (BIAS == kBiasSwin && SL <= 64 && p.swin_rows) {
+                    // xs = s * scale * log2(e) + bias row (+ region mask), log2 units
+                    int h, kind;
+                    swin_slice_info((uint32_t)min(my_slice, p.BH - 1), p.H, p.n_w, p.n_ww, p.n_wh, p.shift, p.fd_h,
+                                    p.fd_w, p.fd_ww, h, kind);
+                    const unsigned char* rowp = sExtraB + (h * SL + my_tok) * SL * 4;
+                    float* dbg_row = (DBG && row_ok) ? p.dbg + ((size_t)my_slice * p.Nq + my_tok) * p.Nk : nullptr;
+                    if (kind) {
+                        const uint32_t* mrow = reinterpret_cast<const uint32_t*>(sExtraB + p.H * SL * SL * 4) +
+                                               ((kind - 1) * SL + my_tok) * (SL / 32);
+                        swin_add_bias_row<SL, true, DBG>(xs, rowp, my_tok & 7, mrow, p.scale_log2, dbg_row, nk);
+                    } else {
+                        swin_add_bias_row<SL, false, DBG>(xs, rowp, my_tok & 7, nullptr, p.scale_log2, dbg_row, nk);
+                    }
+                    sc = 1.0f;
+                } else if constexpr (DBG) {
                     // the scores hold only the bias when debugging (no Q.K^T)
                     if (row_ok) {
                         float* dst = p.dbg + ((size_t)my_slice * p.Nq + my_tok) * p.Nk;
@@ -816,22 +987,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (c0 + t >= nk) xs[c0 + t] = -INFINITY;
                     }
                 }
-                const float m = row_max<SL>(xs) * p.scale_log2;
+                const float m = row_max<SL>(xs) * sc;
                 const float m_use = (m == -INFINITY) ? 0.f : m;
-                uint32_t pk[64];
-#pragma unroll
-                for (int t = 0; t < 64; ++t) pk[t] = 0u;  // other slots' keys: probability 0
                 uint32_t own[SL / 2];
-                l_run = exp_pack<SL>(xs, p.scale_log2, -m_use, bf, own);
+                l_run = exp_pack<SL>(xs, sc, -m_use, bf, own);
+                if constexpr (kDblO) {
+                    // the previous tile's output, while this tile's P waits in
+                    // registers: its P.V has run during this tile's softmax
+                    if (ju > 0) {
+                        __syncwarp();
+                        if (!__all_sync(0xffffffffu, mbar_wait(&bar_o[x], (ju - 1) & 1, abort_flag, kStatusWaitO))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_slice, pv_tok, pv_ok);
+                    }
+                }
+                if (ju == 0) {
+                    // a row's columns outside its own slice stay zero from here on:
+                    // only this row's thread writes them
+                    uint32_t pk[64];
 #pragma unroll
-                for (int s = 0; s < 128 / SL; ++s)
-                    if (s == my_sl)
+                    for (int t = 0; t < 64; ++t) pk[t] = 0u;
 #pragma unroll
-                        for (int t = 0; t < SL / 2; ++t) pk[s * (SL / 2) + t] = own[t];
-                tmem_st64(tP, pk);
+                    for (int s = 0; s < 128 / SL; ++s)
+                        if (s == my_sl)
+#pragma unroll
+                            for (int t = 0; t < SL / 2; ++t) pk[s * (SL / 2) + t] = own[t];
+                    tmem_st64(tP, pk);
+                } else {
+                    tmem_st_cols<SL / 2>(tP + (uint32_t)(my_sl * (SL / 2)), own);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 warp_arrive(&bar_p[x]);
+                if constexpr (kDblO) {
+                    pv_l = l_run;
+                    pv_slice = my_slice;
+                    pv_tok = my_tok;
+                    pv_ok = row_ok;
+                    continue;
+                }
             } else {
                 // ------------------------------------------------- bias row setup
                 float sam_rw_reg[SW > 0 ? SW : 1];
@@ -1010,31 +1207,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_o[x], ju & 1, abort_flag, kStatusWaitO))) { ok = false; break; }
             tc_fence_after();
-            const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
-            uint32_t o[DPAD / 2];
-            {
-                uint32_t v[DPAD];
-                tmem_ld_cols<DPAD>(tO, v);
-                if (bf) {
-#pragma unroll
-                    for (int t = 0; t < DPAD; t += 2)
-                        o[t / 2] = pack_bf16(__uint_as_float(v[t]) * inv_l, __uint_as_float(v[t + 1]) * inv_l);
-                } else {
-#pragma unroll
-                    for (int t = 0; t < DPAD; t += 2)
-                        o[t / 2] = pack_f16(__uint_as_float(v[t]) * inv_l, __uint_as_float(v[t + 1]) * inv_l);
+            epilogue(tO, l_run, my_slice, my_tok, row_ok);
+        }
+        if constexpr (kDblO) {
+            if (ok && ju > 0) {
+                __syncwarp();
+                if (__all_sync(0xffffffffu, mbar_wait(&bar_o[x], (ju - 1) & 1, abort_flag, kStatusWaitO))) {
+                    tc_fence_after();
+                    epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_slice, pv_tok, pv_ok);
                 }
-            }
-            if constexpr (BIAS == kBiasSam) {
-                tc_fence_before();
-                warp_arrive(&bar_oempty[x]);
-            }
-            if (row_ok && !DBG) {
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(p.out) +
-                                                      ((size_t)my_slice * p.Nq + my_tok) * (size_t)p.d * 2);
-#pragma unroll
-                for (int c = 0; c < DPAD / 8; ++c)
-                    if (c * 8 < p.d) dst[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
             }
         }
     }

@@ -208,6 +208,8 @@ int sm_count() {
 // Dynamic shared memory left for the kernel's buffers after the 1 KB
 // alignment pad and its static barriers.
 constexpr size_t kSmemBudget = 227 * 1024 - 1024 - 1024;
+// largest Swin bias-row area (per-head fp32 matrices + region bits)
+constexpr size_t kSwinRowsMax = 96 * 1024;
 
 int run(const void* q, const void* k, const void* v, void* out, float* dbg, int B, int H, int Nq,
         int Nk, int d, float scale, attn_dtype dtype, attn_bias_kind bias_kind,
@@ -312,8 +314,16 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         p.box_q = sl;
         p.box_kv = sl;
         p.nq = 0;
-        if (bias == kBiasSwin) extra = swin_extra_bytes(sl, H);
         p.ring_stage_bytes = (uint32_t)(3 * tile_bytes);
+        if (bias == kBiasSwin) {
+            // bias rows read by the softmax for windows up to 64 tokens when they
+            // fit (and the table fits the first two ring stages, where it is
+            // staged), else bias MMAs
+            const size_t rows = swin_rows_extra_bytes(sl, H);
+            const size_t table = (size_t)(2 * p.win - 1) * (2 * p.win - 1) * H * 4;
+            p.swin_rows = (sl <= 64 && rows <= kSwinRowsMax && table <= 2 * (size_t)p.ring_stage_bytes) ? 1 : 0;
+            extra = p.swin_rows ? rows : swin_extra_bytes(sl, H);
+        }
         const size_t avail = kSmemBudget > extra ? kSmemBudget - extra : 0;
         p.nst = (int)std::min<size_t>(kMaxStages, avail / p.ring_stage_bytes);
         if (p.nst < 2) return fail(ATTN_ERR_UNSUPPORTED, "shared memory too small for the packed tiling (H=%d)", H);

@@ -37,6 +37,24 @@ def test_swin_no_shift():
     full_parity(W["swin_t_stage1"].with_(B=64, shift=0, seed=12))
 
 
+def test_swin_many_heads():
+    # Swin-T stage 2 shape (28x28 tokens, 16 windows, 6 heads): the per-head
+    # bias rows exceed their shared-memory area, the bias goes through MMAs
+    full_parity(W["swin_t_stage1"].with_(B=2 * 16, H=6, grid_h=28, grid_w=28, seed=13))
+
+
+def test_swin_small_window():
+    # 4x4 windows (16 tokens, 32-row slots), shift 2
+    full_parity(W["swin_t_stage1"].with_(B=2 * 16, H=3, win=4, Nq=16, Nk=16, grid_h=16, grid_w=16,
+                                          shift=2, seed=14))
+
+
+def test_swin_large_window():
+    # 10x10 windows (100 tokens, one slice per 128-row tile), shift 5
+    full_parity(W["swin_t_stage1"].with_(B=2 * 4, H=1, win=10, Nq=100, Nk=100, grid_h=20, grid_w=20,
+                                          shift=5, seed=15))
+
+
 def test_sam_window_reduced_full():
     full_parity(W["sam_vith_window"].with_(B=3))
 
@@ -111,11 +129,21 @@ def test_output_not_aliasing_and_repeatable():
 
 # ------------------------------------------------------- bias bit-exactness --
 
-def test_swin_bias_indexing_bit_exact():
-    """table[r, h] = r + 256*h is exact in fp32: the in-kernel gather must
-    return index + 256*h (+ -100 across regions) exactly."""
+SWIN_BIAS_CASES = {
+    "rows": dict(B=64),
+    "mma_many_heads": dict(B=16, H=6, grid_h=28, grid_w=28),
+    "rows_small_window": dict(B=16, win=4, Nq=16, Nk=16, grid_h=16, grid_w=16, shift=2),
+    "mma_large_window": dict(B=4, H=1, win=10, Nq=100, Nk=100, grid_h=20, grid_w=20, shift=5),
+}
+
+
+@pytest.mark.parametrize("case", sorted(SWIN_BIAS_CASES))
+def test_swin_bias_indexing_bit_exact(case):
+    """table[r, h] = r + 256*h is exact in fp32 (and in fp16 up to 2048): the
+    in-kernel gather must return index + 256*h (+ -100 across regions)
+    exactly, for the bias added by the softmax and by MMAs."""
     require_gpu()
-    w = W["swin_t_stage1"].with_(B=64)
+    w = W["swin_t_stage1"].with_(**SWIN_BIAS_CASES[case])
     M, H = w.win, w.H
     table = torch.tensor([[r + 256.0 * h for h in range(H)] for r in range((2 * M - 1) ** 2)])
     inp = make_inputs(w)
