@@ -61,6 +61,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As above, but a thread that finds the phase incomplete is suspended until
+// it completes or about `sleep_ns` pass, instead of spinning on the issue
+// slots its SMSP shares with the compute warps.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t sleep_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(sleep_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  `abort` is
 // a CTA-shared word (or null): non-zero means some role already gave up, so
 // every other wait returns promptly too.  On time-out the wait stores
@@ -70,14 +85,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: every legal wait is mi
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           int code) {
     if (mbar_try_wait(bar, parity)) return true;
-    // try_wait suspends in hardware for a while; the abort word and the
-    // clock are looked at only every 64 / 1024 unsuccessful tries so a wait
-    // wakes promptly once its phase completes.
+    // Each further try sleeps up to 20 us (it wakes as soon as the phase
+    // completes); the abort word is looked at every try, the clock every 16.
     uint64_t t0 = 0;
     for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 63) == 0 && abort && *abort) return false;
-        if ((n & 1023) == 0) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (abort && *abort) return false;
+        if ((n & 15) == 0) {
             const uint64_t now = global_timer_ns();
             if (t0 == 0) {
                 t0 = now;
