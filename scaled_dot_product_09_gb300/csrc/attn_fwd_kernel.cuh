@@ -442,6 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nst = p.nst;
     const bool bf = p.is_bf16 != 0;
 
+    // A kernel launched after this one on the stream may start its set-up
+    // while this grid drains (programmatic dependent launch); it reads
+    // nothing before its own griddepcontrol.wait below.
+    griddep_launch_dependents();
     if (tid == 0) {
         abort_sh = 0;
         for (int x = 0; x < 2; ++x) {
@@ -475,6 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&tm.rw);
         }
     }
+    // Global memory is touched only after the grids this launch depends on
+    // have completed and their writes are visible.
+    griddep_wait();
     if (BIAS == kBiasSwin && SL <= 64 && p.swin_rows) {
         // Per head h: row i (query token), column j (key token) holds
         // table[idx(i, j), h] in log2 units (natural units when debugging);

@@ -24,7 +24,21 @@ cudaError_t launch_one(const LaunchArgs& a) {
     auto kern = attn_fwd_kernel<DPAD, BIAS, MODE, SW, SL, DBG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a.smem);
     if (e != cudaSuccess) return e;
-    kern<<<a.grid, kThreads, a.smem, a.stream>>>(*a.tm, *a.p);
+    // Programmatic dependent launch: the CTAs may become resident while the
+    // previous kernel on the stream drains; the kernel waits for it
+    // (griddepcontrol.wait) before touching global memory.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.grid);
+    cfg.blockDim = dim3((unsigned)kThreads);
+    cfg.dynamicSmemBytes = a.smem;
+    cfg.stream = a.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, *a.tm, *a.p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
