@@ -1038,7 +1038,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 // ------------------------------------------------- bias row setup
-                float sam_rw_reg[SW > 0 ? SW : 1];
+                // rel_w of the row for kw = 2u, 2u + 1, held as fp16 pairs (half the
+                // registers of fp32; grid widths here are even, so a pair never
+                // straddles two key rows)
+                __half2 sam_rw_h2[SW > 0 ? SW / 2 : 1];
                 if constexpr (BIAS == kBiasSam) {
                     const int qh = my_tok / p.s_w, qw = my_tok % p.s_w;
                     __syncwarp();
@@ -1056,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     shift_down(gv, qw);
                     if constexpr (SW > 0) {
 #pragma unroll
-                        for (int kw = 0; kw < SW; ++kw) sam_rw_reg[kw] = gv[SW - 1 - kw];
+                        for (int u = 0; u < SW / 2; ++u) sam_rw_h2[u] = __floats2half2_rn(gv[SW - 1 - 2 * u], gv[SW - 2 - 2 * u]);
                     } else {
 #pragma unroll
                         for (int u = 0; u < kSamMaxSide; ++u)
@@ -1129,8 +1132,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             float b0 = 0.f, b1 = 0.f;
                             if constexpr (BIAS == kBiasSam) {
                                 if constexpr (SW > 0) {
-                                    b0 = rh_tile[c / SW] + sam_rw_reg[c % SW];
-                                    b1 = rh_tile[(c + 1) / SW] + sam_rw_reg[(c + 1) % SW];
+                                    const float2 rw = __half22float2(sam_rw_h2[(c % SW) / 2]);
+                                    b0 = rh_tile[c / SW] + rw.x;
+                                    b1 = rh_tile[c / SW] + rw.y;
                                 } else {
                                     const int k0 = sam_kt[min(key0 + c, p.Nk - 1)];
                                     const int k1 = sam_kt[min(key0 + c + 1, p.Nk - 1)];
@@ -1182,15 +1186,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // O holds the earlier tiles' P.V, complete (with a shared P/S
                         // buffer this score tile was committed after it)
                         const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
-                        uint32_t v[DPAD];
-                        tmem_ld_cols<DPAD>(tO, v);
-#pragma unroll
-                        for (int t = 0; t < DPAD; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
+                        // 16 columns at a time: the score row is live in registers
 #pragma unroll
                         for (int c0 = 0; c0 < DPAD; c0 += 16) {
                             uint32_t w16[16];
+                            tmem_ld16(tO + c0, w16);
 #pragma unroll
-                            for (int t = 0; t < 16; ++t) w16[t] = v[c0 + t];
+                            for (int t = 0; t < 16; ++t) w16[t] = __float_as_uint(__uint_as_float(w16[t]) * alpha);
                             tmem_st16(tO + c0, w16);
                         }
                     }
