@@ -139,6 +139,17 @@ int attn_debug_bias(const void* q, const void* k, const void* v, float* bias_out
  * then stopped early and its output is invalid), or ATTN_ERR_CUDA. */
 int attn_device_status(void* stream);
 
+/* attn_selftest_wait_timeout -- test hook for the failure path of the
+ * kernels' bounded waits; the pages have no counterpart.  Launches on
+ * `stream` one warp that waits on a shared-memory barrier nothing arrives
+ * on, through the same bounded wait the attention kernel uses but with a
+ * limit of `limit_us` microseconds (1 .. 2000000).  The wait gives up, the
+ * kernel stores its code (9) in the device status word and returns, so the
+ * context stays usable; attn_device_status then reports
+ * ATTN_ERR_DEVICE_TIMEOUT.  Returns ATTN_OK once launched, ATTN_ERR_ARG for a
+ * limit out of range (before any CUDA call), ATTN_ERR_CUDA otherwise. */
+int attn_selftest_wait_timeout(unsigned limit_us, void* stream);
+
 /* attn_last_error -- text of the last failure on the calling thread
  * (empty string when none).  The pointer stays valid until the next call
  * on the same thread. */

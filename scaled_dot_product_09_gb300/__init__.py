@@ -21,7 +21,7 @@ import math
 import os
 import threading
 
-__all__ = ["attn_fwd", "attn_debug_bias", "attn_device_status", "SwinBias", "SamBias",
+__all__ = ["attn_fwd", "attn_debug_bias", "attn_device_status", "selftest_wait_timeout", "SwinBias", "SamBias",
            "load_library", "AttnError", "ATTN_OK", "ATTN_ERR_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT", "HEADER_SYMBOLS"]
 
@@ -30,8 +30,8 @@ ATTN_BF16, ATTN_FP16 = 0, 1
 ATTN_BIAS_NONE, ATTN_BIAS_SWIN, ATTN_BIAS_SAM_RELPOS = 0, 1, 2
 
 # Every extern "C" function include/sdpa09.h declares.
-HEADER_SYMBOLS = ("attn_fwd", "attn_debug_bias", "attn_device_status", "attn_last_error",
-                  "attn_abi_version")
+HEADER_SYMBOLS = ("attn_fwd", "attn_debug_bias", "attn_device_status", "attn_selftest_wait_timeout",
+                  "attn_last_error", "attn_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -101,6 +101,8 @@ def load_library(build: bool = True):
         lib.attn_debug_bias.restype = i
         lib.attn_device_status.argtypes = [vp]
         lib.attn_device_status.restype = i
+        lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+        lib.attn_selftest_wait_timeout.restype = i
         lib.attn_last_error.argtypes = []
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_abi_version.argtypes = []
@@ -178,6 +180,15 @@ def attn_debug_bias(q, k, v, scale=None, bias=None, stream=None):
                              _dtype_code(q), kind, args, _stream_ptr(stream))
     _check(lib, rc)
     return dbg
+
+
+def selftest_wait_timeout(limit_us: int, stream=None):
+    """Launch the bounded-wait self-test (a wait that runs out after
+    `limit_us`); read the outcome with attn_device_status."""
+    lib = load_library()
+    rc = lib.attn_selftest_wait_timeout(int(limit_us), _stream_ptr(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, lib.attn_last_error().decode(errors="replace"))
 
 
 def attn_device_status(stream=None):

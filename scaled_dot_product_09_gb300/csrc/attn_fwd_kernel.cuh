@@ -85,6 +85,7 @@ enum DevStatus {
     kStatusWaitO = 6,
     kStatusWaitEmpty = 7,
     kStatusWaitG = 8,
+    kStatusWaitSelfTest = 9,  // the bounded-wait self-test kernel
 };
 
 struct AttnParams {

@@ -58,6 +58,26 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// Exercises the failure path of the bounded waits: one warp waits on an
+// mbarrier that nothing ever arrives on, through the same mbar_wait the
+// attention kernel uses but with a short limit; the wait gives up, records
+// its code in the CTA abort word, and the kernel reports it in the status
+// word exactly as the attention kernel's teardown does.
+__global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_sh;
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    volatile int* abort_flag = &abort_sh;
+    const bool ok = mbar_wait(&bar, 0, abort_flag, kStatusWaitSelfTest, limit_ns);
+    __syncwarp();
+    if (threadIdx.x == 0 && !ok && abort_sh != 0) atomicCAS(status, 0, abort_sh);
+}
+
 int* status_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
@@ -442,6 +462,18 @@ int attn_device_status(void* stream) {
         cudaMemcpyToSymbol(sdpa09::g_status_word, &zero, sizeof(int));
         return sdpa09::fail(ATTN_ERR_DEVICE_TIMEOUT, "a kernel wait ran out of time (code %d)", v);
     }
+    return ATTN_OK;
+}
+
+int attn_selftest_wait_timeout(unsigned limit_us, void* stream) {
+    if (limit_us == 0 || limit_us > 2000000u)
+        return sdpa09::fail(ATTN_ERR_ARG, "limit_us must lie in [1, 2000000] (got %u)", limit_us);
+    int* status = sdpa09::status_ptr();
+    if (!status) return sdpa09::fail(ATTN_ERR_CUDA, "no CUDA device / status word unavailable");
+    sdpa09::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status,
+                                                                                  (uint64_t)limit_us * 1000u);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return sdpa09::fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     return ATTN_OK;
 }
 

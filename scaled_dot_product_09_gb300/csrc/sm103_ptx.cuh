@@ -83,7 +83,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: every legal wait is microseconds
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int code) {
+                                          int code, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     // Each further try sleeps up to 20 us (it wakes as soon as the phase
     // completes); the abort word is looked at every try, the clock every 16.
@@ -95,7 +95,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
             const uint64_t now = global_timer_ns();
             if (t0 == 0) {
                 t0 = now;
-            } else if (now - t0 > kWaitLimitNs) {
+            } else if (now - t0 > limit_ns) {
                 if (abort && code) atomicCAS((int*)abort, 0, code);
                 return false;
             }

@@ -109,3 +109,9 @@ def test_binding_rejects_bad_tensors():
         sdpa.attn_fwd(q, q[:, :1], q)
     with pytest.raises(sdpa.AttnError):
         sdpa.attn_fwd(q.float(), q.float(), q.float())
+
+
+def test_selftest_limit_checked_before_cuda(lib):
+    assert lib.attn_selftest_wait_timeout(0, None) == sdpa.ATTN_ERR_ARG
+    assert lib.attn_selftest_wait_timeout(2000001, None) == sdpa.ATTN_ERR_ARG
+    assert b"limit_us" in lib.attn_last_error()

@@ -197,3 +197,18 @@ def test_sam_window_bias_indexing_bit_exact():
     for s in range(w.B * w.H):
         want = oracle.bias_matrix(flat64(inp.q), w.H, s, w.Nk, b)
         np.testing.assert_array_equal(got.reshape(-1, w.Nq, w.Nk)[s].numpy(), want)
+
+
+# ------------------------------------------------------ bounded-wait failure --
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait that nothing completes gives up after its limit, the status word
+    carries its code, and the next attention call on the same context works."""
+    require_gpu()
+    assert sdpa.attn_device_status() == sdpa.ATTN_OK
+    sdpa.selftest_wait_timeout(20000)  # 20 ms
+    assert sdpa.attn_device_status() == sdpa.ATTN_ERR_DEVICE_TIMEOUT
+    assert b"code 9" in sdpa.load_library().attn_last_error()
+    assert sdpa.attn_device_status() == sdpa.ATTN_OK  # read and cleared
+    full_parity(W["toy"])
+    assert sdpa.attn_device_status() == sdpa.ATTN_OK
