@@ -246,16 +246,18 @@ __device__ __forceinline__ void shift_down(float (&v)[128], int sh) {
 // xs[c] = xs[c] * scale_log2 + bias row c (+ -100 log2(e) where the region
 // bit of column c is set, MASK), the row read as float4 chunks XOR-swizzled by
 // swz. With DBG the bias is in natural units and also written to dbg_row.
-template <int SL, bool MASK, bool DBG>
+template <int SL, int NC, bool MASK, bool DBG>
 __device__ __forceinline__ void swin_add_bias_row(float (&xs)[SL], const unsigned char* rowp, int swz,
                                                   const uint32_t* mrow, float scale_log2, float* dbg_row, int nk) {
+    static_assert(NC <= SL, "columns");
     const float mneg = DBG ? -100.0f : -100.0f * kLog2e;
     const float2 s2 = make_float2(scale_log2, scale_log2);
+    constexpr int kQ = (NC + 3) / 4;  // float4 chunks that hold the first NC columns
 #pragma unroll
-    for (int wd = 0; wd < SL / 32; ++wd) {
+    for (int wd = 0; wd < (kQ + 7) / 8; ++wd) {
         const uint32_t mb = MASK ? mrow[wd] : 0u;
 #pragma unroll
-        for (int q = wd * 8; q < wd * 8 + 8; ++q) {
+        for (int q = wd * 8; q < min(wd * 8 + 8, kQ); ++q) {
             const float4 b4 = *reinterpret_cast<const float4*>(rowp + ((q ^ swz) << 4));
             float b[4] = {b4.x, b4.y, b4.z, b4.w};
             if constexpr (MASK) {
@@ -320,14 +322,16 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[N]) {
 // Max of N floats with independent partial maxima (short dependency chains).
 template <int N>
 __device__ __forceinline__ float row_max(const float* x) {
-    static_assert(N % 16 == 0, "row_max");
+    static_assert(N >= 16, "row_max");
     float m[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) m[i] = fmaxf(x[2 * i], x[2 * i + 1]);
 #pragma unroll
-    for (int c = 16; c < N; c += 16)
+    for (int c = 16; c + 16 <= N; c += 16)
 #pragma unroll
         for (int i = 0; i < 8; ++i) m[i] = max3f(m[i], x[c + 2 * i], x[c + 2 * i + 1]);
+#pragma unroll
+    for (int t = N / 16 * 16; t < N; ++t) m[t % 8] = fmaxf(m[t % 8], x[t]);
     return fmaxf(fmaxf(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5])), fmaxf(m[6], m[7]));
 }
 
@@ -417,6 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // buffers per slot (O_x holds 64 columns), so a tile's output is written
     // while the next tile's P.V runs.
     constexpr bool kDblO = MODE == kModeSeparate && DPAD <= 32 && SL <= 64;
+    // Packed Swin with the key count fixed at compile time (SW > 0, e.g. 49 for
+    // 7x7 windows): the softmax touches only those columns (kNe: rounded up to
+    // a pair), not the whole slot.
+    constexpr int kNc = (MODE == kModeSeparate && BIAS == kBiasSwin && SW > 0) ? SW : (SL > 0 ? SL : 1);
+    constexpr int kNe = (kNc + 1) & ~1;
     static_assert(MODE == kModeShared || kSepP, "the packed tiling uses separate P buffers");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1 KB-aligned base, formed by offsetting the array itself so that the
@@ -972,9 +981,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (kind) {
                         const uint32_t* mrow = reinterpret_cast<const uint32_t*>(sExtraB + p.H * SL * SL * 4) +
                                                ((kind - 1) * SL + my_tok) * (SL / 32);
-                        swin_add_bias_row<SL, true, DBG>(xs, rowp, my_tok & 7, mrow, p.scale_log2, dbg_row, nk);
+                        swin_add_bias_row<SL, kNc, true, DBG>(xs, rowp, my_tok & 7, mrow, p.scale_log2, dbg_row, nk);
                     } else {
-                        swin_add_bias_row<SL, false, DBG>(xs, rowp, my_tok & 7, nullptr, p.scale_log2, dbg_row, nk);
+                        swin_add_bias_row<SL, kNc, false, DBG>(xs, rowp, my_tok & 7, nullptr, p.scale_log2, dbg_row, nk);
                     }
                     sc = 1.0f;
                 } else if constexpr (DBG) {
@@ -986,19 +995,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (c < nk) dst[c] = (BIAS == kBiasSwin) ? xs[c] : 0.f;
                     }
                 }
-                // keys past the slice length: -inf (16-column chunks, uniform branches)
+                if constexpr (kNc == SL) {
+                    // keys past the slice length: -inf (16-column chunks, uniform branches)
 #pragma unroll
-                for (int c0 = 0; c0 < SL; c0 += 16) {
-                    if (c0 + 16 > nk) {
+                    for (int c0 = 0; c0 < SL; c0 += 16) {
+                        if (c0 + 16 > nk) {
 #pragma unroll
-                        for (int t = 0; t < 16; ++t)
-                            if (c0 + t >= nk) xs[c0 + t] = -INFINITY;
+                            for (int t = 0; t < 16; ++t)
+                                if (c0 + t >= nk) xs[c0 + t] = -INFINITY;
+                        }
                     }
+                } else if constexpr (kNe > kNc) {
+                    xs[kNc] = -INFINITY;  // the odd column that completes the last pair
                 }
-                const float m = row_max<SL>(xs) * sc;
+                const float m = row_max<kNc>(xs) * sc;
                 const float m_use = (m == -INFINITY) ? 0.f : m;
                 uint32_t own[SL / 2];
-                l_run = exp_pack<SL>(xs, sc, -m_use, bf, own);
+#pragma unroll
+                for (int t = kNe / 2; t < SL / 2; ++t) own[t] = 0u;  // keys past the window
+                l_run = exp_pack<kNe>(xs, sc, -m_use, bf, own);
                 if constexpr (kDblO) {
                     // the previous tile's output, while this tile's P waits in
                     // registers: its P.V has run during this tile's softmax

@@ -11,7 +11,7 @@ struct LaunchArgs {
     const TmaMaps* tm;
     const AttnParams* p;
     int mode;   // kModeShared / kModeSeparate
-    int sw;     // SAM grid-width specialisation (0 = generic)
+    int sw;     // SAM grid-width specialisation, or the Swin window token count (0 = generic)
     int sl;     // slot rows in separate mode (32, 64, 128)
     bool dbg;
     int grid;
@@ -69,6 +69,7 @@ cudaError_t launch_attn_swin(const LaunchArgs& a) {
     if constexpr (DPAD <= 64) {
         if (a.mode == kModeSeparate) {
             if (a.sl == 32) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 32>(a);
+            if (a.sl == 64 && a.sw == 49) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 49, 64>(a);
             if (a.sl == 64) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 64>(a);
             if (a.sl == 128) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 128>(a);
         }

@@ -325,6 +325,9 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
     int mode;
     if (separate) {
         mode = kModeSeparate;
+        // 7x7 windows (49 tokens in 64-row slots) have a softmax specialised
+        // for that key count
+        if (bias == kBiasSwin && Nk == 49 && sl == 64) sw_spec = 49;
         p.g = kBlockM / sl;
         const int64_t n_tiles = (BH + p.g - 1) / p.g;
         p.n_jobs = (int)((n_tiles + 1) / 2);
