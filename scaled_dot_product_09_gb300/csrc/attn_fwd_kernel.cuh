@@ -285,10 +285,16 @@ __device__ __forceinline__ void swin_add_bias_row(float (&xs)[SL], const unsigne
 // Store N (16, 32 or 64) consecutive TMEM columns of this lane.
 template <int N>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[N]) {
-    static_assert(N == 16 || N == 32 || N == 64, "columns");
-    if constexpr (N == 16) tmem_st16(taddr, v);
-    else if constexpr (N == 32) tmem_st32(taddr, v);
-    else tmem_st64(taddr, v);
+    static_assert(N % 8 == 0 && N <= 64, "columns");
+    if constexpr (N == 64) {
+        tmem_st64(taddr, v);
+    } else {
+        if constexpr (N >= 32) tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]));
+        if constexpr (N % 32 >= 16)
+            tmem_st16(taddr + N / 32 * 32, *reinterpret_cast<const uint32_t(*)[16]>(&v[N / 32 * 32]));
+        if constexpr (N % 16 == 8)
+            tmem_st8(taddr + N / 16 * 16, *reinterpret_cast<const uint32_t(*)[8]>(&v[N / 16 * 16]));
+    }
 }
 
 // Load N (multiple of 16, <= 128) consecutive TMEM columns of this lane.
@@ -399,10 +405,11 @@ __device__ __forceinline__ void issue_bias(uint32_t d_tmem, uint64_t qone_d, uin
 
 // O (+)= P.V over 128 keys: P from TMEM (two 16-bit values per column),
 // V MN-major; 16 keys (512 bytes of V) per MMA.
+template <int NK = kBlockN>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vd, uint32_t idesc,
                                          uint32_t accumulate) {
 #pragma unroll
-    for (int ks = 0; ks < kBlockN / 16; ++ks)
+    for (int ks = 0; ks < NK / 16; ++ks)
         mma_ts(o_tmem, p_tmem + ks * 8, vd + (uint64_t)(ks * (512 / 16)), idesc, (accumulate || ks > 0) ? 1u : 0u);
 }
 
@@ -426,6 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a pair), not the whole slot.
     constexpr int kNc = (MODE == kModeSeparate && BIAS == kBiasSwin && SW > 0) ? SW : (SL > 0 ? SL : 1);
     constexpr int kNe = (kNc + 1) & ~1;
+    // Shared tiling without bias and with all keys in one narrow tile (SW > 0,
+    // e.g. 80 for 77 text tokens): score tiles of kCols columns, P.V over
+    // kCols keys.
+    constexpr int kCols = (MODE == kModeShared && BIAS == kBiasNone && SW > 0) ? SW : 128;
+    static_assert(kCols % 16 == 0 && kCols <= 128, "key columns");
     static_assert(MODE == kModeShared || kSepP, "the packed tiling uses separate P buffers");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1 KB-aligned base, formed by offsetting the array itself so that the
@@ -734,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // after both threads have committed their last use of it.
         if (lane == 0) {
             const int x = warp - kMmaWarp;
-            const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, kBlockN, false);
+            const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, MODE == kModeShared ? kCols : kBlockN, false);
             const uint32_t idesc_o = make_idesc_f16(bf, kBlockM, DPAD, true);
             const uint32_t idesc_b = make_idesc_f16(bf, kBlockM, MODE == kModeSeparate ? SL : 16, false);
             const uint32_t tSx = tmem + 128u * x;
@@ -830,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         ph_p ^= 1;
-                        issue_pv(tOx, tPx, vdesc(smem_u32(sRing + st * p.ring_stage_bytes + T::kBytes)), idesc_o,
+                        issue_pv<kCols>(tOx, tPx, vdesc(smem_u32(sRing + st * p.ring_stage_bytes + T::kBytes)), idesc_o,
                                  j > 0 ? 1u : 0u);
                         if (last) {
                             mma_commit(bo);
@@ -1103,12 +1115,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[x], cnt_s & 1, abort_flag, kStatusWaitS))) { ok = false; break; }
                     ++cnt_s;
                     tc_fence_after();
-                    float xs[128];
+                    float xs[kCols];
                     {
-                        uint32_t v[128];
-                        tmem_ld128(tS, v);
+                        uint32_t v[kCols];
+                        tmem_ld_cols<kCols>(tS, v);
 #pragma unroll
-                        for (int t = 0; t < 128; ++t) xs[t] = __uint_as_float(v[t]);
+                        for (int t = 0; t < kCols; ++t) xs[t] = __uint_as_float(v[t]);
                     }
                     if constexpr (kSepP) {
                         // S_x may now be overwritten by the next tile's scores
@@ -1121,15 +1133,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float sc;      // multiplier applied to xs in the exponent
                     if (BIAS == kBiasNone && !DBG) {
                         // no bias: max on raw scores, p = 2^(s*scale*log2e - m)
-                        if (hi < 128) {
+                        if (hi < kCols) {
 #pragma unroll
-                            for (int c0 = 0; c0 < 128; c0 += 16)
+                            for (int c0 = 0; c0 < kCols; c0 += 16)
                                 if (c0 + 16 > hi)
 #pragma unroll
                                     for (int t = 0; t < 16; ++t)
                                         if (c0 + t >= hi) xs[c0 + t] = -INFINITY;
                         }
-                        m_tile = row_max<128>(xs) * p.scale_log2;
+                        m_tile = row_max<kCols>(xs) * p.scale_log2;
                         sc = p.scale_log2;
                     } else {
                         constexpr int kRows = (BIAS == kBiasSam && SW > 0) ? (128 + (SW > 0 ? SW : 1) - 1) / (SW > 0 ? SW : 1) : 1;
@@ -1144,7 +1156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
 #pragma unroll
-                        for (int c = 0; c < 128; c += 2) {
+                        for (int c = 0; c < kCols; c += 2) {
                             float b0 = 0.f, b1 = 0.f;
                             if constexpr (BIAS == kBiasSam) {
                                 if constexpr (SW > 0) {
@@ -1171,15 +1183,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             xs[c] = y.x;
                             xs[c + 1] = y.y;
                         }
-                        if (hi < 128) {
+                        if (hi < kCols) {
 #pragma unroll
-                            for (int c0 = 0; c0 < 128; c0 += 16)
+                            for (int c0 = 0; c0 < kCols; c0 += 16)
                                 if (c0 + 16 > hi)
 #pragma unroll
                                     for (int t = 0; t < 16; ++t)
                                         if (c0 + t >= hi) xs[c0 + t] = -INFINITY;
                         }
-                        m_tile = row_max<128>(xs);
+                        m_tile = row_max<kCols>(xs);
                         sc = 1.0f;
                     }
                     // With separate P buffers the previous P.V may still be running:
@@ -1217,10 +1229,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m_run = m_new;
                     }
                     const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-                    uint32_t pk[64];
-                    l_run += exp_pack<128>(xs, sc, -m_use, bf, pk);
+                    uint32_t pk[kCols / 2];
+                    l_run += exp_pack<kCols>(xs, sc, -m_use, bf, pk);
                     if (!wait_pv()) { ok = false; break; }
-                    tmem_st64(tP, pk);
+                    tmem_st_cols<kCols / 2>(tP, pk);
                     tmem_st_wait();
                     tc_fence_before();
                     warp_arrive(&bar_p[x]);

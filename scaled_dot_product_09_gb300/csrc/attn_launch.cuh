@@ -56,7 +56,11 @@ cudaError_t launch_attn(const LaunchArgs& a);
 // for head dims up to 64 only.
 template <int DPAD>
 cudaError_t launch_attn_none(const LaunchArgs& a) {
-    if (a.mode == kModeShared) return launch_dbg<DPAD, kBiasNone, kModeShared, 0, 0>(a);
+    if (a.mode == kModeShared) {
+        if constexpr (DPAD <= 64)
+            if (a.sw == 80) return launch_dbg<DPAD, kBiasNone, kModeShared, 80, 0>(a);
+        return launch_dbg<DPAD, kBiasNone, kModeShared, 0, 0>(a);
+    }
     if constexpr (DPAD <= 64) {
         if (a.sl == 32) return launch_dbg<DPAD, kBiasNone, kModeSeparate, 0, 32>(a);
         if (a.sl == 64) return launch_dbg<DPAD, kBiasNone, kModeSeparate, 0, 64>(a);

@@ -356,6 +356,9 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
     } else {
         mode = kModeShared;
         p.g = 1;
+        // no bias and every key in one tile of at most 80 (e.g. 77 text tokens):
+        // 80-column score tiles, P.V over 80 keys
+        if (bias == kBiasNone && Nk <= 80 && dpad <= 64) sw_spec = 80;
         p.kv_w = (bias == kBiasSam && sw_spec) ? (kBlockN / sw_spec) * sw_spec : kBlockN;
         p.kv_cols = kBlockN;  // the key tile always spans 128 columns; keys past kv_w are masked
         p.n_kv = (Nk + p.kv_w - 1) / p.kv_w;
