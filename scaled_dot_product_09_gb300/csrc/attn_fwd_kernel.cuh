@@ -233,13 +233,16 @@ __device__ __forceinline__ void swin_table_group(unsigned char* dst, const float
 // Barrel shift of a 128-entry register row: afterwards v[u] = v_in[u + sh]
 // for every u with u + sh < 128 (0 <= sh < 128).  Unrolled selects keep the
 // row in registers.
-__device__ __forceinline__ void shift_down(float (&v)[128], int sh) {
+template <int W = 128, int BITS = 7>
+__device__ __forceinline__ void shift_down(float (&v)[W], int sh) {
+    // W values, shifts below 2^BITS (a row of G needs 2s - 1 values and a
+    // shift below s, so narrow grids use a narrow, shallow network)
 #pragma unroll
-    for (int b = 0; b < 7; ++b) {
+    for (int b = 0; b < BITS; ++b) {
         const int step = 1 << b;
         const bool on = (sh >> b) & 1;
 #pragma unroll
-        for (int u = 0; u + step < 128; ++u) v[u] = on ? v[u + step] : v[u];
+        for (int u = 0; u + step < W; ++u) v[u] = on ? v[u + step] : v[u];
     }
 }
 
@@ -1076,15 +1079,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!__all_sync(0xffffffffu, mbar_wait(&bar_g[x], ju & 1, abort_flag, kStatusWaitG))) { ok = false; break; }
                     tc_fence_after();
                     const float f = DBG ? 1.0f : kLog2e;
-                    float gv[128];
+                    // square grids of side SW <= 16 need 32-value G rows and 4-bit
+                    // shifts, side 64 needs 6-bit shifts
+                    constexpr int kGW = (SW > 0 && SW <= 16) ? 32 : 128;
+                    constexpr int kGB = (SW > 0 && SW <= 16) ? 4 : (SW > 0 ? 6 : 7);
+                    float gv[kGW];
                     // G_w row: rel_w for key column kw is G_w[qw + s_w - 1 - kw]
                     {
-                        uint32_t v[128];
-                        tmem_ld128(tS, v);
+                        uint32_t v[kGW];
+                        tmem_ld_cols<kGW>(tS, v);
 #pragma unroll
-                        for (int t = 0; t < 128; ++t) gv[t] = __uint_as_float(v[t]) * f;
+                        for (int t = 0; t < kGW; ++t) gv[t] = __uint_as_float(v[t]) * f;
                     }
-                    shift_down(gv, qw);
+                    shift_down<kGW, kGB>(gv, qw);
                     if constexpr (SW > 0) {
 #pragma unroll
                         for (int u = 0; u < SW / 2; ++u) sam_rw_h2[u] = __floats2half2_rn(gv[SW - 1 - 2 * u], gv[SW - 2 - 2 * u]);
@@ -1095,14 +1102,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // G_h row: rel_h for key row kh is G_h[qh + s_h - 1 - kh]
                     {
-                        uint32_t v[128];
-                        tmem_ld128(tO, v);
+                        uint32_t v[kGW];
+                        tmem_ld_cols<kGW>(tO, v);
 #pragma unroll
-                        for (int t = 0; t < 128; ++t) gv[t] = __uint_as_float(v[t]) * f;
+                        for (int t = 0; t < kGW; ++t) gv[t] = __uint_as_float(v[t]) * f;
                     }
-                    shift_down(gv, qh);
+                    shift_down<kGW, kGB>(gv, qh);
 #pragma unroll
-                    for (int u = 0; u < kSamMaxSide; ++u)
+                    for (int u = 0; u < (kSamMaxSide < kGW ? kSamMaxSide : kGW); ++u)
                         if (u < p.s_h) sam_rh[u * kBlockM + r] = gv[u];
                     tc_fence_before();
                     warp_arrive(&bar_gdone[x]);

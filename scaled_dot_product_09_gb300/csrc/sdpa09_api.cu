@@ -311,7 +311,9 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         p.s_w = a->q_w;
         p.n_rh = (2 * a->q_h - 1 + 15) / 16 * 16;
         p.n_rw = (2 * a->q_w - 1 + 15) / 16 * 16;
-        sw_spec = (a->q_w == 64 || a->q_w == 14) ? a->q_w : 0;
+        // square 14x14 and 64x64 grids have specialised kernels (the row of G
+        // that a query needs is then short and its shift has few bits)
+        sw_spec = (a->q_h == a->q_w && (a->q_w == 64 || a->q_w == 14)) ? a->q_w : 0;
         extra = (size_t)sam_extra_floats(sw_spec == 0, a->q_h, a->q_w, Nk) * 4;
         bias = kBiasSam;
     } else if (bias_kind != ATTN_BIAS_NONE) {
