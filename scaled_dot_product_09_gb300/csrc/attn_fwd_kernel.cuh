@@ -421,12 +421,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ TmaMaps tm, const AttnParams p) {
     using T = Tile<DPAD>;
     static_assert(MODE == kModeShared || (SL == 32 || SL == 64 || SL == 128), "slot size");
-    // Head dims up to 64 leave room in tensor memory for separate P buffers:
-    // S_A [0,128) S_B [128,256) P_A [256,320) P_B [320,384) O_A [384,448)
-    // O_B [448,512).  The next score tile of a slot is then issued as soon as
-    // its softmax has read the current one, overlapping Q.K^T with the
-    // softmax.  Larger head dims keep P over the first half of S.
-    constexpr bool kSepP = DPAD <= 64 && BIAS != kBiasSam;
+    // Key columns of a score tile (S MMA N, P.V K): 128, or narrower in shared
+    // tiling when that lets separate P buffers fit tensor memory -- without
+    // bias and every key in one tile (SW > 0, e.g. 80 for 77 text tokens), or
+    // SAM on 14x14 grids (112 = eight grid rows).
+    constexpr int kCols = (MODE == kModeShared && BIAS == kBiasNone && SW > 0)  ? SW
+                          : (MODE == kModeShared && BIAS == kBiasSam && SW == 14) ? 112
+                                                                                  : 128;
+    static_assert(kCols % 16 == 0 && kCols <= 128, "key columns");
+    // Tensor memory: separate P buffers when they fit,
+    //   S_A [0,kCols) S_B [kCols,2kCols) P_A/P_B 64 columns each from 2kCols,
+    //   O_A/O_B kOw columns each from 2kCols + 128,
+    // so the next score tile of a slot is issued as soon as its softmax has
+    // read the current one (Q.K^T overlaps the softmax).  Otherwise P lies
+    // over the first half of S, S_x = 128x, O_x = 256 + 128x.
+    constexpr int kOw = DPAD <= 64 ? 64 : DPAD;
+    constexpr int kOffP = 2 * kCols;
+    constexpr int kOffO = kOffP + 128;
+    constexpr bool kSepP = kOffO + 2 * kOw <= 512 && (BIAS != kBiasSam || SW == 14);
     // Packed tiling with head dims up to 32 and slots up to 64 rows: two O
     // buffers per slot (O_x holds 64 columns), so a tile's output is written
     // while the next tile's P.V runs.
@@ -436,11 +448,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a pair), not the whole slot.
     constexpr int kNc = (MODE == kModeSeparate && BIAS == kBiasSwin && SW > 0) ? SW : (SL > 0 ? SL : 1);
     constexpr int kNe = (kNc + 1) & ~1;
-    // Shared tiling without bias and with all keys in one narrow tile (SW > 0,
-    // e.g. 80 for 77 text tokens): score tiles of kCols columns, P.V over
-    // kCols keys.
-    constexpr int kCols = (MODE == kModeShared && BIAS == kBiasNone && SW > 0) ? SW : 128;
-    static_assert(kCols % 16 == 0 && kCols <= 128, "key columns");
     static_assert(MODE == kModeShared || kSepP, "the packed tiling uses separate P buffers");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1 KB-aligned base, formed by offsetting the array itself so that the
@@ -752,9 +759,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, MODE == kModeShared ? kCols : kBlockN, false);
             const uint32_t idesc_o = make_idesc_f16(bf, kBlockM, DPAD, true);
             const uint32_t idesc_b = make_idesc_f16(bf, kBlockM, MODE == kModeSeparate ? SL : 16, false);
-            const uint32_t tSx = tmem + 128u * x;
-            const uint32_t tPx = kSepP ? tmem + 256u + 64u * x : tSx;
-            const uint32_t tOx = tmem + (kSepP ? 384u + 64u * x : 256u + 128u * x);
+            const uint32_t tSx = tmem + (uint32_t)((kSepP ? kCols : 128) * x);
+            const uint32_t tPx = kSepP ? tmem + (uint32_t)(kOffP + 64 * x) : tSx;
+            const uint32_t tOx = tmem + (uint32_t)(kSepP ? kOffO + kOw * x : 256 + 128 * x);
             uint64_t* const bs = &bar_s[x];
             uint64_t* const bp = &bar_p[x];
             uint64_t* const bo = &bar_o[x];
@@ -900,9 +907,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int x = warp >> 2;                // slot A or B
         const int r = tid & 127;                // row in tile == TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_base + (uint32_t)(x * 128);
-        const uint32_t tP = kSepP ? tmem + lane_base + 256u + (uint32_t)(x * 64) : tS;
-        const uint32_t tO = tmem + lane_base + (kSepP ? 384u + (uint32_t)(x * 64) : 256u + (uint32_t)(x * 128));
+        const uint32_t tS = tmem + lane_base + (uint32_t)((kSepP ? kCols : 128) * x);
+        const uint32_t tP = kSepP ? tmem + lane_base + (uint32_t)(kOffP + 64 * x) : tS;
+        const uint32_t tO = tmem + lane_base + (uint32_t)(kSepP ? kOffO + kOw * x : 256 + 128 * x);
         int pvd_cnt = 0;  // P.V completions of this slot awaited (separate P buffers)
         int cnt_s = 0, ju = 0;
         bool ok = true;

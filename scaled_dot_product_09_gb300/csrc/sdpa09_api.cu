@@ -361,8 +361,10 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         // no bias and every key in one tile of at most 80 (e.g. 77 text tokens):
         // 80-column score tiles, P.V over 80 keys
         if (bias == kBiasNone && Nk <= 80 && dpad <= 64) sw_spec = 80;
-        p.kv_w = (bias == kBiasSam && sw_spec) ? (kBlockN / sw_spec) * sw_spec : kBlockN;
-        p.kv_cols = kBlockN;  // the key tile always spans 128 columns; keys past kv_w are masked
+        // SAM key tiles start on grid rows: 112 keys (8 rows) on the 14-wide
+        // grid, 128 (2 rows) on the 64-wide one
+        p.kv_w = (bias == kBiasSam && sw_spec) ? (sw_spec == 14 ? 112 : (kBlockN / sw_spec) * sw_spec) : kBlockN;
+        p.kv_cols = kBlockN;  // unused by the kernel: its key-tile width is a compile-time constant
         p.n_kv = (Nk + p.kv_w - 1) / p.kv_w;
         p.q_jobs = (Nq + 2 * kBlockM - 1) / (2 * kBlockM);
         const int64_t nj = BH * p.q_jobs;
