@@ -483,7 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 2; ++x) {
             for (int b = 0; b < 2; ++b) {
                 mbar_init(&bar_q_full[x][b], 1);
-                mbar_init(&bar_q_empty[x][b], 1);
+                // double-buffered Q: the softmax warps release it after using it
+                // as output staging; single Q: the last P.V's commit releases it
+                mbar_init(&bar_q_empty[x][b], p.nq == 2 ? 4 : 1);
             }
             mbar_init(&bar_s[x], 1);
             mbar_init(&bar_p[x], 4);
@@ -856,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  j > 0 ? 1u : 0u);
                         if (last) {
                             mma_commit(bo);
-                            mma_commit(&bar_q_empty[x][qb]);
+                            if (p.nq == 1) mma_commit(&bar_q_empty[x][qb]);
                         } else if (kSepP) {
                             mma_commit(bpv);
                         }
@@ -924,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // O / l rounded to the output type and stored (row-per-thread, 16 bytes at a time)
-        auto epilogue = [&](uint32_t tObuf, float l, int slice, int tok, bool rok) {
+        auto epilogue = [&](uint32_t tObuf, float l, int slice, int tok, bool rok, int qbuf) {
             const float inv_l = l > 0.f ? 1.0f / l : 0.f;
             uint32_t o[DPAD / 2];
             {
@@ -945,7 +947,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 warp_arrive(&bar_oempty[x]);
             }
-            if (rok && !DBG) {
+            if (MODE == kModeShared && p.nq == 2) {
+                // The slot's Q tile is no longer read (every P.V of the job is
+                // done): it stages the warp's 32 output rows, consecutive tokens
+                // of one slice, so that each store writes 512 contiguous bytes.
+                // Then the Q buffer is handed back to the producer.
+                const int rb = p.d * 2;  // bytes per output row
+                unsigned char* stg = sQ + (x * p.nq + qbuf) * T::kBytes + (warp & 3) * (32 * rb);
+                if (!DBG) {
+#pragma unroll
+                    for (int c = 0; c < DPAD / 8; ++c)
+                        if (c * 8 < p.d)
+                            *reinterpret_cast<uint4*>(stg + lane * rb + c * 16) =
+                                make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                    __syncwarp();
+                    const int nvalid = __popc(__ballot_sync(0xffffffffu, rok));  // a prefix of the lanes
+                    unsigned char* dst = reinterpret_cast<unsigned char*>(p.out) +
+                                         ((size_t)__shfl_sync(0xffffffffu, slice, 0) * p.Nq +
+                                          __shfl_sync(0xffffffffu, tok, 0)) * (size_t)rb;
+                    const int nch = nvalid * rb / 16;
+                    for (int q = lane; q < nch; q += 32)
+                        *reinterpret_cast<uint4*>(dst + (size_t)q * 16) = *reinterpret_cast<const uint4*>(stg + q * 16);
+                }
+                // generic accesses before the producer's next TMA write here
+                fence_proxy_async_smem();
+                warp_arrive(&bar_q_empty[x][qbuf]);
+            } else if (rok && !DBG) {
                 uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(p.out) +
                                                       ((size_t)slice * p.Nq + tok) * (size_t)p.d * 2);
 #pragma unroll
@@ -1046,7 +1073,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_slice, pv_tok, pv_ok);
+                        epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_slice, pv_tok, pv_ok, 0);
                     }
                 }
                 if (ju == 0) {
@@ -1258,14 +1285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_o[x], ju & 1, abort_flag, kStatusWaitO))) { ok = false; break; }
             tc_fence_after();
-            epilogue(tO, l_run, my_slice, my_tok, row_ok);
+            epilogue(tO, l_run, my_slice, my_tok, row_ok, MODE == kModeShared ? ju % p.nq : 0);
         }
         if constexpr (kDblO) {
             if (ok && ju > 0) {
                 __syncwarp();
                 if (__all_sync(0xffffffffu, mbar_wait(&bar_o[x], (ju - 1) & 1, abort_flag, kStatusWaitO))) {
                     tc_fence_after();
-                    epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_slice, pv_tok, pv_ok);
+                    epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_slice, pv_tok, pv_ok, 0);
                 }
             }
         }
