@@ -180,8 +180,16 @@ def test_sam_bias_indexing_bit_exact():
 
 
 def test_sam_window_bias_indexing_bit_exact():
+    _sam_bias_bit_exact(W["sam_vith_window"].with_(B=2, H=2))
+
+
+def test_sam_global_64x64_bias_indexing_bit_exact():
+    # the kernel specialised for 64x64 grids (6-bit G-row shifts, 2-row key tiles)
+    _sam_bias_bit_exact(W["sam_vith_global"].with_(B=1, H=2), slices=(0, 1), rows=range(0, 4096, 37))
+
+
+def _sam_bias_bit_exact(w, slices=None, rows=None):
     require_gpu()
-    w = W["sam_vith_window"].with_(B=2, H=2)
     inp = make_inputs(w)
     Rh = torch.zeros(2 * w.s_h - 1, w.d)
     Rh[:, 0] = torch.arange(2 * w.s_h - 1)
@@ -193,10 +201,12 @@ def test_sam_window_bias_indexing_bit_exact():
     inp.q = qq.to(torch.bfloat16)
     q, k, v = (x.cuda() for x in (inp.q, inp.k, inp.v))
     got = sdpa.attn_debug_bias(q, k, v, scale=w.scale, bias=gpu_bias(w, inp)).cpu().double()
+    got = got.reshape(-1, w.Nq, w.Nk)
     b = oracle_bias(w, inp)
-    for s in range(w.B * w.H):
+    for s in (slices if slices is not None else range(w.B * w.H)):
         want = oracle.bias_matrix(flat64(inp.q), w.H, s, w.Nk, b)
-        np.testing.assert_array_equal(got.reshape(-1, w.Nq, w.Nk)[s].numpy(), want)
+        r = list(rows) if rows is not None else slice(None)
+        np.testing.assert_array_equal(got[s].numpy()[r], want[r])
 
 
 # ------------------------------------------------------ bounded-wait failure --
