@@ -192,3 +192,28 @@ def swin_index(M, ri, ci, rj, cj) -> int:
 
 def swin_mask(M, grid_h, grid_w, shift, window, ti, tj) -> float:
     return _load().oracle_swin_mask(M, grid_h, grid_w, shift, window, ti, tj)
+
+
+def swin_partition(x, win: int, shift: int):
+    """Cyclic shift then window partition of image-layout tokens, the plain
+    definition ("视觉大模型训练和推理加速" section 一: attention inside windows
+    of the shifted feature map; section 二: both steps are index mapping).
+
+    x: [B_img, G_h, G_w, H, d] -> [B_img * nW, H, win * win, d], windows
+    row-major over the image, tokens row-major inside a window.  Token (r, c)
+    of window (wr, wc) is the image token at ((wr*win + r + shift) mod G_h,
+    (wc*win + c + shift) mod G_w)."""
+    x = np.roll(np.asarray(x), shift=(-shift, -shift), axis=(1, 2))
+    B, Gh, Gw, H, d = x.shape
+    x = x.reshape(B, Gh // win, win, Gw // win, win, H, d).transpose(0, 1, 3, 5, 2, 4, 6)
+    return np.ascontiguousarray(x.reshape(B * (Gh // win) * (Gw // win), H, win * win, d))
+
+
+def swin_unpartition(xw, B_img: int, G_h: int, G_w: int, win: int, shift: int):
+    """Inverse of swin_partition: windows back to the image, then the
+    cyclic shift undone.  xw: [B_img * nW, H, win * win, d]."""
+    xw = np.asarray(xw)
+    H, d = xw.shape[1], xw.shape[3]
+    x = xw.reshape(B_img, G_h // win, G_w // win, H, win, win, d).transpose(0, 1, 4, 2, 5, 3, 6)
+    x = x.reshape(B_img, G_h, G_w, H, d)
+    return np.ascontiguousarray(np.roll(x, shift=(shift, shift), axis=(1, 2)))

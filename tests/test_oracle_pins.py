@@ -369,3 +369,38 @@ def test_workload_inputs_are_seeded_and_shaped():
     sm = WORKLOADS["sam_vith_window"].with_(B=2)
     i = make_inputs(sm)
     assert i.rel_h.shape == (27, 80) and i.rel_h.dtype == torch.bfloat16
+
+
+# ------------------------------------------- Swin shift + window partition --
+
+def test_swin_partition_matches_index_definition_by_brute_force():
+    rng = np.random.default_rng(7)
+    B, Gh, Gw, H, d, M, s = 2, 4, 6, 2, 3, 2, 1
+    x = rng.standard_normal((B, Gh, Gw, H, d))
+    xw = oracle.swin_partition(x, M, s)
+    nwh, nww = Gh // M, Gw // M
+    assert xw.shape == (B * nwh * nww, H, M * M, d)
+    for b in range(B):
+        for wr in range(nwh):
+            for wc in range(nww):
+                for h in range(H):
+                    for r in range(M):
+                        for c in range(M):
+                            want = x[b, (wr * M + r + s) % Gh, (wc * M + c + s) % Gw, h]
+                            got = xw[(b * nwh + wr) * nww + wc, h, r * M + c]
+                            np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("shift", [0, 1, 3])
+def test_swin_unpartition_inverts_partition(shift):
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((2, 14, 21, 3, 4))
+    back = oracle.swin_unpartition(oracle.swin_partition(x, 7, shift), 2, 14, 21, 7, shift)
+    np.testing.assert_array_equal(back, x)
+
+
+def test_swin_partition_without_shift_is_a_reshape():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((1, 3, 3, 2, 5))  # one 3x3 window
+    xw = oracle.swin_partition(x, 3, 0)
+    np.testing.assert_array_equal(xw[0], x[0].reshape(9, 2, 5).transpose(1, 0, 2))
