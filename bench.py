@@ -166,26 +166,35 @@ def _max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
-def _gpu_bias(w, inp, dev):
+def _gpu_bias(w, inp, dev, image=False):
     import scaled_dot_product_09_gb300 as sdpa
     if w.bias == "swin":
-        return sdpa.SwinBias(inp.table.to(dev), w.win, w.grid_h, w.grid_w, w.shift)
+        return sdpa.SwinBias(inp.table.to(dev), w.win, w.grid_h, w.grid_w, w.shift,
+                             layout="image" if image else "windows")
     if w.bias == "sam":
         return sdpa.SamBias(inp.rel_h.to(dev), inp.rel_w.to(dev), w.s_h, w.s_w)
     return None
 
 
 class DeviceSets:
-    """Rotating input sets resident in HBM, totalling > 3x L2."""
+    """Rotating input sets resident in HBM, totalling > 3x L2.  image=True
+    (Swin) views the same random tokens as [images, grid_h, grid_w, H, d]
+    feature maps, which the kernel shifts and partitions itself."""
 
-    def __init__(self, w: Workload, inp, dev):
+    def __init__(self, w: Workload, inp, dev, image=False):
         per = w.io_bytes
         self.n = max(2, math.ceil(3 * L2_BYTES / per) + 1)
-        self.q = [inp.q.to(dev) for _ in range(self.n)]
-        self.k = [inp.k.to(dev) for _ in range(self.n)]
-        self.v = [inp.v.to(dev) for _ in range(self.n)]
+
+        def put(t):
+            if image:
+                t = t.reshape(w.B // ((w.grid_h // w.win) * (w.grid_w // w.win)), w.grid_h, w.grid_w, w.H, w.d)
+            return t.to(dev)
+
+        self.q = [put(inp.q) for _ in range(self.n)]
+        self.k = [put(inp.k) for _ in range(self.n)]
+        self.v = [put(inp.v) for _ in range(self.n)]
         self.o = [torch.empty_like(self.q[0]) for _ in range(self.n)]
-        self.bias = _gpu_bias(w, inp, dev)
+        self.bias = _gpu_bias(w, inp, dev, image)
 
 
 def _time_device(w: Workload, sets: DeviceSets, steps: int, warmup: int, stream):
@@ -265,12 +274,14 @@ def _time_e2e(w: Workload, inp, steps: int, warmup: int, stream, dev):
 
 
 def _suite(stream, dev, peaks, names):
-    """Quick device-only numbers for the other workloads (same method)."""
+    """Quick device-only numbers for the other workloads (same method).  A
+    name ending in "@image" times that Swin workload in the image layout."""
     out = {}
     for name in names:
-        w = WORKLOADS[name]
+        base, _, layout = name.partition("@")
+        w = WORKLOADS[base]
         inp = make_inputs(w)
-        sets = DeviceSets(w, inp, dev)
+        sets = DeviceSets(w, inp, dev, image=layout == "image")
         steps = max(20, min(2000, int(0.3 / max(w.flops / 1e15, 1e-6))))
         sec, _ = _time_device(w, sets, steps, 3, stream)
         t = sec / steps
@@ -424,7 +435,7 @@ def main(argv=None):
     if rank == 0 and not args.no_suite:
         del sets
         torch.cuda.empty_cache()
-        suite = _suite(stream, dev, peaks, [n for n in ("sam_vith_window", "sam_vith_global",
+        suite = _suite(stream, dev, peaks, [n for n in ("swin_t_stage1@image", "sam_vith_window", "sam_vith_global",
                                                         "sd_unet_self", "sd_unet_cross") if n != w.name])
     if rank == 0:
         line = {

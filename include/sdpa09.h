@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define SDPA09_ABI_VERSION 1
+#define SDPA09_ABI_VERSION 2
 
 typedef enum {
     ATTN_BF16 = 0, /* bfloat16 Q/K/V/O ("model.to(torch.bfloat16)" in the SAM rewrite) */
@@ -83,7 +83,19 @@ typedef struct {
     int win;            /* M, window side in tokens (7 for Swin-T) */
     int grid_h, grid_w; /* tokens per image side, multiples of win (56, 56) */
     int shift;          /* cyclic shift, 0 <= shift < win; 0 = no mask */
+    int layout;         /* ATTN_SWIN_WINDOWS or ATTN_SWIN_IMAGE, see below */
 } attn_swin_args;
+
+/* Token layouts of q, k, v and out under the Swin bias.
+ *   ATTN_SWIN_WINDOWS: [B windows][H][win*win][d] -- already cyclically
+ *     shifted and partitioned, windows row-major within each image.
+ *   ATTN_SWIN_IMAGE:   [B / nW images][grid_h][grid_w][H][d] -- the natural
+ *     token layout of the feature map; the call applies the cyclic shift by
+ *     -shift and the window partition while loading ("视觉大模型训练和推理加速"
+ *     section 一, window attention on the shifted map; section 二, both are
+ *     index mapping) and their inverse while storing, so no rolled or
+ *     partitioned copy is made.  B still counts windows. */
+enum { ATTN_SWIN_WINDOWS = 0, ATTN_SWIN_IMAGE = 1 };
 
 typedef struct {
     const void* rel_h;  /* device, [2*q_h-1][d], same dtype as Q */

@@ -28,6 +28,7 @@ __all__ = ["attn_fwd", "attn_debug_bias", "attn_device_status", "selftest_wait_t
 ATTN_OK, ATTN_ERR_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = 0, -1, -2, -3, -4
 ATTN_BF16, ATTN_FP16 = 0, 1
 ATTN_BIAS_NONE, ATTN_BIAS_SWIN, ATTN_BIAS_SAM_RELPOS = 0, 1, 2
+ATTN_SWIN_WINDOWS, ATTN_SWIN_IMAGE = 0, 1
 
 # Every extern "C" function include/sdpa09.h declares.
 HEADER_SYMBOLS = ("attn_fwd", "attn_debug_bias", "attn_device_status", "attn_selftest_wait_timeout",
@@ -45,7 +46,7 @@ class AttnError(RuntimeError):
 
 class _SwinArgs(ctypes.Structure):
     _fields_ = [("table", ctypes.c_void_p), ("win", ctypes.c_int), ("grid_h", ctypes.c_int),
-                ("grid_w", ctypes.c_int), ("shift", ctypes.c_int)]
+                ("grid_w", ctypes.c_int), ("shift", ctypes.c_int), ("layout", ctypes.c_int)]
 
 
 class _SamArgs(ctypes.Structure):
@@ -55,13 +56,21 @@ class _SamArgs(ctypes.Structure):
 
 class SwinBias:
     """Swin relative-position bias + shifted-window mask.
-    table: device fp32 [(2*win-1)^2, H]; grid_h/grid_w: tokens per image side."""
+    table: device fp32 [(2*win-1)^2, H]; grid_h/grid_w: tokens per image side.
+    layout "windows": q/k/v/out are [B windows, H, win*win, d], already shifted
+    and partitioned; layout "image": they are [images, grid_h, grid_w, H, d]
+    and the kernel applies the shift and partition (and their inverse on the
+    output) itself."""
 
-    def __init__(self, table, win, grid_h, grid_w, shift):
+    def __init__(self, table, win, grid_h, grid_w, shift, layout="windows"):
+        if layout not in ("windows", "image"):
+            raise ValueError(f"layout must be 'windows' or 'image', not {layout!r}")
         self.table, self.win, self.grid_h, self.grid_w, self.shift = table, win, grid_h, grid_w, shift
+        self.layout = layout
 
     def _c(self):
-        return _SwinArgs(_ptr(self.table), self.win, self.grid_h, self.grid_w, self.shift)
+        return _SwinArgs(_ptr(self.table), self.win, self.grid_h, self.grid_w, self.shift,
+                         ATTN_SWIN_IMAGE if self.layout == "image" else ATTN_SWIN_WINDOWS)
 
 
 class SamBias:
@@ -140,6 +149,23 @@ def _stream_ptr(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _is_image(bias):
+    return isinstance(bias, SwinBias) and bias.layout == "image"
+
+
+def _shape_image(q, k, v, bias):
+    if q.dim() != 5 or q.shape != k.shape or q.shape != v.shape:
+        raise AttnError(ATTN_ERR_ARG, "image layout needs q, k, v of one shape [images, grid_h, grid_w, H, d]")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise AttnError(ATTN_ERR_ARG, "q, k, v must be contiguous")
+    n_img, gh, gw, H, d = q.shape
+    if (gh, gw) != (bias.grid_h, bias.grid_w) or gh % bias.win or gw % bias.win:
+        raise AttnError(ATTN_ERR_ARG, "image grid does not match the Swin arguments")
+    n = bias.win * bias.win
+    return n_img * (gh // bias.win) * (gw // bias.win), H, n, n, d
+
+
 def _shape(q, k, v):
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise AttnError(ATTN_ERR_ARG, "q, k, v must be [B, H, N, d]")
@@ -154,10 +180,12 @@ def _shape(q, k, v):
 
 def attn_fwd(q, k, v, out=None, scale=None, bias=None, stream=None):
     """O = softmax(scale*Q.K^T + bias).V on the GPU.  q [B,H,Nq,d], k/v
-    [B,H,Nk,d] contiguous bf16/fp16 CUDA tensors; returns out [B,H,Nq,d]."""
+    [B,H,Nk,d] contiguous bf16/fp16 CUDA tensors; returns out [B,H,Nq,d].
+    With SwinBias(layout="image") q/k/v/out are [images, grid_h, grid_w, H, d]
+    instead (B then counts windows)."""
     import torch
     lib = load_library()
-    B, H, Nq, Nk, d = _shape(q, k, v)
+    B, H, Nq, Nk, d = _shape_image(q, k, v, bias) if _is_image(bias) else _shape(q, k, v)
     if out is None:
         out = torch.empty_like(q)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)

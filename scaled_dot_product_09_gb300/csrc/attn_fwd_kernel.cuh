@@ -114,6 +114,9 @@ struct AttnParams {
     int win, grid_h, grid_w, shift, n_w, n_ww, n_wh;
     uint32_t fd_h[2], fd_w[2], fd_ww[2];  // magic/shift pairs dividing by H, n_w, n_ww
     int swin_rows;  // 1: bias rows in shared memory, added by the softmax; 0: added by MMAs
+    int swin_image;                 // 1: q/k/v/out in image layout [images][grid_h][grid_w][H][d]
+    uint32_t fd_m[2];               // magic/shift pair dividing by win
+    const void *q, *k, *v;          // operand bases (image layout gathers them directly)
     // SAM
     int s_h, s_w, n_rh, n_rw;
 };
@@ -174,6 +177,30 @@ __device__ __forceinline__ void swin_slice_info(uint32_t slice, int H, int n_w, 
     const uint32_t wr = fast_div(w, fd_ww);
     const uint32_t wc = w - wr * (uint32_t)n_ww;
     kind = shift ? (((int)wc == n_ww - 1 ? 1 : 0) | ((int)wr == n_wh - 1 ? 2 : 0)) : 0;
+}
+
+// Image-layout row of token t of Swin slice `slice`: the slice's window
+// (wr, wc) and head h, token (r, c) = (t / win, t % win) of that window, taken
+// from image position ((wr*win + r + shift) mod grid_h, (wc*win + c + shift)
+// mod grid_w) -- the cyclic shift and window partition of "视觉大模型训练和推理
+// 加速" section 一, as index mapping (section 二).  Rows are [image][y][x][head].
+__device__ __forceinline__ size_t swin_image_row(uint32_t slice, uint32_t t, int H, int n_w, int n_ww, int win,
+                                                 int grid_h, int grid_w, int shift, const uint32_t (&fd_h)[2],
+                                                 const uint32_t (&fd_w)[2], const uint32_t (&fd_ww)[2],
+                                                 const uint32_t (&fd_m)[2]) {
+    const uint32_t bimg = fast_div(slice, fd_h);
+    const int h = (int)(slice - bimg * (uint32_t)H);
+    const uint32_t img = fast_div(bimg, fd_w);
+    const uint32_t w = bimg - img * (uint32_t)n_w;
+    const uint32_t wr = fast_div(w, fd_ww);
+    const int wc = (int)(w - wr * (uint32_t)n_ww);
+    const uint32_t r = fast_div(t, fd_m);
+    const int c = (int)(t - r * (uint32_t)win);
+    int y = (int)wr * win + (int)r + shift;
+    if (y >= grid_h) y -= grid_h;
+    int x = wc * win + c + shift;
+    if (x >= grid_w) x -= grid_w;
+    return ((size_t)(img * (uint32_t)grid_h + (uint32_t)y) * (size_t)grid_w + (size_t)x) * (size_t)H + (size_t)h;
 }
 
 __device__ __forceinline__ int swin_strip(int pos, int G, int M, int s) {
@@ -660,7 +687,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       regs_dec<kControlRegs>();
       if (warp == kProducerWarp) {
         // =========================================================== producer
-        if (lane == 0) {
+        if (MODE == kModeSeparate && BIAS == kBiasSwin && p.swin_image) {
+            // Image layout: the whole warp gathers each window's tokens with
+            // 16-byte cp.async copies, the cyclic shift and the window
+            // partition folded into the source addresses, into the swizzled
+            // tiles the TMA path lands; padding rows and columns read as zero.
+            // kLanesRow consecutive lanes copy one token row, so one warp
+            // instruction touches 32 / kLanesRow rows.  A stage is signalled
+            // once its copies are complete and fenced for the tensor core.  Up
+            // to `depth` tiles stay in flight, fewer than the ring has stages,
+            // so the stage the next tile waits on has always been signalled.
+            constexpr int kChunks = DPAD / 8;  // 16-byte chunks of a padded row
+            constexpr int kLanesRow = kChunks <= 2 ? 2 : (kChunks <= 4 ? 4 : 8);
+            constexpr int kRowsIt = 32 / kLanesRow;  // rows per warp instruction
+            constexpr int kSL = SL > 0 ? SL : kBlockM;  // (SL is 0 only in shared mode)
+            constexpr int kG = kBlockM / kSL;            // slices per tile
+            static_assert(kSL % kRowsIt == 0, "a warp instruction stays inside one slice");
+            const int depth = nst - 1 < 3 ? nst - 1 : 3;
+            const int c = lane % kLanesRow;  // this lane's chunk of every row it copies
+            const int rsub = lane / kLanesRow;
+            const bool lane_on = c < kChunks;            // lanes past the padded row copy nothing
+            const bool c_data = c * 8 < p.d;             // else the chunk is zero padding
+            const uint32_t dchunk = (uint32_t)((c >> 1) * (kBlockM * 32));
+            const size_t rowb = (size_t)p.d * 2;
+            int ring = 0, npend = 0;
+            bool ok = true;
+            for (int job = job0; ok && job < p.n_jobs; job += job_step) {
+                for (int x = 0; x < 2; ++x) {
+                    const int st = ring % nst;
+                    if (ring >= nst) {
+                        __syncwarp();
+                        if (!__all_sync(0xffffffffu, mbar_wait(&bar_empty[st], ((ring / nst) + 1) & 1, abort_flag,
+                                                               kStatusWaitEmpty))) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    ++ring;
+                    const int tile = 2 * job + x;
+                    unsigned char* base = sRing + st * p.ring_stage_bytes;
+                    if (lane_on) {
+#pragma unroll 1
+                        for (int g = 0; g < kG; ++g) {
+                            // the slice's image, window origin after the shift
+                            // and head; rows of a missing slice read as zero
+                            const uint32_t slice = (uint32_t)(tile * kG + g);
+                            const bool sv = (int)slice < p.BH;
+                            const uint32_t bimg = fast_div(slice, p.fd_h);
+                            const uint32_t hh = slice - bimg * (uint32_t)p.H;
+                            const uint32_t img = fast_div(bimg, p.fd_w);
+                            const uint32_t w = bimg - img * (uint32_t)p.n_w;
+                            const uint32_t wr = fast_div(w, p.fd_ww);
+                            const uint32_t ib = img * (uint32_t)p.grid_h;
+                            const uint32_t yb = wr * (uint32_t)p.win + (uint32_t)p.shift;
+                            const uint32_t xb = (w - wr * (uint32_t)p.n_ww) * (uint32_t)p.win + (uint32_t)p.shift;
+#pragma unroll 4
+                            for (int it = 0; it < kSL / kRowsIt; ++it) {
+                                const uint32_t t = (uint32_t)(it * kRowsIt + rsub);
+                                const int R = g * kSL + (int)t;
+                                const uint32_t r = fast_div(t, p.fd_m);
+                                uint32_t yy = yb + r;
+                                if (yy >= (uint32_t)p.grid_h) yy -= (uint32_t)p.grid_h;
+                                uint32_t xx = xb + (t - r * (uint32_t)p.win);
+                                if (xx >= (uint32_t)p.grid_w) xx -= (uint32_t)p.grid_w;
+                                const bool on = c_data && sv && (int)t < p.Nk;
+                                const size_t row = ((size_t)(ib + yy) * (size_t)p.grid_w + xx) * (size_t)p.H + hh;
+                                const size_t off = on ? row * rowb + (size_t)c * 16 : 0;
+                                const uint32_t dst = smem_u32(base + R * 32) + dchunk +
+                                                     ((((uint32_t)c & 1u) ^ (((uint32_t)R >> 2) & 1u)) << 4);
+                                const uint32_t nb = on ? 16u : 0u;
+                                cp_async16(dst, static_cast<const unsigned char*>(p.q) + off, nb);
+                                cp_async16(dst + T::kBytes, static_cast<const unsigned char*>(p.k) + off, nb);
+                                cp_async16(dst + 2 * T::kBytes, static_cast<const unsigned char*>(p.v) + off, nb);
+                            }
+                        }
+                    }
+                    cp_async_commit();
+                    if (++npend > depth) {
+                        cp_async_wait_n(depth);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar_full_k[(ring - npend) % nst]);
+                        --npend;
+                    }
+                }
+            }
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                for (; npend > 0; --npend) mbar_arrive(&bar_full_k[(ring - npend) % nst]);
+        } else if (lane == 0) {
             const uint32_t q_tx = (uint32_t)T::kAtoms * (uint32_t)p.box_q * 32u;
             const uint32_t kv_tx = (uint32_t)T::kAtoms * (uint32_t)p.box_kv * 32u;
             int ring = 0;  // stage uses issued
@@ -875,14 +992,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // separate mode: this slot's tile of the job is ring use `ring + x`
                     const int u = ring + x;
                     const uint32_t qa = smem_u32(sRing + (u % nst) * p.ring_stage_bytes);
-                    if (ju == 0) {
-                        if (!waitb(&bar_full_k[u % nst], (u / nst) & 1, kStatusWaitK)) { ok = false; break; }
+                    // The next tile's scores are issued ahead (they overlap this
+                    // tile's softmax) while this tile holds its stage: with both
+                    // slots doing so that needs three stages, else a slot would
+                    // wait for the stage it holds.
+                    const bool ahead = nst >= 3;
+                    if (ju == 0 || !ahead) {
+                        if (!waitb(&bar_full_k[u % nst], (u / nst) & 1, kStatusWaitK) || !s_free()) { ok = false; break; }
                         sep_scores(2 * job + x, qa);
                         mma_commit(bs);
                         ++s_cnt;
                     }
                     const int next = job + job_step;
-                    if (next < p.n_jobs) {
+                    if (ahead && next < p.n_jobs) {
                         // next tile's scores first: they overlap this tile's softmax
                         const int u2 = u + 2;
                         if (!waitb(&bar_full_k[u2 % nst], (u2 / nst) & 1, kStatusWaitK) || !s_free()) { ok = false; break; }
@@ -973,8 +1095,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 warp_arrive(&bar_q_empty[x][qbuf]);
             } else if (rok && !DBG) {
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(p.out) +
-                                                      ((size_t)slice * p.Nq + tok) * (size_t)p.d * 2);
+                // windows layout: [slice][token]; image layout: the token's
+                // place in the image (shift and partition undone)
+                const size_t orow = (MODE == kModeSeparate && BIAS == kBiasSwin && p.swin_image)
+                                        ? swin_image_row((uint32_t)slice, (uint32_t)tok, p.H, p.n_w, p.n_ww, p.win,
+                                                         p.grid_h, p.grid_w, p.shift, p.fd_h, p.fd_w, p.fd_ww, p.fd_m)
+                                        : (size_t)slice * p.Nq + tok;
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(p.out) + orow * (size_t)p.d * 2);
 #pragma unroll
                 for (int c = 0; c < DPAD / 8; ++c)
                     if (c * 8 < p.d) dst[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);

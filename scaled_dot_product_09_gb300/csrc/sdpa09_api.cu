@@ -264,6 +264,9 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.is_bf16 = dtype == ATTN_BF16;
+    p.q = q;
+    p.k = k;
+    p.v = v;
     const int dpad = dpad_for(d);
     const size_t tile_bytes = (size_t)(dpad / 16) * kBlockM * 32;
     size_t extra = 0;
@@ -280,6 +283,8 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         if (a->grid_h < M || a->grid_w < M || a->grid_h % M || a->grid_w % M)
             return fail(ATTN_ERR_ARG, "grid_h and grid_w must be positive multiples of win");
         if (a->shift < 0 || a->shift >= M) return fail(ATTN_ERR_ARG, "shift must lie in [0, win)");
+        if (a->layout != ATTN_SWIN_WINDOWS && a->layout != ATTN_SWIN_IMAGE)
+            return fail(ATTN_ERR_ARG, "unknown Swin token layout %d", a->layout);
         const int nW = (a->grid_h / M) * (a->grid_w / M);
         if (B % nW) return fail(ATTN_ERR_ARG, "B (windows) must be a multiple of the windows per image");
         if (dpad > 64) return fail(ATTN_ERR_UNSUPPORTED, "SWIN with d > 64 is not supported");
@@ -294,6 +299,8 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         fast_div_params((uint32_t)H, p.fd_h);
         fast_div_params((uint32_t)nW, p.fd_w);
         fast_div_params((uint32_t)p.n_ww, p.fd_ww);
+        fast_div_params((uint32_t)M, p.fd_m);
+        p.swin_image = a->layout == ATTN_SWIN_IMAGE ? 1 : 0;
         bias = kBiasSwin;
     } else if (bias_kind == ATTN_BIAS_SAM_RELPOS) {
         const attn_sam_args* a = static_cast<const attn_sam_args*>(bias_args);

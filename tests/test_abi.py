@@ -41,7 +41,8 @@ def test_library_targets_sm103a_only():
 
 
 def test_abi_version(lib):
-    assert lib.attn_abi_version() == 1
+    # 2: attn_swin_args gained its token layout field
+    assert lib.attn_abi_version() == 2
 
 
 def _call(lib, q=FAKE, k=FAKE + 4096, v=FAKE + 8192, out=FAKE + 1 << 20, B=1, H=1, Nq=64, Nk=64,
@@ -84,6 +85,21 @@ def test_swin_argument_checks(lib):
     # windows above 128 tokens
     big = sdpa._SwinArgs(FAKE, 12, 24, 24, 0)
     assert _call(lib, B=4, Nq=144, Nk=144, kind=1, args=ctypes.byref(big)) == sdpa.ATTN_ERR_UNSUPPORTED
+    # unknown token layout
+    lay = sdpa._SwinArgs(FAKE, 7, 56, 56, 3, 2)
+    assert _call(lib, B=64, Nq=49, Nk=49, kind=1, args=ctypes.byref(lay)) == sdpa.ATTN_ERR_ARG
+    assert b"layout" in lib.attn_last_error()
+
+
+def test_image_layout_binding_checks():
+    import torch
+    b = sdpa.SwinBias(torch.zeros(169, 3), 7, 56, 56, 3, layout="image")
+    q = torch.zeros(2, 56, 56, 3, 32, dtype=torch.float16)
+    assert sdpa._shape_image(q, q, q, b) == (2 * 64, 3, 49, 49, 32)
+    with pytest.raises(sdpa.AttnError):
+        sdpa._shape_image(q[:, :49], q[:, :49], q[:, :49], b)  # grid mismatch
+    with pytest.raises(ValueError):
+        sdpa.SwinBias(torch.zeros(169, 3), 7, 56, 56, 3, layout="rows")
 
 
 def test_sam_argument_checks(lib):

@@ -209,6 +209,75 @@ def _sam_bias_bit_exact(w, slices=None, rows=None):
         np.testing.assert_array_equal(got[s].numpy()[r], want[r])
 
 
+# ----------------------------------------------- Swin image token layout --
+# q/k/v/out as [images, grid_h, grid_w, H, d]: the kernel folds the cyclic
+# shift and the window partition into its loads and their inverse into its
+# stores.  Image inputs are the windows-layout inputs mapped back through the
+# oracle's inverse partition (an exact index permutation); the expected output
+# is the oracle's window attention mapped the same way.
+
+SWIN_IMAGE_CASES = {
+    "stage1": dict(B=2 * 64),
+    "no_shift": dict(B=64, shift=0, seed=12),
+    "ragged_tail": dict(B=9, grid_h=21, grid_w=21, seed=11),
+    "mma_many_heads": dict(B=2 * 16, H=6, grid_h=28, grid_w=28, seed=13),
+    "small_window": dict(B=2 * 16, win=4, Nq=16, Nk=16, grid_h=16, grid_w=16, shift=2, seed=14),
+    "large_window": dict(B=2 * 4, H=1, win=10, Nq=100, Nk=100, grid_h=20, grid_w=20, shift=5, seed=15),
+    # d=64 with bias MMAs leaves a two-stage ring, and 192 jobs make CTAs wrap it
+    "d64_two_stage_ring": dict(B=32 * 4, H=6, d=64, grid_h=14, grid_w=14, seed=16),
+    "bf16": dict(B=64, dtype="bf16", seed=17),
+}
+
+
+def _images(w):
+    return w.B // ((w.grid_h // w.win) * (w.grid_w // w.win))
+
+
+def _to_image(t, w):
+    """[B windows, H, win^2, d] -> [images, grid_h, grid_w, H, d], bit-exact."""
+    raw = t.view(torch.int16).numpy()
+    img = oracle.swin_unpartition(raw, _images(w), w.grid_h, w.grid_w, w.win, w.shift)
+    return torch.from_numpy(img).view(t.dtype)
+
+
+def _image_bias(w, inp):
+    return sdpa.SwinBias(inp.table.cuda(), w.win, w.grid_h, w.grid_w, w.shift, layout="image")
+
+
+@pytest.mark.parametrize("case", sorted(SWIN_IMAGE_CASES))
+def test_swin_image_layout_full(case):
+    require_gpu()
+    w = W["swin_t_stage1"].with_(**SWIN_IMAGE_CASES[case])
+    inp = make_inputs(w)
+    q, k, v = (_to_image(x, w).cuda() for x in (inp.q, inp.k, inp.v))
+    out = sdpa.attn_fwd(q, k, v, scale=w.scale, bias=_image_bias(w, inp))
+    torch.cuda.synchronize()
+    assert sdpa.attn_device_status() == sdpa.ATTN_OK
+    assert out.shape == (_images(w), w.grid_h, w.grid_w, w.H, w.d)
+    want, _ = oracle.attn_fwd(flat64(inp.q), flat64(inp.k), flat64(inp.v), w.H, w.scale, oracle_bias(w, inp))
+    want = oracle.swin_unpartition(want.reshape(w.B, w.H, w.Nq, w.d), _images(w), w.grid_h, w.grid_w,
+                                   w.win, w.shift)
+    compare(out.cpu().double().numpy(), want, what=f"swin image {case}")
+    # same smem tiles as the windows-layout path: identical bits
+    win_out = run_gpu(w, inp)
+    assert torch.equal(out.cpu().view(torch.int16), _to_image(win_out, w).view(torch.int16))
+
+
+def test_swin_image_layout_full_size_matches_windows_layout():
+    """Full Swin-T stage-1 batch: the image-layout call returns, bit for bit,
+    the windows-layout result mapped back to the image (the windows layout is
+    itself checked against the oracle at this size)."""
+    require_gpu()
+    w = W["swin_t_stage1"]
+    inp = make_inputs(w)
+    win_out = run_gpu(w, inp)
+    q, k, v = (_to_image(x, w).cuda() for x in (inp.q, inp.k, inp.v))
+    out = sdpa.attn_fwd(q, k, v, scale=w.scale, bias=_image_bias(w, inp))
+    torch.cuda.synchronize()
+    assert sdpa.attn_device_status() == sdpa.ATTN_OK
+    assert torch.equal(out.cpu().view(torch.int16), _to_image(win_out, w).view(torch.int16))
+
+
 # ------------------------------------------------------ bounded-wait failure --
 
 def test_bounded_wait_reports_timeout_and_context_survives():
