@@ -695,15 +695,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // kLanesRow consecutive lanes copy one token row, so one warp
             // instruction touches 32 / kLanesRow rows.  A stage is signalled
             // once its copies are complete and fenced for the tensor core.  Up
-            // to `depth` tiles stay in flight, fewer than the ring has stages,
-            // so the stage the next tile waits on has always been signalled.
+            // to `depth` tiles stay in flight unsignalled.  Before the producer
+            // waits for stage use n - nst to be released, the MMA slot holding
+            // it must have seen the tile it looks ahead to, use n - nst + 2
+            // (n - nst without the lookahead, which needs three stages), so
+            // depth is at most nst - 3 (nst - 1 for a two-stage ring).
             constexpr int kChunks = DPAD / 8;  // 16-byte chunks of a padded row
             constexpr int kLanesRow = kChunks <= 2 ? 2 : (kChunks <= 4 ? 4 : 8);
             constexpr int kRowsIt = 32 / kLanesRow;  // rows per warp instruction
             constexpr int kSL = SL > 0 ? SL : kBlockM;  // (SL is 0 only in shared mode)
             constexpr int kG = kBlockM / kSL;            // slices per tile
             static_assert(kSL % kRowsIt == 0, "a warp instruction stays inside one slice");
-            const int depth = nst - 1 < 3 ? nst - 1 : 3;
+            const int depth = nst < 3 ? nst - 1 : (nst - 3 < 3 ? nst - 3 : 3);
             const int c = lane % kLanesRow;  // this lane's chunk of every row it copies
             const int rsub = lane / kLanesRow;
             const bool lane_on = c < kChunks;            // lanes past the padded row copy nothing

@@ -116,7 +116,8 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// the same with a run-time N in [0, 3] (larger N waits as for 3)
+// the same with a run-time N in [0, 3] (a larger N waits as for 3, which is
+// safe: it only waits longer)
 __device__ __forceinline__ void cp_async_wait_n(int n) {
     switch (n) {
         case 0: cp_async_wait<0>(); break;

@@ -223,8 +223,16 @@ SWIN_IMAGE_CASES = {
     "mma_many_heads": dict(B=2 * 16, H=6, grid_h=28, grid_w=28, seed=13),
     "small_window": dict(B=2 * 16, win=4, Nq=16, Nk=16, grid_h=16, grid_w=16, shift=2, seed=14),
     "large_window": dict(B=2 * 4, H=1, win=10, Nq=100, Nk=100, grid_h=20, grid_w=20, shift=5, seed=15),
-    # d=64 with bias MMAs leaves a two-stage ring, and 192 jobs make CTAs wrap it
-    "d64_two_stage_ring": dict(B=32 * 4, H=6, d=64, grid_h=14, grid_w=14, seed=16),
+    # rings of 2..5 stages, each with enough jobs that CTAs wrap their ring
+    # (the gather keeps fewer tiles in flight on shorter rings):
+    # d=64 with bias MMAs: 2 stages, 192 jobs
+    "ring2_d64_mma": dict(B=32 * 4, H=6, d=64, grid_h=14, grid_w=14, seed=16),
+    # d=64 with bias rows: 3 stages, 192 jobs
+    "ring3_d64_rows": dict(B=4 * 64, d=64, seed=18),
+    # d=48 with bias rows: 4 stages, 384 jobs
+    "ring4_d48_rows": dict(B=8 * 64, d=48, seed=19),
+    # 6 heads, bias MMAs: 5 stages, 384 jobs
+    "ring5_mma_many_heads": dict(B=16 * 16, H=6, grid_h=28, grid_w=28, seed=20),
     "bf16": dict(B=64, dtype="bf16", seed=17),
 }
 
