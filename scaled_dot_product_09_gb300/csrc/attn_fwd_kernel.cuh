@@ -65,6 +65,7 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kGatherWarp = 11;  // second copy warp of the image-layout Swin gather, else idle
 constexpr int kTmemCols = 512;
 constexpr int kMaxStages = 8;
 constexpr int kSamMaxSide = 64;  // rel-pos grids up to 64 x 64
@@ -524,7 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar_pvd[x], 1);
         }
         for (int i = 0; i < kMaxStages; ++i) {
-            mbar_init(&bar_full_k[i], 1);
+            // the image-layout Swin stages are filled by two warps
+            mbar_init(&bar_full_k[i], (MODE == kModeSeparate && BIAS == kBiasSwin && p.swin_image) ? 2 : 1);
             mbar_init(&bar_full_v[i], 1);
             mbar_init(&bar_empty[i], MODE == kModeShared ? 2 : 1);
         }
@@ -685,40 +687,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= 8) {
       regs_dec<kControlRegs>();
-      if (warp == kProducerWarp) {
+      if (warp == kProducerWarp || (warp == kGatherWarp && MODE == kModeSeparate && BIAS == kBiasSwin && p.swin_image)) {
         // =========================================================== producer
         if (MODE == kModeSeparate && BIAS == kBiasSwin && p.swin_image) {
-            // Image layout: the whole warp gathers each window's tokens with
-            // 16-byte cp.async copies, the cyclic shift and the window
-            // partition folded into the source addresses, into the swizzled
-            // tiles the TMA path lands; padding rows and columns read as zero.
-            // kLanesRow consecutive lanes copy one token row, so one warp
-            // instruction touches 32 / kLanesRow rows.  A stage is signalled
-            // once its copies are complete and fenced for the tensor core.  Up
-            // to `depth` tiles stay in flight unsignalled.  Before the producer
-            // waits for stage use n - nst to be released, the MMA slot holding
-            // it must have seen the tile it looks ahead to, use n - nst + 2
-            // (n - nst without the lookahead, which needs three stages), so
-            // depth is at most nst - 3 (nst - 1 for a two-stage ring).
+            // Image layout: this warp and the gather warp copy each window's
+            // token rows with 16-byte cp.async copies, the cyclic shift and
+            // the window partition folded into the source addresses,
+            // kLanesRow lanes per row, into the swizzled tiles the TMA path
+            // lands (padding rows and columns written as zeros).  The warps
+            // take alternate slices of a tile, or alternate row groups when a
+            // tile holds one slice.  (Rows of one head are 2d bytes out of
+            // every 2Hd, too short for box copies to pay.)  A stage's barrier
+            // takes one arrival per warp, made once that warp's copies into
+            // the stage have landed.
             constexpr int kChunks = DPAD / 8;  // 16-byte chunks of a padded row
             constexpr int kLanesRow = kChunks <= 2 ? 2 : (kChunks <= 4 ? 4 : 8);
-            constexpr int kRowsIt = 32 / kLanesRow;  // rows per warp instruction
+            constexpr int kRowsIt = 32 / kLanesRow;      // rows per warp instruction
             constexpr int kSL = SL > 0 ? SL : kBlockM;  // (SL is 0 only in shared mode)
             constexpr int kG = kBlockM / kSL;            // slices per tile
             static_assert(kSL % kRowsIt == 0, "a warp instruction stays inside one slice");
-            const int depth = nst < 3 ? nst - 1 : (nst - 3 < 3 ? nst - 3 : 3);
+            const int half = warp == kProducerWarp ? 0 : 1;  // which slices (or row groups) this warp copies
             const int c = lane % kLanesRow;  // this lane's chunk of every row it copies
             const int rsub = lane / kLanesRow;
-            const bool lane_on = c < kChunks;            // lanes past the padded row copy nothing
-            const bool c_data = c * 8 < p.d;             // else the chunk is zero padding
+            const bool lane_on = c < kChunks;  // lanes past the padded row copy nothing
+            const bool c_data = c * 8 < p.d;   // else the chunk is zero padding
             const uint32_t dchunk = (uint32_t)((c >> 1) * (kBlockM * 32));
             const size_t rowb = (size_t)p.d * 2;
-            int ring = 0, npend = 0;
+            // Ring uses whose copies are in flight, oldest first.  The MMA
+            // slot holding use u releases it only after the tile it looks
+            // ahead to, u + 2, has landed, so before waiting for use n - nst to
+            // be released this warp signals every use up to n - nst + 2.
+            int pend0 = 0, pend1 = 0, pend2 = 0, pend3 = 0;  // (scalars: no local-memory array)
+            int npend = 0;
+            auto pop_oldest = [&](int keep) {
+                cp_async_wait_n(keep);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_full_k[pend0 % nst]);
+                pend0 = pend1;
+                pend1 = pend2;
+                pend2 = pend3;
+                --npend;
+            };
+            int ring = 0;
             bool ok = true;
             for (int job = job0; ok && job < p.n_jobs; job += job_step) {
                 for (int x = 0; x < 2; ++x) {
                     const int st = ring % nst;
                     if (ring >= nst) {
+                        while (npend > 0 && pend0 <= ring - nst + 2) pop_oldest(npend - 1);
                         __syncwarp();
                         if (!__all_sync(0xffffffffu, mbar_wait(&bar_empty[st], ((ring / nst) + 1) & 1, abort_flag,
                                                                kStatusWaitEmpty))) {
@@ -726,14 +743,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                     }
-                    ++ring;
+                    const int use = ring++;
                     const int tile = 2 * job + x;
                     unsigned char* base = sRing + st * p.ring_stage_bytes;
                     if (lane_on) {
 #pragma unroll 1
-                        for (int g = 0; g < kG; ++g) {
+                        for (int g = (kG > 1 ? half : 0); g < kG; g += (kG > 1 ? 2 : 1)) {
                             // the slice's image, window origin after the shift
-                            // and head; rows of a missing slice read as zero
+                            // and head; rows past the window or of a missing
+                            // slice read as zero
                             const uint32_t slice = (uint32_t)(tile * kG + g);
                             const bool sv = (int)slice < p.BH;
                             const uint32_t bimg = fast_div(slice, p.fd_h);
@@ -745,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t yb = wr * (uint32_t)p.win + (uint32_t)p.shift;
                             const uint32_t xb = (w - wr * (uint32_t)p.n_ww) * (uint32_t)p.win + (uint32_t)p.shift;
 #pragma unroll 4
-                            for (int it = 0; it < kSL / kRowsIt; ++it) {
+                            for (int it = (kG > 1 ? 0 : half); it < kSL / kRowsIt; it += (kG > 1 ? 1 : 2)) {
                                 const uint32_t t = (uint32_t)(it * kRowsIt + rsub);
                                 const int R = g * kSL + (int)t;
                                 const uint32_t r = fast_div(t, p.fd_m);
@@ -766,20 +784,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     cp_async_commit();
-                    if (++npend > depth) {
-                        cp_async_wait_n(depth);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&bar_full_k[(ring - npend) % nst]);
-                        --npend;
-                    }
+                    if (npend == 0) pend0 = use;
+                    else if (npend == 1) pend1 = use;
+                    else if (npend == 2) pend2 = use;
+                    else pend3 = use;
+                    if (++npend > 3) pop_oldest(3);
                 }
             }
-            cp_async_wait<0>();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                for (; npend > 0; --npend) mbar_arrive(&bar_full_k[(ring - npend) % nst]);
+            while (npend > 0) pop_oldest(npend - 1);
         } else if (lane == 0) {
             const uint32_t q_tx = (uint32_t)T::kAtoms * (uint32_t)p.box_q * 32u;
             const uint32_t kv_tx = (uint32_t)T::kAtoms * (uint32_t)p.box_kv * 32u;
