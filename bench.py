@@ -12,7 +12,9 @@ input sets rotate so their total exceeds 3x the L2 size (no L2 reuse
 between consecutive steps).  SM clocks are sampled with nvidia-smi during
 the timed region.  ``e2e`` repeats the measurement through the same C-ABI
 call with pinned host buffers: each step copies Q, K, V host->device, runs
-the kernel and copies O device->host, all inside the timed region.
+the kernel and copies O device->host, all inside the timed region; steps
+are pipelined over two device buffer sets, so the copies of one step overlap
+the kernel of another.
 
 ``--impl reference`` times the fp64 CPU oracle (test infrastructure, as it
 stands) on the host cores on a bounded sample of the same workload.
@@ -239,37 +241,57 @@ def _time_device(w: Workload, sets: DeviceSets, steps: int, warmup: int, stream)
     return start.elapsed_time(end) / 1e3, steps
 
 
-def _time_e2e(w: Workload, inp, steps: int, warmup: int, stream, dev):
-    """Pinned host buffers; per step: H2D of q,k,v, kernel, D2H of O."""
+def _time_e2e(w: Workload, inp, steps: int, warmup: int, stream, dev, depth: int = 2):
+    """Pinned host buffers; every step copies its Q, K, V host->device, runs
+    attn_fwd and copies O device->host.  Steps are pipelined over `depth`
+    device buffer sets with one stream per copy direction, so one step's
+    copies overlap another step's kernel; events keep
+    each set's copy-in, kernel and copy-out in order.  Returns the seconds,
+    H2D bytes and D2H bytes per step."""
     import scaled_dot_product_09_gb300 as sdpa
     hq, hk, hv = (x.pin_memory() for x in (inp.q, inp.k, inp.v))
-    ho = torch.empty_like(hq).pin_memory()
-    dq, dk, dv = (torch.empty_like(x, device=dev) for x in (hq, hk, hv))
-    do = torch.empty_like(dq)
+    hos = [torch.empty_like(hq).pin_memory() for _ in range(depth)]
+    sets = [tuple(torch.empty_like(x, device=dev) for x in (hq, hk, hv, hq)) for _ in range(depth)]
     bias = _gpu_bias(w, inp, dev)
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(depth)]    # set j's inputs landed
+    ev_run = [torch.cuda.Event() for _ in range(depth)]   # set j's kernel finished
+    ev_out = [torch.cuda.Event() for _ in range(depth)]   # set j's output copied back
 
-    def step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
+    def step(i):
+        j = i % depth
+        dq, dk, dv, do = sets[j]
+        s_in.wait_event(ev_run[j])  # the set's previous kernel has read its inputs
+        with torch.cuda.stream(s_in):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+        ev_in[j].record(s_in)
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_out[j])  # the set's previous output has been copied back
         sdpa.attn_fwd(dq, dk, dv, out=do, scale=w.scale, bias=bias, stream=stream)
-        ho.copy_(do, non_blocking=True)
+        ev_run[j].record(stream)
+        s_out.wait_event(ev_run[j])
+        with torch.cuda.stream(s_out):
+            hos[j].copy_(do, non_blocking=True)
+        ev_out[j].record(s_out)
 
-    n = max(1, min(steps, 200))
-    with torch.cuda.stream(stream):
-        for _ in range(max(warmup, 3)):
-            step()
-        torch.cuda.synchronize()
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for _ in range(n):
-            step()
-        end.record(stream)
+    n = max(depth, min(steps, 200))
+    for i in range(max(warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    for i in range(n):
+        step(i)
+    end.record(s_out)  # after the last copy-out, which follows every earlier step
     end.synchronize()
+    torch.cuda.synchronize()
     sec = start.elapsed_time(end) / 1e3 / n
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
-    d2h = ho.numel() * ho.element_size()
+    d2h = hos[0].numel() * hos[0].element_size()
     return sec, h2d, d2h
 
 
