@@ -13,7 +13,9 @@ Definition followed (per slice): S = scale*Q.K^T + bias, P = softmax_rows(S),
 O = P.V -- "视觉大模型训练和推理加速" section 一 (attention map from query and
 key with softmax, weighting the values) and "Accelerated Diffusers with
 PyTorch 2.0" section 加速 Transformer 块 (all SDPA backends compute the same
-function; the native C++ one is the high-precision path).
+function; the native C++ one is the high-precision path).  Variable-length
+batches (``attn_varlen``) apply that definition to each sequence of the
+batch on its own.
 """
 from __future__ import annotations
 
@@ -217,3 +219,32 @@ def swin_unpartition(xw, B_img: int, G_h: int, G_w: int, win: int, shift: int):
     x = xw.reshape(B_img, G_h // win, G_w // win, H, win, win, d).transpose(0, 1, 4, 2, 5, 3, 6)
     x = x.reshape(B_img, G_h, G_w, H, d)
     return np.ascontiguousarray(np.roll(x, shift=(shift, shift), axis=(1, 2)))
+
+
+def attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, H, scale, nthreads: int = 0):
+    """Attention over a batch of sequences of different lengths, each
+    attending only to itself, no bias -- a nested tensor ("PyTorch团队重写
+    「分割一切」模型", Nested Tensor: data of non-uniform size, such as images
+    of different sizes, batched in one tensor as {tensor, mask}).
+
+    q [H * sum(Lq), d] is the concatenation over sequences s of [H][Lq_s][d]
+    (Lq_s = cu_seqlens_q[s+1] - cu_seqlens_q[s]); k, v likewise with Lk_s.
+    Each sequence is one call of ``attn_fwd`` with H slices.  Returns out
+    [H * sum(Lq), d] float64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    d = q.shape[-1]
+    out = np.zeros((q.shape[0], d), dtype=np.float64)
+    for s in range(len(cu_seqlens_q) - 1):
+        lq = cu_seqlens_q[s + 1] - cu_seqlens_q[s]
+        lk = cu_seqlens_k[s + 1] - cu_seqlens_k[s]
+        if lq == 0:
+            continue
+        if lk == 0:
+            raise ValueError(f"sequence {s} has queries but no keys")
+        q0, k0 = H * cu_seqlens_q[s], H * cu_seqlens_k[s]
+        qs = q[q0:q0 + H * lq].reshape(H, lq, d)
+        ks = k[k0:k0 + H * lk].reshape(H, lk, d)
+        vs = v[k0:k0 + H * lk].reshape(H, lk, d)
+        o, _ = attn_fwd(qs, ks, vs, H, scale, None, nthreads)
+        out[q0:q0 + H * lq] = o.reshape(H * lq, d)
+    return out

@@ -10,7 +10,9 @@ tables; q/k/v are N(0, 1) and cast with round-to-nearest-even to the
 workload dtype; the Swin table is N(0, 0.02) kept in fp32; the SAM tables
 R_h, R_w are N(0, 0.02) cast to the workload dtype.  Layout is
 [B, H, N, d] contiguous with d innermost.  For Swin, B counts windows:
-b' = image * nW + w with w row-major over the window grid.
+b' = image * nW + w with w row-major over the window grid.  A variable-length
+batch (``seqlens_q`` set) draws q as one [H * sum(Lq), d] buffer -- the
+concatenation over sequences of [H][Lq_s][d] -- and k, v likewise.
 
 The workloads stand in for real images through the models the pages
 profile (SAM image encoder, Swin-T stage 1, Stable Diffusion UNet): those
@@ -19,6 +21,7 @@ need datasets and trained weights, so the shapes alone are reproduced.
 from __future__ import annotations
 
 import dataclasses
+import itertools
 import math
 
 import torch
@@ -43,7 +46,22 @@ class Workload:
     # SAM grid (query grid == key grid)
     s_h: int = 0
     s_w: int = 0
+    # variable-length batch: per-sequence query / key token counts (B of each)
+    seqlens_q: tuple = ()
+    seqlens_k: tuple = ()
     note: str = ""
+
+    @property
+    def varlen(self) -> bool:
+        return len(self.seqlens_q) > 0
+
+    @property
+    def cu_seqlens_q(self) -> list:
+        return [0] + list(itertools.accumulate(self.seqlens_q))
+
+    @property
+    def cu_seqlens_k(self) -> list:
+        return [0] + list(itertools.accumulate(self.seqlens_k))
 
     @property
     def scale(self) -> float:
@@ -55,7 +73,10 @@ class Workload:
 
     @property
     def flops(self) -> int:
-        """4*B*H*Nq*Nk*d with the true head dim (two GEMMs, 2 flops/MAC)."""
+        """4*B*H*Nq*Nk*d with the true head dim (two GEMMs, 2 flops/MAC);
+        summed over the sequences of a variable-length batch."""
+        if self.varlen:
+            return sum(4 * self.H * a * b * self.d for a, b in zip(self.seqlens_q, self.seqlens_k))
         return 4 * self.B * self.H * self.Nq * self.Nk * self.d
 
     @property
@@ -63,6 +84,8 @@ class Workload:
         """Algorithmic HBM bytes: Q, K, V read once, O written once, plus
         the bias tables."""
         e = 2
+        if self.varlen:
+            return 2 * self.H * (sum(self.seqlens_q) + sum(self.seqlens_k)) * self.d * e
         qo = 2 * self.B * self.H * self.Nq * self.d * e
         kv = 2 * self.B * self.H * self.Nk * self.d * e
         tab = 0
@@ -75,6 +98,9 @@ class Workload:
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
 
+
+# latent tokens of images of 512, 384, 256 and 448 pixels per side
+_SD_RAGGED = tuple([64 * 64, 48 * 48, 32 * 32, 56 * 56] * 4)
 
 WORKLOADS = {
     "toy": Workload("toy", B=1, H=2, Nq=64, Nk=64, d=32, dtype="bf16", bias="none", seed=0,
@@ -96,6 +122,11 @@ WORKLOADS = {
     "sd_unet_cross": Workload(
         "sd_unet_cross", B=16, H=8, Nq=4096, Nk=77, d=40, dtype="fp16", bias="none", seed=5,
         note="Stable Diffusion UNet cross-attention over 77 text tokens"),
+    "sd_unet_self_varlen": Workload(
+        "sd_unet_self_varlen", B=16, H=8, Nq=4096, Nk=4096, d=40, dtype="fp16", bias="none", seed=6,
+        seqlens_q=_SD_RAGGED, seqlens_k=_SD_RAGGED,
+        note="Stable Diffusion UNet self-attention over a nested batch of 16 images of "
+             "different sizes (latent grids 64x64, 48x48, 32x32, 56x56, four of each)"),
 }
 
 
@@ -118,6 +149,12 @@ def make_inputs(w: Workload, seed: int | None = None) -> Inputs:
     def normal(shape, std=1.0):
         return torch.randn(shape, generator=g, dtype=torch.float32) * std
 
+    if w.varlen:
+        tq, tk = sum(w.seqlens_q), sum(w.seqlens_k)
+        q = normal((w.H * tq, w.d)).to(dt)
+        k = normal((w.H * tk, w.d)).to(dt)
+        v = normal((w.H * tk, w.d)).to(dt)
+        return Inputs(q, k, v)
     q = normal((w.B, w.H, w.Nq, w.d)).to(dt)
     k = normal((w.B, w.H, w.Nk, w.d)).to(dt)
     v = normal((w.B, w.H, w.Nk, w.d)).to(dt)

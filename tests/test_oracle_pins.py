@@ -404,3 +404,80 @@ def test_swin_partition_without_shift_is_a_reshape():
     x = rng.standard_normal((1, 3, 3, 2, 5))  # one 3x3 window
     xw = oracle.swin_partition(x, 3, 0)
     np.testing.assert_array_equal(xw[0], x[0].reshape(9, 2, 5).transpose(1, 0, 2))
+
+
+# --------------------------------------------------- variable-length batch --
+# A nested tensor packs {tensor, mask}: the packed-batch attention must equal
+# attention over the zero-padded batch whose padded keys are masked out.
+
+def _packed_to_padded(x, cu, H, fill):
+    """[H * sum(L), d] packed as [H][L_s][d] per sequence -> [n, H, max L, d]."""
+    n, d = len(cu) - 1, x.shape[-1]
+    L = max(cu[s + 1] - cu[s] for s in range(n))
+    out = fill((n, H, L, d))
+    for s in range(n):
+        ls = cu[s + 1] - cu[s]
+        out[s, :, :ls] = x[H * cu[s]:H * cu[s + 1]].reshape(H, ls, d)
+    return out
+
+
+def test_varlen_equals_padded_batch_with_key_mask():
+    rng = np.random.default_rng(21)
+    H, d = 3, 8
+    lq = [5, 0, 17, 1, 9]
+    lk = [7, 4, 17, 1, 3]   # cross lengths, an empty query set, single tokens
+    cu_q = [0] + list(np.cumsum(lq))
+    cu_k = [0] + list(np.cumsum(lk))
+    q = rng.standard_normal((H * cu_q[-1], d))
+    k = rng.standard_normal((H * cu_k[-1], d))
+    v = rng.standard_normal((H * cu_k[-1], d))
+    scale = 0.37
+    got = oracle.attn_varlen(q, k, v, cu_q, cu_k, H, scale)
+    # padded rows and keys hold junk, not zeros, so a missing mask shows
+    junk = lambda shape: rng.standard_normal(shape) * 5.0  # noqa: E731
+    Qp = torch.from_numpy(_packed_to_padded(q, cu_q, H, junk))
+    Kp = torch.from_numpy(_packed_to_padded(k, cu_k, H, junk))
+    Vp = torch.from_numpy(_packed_to_padded(v, cu_k, H, junk))
+    mask = torch.zeros((len(lq), 1, Qp.shape[2], Kp.shape[2]), dtype=torch.bool)
+    for s, n in enumerate(lk):
+        mask[s, :, :, :n] = True
+    want = torch.nn.functional.scaled_dot_product_attention(Qp, Kp, Vp, attn_mask=mask, scale=scale).numpy()
+    for s in range(len(lq)):
+        if lq[s] == 0:
+            continue
+        blk = got[H * cu_q[s]:H * cu_q[s + 1]].reshape(H, lq[s], d)
+        np.testing.assert_allclose(blk, want[s, :, :lq[s]], rtol=0, atol=1e-12)
+
+
+def test_varlen_sequence_order_does_not_matter():
+    rng = np.random.default_rng(22)
+    H, d = 2, 4
+    lens = [6, 2, 11]
+    blocks_q = [rng.standard_normal((H * n, d)) for n in lens]
+    blocks_k = [rng.standard_normal((H * n, d)) for n in lens]
+    blocks_v = [rng.standard_normal((H * n, d)) for n in lens]
+    cu = [0] + list(np.cumsum(lens))
+    fwd = oracle.attn_varlen(np.concatenate(blocks_q), np.concatenate(blocks_k), np.concatenate(blocks_v),
+                             cu, cu, H, 0.5)
+    rl = lens[::-1]
+    rcu = [0] + list(np.cumsum(rl))
+    rev = oracle.attn_varlen(np.concatenate(blocks_q[::-1]), np.concatenate(blocks_k[::-1]),
+                             np.concatenate(blocks_v[::-1]), rcu, rcu, H, 0.5)
+    for s, n in enumerate(lens):
+        r = len(lens) - 1 - s
+        np.testing.assert_array_equal(fwd[H * cu[s]:H * cu[s + 1]], rev[H * rcu[r]:H * rcu[r + 1]])
+
+
+def test_varlen_single_key_returns_its_value():
+    rng = np.random.default_rng(23)
+    H, d = 2, 5
+    cu_q, cu_k = [0, 4, 7], [0, 1, 2]
+    q = rng.standard_normal((H * 7, d))
+    k = rng.standard_normal((H * 2, d))
+    v = rng.standard_normal((H * 2, d))
+    out = oracle.attn_varlen(q, k, v, cu_q, cu_k, H, 1.0)
+    for s in range(2):
+        lq = cu_q[s + 1] - cu_q[s]
+        blk = out[H * cu_q[s]:H * cu_q[s + 1]].reshape(H, lq, d)
+        for h in range(H):
+            np.testing.assert_array_equal(blk[h], np.broadcast_to(v[H * cu_k[s] + h], (lq, d)))
