@@ -199,14 +199,23 @@ class DeviceSets:
         self.bias = _gpu_bias(w, inp, dev, image)
 
 
+def _attn(w: Workload, q, k, v, out, bias, stream):
+    """One step through the public API: attn_fwd, or attn_fwd_varlen for a
+    nested batch."""
+    import scaled_dot_product_09_gb300 as sdpa
+    if w.varlen:
+        sdpa.attn_fwd_varlen(q, k, v, w.cu_seqlens_q, w.cu_seqlens_k, w.H, out=out, scale=w.scale, stream=stream)
+    else:
+        sdpa.attn_fwd(q, k, v, out=out, scale=w.scale, bias=bias, stream=stream)
+
+
 def _time_device(w: Workload, sets: DeviceSets, steps: int, warmup: int, stream):
     """Returns (total seconds of the K timed steps, number of launches)."""
     import scaled_dot_product_09_gb300 as sdpa
 
     def step(i):
         j = i % sets.n
-        sdpa.attn_fwd(sets.q[j], sets.k[j], sets.v[j], out=sets.o[j], scale=w.scale,
-                      bias=sets.bias, stream=stream)
+        _attn(w, sets.q[j], sets.k[j], sets.v[j], sets.o[j], sets.bias, stream)
 
     with torch.cuda.stream(stream):
         for i in range(max(warmup, 3)):
@@ -270,7 +279,7 @@ def _time_e2e(w: Workload, inp, steps: int, warmup: int, stream, dev, depth: int
         ev_in[j].record(s_in)
         stream.wait_event(ev_in[j])
         stream.wait_event(ev_out[j])  # the set's previous output has been copied back
-        sdpa.attn_fwd(dq, dk, dv, out=do, scale=w.scale, bias=bias, stream=stream)
+        _attn(w, dq, dk, dv, do, bias, stream)
         ev_run[j].record(stream)
         s_out.wait_event(ev_run[j])
         with torch.cuda.stream(s_out):
@@ -319,13 +328,21 @@ def _suite(stream, dev, peaks, names):
 
 
 def _oracle_sample(w: Workload, inp, budget_s: float, nthreads: int = 0):
-    """Time the oracle on whole slices until ~budget_s; returns
-    (TFLOP/s, seconds, slices, threads)."""
+    """Time the oracle on whole rows until ~budget_s; returns (TFLOP/s,
+    seconds, rows, threads).  A nested batch is sampled on its first
+    sequence."""
     import oracle
+    if w.varlen:
+        lq, lk = w.seqlens_q[0], w.seqlens_k[0]
+        q = inp.q[:w.H * lq].double().reshape(w.H, lq, w.d).numpy()
+        k = inp.k[:w.H * lk].double().reshape(w.H, lk, w.d).numpy()
+        v = inp.v[:w.H * lk].double().reshape(w.H, lk, w.d).numpy()
+        w = w.with_(B=1, Nq=lq, Nk=lk, seqlens_q=(), seqlens_k=())
+    else:
+        q = inp.q.double().reshape(w.B * w.H, w.Nq, w.d).numpy()
+        k = inp.k.double().reshape(w.B * w.H, w.Nk, w.d).numpy()
+        v = inp.v.double().reshape(w.B * w.H, w.Nk, w.d).numpy()
     BH = w.B * w.H
-    q = inp.q.double().reshape(BH, w.Nq, w.d).numpy()
-    k = inp.k.double().reshape(BH, w.Nk, w.d).numpy()
-    v = inp.v.double().reshape(BH, w.Nk, w.d).numpy()
     if w.bias == "swin":
         b = oracle.Bias("swin", table=inp.table.double().numpy(), win=w.win, grid_h=w.grid_h,
                         grid_w=w.grid_w, shift=w.shift)
@@ -363,13 +380,18 @@ def run_reference(args, w: Workload, world, rank):
     per_step_budget = max(0.05, min(5.0, 60.0 / max(1, steps + warmup)))
     for _ in range(warmup):
         _oracle_sample(w, inp, per_step_budget)
-    rates, secs, rows_total, used = [], 0.0, 0, 0
+    flops, secs, rows_total, used = 0.0, 0.0, 0, 0
     for _ in range(steps):
         tf, sec, rows, used = _oracle_sample(w, inp, per_step_budget)
-        rates.append(tf)
+        flops += tf * 1e12 * sec
         secs += sec
         rows_total += rows
-    value = (4.0 * rows_total * w.Nk * w.d) / secs / 1e12
+    value = flops / secs / 1e12
+    total = w.H * w.seqlens_q[0] if w.varlen else w.B * w.H * w.Nq
+    of_seq = " of the first sequence" if w.varlen else ""
+    rows_step = rows_total // steps
+    per = (f"{rows_step} of {total} query rows{of_seq}" if rows_step <= total
+           else f"{rows_step // total} whole passes over the {total} query rows{of_seq}")
     line = {
         "impl": "reference", "metric": args.metric, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": steps, "warmup": warmup,
@@ -378,8 +400,7 @@ def run_reference(args, w: Workload, world, rank):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
                    "bias": w.bias, "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
-                         "sample": f"{rows_total // steps} of {w.B * w.H * w.Nq} query rows per step "
-                                   "(whole rows, fp64 oracle, OpenMP over rows)"},
+                         "sample": f"{per} per step (whole rows, fp64 oracle, OpenMP over rows)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -417,9 +438,11 @@ def main(argv=None):
     if rank == 0 and world == 1 and not args.no_cpu:
         inp_cpu = make_inputs(w)
         tf, sec, rows, used = _oracle_sample(w, inp_cpu, 15.0)
-        total = w.B * w.H * w.Nq
+        total = w.H * w.seqlens_q[0] if w.varlen else w.B * w.H * w.Nq
         what = (f"{rows} of {total} query rows" if rows <= total
                 else f"{rows // total} whole passes over all {total} query rows")
+        if w.varlen:
+            what += " of the first sequence"
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
                "sample": f"{what} ({sec:.1f} s, fp64, OpenMP over rows)"}
 
@@ -458,7 +481,8 @@ def main(argv=None):
         del sets
         torch.cuda.empty_cache()
         suite = _suite(stream, dev, peaks, [n for n in ("swin_t_stage1@image", "sam_vith_window", "sam_vith_global",
-                                                        "sd_unet_self", "sd_unet_cross") if n != w.name])
+                                                        "sd_unet_self", "sd_unet_cross", "sd_unet_self_varlen")
+                                            if n != w.name])
     if rank == 0:
         line = {
             "metric": args.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,

@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define SDPA09_ABI_VERSION 2
+#define SDPA09_ABI_VERSION 3
 
 typedef enum {
     ATTN_BF16 = 0, /* bfloat16 Q/K/V/O ("model.to(torch.bfloat16)" in the SAM rewrite) */
@@ -133,6 +133,37 @@ enum {
 int attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int H, int Nq,
              int Nk, int d, float scale, attn_dtype dtype, attn_bias_kind bias_kind,
              const void* bias_args, void* stream);
+
+/* attn_fwd_varlen -- attention over a batch of sequences of different
+ * lengths packed in one buffer, each sequence attending only to itself: a
+ * nested tensor ("PyTorch团队重写「分割一切」模型" and its translations: Nested
+ * Tensor batches data of non-uniform size, such as images of different
+ * sizes, in one tensor, packing {tensor, mask}).  For sequence s with
+ * Lq_s = cu_seqlens_q[s+1] - cu_seqlens_q[s] queries and Lk_s keys,
+ * O_s = softmax(scale * Q_s.K_s^T) . V_s per head, no bias -- the same as a
+ * padded batch whose padded keys are masked out.
+ *
+ *  q, out     device, the concatenation over s of [H][Lq_s][d]: the buffer of
+ *             a contiguous (n_seq, H, Lq*, d) nested tensor; out is fully
+ *             overwritten and must not alias q, k or v.
+ *  k, v       device, the concatenation over s of [H][Lk_s][d].
+ *  cu_seqlens_q, cu_seqlens_k
+ *             HOST int32 [n_seq + 1]: token offsets, starting at 0 and
+ *             nondecreasing; read during the call.  Lk_s >= 1 wherever
+ *             Lq_s >= 1; Lk_s <= 2^20.
+ *  n_seq      1 .. ATTN_VARLEN_MAX_SEQ sequences.
+ *  H, d, scale, dtype, stream   as for attn_fwd.
+ *
+ * Returns ATTN_OK (also when no sequence has a query: then nothing is
+ * launched and the tensor pointers may be null), ATTN_ERR_ARG,
+ * ATTN_ERR_UNSUPPORTED (more than ATTN_VARLEN_MAX_SEQ sequences, d > 128)
+ * or ATTN_ERR_CUDA.  Inputs must be finite: a tile's rows past its
+ * sequence are read from the next one and weighted by zero.
+ */
+#define ATTN_VARLEN_MAX_SEQ 128
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, const int* cu_seqlens_q,
+                    const int* cu_seqlens_k, int n_seq, int H, int d, float scale, attn_dtype dtype,
+                    void* stream);
 
 /* attn_debug_bias -- test hook for the in-kernel bias builders.
  *

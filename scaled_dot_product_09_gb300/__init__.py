@@ -21,7 +21,7 @@ import math
 import os
 import threading
 
-__all__ = ["attn_fwd", "attn_debug_bias", "attn_device_status", "selftest_wait_timeout", "SwinBias", "SamBias",
+__all__ = ["attn_fwd", "attn_fwd_varlen", "attn_debug_bias", "attn_device_status", "selftest_wait_timeout", "SwinBias", "SamBias",
            "load_library", "AttnError", "ATTN_OK", "ATTN_ERR_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT", "HEADER_SYMBOLS"]
 
@@ -31,8 +31,9 @@ ATTN_BIAS_NONE, ATTN_BIAS_SWIN, ATTN_BIAS_SAM_RELPOS = 0, 1, 2
 ATTN_SWIN_WINDOWS, ATTN_SWIN_IMAGE = 0, 1
 
 # Every extern "C" function include/sdpa09.h declares.
-HEADER_SYMBOLS = ("attn_fwd", "attn_debug_bias", "attn_device_status", "attn_selftest_wait_timeout",
-                  "attn_last_error", "attn_abi_version")
+HEADER_SYMBOLS = ("attn_fwd", "attn_fwd_varlen", "attn_debug_bias", "attn_device_status",
+                  "attn_selftest_wait_timeout", "attn_last_error", "attn_abi_version")
+ATTN_VARLEN_MAX_SEQ = 128
 
 _lock = threading.Lock()
 _lib = None
@@ -106,6 +107,9 @@ def load_library(build: bool = True):
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp]
         lib.attn_fwd.restype = i
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, ip, ip, i, i, i, f, i, vp]
+        lib.attn_fwd_varlen.restype = i
         lib.attn_debug_bias.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp]
         lib.attn_debug_bias.restype = i
         lib.attn_device_status.argtypes = [vp]
@@ -192,6 +196,37 @@ def attn_fwd(q, k, v, out=None, scale=None, bias=None, stream=None):
     kind, _keep, args = _bias_args(bias)
     rc = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Nq, Nk, d, scale,
                       _dtype_code(q), kind, args, _stream_ptr(stream))
+    _check(lib, rc)
+    return out
+
+
+def _cu_array(cu):
+    vals = [int(x) for x in (cu.tolist() if hasattr(cu, "tolist") else cu)]
+    return (ctypes.c_int * len(vals))(*vals), vals
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, H, out=None, scale=None, stream=None):
+    """Attention over a nested batch of sequences of different lengths,
+    each attending only to itself (no bias).  q/out hold the concatenation
+    over sequences s of [H][Lq_s][d], k/v of [H][Lk_s][d], as contiguous
+    bf16/fp16 CUDA tensors whose last dim is d (e.g. [H * total, d]);
+    cu_seqlens_q/k are the host token offsets [n_seq + 1] (list, numpy or CPU
+    tensor).  Returns out."""
+    import torch
+    lib = load_library()
+    cq, vq = _cu_array(cu_seqlens_q)
+    ck, vk = _cu_array(cu_seqlens_k)
+    if len(vq) != len(vk) or len(vq) < 2:
+        raise AttnError(ATTN_ERR_ARG, "cu_seqlens_q and cu_seqlens_k need the same n_seq + 1 >= 2 entries")
+    d = q.shape[-1]
+    for t, tot in ((q, vq[-1]), (k, vk[-1]), (v, vk[-1])):
+        if not t.is_contiguous() or t.shape[-1] != d or t.numel() != H * tot * d:
+            raise AttnError(ATTN_ERR_ARG, "q, k, v must be contiguous with H * total tokens rows of d")
+    if out is None:
+        out = torch.empty_like(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib.attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), cq, ck, len(vq) - 1, H, d, scale,
+                             _dtype_code(q), _stream_ptr(stream))
     _check(lib, rc)
     return out
 

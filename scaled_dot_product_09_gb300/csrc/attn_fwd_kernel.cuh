@@ -122,6 +122,80 @@ struct AttnParams {
     int s_h, s_w, n_rh, n_rw;
 };
 
+// Variable-length batches (no bias, shared tiling): Q/O are the concatenation
+// over sequences s of [H][Lq_s][d] and K/V of [H][Lk_s][d] -- the buffer of a
+// nested tensor of (B, H, N*, d) -- and each sequence attends to itself only
+// ("PyTorch团队重写「分割一切」模型" on Nested Tensor: data of non-uniform
+// size, e.g. images of different sizes, batched in one tensor).  The table
+// travels by value with the launch.  Its entries are the sequences that have
+// queries, longest key range first, so that the CTAs' round-robin share of
+// the jobs comes out even (longest-processing-time order).
+constexpr int kVarlenMaxSeq = 128;
+struct VarlenTable {
+    int n_seq;                      // entries
+    int jobs_end[kVarlenMaxSeq];    // jobs of entries 0..s; an entry has H * ceil(Lq / 256)
+    int q_off[kVarlenMaxSeq];       // first token of the entry's sequence in Q/O
+    int q_len[kVarlenMaxSeq];       // and its query count (>= 1)
+    int k_off[kVarlenMaxSeq];       // first token in K/V
+    int k_len[kVarlenMaxSeq];       // key count (>= 1)
+};
+template <bool VL>
+struct VarlenArg {
+    int unused;
+};
+template <>
+struct VarlenArg<true> : VarlenTable {};
+
+// Rows of one shared-tiling job: TMA coordinates (row, slice) of its first
+// query row (slot A) and of its key row 0, the row of its slice's token 0 in
+// the output viewed as [rows][d], its query and key counts and key tiles.
+struct JobRows {
+    int q_row, q_slice, k_row, k_slice;
+    int out_row0;  // output row of token 0 of the job's (sequence, head) slice
+    int q0;        // token of the job's first query row within the slice
+    int nq, nk, n_kv;
+};
+template <bool VL>
+__device__ __forceinline__ JobRows shared_job(const AttnParams& p, const VarlenArg<VL>& vt, int job) {
+    JobRows j;
+    if constexpr (!VL) {
+        const int slice = job / p.q_jobs;
+        j.q0 = (job - slice * p.q_jobs) * 2 * kBlockM;
+        j.q_row = j.q0;
+        j.q_slice = slice;
+        j.k_row = 0;
+        j.k_slice = slice;
+        j.out_row0 = slice * p.Nq;
+        j.nq = p.Nq;
+        j.nk = p.Nk;
+        j.n_kv = p.n_kv;
+    } else {
+        // the entry: the first whose job range ends past `job`
+        int lo = 0, hi = vt.n_seq - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (vt.jobs_end[mid] > job) hi = mid;
+            else lo = mid + 1;
+        }
+        const int s = lo;
+        const int local = job - (s > 0 ? vt.jobs_end[s - 1] : 0);
+        const int lq = vt.q_len[s];
+        const int lk = vt.k_len[s];
+        const int nqb = (lq + 2 * kBlockM - 1) / (2 * kBlockM);
+        const int h = local / nqb;
+        j.q0 = (local - h * nqb) * 2 * kBlockM;
+        j.out_row0 = p.H * vt.q_off[s] + h * lq;
+        j.q_row = j.out_row0 + j.q0;
+        j.q_slice = 0;
+        j.k_row = p.H * vt.k_off[s] + h * lk;
+        j.k_slice = 0;
+        j.nq = lq;
+        j.nk = lk;
+        j.n_kv = (lk + p.kv_w - 1) / p.kv_w;
+    }
+    return j;
+}
+
 // Shared memory after the ring ("extra"):
 //   Swin (separate mode, slot SL), rows variant: per head an fp32 bias matrix
 //        [SL query tokens][SL key tokens] (16-byte chunks of a row XOR-swizzled
@@ -444,9 +518,9 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
         mma_ts(o_tmem, p_tmem + ks * 8, vd + (uint64_t)(ks * (512 / 16)), idesc, (accumulate || ks > 0) ? 1u : 0u);
 }
 
-template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG>
+template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ TmaMaps tm, const AttnParams p) {
+    attn_fwd_kernel(const __grid_constant__ TmaMaps tm, const AttnParams p, const __grid_constant__ VarlenArg<VL> vt) {
     using T = Tile<DPAD>;
     static_assert(MODE == kModeShared || (SL == 32 || SL == 64 || SL == 128), "slot size");
     // Key columns of a score tile (S MMA N, P.V K): 128, or narrower in shared
@@ -800,8 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int ju = 0;
             for (int job = job0; ok && job < p.n_jobs; job += job_step, ++ju) {
                 if constexpr (MODE == kModeShared) {
-                    const int slice = job / p.q_jobs;
-                    const int q0 = (job % p.q_jobs) * 2 * kBlockM;
+                    const JobRows jr = shared_job<VL>(p, vt, job);
                     const int qb = ju % p.nq;
                     for (int x = 0; x < 2; ++x) {
                         if (ju >= p.nq &&
@@ -811,10 +884,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         unsigned char* dq = sQ + (x * p.nq + qb) * T::kBytes;
                         mbar_arrive_expect_tx(&bar_q_full[x][qb], q_tx);
-                        tma_load_4d(dq, &tm.q, &bar_q_full[x][qb], 0, q0 + x * kBlockM, slice, 0);
-                        if (p.part) tma_load_3d(dq + p.full_atoms * kBlockM * 32, &tm.qp, &bar_q_full[x][qb], 0, q0 + x * kBlockM, slice);
+                        tma_load_4d(dq, &tm.q, &bar_q_full[x][qb], 0, jr.q_row + x * kBlockM, jr.q_slice, 0);
+                        if (p.part)
+                            tma_load_3d(dq + p.full_atoms * kBlockM * 32, &tm.qp, &bar_q_full[x][qb], 0, jr.q_row + x * kBlockM,
+                                        jr.q_slice);
                     }
-                    const int n_uses = p.n_kv + (BIAS == kBiasSam ? 1 : 0);
+                    const int n_uses = jr.n_kv + (BIAS == kBiasSam ? 1 : 0);
                     for (int u = 0; ok && u < n_uses; ++u) {
                         const int st = ring % nst;
                         if (ring >= nst &&
@@ -836,12 +911,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (p.part) tma_load_2d(dv + p.full_atoms * kBlockN * 32, &tm.rhp, &bar_full_v[st], 0, 0);
                         } else {
                             const int j = u - (BIAS == kBiasSam ? 1 : 0);
+                            const int kr = jr.k_row + j * p.kv_w;
                             mbar_arrive_expect_tx(&bar_full_k[st], kv_tx);
-                            tma_load_4d(dk, &tm.k, &bar_full_k[st], 0, j * p.kv_w, slice, 0);
-                            if (p.part) tma_load_3d(dk + p.full_atoms * kBlockN * 32, &tm.kp, &bar_full_k[st], 0, j * p.kv_w, slice);
+                            tma_load_4d(dk, &tm.k, &bar_full_k[st], 0, kr, jr.k_slice, 0);
+                            if (p.part) tma_load_3d(dk + p.full_atoms * kBlockN * 32, &tm.kp, &bar_full_k[st], 0, kr, jr.k_slice);
                             mbar_arrive_expect_tx(&bar_full_v[st], kv_tx);
-                            tma_load_4d(dv, &tm.v, &bar_full_v[st], 0, j * p.kv_w, slice, 0);
-                            if (p.part) tma_load_3d(dv + p.full_atoms * kBlockN * 32, &tm.vp, &bar_full_v[st], 0, j * p.kv_w, slice);
+                            tma_load_4d(dv, &tm.v, &bar_full_v[st], 0, kr, jr.k_slice, 0);
+                            if (p.part) tma_load_3d(dv + p.full_atoms * kBlockN * 32, &tm.vp, &bar_full_v[st], 0, kr, jr.k_slice);
                         }
                     }
                 } else {
@@ -957,7 +1033,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_commit(&bar_empty[st]);
                         ++ring;
                     }
-                    const int n = p.n_kv;
+                    const int n = shared_job<VL>(p, vt, job).n_kv;
                     {
                         const int st = ring % nst;
                         if (!waitb(&bar_full_k[st], (ring / nst) & 1, kStatusWaitK)) { ok = false; break; }
@@ -1131,10 +1207,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ------------------------------------------------- row of this job
             int my_slice, my_tok, my_sl = 0;
             bool row_ok;
+            JobRows jr{};
             if constexpr (MODE == kModeShared) {
-                my_slice = job / p.q_jobs;
-                my_tok = (job % p.q_jobs) * 2 * kBlockM + x * kBlockM + r;
-                row_ok = my_tok < p.Nq;
+                jr = shared_job<VL>(p, vt, job);
+                my_slice = jr.q_slice;
+                my_tok = jr.q0 + x * kBlockM + r;
+                row_ok = my_tok < jr.nq;
             } else {
                 const int tile = 2 * job + x;
                 my_sl = r / SL;
@@ -1293,7 +1371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // ------------------------------------------------------ key tiles
                 float m_run = -INFINITY;
-                for (int j = 0; j < p.n_kv; ++j) {
+                for (int j = 0; j < jr.n_kv; ++j) {
                     __syncwarp();
                     if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[x], cnt_s & 1, abort_flag, kStatusWaitS))) { ok = false; break; }
                     ++cnt_s;
@@ -1311,7 +1389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         warp_arrive(&bar_sfree[x]);
                     }
                     const int key0 = j * p.kv_w;
-                    const int hi = min(p.kv_w, p.Nk - key0);  // valid key columns [0, hi)
+                    const int hi = min(p.kv_w, jr.nk - key0);  // valid key columns [0, hi)
                     float m_tile;  // log2 units
                     float sc;      // multiplier applied to xs in the exponent
                     if (BIAS == kBiasNone && !DBG) {
@@ -1427,7 +1505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_o[x], ju & 1, abort_flag, kStatusWaitO))) { ok = false; break; }
             tc_fence_after();
-            epilogue(tO, l_run, my_slice, my_tok, row_ok, MODE == kModeShared ? ju % p.nq : 0);
+            if constexpr (VL)  // output rows counted from the buffer start
+                epilogue(tO, l_run, 0, jr.out_row0 + my_tok, row_ok, ju % p.nq);
+            else
+                epilogue(tO, l_run, my_slice, my_tok, row_ok, MODE == kModeShared ? ju % p.nq : 0);
         }
         if constexpr (kDblO) {
             if (ok && ju > 0) {

@@ -17,11 +17,12 @@ struct LaunchArgs {
     int grid;
     size_t smem;
     cudaStream_t stream;
+    const VarlenTable* vt;  // variable-length batch table, or null
 };
 
-template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG>
+template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL = false>
 cudaError_t launch_one(const LaunchArgs& a) {
-    auto kern = attn_fwd_kernel<DPAD, BIAS, MODE, SW, SL, DBG>;
+    auto kern = attn_fwd_kernel<DPAD, BIAS, MODE, SW, SL, DBG, VL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a.smem);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the CTAs may become resident while the
@@ -37,7 +38,9 @@ cudaError_t launch_one(const LaunchArgs& a) {
     cfg.stream = a.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, *a.tm, *a.p);
+    VarlenArg<VL> vt{};
+    if constexpr (VL) static_cast<VarlenTable&>(vt) = *a.vt;
+    e = cudaLaunchKernelEx(&cfg, kern, *a.tm, *a.p, vt);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -56,6 +59,10 @@ cudaError_t launch_attn(const LaunchArgs& a);
 // for head dims up to 64 only.
 template <int DPAD>
 cudaError_t launch_attn_none(const LaunchArgs& a) {
+    if (a.vt) {
+        if (a.mode != kModeShared || a.sw != 0 || a.dbg) return cudaErrorInvalidValue;
+        return launch_one<DPAD, kBiasNone, kModeShared, 0, 0, false, true>(a);
+    }
     if (a.mode == kModeShared) {
         if constexpr (DPAD <= 64)
             if (a.sw == 80) return launch_dbg<DPAD, kBiasNone, kModeShared, 80, 0>(a);

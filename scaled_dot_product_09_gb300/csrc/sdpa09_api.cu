@@ -9,12 +9,12 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
-#include <algorithm>
 #include <mutex>
 #include <string>
 
@@ -231,9 +231,11 @@ constexpr size_t kSmemBudget = 227 * 1024 - 1024 - 1024;
 // largest Swin bias-row area (per-head fp32 matrices + region bits)
 constexpr size_t kSwinRowsMax = 96 * 1024;
 
+// vt: a variable-length batch (no bias): B = 1, Nq / Nk = total query / key
+// tokens of all sequences, the operands viewed as [H * total][d] rows.
 int run(const void* q, const void* k, const void* v, void* out, float* dbg, int B, int H, int Nq,
         int Nk, int d, float scale, attn_dtype dtype, attn_bias_kind bias_kind,
-        const void* bias_args, void* stream) {
+        const void* bias_args, void* stream, const VarlenTable* vt = nullptr) {
     g_last_error.clear();
     if (!q || !k || !v || !(out || dbg)) return fail(ATTN_ERR_ARG, "null tensor pointer");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out ? out : (void*)dbg))
@@ -246,7 +248,7 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
     const int64_t BH = (int64_t)B * H;
     if (BH * Nq >= (int64_t(1) << 31) || BH * Nk >= (int64_t(1) << 31))
         return fail(ATTN_ERR_UNSUPPORTED, "B*H*N must stay below 2^31 rows");
-    if (Nk > (1 << 20)) return fail(ATTN_ERR_UNSUPPORTED, "Nk > 2^20");
+    if (!vt && Nk > (1 << 20)) return fail(ATTN_ERR_UNSUPPORTED, "Nk > 2^20");
     const size_t q_bytes = (size_t)BH * Nq * d * 2, kv_bytes = (size_t)BH * Nk * d * 2;
     if (out && (overlaps(out, q_bytes, q, q_bytes) || overlaps(out, q_bytes, k, kv_bytes) ||
                 overlaps(out, q_bytes, v, kv_bytes)))
@@ -330,7 +332,7 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
     // ---- job layout
     const int nmax = std::max(Nq, Nk);
     const int sl = nmax <= 32 ? 32 : (nmax <= 64 ? 64 : 128);
-    const bool separate = bias == kBiasSwin || (bias == kBiasNone && sl <= 64 && dpad <= 64);
+    const bool separate = !vt && (bias == kBiasSwin || (bias == kBiasNone && sl <= 64 && dpad <= 64));
     int mode;
     if (separate) {
         mode = kModeSeparate;
@@ -367,14 +369,15 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         p.g = 1;
         // no bias and every key in one tile of at most 80 (e.g. 77 text tokens):
         // 80-column score tiles, P.V over 80 keys
-        if (bias == kBiasNone && Nk <= 80 && dpad <= 64) sw_spec = 80;
+        if (!vt && bias == kBiasNone && Nk <= 80 && dpad <= 64) sw_spec = 80;
         // SAM key tiles start on grid rows: 112 keys (8 rows) on the 14-wide
         // grid, 128 (2 rows) on the 64-wide one
         p.kv_w = (bias == kBiasSam && sw_spec) ? (sw_spec == 14 ? 112 : (kBlockN / sw_spec) * sw_spec) : kBlockN;
         p.kv_cols = kBlockN;  // unused by the kernel: its key-tile width is a compile-time constant
         p.n_kv = (Nk + p.kv_w - 1) / p.kv_w;
         p.q_jobs = (Nq + 2 * kBlockM - 1) / (2 * kBlockM);
-        const int64_t nj = BH * p.q_jobs;
+        // a variable-length batch has H * ceil(Lq_s / 256) jobs per sequence
+        const int64_t nj = vt ? (int64_t)vt->jobs_end[vt->n_seq - 1] : BH * p.q_jobs;
         if (nj > 0x7fffffff) return fail(ATTN_ERR_UNSUPPORTED, "too many jobs");
         p.n_jobs = (int)nj;
         p.box_q = kBlockM;
@@ -415,6 +418,11 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         if ((rc = encode_operand(&tm.q, &tm.qp, q, bf, d, Nq, BH, atoms, sl, p.g))) return rc;
         if ((rc = encode_operand(&tm.k, &tm.kp, k, bf, d, Nk, BH, atoms, sl, p.g))) return rc;
         if ((rc = encode_operand(&tm.v, &tm.vp, v, bf, d, Nk, BH, atoms, sl, p.g))) return rc;
+    } else if (vt) {
+        // one slice of H * total rows: a job addresses its sequence's rows
+        if ((rc = encode_operand(&tm.q, &tm.qp, q, bf, d, BH * Nq, 1, atoms, kBlockM, 1))) return rc;
+        if ((rc = encode_operand(&tm.k, &tm.kp, k, bf, d, BH * Nk, 1, atoms, kBlockN, 1))) return rc;
+        if ((rc = encode_operand(&tm.v, &tm.vp, v, bf, d, BH * Nk, 1, atoms, kBlockN, 1))) return rc;
     } else {
         if ((rc = encode_operand(&tm.q, &tm.qp, q, bf, d, Nq, BH, atoms, kBlockM, 1))) return rc;
         if ((rc = encode_operand(&tm.k, &tm.kp, k, bf, d, Nk, BH, atoms, kBlockN, 1))) return rc;
@@ -439,6 +447,7 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
     la.grid = grid;
     la.smem = smem;
     la.stream = static_cast<cudaStream_t>(stream);
+    la.vt = vt;
     cudaError_t e = dispatch(dpad, bias, la);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     static const bool debug_env = getenv("SDPA09_DEBUG") && getenv("SDPA09_DEBUG")[0] == '1';
@@ -457,6 +466,51 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int 
     if (!out) return sdpa09::fail(ATTN_ERR_ARG, "null output pointer");
     return sdpa09::run(q, k, v, out, nullptr, B, H, Nq, Nk, d, scale, dtype, bias_kind, bias_args,
                        stream);
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, const int* cu_seqlens_q,
+                    const int* cu_seqlens_k, int n_seq, int H, int d, float scale, attn_dtype dtype,
+                    void* stream) {
+    using sdpa09::fail;
+    static_assert(ATTN_VARLEN_MAX_SEQ == sdpa09::kVarlenMaxSeq, "header and kernel table sizes");
+    sdpa09::g_last_error.clear();
+    if (!cu_seqlens_q || !cu_seqlens_k) return fail(ATTN_ERR_ARG, "null cu_seqlens pointer");
+    if (n_seq < 1) return fail(ATTN_ERR_ARG, "n_seq must be >= 1");
+    if (n_seq > sdpa09::kVarlenMaxSeq)
+        return fail(ATTN_ERR_UNSUPPORTED, "more than %d sequences", sdpa09::kVarlenMaxSeq);
+    if (H < 1) return fail(ATTN_ERR_ARG, "H must be >= 1");
+    if (cu_seqlens_q[0] != 0 || cu_seqlens_k[0] != 0) return fail(ATTN_ERR_ARG, "cu_seqlens must start at 0");
+    int order[sdpa09::kVarlenMaxSeq];
+    int n_q = 0;  // sequences with queries
+    for (int s = 0; s < n_seq; ++s) {
+        const int lq = cu_seqlens_q[s + 1] - cu_seqlens_q[s], lk = cu_seqlens_k[s + 1] - cu_seqlens_k[s];
+        if (lq < 0 || lk < 0) return fail(ATTN_ERR_ARG, "cu_seqlens must be nondecreasing (sequence %d)", s);
+        if (lq > 0 && lk == 0) return fail(ATTN_ERR_ARG, "sequence %d has queries but no keys", s);
+        if (lk > (1 << 20)) return fail(ATTN_ERR_UNSUPPORTED, "sequence %d has more than 2^20 keys", s);
+        if (lq > 0) order[n_q++] = s;
+    }
+    // longest key range first: the CTAs take jobs round-robin, and this
+    // order evens out their totals
+    std::stable_sort(order, order + n_q, [&](int a, int b) {
+        return cu_seqlens_k[a + 1] - cu_seqlens_k[a] > cu_seqlens_k[b + 1] - cu_seqlens_k[b];
+    });
+    sdpa09::VarlenTable vt;
+    memset(&vt, 0, sizeof(vt));
+    vt.n_seq = n_q;
+    int64_t jobs = 0;
+    for (int e = 0; e < n_q; ++e) {
+        const int s = order[e];
+        vt.q_off[e] = cu_seqlens_q[s];
+        vt.q_len[e] = cu_seqlens_q[s + 1] - cu_seqlens_q[s];
+        vt.k_off[e] = cu_seqlens_k[s];
+        vt.k_len[e] = cu_seqlens_k[s + 1] - cu_seqlens_k[s];
+        jobs += (int64_t)H * ((vt.q_len[e] + 2 * sdpa09::kBlockM - 1) / (2 * sdpa09::kBlockM));
+        if (jobs > 0x7fffffff) return fail(ATTN_ERR_UNSUPPORTED, "too many jobs");
+        vt.jobs_end[e] = (int)jobs;
+    }
+    if (jobs == 0) return ATTN_OK;  // no sequence has a query (the tensors may be empty)
+    return sdpa09::run(q, k, v, out, nullptr, 1, H, cu_seqlens_q[n_seq], cu_seqlens_k[n_seq], d, scale, dtype,
+                       ATTN_BIAS_NONE, nullptr, stream, &vt);
 }
 
 int attn_debug_bias(const void* q, const void* k, const void* v, float* bias_out, int B, int H,

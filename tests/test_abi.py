@@ -41,8 +41,8 @@ def test_library_targets_sm103a_only():
 
 
 def test_abi_version(lib):
-    # 2: attn_swin_args gained its token layout field
-    assert lib.attn_abi_version() == 2
+    # 2: attn_swin_args gained its token layout field; 3: attn_fwd_varlen
+    assert lib.attn_abi_version() == 3
 
 
 def _call(lib, q=FAKE, k=FAKE + 4096, v=FAKE + 8192, out=FAKE + 1 << 20, B=1, H=1, Nq=64, Nk=64,
@@ -131,3 +131,36 @@ def test_selftest_limit_checked_before_cuda(lib):
     assert lib.attn_selftest_wait_timeout(0, None) == sdpa.ATTN_ERR_ARG
     assert lib.attn_selftest_wait_timeout(2000001, None) == sdpa.ATTN_ERR_ARG
     assert b"limit_us" in lib.attn_last_error()
+
+
+def _varlen(lib, cu_q, cu_k, n_seq=None, H=2, d=32, q=FAKE, out=FAKE + (1 << 20)):
+    cq = (ctypes.c_int * len(cu_q))(*cu_q)
+    ck = (ctypes.c_int * len(cu_k))(*cu_k)
+    n = len(cu_q) - 1 if n_seq is None else n_seq
+    return lib.attn_fwd_varlen(q, FAKE + 4096, FAKE + 8192, out, cq, ck, n, H, d, 0.125, 0, None)
+
+
+def test_varlen_argument_checks(lib):
+    ok_q, ok_k = [0, 5, 9], [0, 3, 9]
+    assert _varlen(lib, ok_q, ok_k, q=None) == sdpa.ATTN_ERR_ARG
+    assert _varlen(lib, ok_q, ok_k, n_seq=0) == sdpa.ATTN_ERR_ARG
+    assert _varlen(lib, ok_q, ok_k, H=0) == sdpa.ATTN_ERR_ARG
+    assert _varlen(lib, [1, 5, 9], ok_k) == sdpa.ATTN_ERR_ARG            # does not start at 0
+    assert _varlen(lib, [0, 5, 4], ok_k) == sdpa.ATTN_ERR_ARG            # decreasing
+    assert b"nondecreasing" in lib.attn_last_error()
+    assert _varlen(lib, [0, 5, 9], [0, 0, 9]) == sdpa.ATTN_ERR_ARG       # queries without keys
+    assert b"no keys" in lib.attn_last_error()
+    assert _varlen(lib, ok_q, ok_k, d=36) == sdpa.ATTN_ERR_ARG           # checked as for attn_fwd
+    big = list(range(0, 130))
+    assert _varlen(lib, big, big) == sdpa.ATTN_ERR_UNSUPPORTED           # 129 sequences
+    # no sequence has a query: nothing to launch
+    assert _varlen(lib, [0, 0, 0], [0, 4, 4]) == sdpa.ATTN_OK
+
+
+def test_varlen_binding_checks():
+    import torch
+    q = torch.zeros(2 * 9, 32, dtype=torch.float16)
+    with pytest.raises(sdpa.AttnError):
+        sdpa.attn_fwd_varlen(q, q, q, [0, 5, 9], [0, 4], H=2)             # different n_seq
+    with pytest.raises(sdpa.AttnError):
+        sdpa.attn_fwd_varlen(q, q, q, [0, 5, 10], [0, 4, 9], H=2)        # q too short for the offsets

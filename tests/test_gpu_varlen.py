@@ -1,0 +1,109 @@
+"""GPU parity of the variable-length (nested) batch: each sequence of a packed
+[H][L_s][d] batch attends only to itself.  The CUDA path, through the C ABI,
+against the fp64 oracle on the same seeded inputs; tolerance as for attn_fwd
+(max |err| <= 2e-2, mean |err| <= 2e-3)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scaled_dot_product_09_gb300 as sdpa
+from scaled_dot_product_09_gb300.workloads import WORKLOADS, Workload, make_inputs
+
+from gpu_util import compare, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _varlen_workload(lq, lk, H=4, d=64, dtype="fp16", seed=30):
+    return Workload("varlen_case", B=len(lq), H=H, Nq=max(lq), Nk=max(lk), d=d, dtype=dtype, bias="none",
+                    seed=seed, seqlens_q=tuple(lq), seqlens_k=tuple(lk))
+
+
+def _run(w, inp):
+    require_gpu()
+    q, k, v = (x.cuda() for x in (inp.q, inp.k, inp.v))
+    out = sdpa.attn_fwd_varlen(q, k, v, w.cu_seqlens_q, w.cu_seqlens_k, w.H, scale=w.scale)
+    torch.cuda.synchronize()
+    assert sdpa.attn_device_status() == sdpa.ATTN_OK
+    return out.cpu()
+
+
+def _full(w):
+    inp = make_inputs(w)
+    got = _run(w, inp).double().numpy()
+    want = oracle.attn_varlen(inp.q.double().numpy(), inp.k.double().numpy(), inp.v.double().numpy(),
+                              w.cu_seqlens_q, w.cu_seqlens_k, w.H, w.scale)
+    # rows of sequences without queries do not exist; every row of q is some sequence's
+    return compare(got, want, what=w.name)
+
+
+def test_varlen_mixed_lengths():
+    # tile-edge lengths (255/256/257), one token, an empty sequence, long ones
+    lens = [300, 1, 0, 257, 1000, 77, 256, 513, 255]
+    _full(_varlen_workload(lens, lens))
+
+
+def test_varlen_cross_lengths():
+    # queries and keys of different lengths per sequence (one key; many keys)
+    _full(_varlen_workload([129, 7, 600, 64], [1, 300, 129, 1100], seed=31))
+
+
+def test_varlen_bf16_partial_column_block():
+    # d = 40: two full 16-column blocks and a partial one
+    lens = [200, 450, 31]
+    _full(_varlen_workload(lens, lens, H=8, d=40, dtype="bf16", seed=32))
+
+
+@pytest.mark.parametrize("d", [32, 80, 128])
+def test_varlen_head_dims(d):
+    lens = [130, 390]
+    _full(_varlen_workload(lens, lens, H=2, d=d, seed=33 + d))
+
+
+def test_varlen_many_sequences():
+    # the most sequences one call takes, lengths 1..300
+    rng = np.random.default_rng(40)
+    lens = [int(x) for x in rng.integers(1, 301, sdpa.ATTN_VARLEN_MAX_SEQ)]
+    _full(_varlen_workload(lens, lens, H=2, d=32, seed=41))
+
+
+def test_varlen_no_queries_is_a_no_op():
+    require_gpu()
+    k = torch.randn(2 * 5, 32, dtype=torch.float16, device="cuda")
+    q = torch.empty(0, 32, dtype=torch.float16, device="cuda")
+    out = sdpa.attn_fwd_varlen(q, k, k, [0, 0, 0], [0, 2, 5], H=2)
+    assert out.numel() == 0
+
+
+def test_varlen_single_sequence_matches_attn_fwd_bit_for_bit():
+    """One sequence's [H][L][d] block is attn_fwd's [1][H][L][d] layout; both
+    run the shared tiling with 128-key tiles, so the bits agree (rows and keys
+    past the sequence are weighted by exact zeros in either)."""
+    w = _varlen_workload([1000], [1000], H=2, d=64, seed=42)
+    inp = make_inputs(w)
+    got = _run(w, inp)
+    q, k, v = (x.reshape(1, w.H, 1000, w.d).cuda() for x in (inp.q, inp.k, inp.v))
+    ref = sdpa.attn_fwd(q, k, v, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), ref.cpu().reshape(-1, w.d).view(torch.int16))
+
+
+def test_varlen_full_size_sampled():
+    """The ragged Stable Diffusion batch at full size; the oracle computes a
+    sample of rows one by one (first, last and random rows of every sequence
+    and head)."""
+    w = WORKLOADS["sd_unet_self_varlen"]
+    inp = make_inputs(w)
+    got = _run(w, inp).double().numpy()
+    rng = np.random.default_rng(43)
+    q, k, v = (x.double().numpy() for x in (inp.q, inp.k, inp.v))
+    cq, ck, H, d = w.cu_seqlens_q, w.cu_seqlens_k, w.H, w.d
+    for s in range(w.B):
+        lq, lk = cq[s + 1] - cq[s], ck[s + 1] - ck[s]
+        qs = q[H * cq[s]:H * cq[s + 1]].reshape(H, lq, d)
+        ks = k[H * ck[s]:H * ck[s + 1]].reshape(H, lk, d)
+        vs = v[H * ck[s]:H * ck[s + 1]].reshape(H, lk, d)
+        ids = np.unique(np.concatenate([[0, lq - 1, H * lq - 1], rng.integers(0, H * lq, 6)]))
+        want, _ = oracle.attn_rows(qs, ks, vs, H, w.scale, ids)
+        compare(got[H * cq[s] + ids], want, what=f"{w.name} sequence {s} (sampled)")
