@@ -537,8 +537,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // so the next score tile of a slot is issued as soon as its softmax has
     // read the current one (Q.K^T overlaps the softmax).  Otherwise P lies
     // over the first half of S, S_x = 128x, O_x = 256 + 128x.
-    constexpr int kOw = DPAD <= 64 ? 64 : DPAD;
     constexpr int kOffP = 2 * kCols;
+    // Shared tiling with every key in one narrow tile (no bias, SW > 0, e.g.
+    // 77 text tokens): a job is one score tile, so the next job's S is issued
+    // as soon as the softmax has read this one, and a job's output is written
+    // after the next job's softmax, while that job's P.V runs (two O buffers
+    // per slot).  The output is staged in its own shared-memory area, so a Q
+    // buffer is free again once its S is computed.
+    constexpr bool kShDbl = MODE == kModeShared && BIAS == kBiasNone && SW > 0 && !DBG &&
+                            kOffP + 128 + 4 * DPAD <= 512;
+    constexpr int kOw = kShDbl ? 2 * DPAD : (DPAD <= 64 ? 64 : DPAD);
     constexpr int kOffO = kOffP + 128;
     constexpr bool kSepP = kOffO + 2 * kOw <= 512 && (BIAS != kBiasSam || SW == 14);
     // Packed tiling with head dims up to 32 and slots up to 64 rows: two O
@@ -586,8 +594,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < 2; ++b) {
                 mbar_init(&bar_q_full[x][b], 1);
                 // double-buffered Q: the softmax warps release it after using it
-                // as output staging; single Q: the last P.V's commit releases it
-                mbar_init(&bar_q_empty[x][b], p.nq == 2 ? 4 : 1);
+                // as output staging; single Q: the last P.V's commit releases it;
+                // the one-tile pipeline: the commit of its S releases it
+                mbar_init(&bar_q_empty[x][b], (p.nq == 2 && !kShDbl) ? 4 : 1);
             }
             mbar_init(&bar_s[x], 1);
             mbar_init(&bar_p[x], 4);
@@ -1012,7 +1021,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             for (int job = job0; ok && job < p.n_jobs; job += job_step, ++ju) {
-                if constexpr (MODE == kModeShared) {
+                if constexpr (kShDbl) {
+                    // one score tile per job: S of the next job as soon as the
+                    // softmax has read this one, then this job's P.V into O
+                    // buffer ju & 1; Q is released by the commit of its S
+                    const int st = ring % nst;
+                    if (ju == 0) {
+                        if (!waitb(&bar_q_full[x][0], 0, kStatusWaitQ) || !waitb(&bar_full_k[st], (ring / nst) & 1, kStatusWaitK)) {
+                            ok = false;
+                            break;
+                        }
+                        issue_qk<DPAD>(tSx, kdesc(smem_u32(sQ + (x * p.nq) * T::kBytes)),
+                                       kdesc(smem_u32(sRing + st * p.ring_stage_bytes)), idesc_s);
+                        mma_commit(bs);
+                        mma_commit(&bar_q_empty[x][0]);
+                        ++s_cnt;
+                    }
+                    if (job + job_step < p.n_jobs) {
+                        const int ju2 = ju + 1, qb2 = ju2 % p.nq, st2 = (ring + 1) % nst;
+                        if (!waitb(&bar_q_full[x][qb2], (ju2 / p.nq) & 1, kStatusWaitQ) ||
+                            !waitb(&bar_full_k[st2], ((ring + 1) / nst) & 1, kStatusWaitK) || !s_free()) {
+                            ok = false;
+                            break;
+                        }
+                        issue_qk<DPAD>(tSx, kdesc(smem_u32(sQ + (x * p.nq + qb2) * T::kBytes)),
+                                       kdesc(smem_u32(sRing + st2 * p.ring_stage_bytes)), idesc_s);
+                        mma_commit(bs);
+                        mma_commit(&bar_q_empty[x][qb2]);
+                        ++s_cnt;
+                    }
+                    if (!waitb(bp, ph_p, kStatusWaitP) || !waitb(&bar_full_v[st], (ring / nst) & 1, kStatusWaitV)) {
+                        ok = false;
+                        break;
+                    }
+                    ph_p ^= 1;
+                    issue_pv<kCols>(tOx + (uint32_t)((ju & 1) * DPAD), tPx,
+                                    vdesc(smem_u32(sRing + st * p.ring_stage_bytes + T::kBytes)), idesc_o, 0u);
+                    mma_commit(bo);
+                    mma_commit(&bar_empty[st]);
+                    ring += 1;
+                } else if constexpr (MODE == kModeShared) {
                     const int qb = ju % p.nq;
                     const uint64_t qa = kdesc(smem_u32(sQ + (x * p.nq + qb) * T::kBytes));
                     if (!waitb(&bar_q_full[x][qb], (ju / p.nq) & 1, kStatusWaitQ)) { ok = false; break; }
@@ -1160,13 +1208,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 warp_arrive(&bar_oempty[x]);
             }
-            if (MODE == kModeShared && p.nq == 2) {
-                // The slot's Q tile is no longer read (every P.V of the job is
-                // done): it stages the warp's 32 output rows, consecutive tokens
-                // of one slice, so that each store writes 512 contiguous bytes.
-                // Then the Q buffer is handed back to the producer.
+            if (MODE == kModeShared && (kShDbl || p.nq == 2)) {
+                // The warp's 32 output rows, consecutive tokens of one slice,
+                // are staged so that each store writes 512 contiguous bytes: in
+                // the slot's finished Q tile (every P.V of the job is done),
+                // which then goes back to the producer, or in the one-tile
+                // pipeline's own staging area.
                 const int rb = p.d * 2;  // bytes per output row
-                unsigned char* stg = sQ + (x * p.nq + qbuf) * T::kBytes + (warp & 3) * (32 * rb);
+                unsigned char* stg = (kShDbl ? sExtraB + x * (kBlockM * rb) : sQ + (x * p.nq + qbuf) * T::kBytes) +
+                                     (warp & 3) * (32 * rb);
                 if (!DBG) {
 #pragma unroll
                     for (int c = 0; c < DPAD / 8; ++c)
@@ -1182,9 +1232,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int q = lane; q < nch; q += 32)
                         *reinterpret_cast<uint4*>(dst + (size_t)q * 16) = *reinterpret_cast<const uint4*>(stg + q * 16);
                 }
-                // generic accesses before the producer's next TMA write here
-                fence_proxy_async_smem();
-                warp_arrive(&bar_q_empty[x][qbuf]);
+                if constexpr (!kShDbl) {
+                    // generic accesses before the producer's next TMA write here
+                    fence_proxy_async_smem();
+                    warp_arrive(&bar_q_empty[x][qbuf]);
+                } else {
+                    __syncwarp();  // staged rows read before the next job writes them
+                }
             } else if (rok && !DBG) {
                 // windows layout: [slice][token]; image layout: the token's
                 // place in the image (shift and partition undone)
@@ -1493,6 +1547,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[kCols / 2];
                     l_run += exp_pack<kCols>(xs, sc, -m_use, bf, pk);
                     if (!wait_pv()) { ok = false; break; }
+                    if constexpr (kShDbl) {
+                        // the previous job's output, while this job's P waits in
+                        // registers: its P.V ran during this softmax (and P_x
+                        // is free once it has)
+                        if (ju > 0) {
+                            __syncwarp();
+                            if (!__all_sync(0xffffffffu, mbar_wait(&bar_o[x], (ju - 1) & 1, abort_flag, kStatusWaitO))) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_slice, pv_tok, pv_ok, 0);
+                        }
+                    }
                     tmem_st_cols<kCols / 2>(tP, pk);
                     tmem_st_wait();
                     tc_fence_before();
@@ -1502,6 +1570,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             // -------------------------------------------------------- epilogue
+            if constexpr (kShDbl) {  // written during the next job (or after the last)
+                pv_l = l_run;
+                pv_slice = my_slice;
+                pv_tok = my_tok;
+                pv_ok = row_ok;
+                continue;
+            }
             __syncwarp();
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_o[x], ju & 1, abort_flag, kStatusWaitO))) { ok = false; break; }
             tc_fence_after();
@@ -1510,7 +1585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
                 epilogue(tO, l_run, my_slice, my_tok, row_ok, MODE == kModeShared ? ju % p.nq : 0);
         }
-        if constexpr (kDblO) {
+        if constexpr (kDblO || kShDbl) {
             if (ok && ju > 0) {
                 __syncwarp();
                 if (__all_sync(0xffffffffu, mbar_wait(&bar_o[x], (ju - 1) & 1, abort_flag, kStatusWaitO))) {

@@ -370,6 +370,10 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         // no bias and every key in one tile of at most 80 (e.g. 77 text tokens):
         // 80-column score tiles, P.V over 80 keys
         if (!vt && bias == kBiasNone && Nk <= 80 && dpad <= 64) sw_spec = 80;
+        // with head dims up to 48 that kernel pipelines its jobs (two O buffers
+        // per slot in tensor memory) and stages each slot's 128 output rows in
+        // an area of its own
+        if (sw_spec == 80 && 2 * 80 + 128 + 4 * dpad <= 512 && !dbg) extra = 2 * (size_t)kBlockM * d * 2;
         // SAM key tiles start on grid rows: 112 keys (8 rows) on the 14-wide
         // grid, 128 (2 rows) on the 64-wide one
         p.kv_w = (bias == kBiasSam && sw_spec) ? (sw_spec == 14 ? 112 : (kBlockN / sw_spec) * sw_spec) : kBlockN;

@@ -100,6 +100,15 @@ def test_lengths(nq, nk):
     full_parity(w)
 
 
+@pytest.mark.parametrize("d,nk", [(16, 77), (32, 1), (40, 77), (48, 80), (40, 33)])
+def test_one_key_tile_pipeline(d, nk):
+    """At most 80 keys and head dims up to 48: jobs of one score tile, the
+    next job's S issued early and each output written during the next job;
+    256 jobs over the CTAs, so CTAs run several in a row."""
+    w = Workload("cross", B=4, H=8, Nq=2000, Nk=nk, d=d, dtype="fp16", bias="none", seed=60 + d + nk)
+    full_parity(w)
+
+
 def test_single_slice():
     full_parity(Workload("bh1", B=1, H=1, Nq=77, Nk=333, d=40, dtype="fp16", bias="none", seed=5))
 
