@@ -48,6 +48,10 @@ class _Bias(ctypes.Structure):
         ("rel_w", ctypes.c_void_p),
         ("s_h", ctypes.c_int),
         ("s_w", ctypes.c_int),
+        ("k_h", ctypes.c_int),
+        ("k_w", ctypes.c_int),
+        ("idx_h", ctypes.c_void_p),
+        ("idx_w", ctypes.c_void_p),
     ]
 
 
@@ -105,22 +109,71 @@ class Bias:
     """Bias description in fp64.  kind: 'none' | 'swin' | 'sam'.
 
     swin: table [(2M-1)^2, H], win=M, grid_h, grid_w, shift.
-    sam:  rel_h [2*s_h-1, d], rel_w [2*s_w-1, d], s_h, s_w.
+    sam:  rel_h [L_h, d], rel_w [L_w, d] as the model holds them, query grid
+          s_h x s_w, key grid k_h x k_w (default: the query grid).  Tables
+          whose length is not 2*max(query, key) - 1 are resized
+          (``sam_resize``) and rows are picked by ``sam_rel_index``.
     """
 
     def __init__(self, kind="none", table=None, win=0, grid_h=0, grid_w=0, shift=0,
-                 rel_h=None, rel_w=None, s_h=0, s_w=0):
+                 rel_h=None, rel_w=None, s_h=0, s_w=0, k_h=0, k_w=0):
         self.kind = kind
         self.table = None if table is None else _f64(table)
         self.rel_h = None if rel_h is None else _f64(rel_h)
         self.rel_w = None if rel_w is None else _f64(rel_w)
         self.win, self.grid_h, self.grid_w, self.shift = win, grid_h, grid_w, shift
         self.s_h, self.s_w = s_h, s_w
+        self.k_h, self.k_w = (k_h or s_h), (k_w or s_w)
+        if kind == "sam":
+            self._rh = _f64(sam_resize(self.rel_h, 2 * max(s_h, self.k_h) - 1))
+            self._rw = _f64(sam_resize(self.rel_w, 2 * max(s_w, self.k_w) - 1))
+            self._ih = np.ascontiguousarray(sam_rel_index(s_h, self.k_h), dtype=np.int32)
+            self._iw = np.ascontiguousarray(sam_rel_index(s_w, self.k_w), dtype=np.int32)
 
     def _c(self):
         k = {"none": BIAS_NONE, "swin": BIAS_SWIN, "sam": BIAS_SAM}[self.kind]
-        return _Bias(k, _ptr(self.table), self.win, self.grid_h, self.grid_w, self.shift,
-                     _ptr(self.rel_h), _ptr(self.rel_w), self.s_h, self.s_w)
+        if self.kind != "sam":
+            return _Bias(k, _ptr(self.table), self.win, self.grid_h, self.grid_w, self.shift)
+        return _Bias(k, None, 0, 0, 0, 0, _ptr(self._rh), _ptr(self._rw), self.s_h, self.s_w,
+                     self.k_h, self.k_w, _ptr(self._ih), _ptr(self._iw))
+
+
+def sam_rel_index(q_size: int, k_size: int):
+    """Table row for each (query, key) coordinate pair along one axis of
+    SAM's decomposed relative position ("Accelerating Generative AI (part 1),
+    Segment Anything", section Bfloat16 半精度: q_coords and k_coords are
+    coordinate scalers indexing rel_pos_resized).  Published definition:
+    query coordinates scaled by max(k/q, 1), key coordinates by max(q/k, 1),
+    offset by (k-1) * max(q/k, 1); evaluated in float32 as the published code
+    does, then truncated.  Equal sizes give q_i - k_j + q - 1.  Returns
+    [q_size, k_size] int64."""
+    qs = np.float32(max(k_size / q_size, 1.0))
+    ks = np.float32(max(q_size / k_size, 1.0))
+    qc = np.arange(q_size, dtype=np.float32)[:, None] * qs
+    kc = np.arange(k_size, dtype=np.float32)[None, :] * ks
+    rel = (qc - kc) + np.float32((k_size - 1) * max(q_size / k_size, 1.0))
+    return rel.astype(np.int64)
+
+
+def sam_resize(table, L_out: int):
+    """rel_pos_resized: the table linearly resampled to L_out rows when its
+    length differs (half-pixel centres, source position clamped at 0, the
+    upper neighbour clamped to the last row -- 1-D linear interpolation
+    without corner alignment).  fp64; a table of the right length is
+    returned as is."""
+    t = np.asarray(table, dtype=np.float64)
+    L_in = t.shape[0]
+    if L_in == L_out:
+        return t
+    out = np.empty((L_out, t.shape[1]), dtype=np.float64)
+    scale = L_in / L_out
+    for m in range(L_out):
+        src = max(scale * (m + 0.5) - 0.5, 0.0)
+        i0 = int(src)
+        i1 = min(i0 + 1, L_in - 1)
+        w1 = src - i0
+        out[m] = (1.0 - w1) * t[i0] + w1 * t[i1]
+    return out
 
 
 def _shape(q, k):

@@ -30,9 +30,12 @@
  *    * SAM_RELPOS: "Accelerating Generative AI (part 1), Segment Anything"
  *      section Bfloat16 半精度 names the image encoder's relative position
  *      term indexed through q_coords / k_coords into rel_pos_resized.  The
- *      concrete form (decomposed rel_h = Q . R_h[qh-kh+S_h-1],
- *      rel_w = Q . R_w[qw-kw+S_w-1] with the unscaled Q, broadcast-added) is
- *      the published SAM definition, restated here.
+ *      concrete form (decomposed rel_h = Q . R_h[idx_h(qh, kh)],
+ *      rel_w = Q . R_w[idx_w(qw, kw)] with the unscaled Q, broadcast-added;
+ *      idx = qh - kh + S_h - 1 on equal grids) is the published SAM
+ *      definition, restated here.  For unequal query and key grids the
+ *      caller passes the resized tables and the coordinate-scaled index
+ *      tables (oracle/__init__.py computes both from the definition).
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - scale multiplies Q.K^T only; the bias is added after scaling.
@@ -40,7 +43,8 @@
  *  - Swin relative index uses (query - key) offsets; table row-major
  *    [(2M-1)^2][H], fp32 values.
  *  - slice b' of a Swin batch is image * nW + w, windows row-major.
- *  - SAM requires equal query and key grids.
+ *  - SAM indices on unequal grids are computed in float32, as the
+ *    published code's coordinate scalers are.
  *
  * Everything is double precision.  Inputs arrive as fp64 arrays that the
  * caller converted exactly from the half-precision tensors.
@@ -64,9 +68,12 @@ typedef struct {
     int grid_h, grid_w;  /* tokens per image side (multiples of M) */
     int shift;           /* 0 = no mask */
     /* SAM */
-    const double* rel_h; /* [2*S_h-1][d] */
-    const double* rel_w; /* [2*S_w-1][d] */
-    int s_h, s_w;        /* query grid == key grid = s_h x s_w */
+    const double* rel_h; /* [L_h][d], L_h = 2*max(S_h, K_h)-1 (resized if needed) */
+    const double* rel_w; /* [L_w][d] */
+    int s_h, s_w;        /* query grid s_h x s_w */
+    int k_h, k_w;        /* key grid (0, 0: the query grid) */
+    const int* idx_h;    /* [s_h][k_h] table row of (qh, kh), or NULL: qh - kh + s_h - 1 */
+    const int* idx_w;    /* [s_w][k_w] */
 } oracle_bias_t;
 
 /* ---------------------------------------------------------------- Swin -- */
@@ -121,13 +128,17 @@ static double swin_bias(const oracle_bias_t* a, int H, int bp, int h, int i, int
 /* ----------------------------------------------------------------- SAM -- */
 
 /* Decomposed relative position term for query row i (vector q_i of length
- * d, unscaled) against key j on an s_h x s_w grid (row-major tokens). */
+ * d, unscaled) of the s_h x s_w query grid against key j of the key grid
+ * (row-major tokens on both). */
 static double sam_bias(const oracle_bias_t* a, const double* qi, int d, int i, int j)
 {
+    int kgh = a->k_h ? a->k_h : a->s_h, kgw = a->k_w ? a->k_w : a->s_w;
     int qh = i / a->s_w, qw = i % a->s_w;
-    int kh = j / a->s_w, kw = j % a->s_w;
-    const double* rh = a->rel_h + (size_t)(qh - kh + a->s_h - 1) * d;
-    const double* rw = a->rel_w + (size_t)(qw - kw + a->s_w - 1) * d;
+    int kh = j / kgw, kw = j % kgw;
+    int ih = a->idx_h ? a->idx_h[qh * kgh + kh] : qh - kh + a->s_h - 1;
+    int iw = a->idx_w ? a->idx_w[qw * kgw + kw] : qw - kw + a->s_w - 1;
+    const double* rh = a->rel_h + (size_t)ih * d;
+    const double* rw = a->rel_w + (size_t)iw * d;
     double h = 0.0, w = 0.0;
     for (int c = 0; c < d; ++c) {
         h += qi[c] * rh[c];
@@ -197,7 +208,10 @@ static int check_args(int BH, int H, int Nq, int Nk, int d, const oracle_bias_t*
         if (a->grid_h % M || a->grid_w % M || a->shift < 0 || a->shift >= M) return -1;
     }
     if (a && a->kind == OR_BIAS_SAM) {
-        if (a->s_h <= 0 || a->s_w <= 0 || Nq != a->s_h * a->s_w || Nk != Nq) return -1;
+        int kgh = a->k_h ? a->k_h : a->s_h, kgw = a->k_w ? a->k_w : a->s_w;
+        if (a->s_h <= 0 || a->s_w <= 0 || kgh <= 0 || kgw <= 0 || Nq != a->s_h * a->s_w || Nk != kgh * kgw)
+            return -1;
+        if ((kgh != a->s_h || kgw != a->s_w) && (!a->idx_h || !a->idx_w)) return -1;
         if (!a->rel_h || !a->rel_w) return -1;
     }
     return 0;

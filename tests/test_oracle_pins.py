@@ -481,3 +481,94 @@ def test_varlen_single_key_returns_its_value():
         blk = out[H * cu_q[s]:H * cu_q[s + 1]].reshape(H, lq, d)
         for h in range(H):
             np.testing.assert_array_equal(blk[h], np.broadcast_to(v[H * cu_k[s] + h], (lq, d)))
+
+
+# ------------------------------------- SAM rel-pos on unequal query/key grids --
+# Published definition: coordinates scaled by max(k/q, 1) (queries) and
+# max(q/k, 1) (keys), offset (k-1)*max(q/k, 1), evaluated in float32 and
+# truncated; tables whose length is not 2*max(q, k)-1 are resampled linearly.
+
+def test_sam_rel_index_hand_computed():
+    # q=2, k=4: 2i - j + 3
+    np.testing.assert_array_equal(oracle.sam_rel_index(2, 4), [[3, 2, 1, 0], [5, 4, 3, 2]])
+    # q=4, k=2: i - 2j + 2
+    np.testing.assert_array_equal(oracle.sam_rel_index(4, 2), [[2, 0], [3, 1], [4, 2], [5, 3]])
+    # q=2, k=3: 1.5i - j + 2, truncated: 3.5 -> 3, 2.5 -> 2, 1.5 -> 1
+    np.testing.assert_array_equal(oracle.sam_rel_index(2, 3), [[2, 1, 0], [3, 2, 1]])
+    # equal sizes: i - j + q - 1
+    np.testing.assert_array_equal(oracle.sam_rel_index(3, 3), [[2, 1, 0], [3, 2, 1], [4, 3, 2]])
+
+
+@pytest.mark.parametrize("q,k", [(14, 64), (64, 14), (5, 7), (7, 5), (64, 64), (3, 40)])
+def test_sam_rel_index_in_float32_like_torch(q, k):
+    """torch evaluates the scaled coordinates of an int arange in float32."""
+    qc = torch.arange(q)[:, None] * max(k / q, 1.0)
+    kc = torch.arange(k)[None, :] * max(q / k, 1.0)
+    want = ((qc - kc) + (k - 1) * max(q / k, 1.0)).long().numpy()
+    got = oracle.sam_rel_index(q, k)
+    np.testing.assert_array_equal(got, want)
+    assert got.min() >= 0 and got.max() <= 2 * max(q, k) - 2
+
+
+@pytest.mark.parametrize("L_in,L_out", [(27, 127), (127, 27), (10, 13), (13, 10), (9, 9)])
+def test_sam_resize_is_linear_interpolation(L_in, L_out):
+    rng = np.random.default_rng(L_in * 131 + L_out)
+    t = rng.standard_normal((L_in, 6))
+    want = torch.nn.functional.interpolate(torch.from_numpy(t).T[None], size=L_out, mode="linear",
+                                           align_corners=False)[0].T.numpy()
+    np.testing.assert_allclose(oracle.sam_resize(t, L_out), want, rtol=0, atol=1e-12)
+
+
+def _sam_bias_brute(q, qg, kg, Rh, Rw):
+    """Bias of every (query, key) pair from torch-resized tables and torch's
+    float32 coordinate scaling."""
+    (qh_n, qw_n), (kh_n, kw_n) = qg, kg
+
+    def rows(R, a, b):
+        L = 2 * max(a, b) - 1
+        Rt = torch.from_numpy(R)
+        if R.shape[0] != L:
+            Rt = torch.nn.functional.interpolate(Rt.T[None], size=L, mode="linear", align_corners=False)[0].T
+        qc = torch.arange(a)[:, None] * max(b / a, 1.0)
+        kc = torch.arange(b)[None, :] * max(a / b, 1.0)
+        return Rt.numpy(), ((qc - kc) + (b - 1) * max(a / b, 1.0)).long().numpy()
+
+    Rh_r, ih = rows(Rh, qh_n, kh_n)
+    Rw_r, iw = rows(Rw, qw_n, kw_n)
+    out = np.empty((qh_n * qw_n, kh_n * kw_n))
+    for i in range(qh_n * qw_n):
+        for j in range(kh_n * kw_n):
+            a, b = divmod(i, qw_n)
+            c, e = divmod(j, kw_n)
+            out[i, j] = q[i] @ Rh_r[ih[a, c]] + q[i] @ Rw_r[iw[b, e]]
+    return out
+
+
+def test_sam_unequal_grids_bias_by_brute_force():
+    rng = np.random.default_rng(51)
+    qg, kg, d = (3, 4), (5, 2), 6
+    Rh = rng.standard_normal((7, d))    # 2*max(3,5)-1 = 9 rows needed: upsampled
+    Rw = rng.standard_normal((11, d))   # 2*max(4,2)-1 = 7 rows needed: downsampled
+    q = rng.standard_normal((1, 12, d))
+    b = oracle.Bias("sam", rel_h=Rh, rel_w=Rw, s_h=3, s_w=4, k_h=5, k_w=2)
+    got = oracle.bias_matrix(q, 1, 0, 10, b)
+    np.testing.assert_allclose(got, _sam_bias_brute(q[0], qg, kg, Rh, Rw), rtol=0, atol=1e-12)
+
+
+def test_sam_unequal_grids_attention_matches_torch_sdpa():
+    rng = np.random.default_rng(52)
+    qg, kg, d, H = (4, 3), (2, 5), 8, 2
+    Nq, Nk = 12, 10
+    Rh = rng.standard_normal((5, d)) * 0.3
+    Rw = rng.standard_normal((9, d)) * 0.3
+    q = rng.standard_normal((H, Nq, d))
+    k = rng.standard_normal((H, Nk, d))
+    v = rng.standard_normal((H, Nk, d))
+    b = oracle.Bias("sam", rel_h=Rh, rel_w=Rw, s_h=4, s_w=3, k_h=2, k_w=5)
+    got, _ = oracle.attn_fwd(q, k, v, H, 0.4, b)
+    for h in range(H):
+        bias = torch.from_numpy(_sam_bias_brute(q[h], qg, kg, Rh, Rw))
+        want = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[h])[None], torch.from_numpy(k[h])[None], torch.from_numpy(v[h])[None],
+            attn_mask=bias[None], scale=0.4)[0].numpy()
+        np.testing.assert_allclose(got[h], want, rtol=0, atol=1e-12)
