@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define SDPA09_ABI_VERSION 3
+#define SDPA09_ABI_VERSION 4
 
 typedef enum {
     ATTN_BF16 = 0, /* bfloat16 Q/K/V/O ("model.to(torch.bfloat16)" in the SAM rewrite) */
@@ -97,17 +97,27 @@ typedef struct {
  *     partitioned copy is made.  B still counts windows. */
 enum { ATTN_SWIN_WINDOWS = 0, ATTN_SWIN_IMAGE = 1 };
 
+/* SAM decomposed relative position ("Accelerating Generative AI (part 1),
+ * Segment Anything", section Bfloat16 半精度: the image encoder's rel-pos term,
+ * q_coords / k_coords indexing rel_pos_resized).  For query (qh, qw) and key
+ * (kh, kw) the bias is Q . R_h'[ih] + Q . R_w'[iw] with the unscaled Q, where
+ * R' is the table resampled linearly to 2*max(q, k)-1 rows when its length
+ * differs (half-pixel centres, no corner alignment) and, per axis,
+ * i = trunc(q_i * max(k/q, 1) - k_j * max(q/k, 1) + (k-1) * max(q/k, 1)) in
+ * float32 -- on equal grids simply qh - kh + q_h - 1. */
 typedef struct {
-    const void* rel_h;  /* device, [2*q_h-1][d], same dtype as Q */
-    const void* rel_w;  /* device, [2*q_w-1][d], same dtype as Q */
-    int q_h, q_w;       /* query grid; Nq = q_h * q_w */
-    int k_h, k_w;       /* key grid; must equal the query grid */
+    const void* rel_h;  /* device, [rel_h_len][d], same dtype as Q */
+    const void* rel_w;  /* device, [rel_w_len][d], same dtype as Q */
+    int q_h, q_w;       /* query grid; Nq = q_h * q_w (sides <= 64) */
+    int k_h, k_w;       /* key grid; Nk = k_h * k_w (sides <= 64) */
+    int rel_h_len;      /* rows of rel_h, 1..128; 0 = 2*max(q_h, k_h)-1 */
+    int rel_w_len;      /* rows of rel_w, 1..128; 0 = 2*max(q_w, k_w)-1 */
 } attn_sam_args;
 
 enum {
     ATTN_OK = 0,
     ATTN_ERR_ARG = -1,            /* null/misaligned pointer, bad size, bad bias args */
-    ATTN_ERR_UNSUPPORTED = -2,    /* valid but not implemented (e.g. d > 128, SAM q grid != k grid) */
+    ATTN_ERR_UNSUPPORTED = -2,    /* valid but not implemented (e.g. d > 128, SAM grid sides > 64) */
     ATTN_ERR_CUDA = -3,           /* a CUDA runtime/driver call or the launch failed */
     ATTN_ERR_DEVICE_TIMEOUT = -4  /* a kernel wait ran out of time (attn_device_status) */
 };

@@ -52,7 +52,8 @@ class _SwinArgs(ctypes.Structure):
 
 class _SamArgs(ctypes.Structure):
     _fields_ = [("rel_h", ctypes.c_void_p), ("rel_w", ctypes.c_void_p), ("q_h", ctypes.c_int),
-                ("q_w", ctypes.c_int), ("k_h", ctypes.c_int), ("k_w", ctypes.c_int)]
+                ("q_w", ctypes.c_int), ("k_h", ctypes.c_int), ("k_w", ctypes.c_int),
+                ("rel_h_len", ctypes.c_int), ("rel_w_len", ctypes.c_int)]
 
 
 class SwinBias:
@@ -75,8 +76,11 @@ class SwinBias:
 
 
 class SamBias:
-    """SAM decomposed relative position.  rel_h [2*q_h-1, d], rel_w [2*q_w-1, d]
-    on the device in the Q dtype; query grid == key grid."""
+    """SAM decomposed relative position.  rel_h [L_h, d], rel_w [L_w, d] on
+    the device in the Q dtype; query grid q_h x q_w, key grid k_h x k_w
+    (default: the query grid).  Tables whose length is not 2*max(q, k) - 1
+    are resampled linearly in the kernel; unequal grids index them through
+    the coordinate scalers."""
 
     def __init__(self, rel_h, rel_w, q_h, q_w, k_h=None, k_w=None):
         self.rel_h, self.rel_w, self.q_h, self.q_w = rel_h, rel_w, q_h, q_w
@@ -84,7 +88,8 @@ class SamBias:
         self.k_w = q_w if k_w is None else k_w
 
     def _c(self):
-        return _SamArgs(_ptr(self.rel_h), _ptr(self.rel_w), self.q_h, self.q_w, self.k_h, self.k_w)
+        return _SamArgs(_ptr(self.rel_h), _ptr(self.rel_w), self.q_h, self.q_w, self.k_h, self.k_w,
+                        int(self.rel_h.shape[0]), int(self.rel_w.shape[0]))
 
 
 def _ptr(t):

@@ -119,7 +119,15 @@ struct AttnParams {
     uint32_t fd_m[2];               // magic/shift pair dividing by win
     const void *q, *k, *v;          // operand bases (image layout gathers them directly)
     // SAM
-    int s_h, s_w, n_rh, n_rw;
+    int s_h, s_w, n_rh, n_rw;  // query grid; MMA widths of the R_h / R_w tables as given
+    int k_h, k_w;              // key grid (the query grid unless general)
+    // General SAM (unequal grids or tables of another length, generic kernel
+    // only): per axis the float32 coordinate scalers of the query and key
+    // coordinates and the offset, the table length as given and the length
+    // the index addresses (2 * max(q, k) - 1)
+    int sam_general;
+    float sam_qs_h, sam_ks_h, sam_off_h, sam_qs_w, sam_ks_w, sam_off_w;
+    int sam_lin_h, sam_lout_h, sam_lin_w, sam_lout_w;
 };
 
 // Variable-length batches (no bias, shared tiling): Q/O are the concatenation
@@ -204,8 +212,8 @@ __device__ __forceinline__ JobRows shared_job(const AttnParams& p, const VarlenA
 //   Swin, MMA variant: Qone [128 rows][SL] then H + 3 bias blocks
 //        [SL][SL] (per-head tables, then last-column / last-row / corner
 //        masks), all 16-bit K-major 32B-swizzled
-//   SAM : rel_h [2 slots][s_h][128] fp32, then for generic grids rel_w
-//        [2][s_w][128] and a key table [Nk]
+//   SAM : rel_h [2 slots][k_h][128] fp32, then for generic grids rel_w
+//        [2][k_w][128] and a key table [Nk] (k_h x k_w: the key grid)
 __host__ __device__ constexpr uint32_t swin_rows_extra_bytes(int sl, int H) {
     return (uint32_t)(H * sl * sl * 4 + 3 * sl * (sl / 32) * 4);
 }
@@ -518,6 +526,55 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
         mma_ts(o_tmem, p_tmem + ks * 8, vd + (uint64_t)(ks * (512 / 16)), idesc, (accumulate || ks > 0) ? 1u : 0u);
 }
 
+// Table row of SAM's decomposed relative position for query coordinate i and
+// key coordinate j along one axis: i * qs - j * ks + off in float32 (the
+// published coordinate scalers), truncated ("Accelerating Generative AI
+// (part 1), Segment Anything", section Bfloat16 半精度: q_coords / k_coords
+// index rel_pos_resized).  Clamped to the table.
+__device__ __forceinline__ int sam_rel_row(int i, int j, float qs, float ks, float off, int lout) {
+    const float rel = __fadd_rn(__fsub_rn(__fmul_rn((float)i, qs), __fmul_rn((float)j, ks)), off);
+    return min(max((int)rel, 0), lout - 1);
+}
+
+// Row m of the table resampled from lin to lout rows (linear, half-pixel
+// centres, clamped) read off g, the row's dot products with the table as
+// given: resampling is linear, so it commutes with Q.R.
+__device__ __forceinline__ float sam_resampled(const float* g, int m, int lin, int lout) {
+    if (lin == lout) return g[m];
+    const float src = fmaxf(__fmul_rn((float)lin / (float)lout, (float)m + 0.5f) - 0.5f, 0.f);
+    const int i0 = min((int)src, lin - 1);
+    const int i1 = min(i0 + 1, lin - 1);
+    const float w1 = src - (float)i0;
+    return (1.f - w1) * g[i0] + w1 * g[i1];
+}
+
+// General SAM bias rows of one query row (qh, qw): rel_h for every key row
+// and rel_w for every key column, from G_h (in tO) and G_w (in tS), stored
+// reversed like the generic grids' rows (entry k_h - 1 - kh).  The G rows go
+// through a local array because the rows they are read at vary per thread.
+static __device__ __noinline__ void sam_general_rows(uint32_t tS, uint32_t tO, const AttnParams& p, int qh, int qw,
+                                                     float f, float* sam_rh, float* sam_rw, int r) {
+    float g[kBlockN];
+    {
+        uint32_t v[kBlockN];
+        tmem_ld_cols<kBlockN>(tS, v);
+        for (int t = 0; t < kBlockN; ++t) g[t] = __uint_as_float(v[t]) * f;
+    }
+    for (int kw = 0; kw < p.k_w; ++kw) {
+        const int m = sam_rel_row(qw, kw, p.sam_qs_w, p.sam_ks_w, p.sam_off_w, p.sam_lout_w);
+        sam_rw[(p.k_w - 1 - kw) * kBlockM + r] = sam_resampled(g, m, p.sam_lin_w, p.sam_lout_w);
+    }
+    {
+        uint32_t v[kBlockN];
+        tmem_ld_cols<kBlockN>(tO, v);
+        for (int t = 0; t < kBlockN; ++t) g[t] = __uint_as_float(v[t]) * f;
+    }
+    for (int kh = 0; kh < p.k_h; ++kh) {
+        const int m = sam_rel_row(qh, kh, p.sam_qs_h, p.sam_ks_h, p.sam_off_h, p.sam_lout_h);
+        sam_rh[(p.k_h - 1 - kh) * kBlockM + r] = sam_resampled(g, m, p.sam_lin_h, p.sam_lout_h);
+    }
+}
+
 template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ TmaMaps tm, const AttnParams p, const __grid_constant__ VarlenArg<VL> vt) {
@@ -751,11 +808,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if constexpr (MODE == kModeSeparate) fence_proxy_async_smem();
     if constexpr (BIAS == kBiasSam && SW == 0) {
-        // key table for generic grids: (s_h-1-kh) | (s_w-1-kw) << 16
-        int* kt = reinterpret_cast<int*>(sExtra + 2 * (p.s_h + p.s_w) * kBlockM);
+        // key table for generic grids: (k_h-1-kh) | (k_w-1-kw) << 16
+        int* kt = reinterpret_cast<int*>(sExtra + 2 * (p.k_h + p.k_w) * kBlockM);
         for (int k = tid; k < p.Nk; k += kThreads) {
-            const int kh = k / p.s_w, kw = k % p.s_w;
-            kt[k] = (p.s_h - 1 - kh) | ((p.s_w - 1 - kw) << 16);
+            const int kh = k / p.k_w, kw = k % p.k_w;
+            kt[k] = (p.k_h - 1 - kh) | ((p.k_w - 1 - kw) << 16);
         }
     }
     if (warp == kMmaWarp) {
@@ -1181,9 +1238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* sam_rw = nullptr;
         const int* sam_kt = nullptr;
         if constexpr (BIAS == kBiasSam) {
-            sam_rh = sExtra + x * (p.s_h * kBlockM);
-            sam_rw = sExtra + 2 * p.s_h * kBlockM + x * (p.s_w * kBlockM);
-            sam_kt = reinterpret_cast<const int*>(sExtra + 2 * (p.s_h + p.s_w) * kBlockM);
+            sam_rh = sExtra + x * (p.k_h * kBlockM);
+            sam_rw = sExtra + 2 * p.k_h * kBlockM + x * (p.k_w * kBlockM);
+            sam_kt = reinterpret_cast<const int*>(sExtra + 2 * (p.k_h + p.k_w) * kBlockM);
         }
 
         // O / l rounded to the output type and stored (row-per-thread, 16 bytes at a time)
@@ -1387,6 +1444,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!__all_sync(0xffffffffu, mbar_wait(&bar_g[x], ju & 1, abort_flag, kStatusWaitG))) { ok = false; break; }
                     tc_fence_after();
                     const float f = DBG ? 1.0f : kLog2e;
+                    if (SW == 0 && p.sam_general) {
+                        // unequal grids or tables of another length: each key row /
+                        // column reads its table row through the coordinate scalers,
+                        // linearly resampled from G (resampling commutes with Q.R)
+                        sam_general_rows(tS, tO, p, min(qh, p.s_h - 1), min(qw, p.s_w - 1), f, sam_rh, sam_rw, r);
+                        tc_fence_before();
+                        warp_arrive(&bar_gdone[x]);
+                    } else {
                     // square grids of side SW <= 16 need 32-value G rows and 4-bit
                     // shifts, side 64 needs 6-bit shifts
                     constexpr int kGW = (SW > 0 && SW <= 16) ? 32 : 128;
@@ -1421,6 +1486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (u < p.s_h) sam_rh[u * kBlockM + r] = gv[u];
                     tc_fence_before();
                     warp_arrive(&bar_gdone[x]);
+                    }
                 }
 
                 // ------------------------------------------------------ key tiles
@@ -1466,8 +1532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int kh0 = key0 / SW;
 #pragma unroll
                             for (int rr = 0; rr < kRows; ++rr) {
-                                const int kh = min(kh0 + rr, p.s_h - 1);
-                                rh_tile[rr] = sam_rh[(p.s_h - 1 - kh) * kBlockM + r];
+                                const int kh = min(kh0 + rr, p.k_h - 1);
+                                rh_tile[rr] = sam_rh[(p.k_h - 1 - kh) * kBlockM + r];
                             }
                         }
 #pragma unroll

@@ -308,22 +308,42 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         const attn_sam_args* a = static_cast<const attn_sam_args*>(bias_args);
         if (!a || !a->rel_h || !a->rel_w) return fail(ATTN_ERR_ARG, "SAM bias needs attn_sam_args with rel_h, rel_w");
         if (a->q_h < 1 || a->q_w < 1 || a->k_h < 1 || a->k_w < 1) return fail(ATTN_ERR_ARG, "SAM grid sizes must be >= 1");
-        if (a->q_h != a->k_h || a->q_w != a->k_w)
-            return fail(ATTN_ERR_UNSUPPORTED, "SAM with different query and key grids");
-        if (a->q_h * a->q_w != Nq || Nk != Nq) return fail(ATTN_ERR_ARG, "SAM needs Nq == Nk == q_h*q_w");
-        if (a->q_h > kSamMaxSide || a->q_w > kSamMaxSide)
+        if (a->q_h * a->q_w != Nq || a->k_h * a->k_w != Nk)
+            return fail(ATTN_ERR_ARG, "SAM needs Nq == q_h*q_w and Nk == k_h*k_w");
+        if (a->q_h > kSamMaxSide || a->q_w > kSamMaxSide || a->k_h > kSamMaxSide || a->k_w > kSamMaxSide)
             return fail(ATTN_ERR_UNSUPPORTED, "SAM grid sides above %d", kSamMaxSide);
+        // table lengths as given (0: 2*max(q, k)-1, the length the index addresses)
+        const int lout_h = 2 * std::max(a->q_h, a->k_h) - 1, lout_w = 2 * std::max(a->q_w, a->k_w) - 1;
+        const int lin_h = a->rel_h_len ? a->rel_h_len : lout_h, lin_w = a->rel_w_len ? a->rel_w_len : lout_w;
+        if (lin_h < 1 || lin_w < 1) return fail(ATTN_ERR_ARG, "SAM table lengths must be >= 1");
+        if (lin_h > kBlockN || lin_w > kBlockN)
+            return fail(ATTN_ERR_UNSUPPORTED, "SAM tables longer than %d rows", kBlockN);
         if (!aligned16(a->rel_h) || !aligned16(a->rel_w)) return fail(ATTN_ERR_ARG, "rel_h/rel_w must be 16-byte aligned");
         rel_h = a->rel_h;
         rel_w = a->rel_w;
         p.s_h = a->q_h;
         p.s_w = a->q_w;
-        p.n_rh = (2 * a->q_h - 1 + 15) / 16 * 16;
-        p.n_rw = (2 * a->q_w - 1 + 15) / 16 * 16;
+        p.k_h = a->k_h;
+        p.k_w = a->k_w;
+        p.n_rh = (lin_h + 15) / 16 * 16;
+        p.n_rw = (lin_w + 15) / 16 * 16;
+        p.sam_lin_h = lin_h;
+        p.sam_lin_w = lin_w;
+        p.sam_lout_h = lout_h;
+        p.sam_lout_w = lout_w;
+        // unequal grids or resized tables: rows through the coordinate
+        // scalers, in float32 as the published code computes them
+        p.sam_general = (a->q_h != a->k_h || a->q_w != a->k_w || lin_h != lout_h || lin_w != lout_w) ? 1 : 0;
+        p.sam_qs_h = (float)std::max((double)a->k_h / a->q_h, 1.0);
+        p.sam_ks_h = (float)std::max((double)a->q_h / a->k_h, 1.0);
+        p.sam_off_h = (float)((a->k_h - 1) * std::max((double)a->q_h / a->k_h, 1.0));
+        p.sam_qs_w = (float)std::max((double)a->k_w / a->q_w, 1.0);
+        p.sam_ks_w = (float)std::max((double)a->q_w / a->k_w, 1.0);
+        p.sam_off_w = (float)((a->k_w - 1) * std::max((double)a->q_w / a->k_w, 1.0));
         // square 14x14 and 64x64 grids have specialised kernels (the row of G
         // that a query needs is then short and its shift has few bits)
-        sw_spec = (a->q_h == a->q_w && (a->q_w == 64 || a->q_w == 14)) ? a->q_w : 0;
-        extra = (size_t)sam_extra_floats(sw_spec == 0, a->q_h, a->q_w, Nk) * 4;
+        sw_spec = (!p.sam_general && a->q_h == a->q_w && (a->q_w == 64 || a->q_w == 14)) ? a->q_w : 0;
+        extra = (size_t)sam_extra_floats(sw_spec == 0, a->k_h, a->k_w, Nk) * 4;
         bias = kBiasSam;
     } else if (bias_kind != ATTN_BIAS_NONE) {
         return fail(ATTN_ERR_ARG, "unknown bias kind %d", (int)bias_kind);
@@ -433,8 +453,8 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         if ((rc = encode_operand(&tm.v, &tm.vp, v, bf, d, Nk, BH, atoms, kBlockN, 1))) return rc;
     }
     if (bias == kBiasSam) {
-        if ((rc = encode_operand(&tm.rh, &tm.rhp, rel_h, bf, d, 2 * p.s_h - 1, 0, atoms, kBlockN, 1))) return rc;
-        if ((rc = encode_operand(&tm.rw, &tm.rwp, rel_w, bf, d, 2 * p.s_w - 1, 0, atoms, kBlockN, 1))) return rc;
+        if ((rc = encode_operand(&tm.rh, &tm.rhp, rel_h, bf, d, p.sam_lin_h, 0, atoms, kBlockN, 1))) return rc;
+        if ((rc = encode_operand(&tm.rw, &tm.rwp, rel_w, bf, d, p.sam_lin_w, 0, atoms, kBlockN, 1))) return rc;
     } else {
         tm.rh = tm.rhp = tm.rw = tm.rwp = tm.q;
     }

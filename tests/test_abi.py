@@ -41,8 +41,9 @@ def test_library_targets_sm103a_only():
 
 
 def test_abi_version(lib):
-    # 2: attn_swin_args gained its token layout field; 3: attn_fwd_varlen
-    assert lib.attn_abi_version() == 3
+    # 2: attn_swin_args gained its token layout field; 3: attn_fwd_varlen;
+    # 4: attn_sam_args gained the table lengths (unequal grids, resampling)
+    assert lib.attn_abi_version() == 4
 
 
 def _call(lib, q=FAKE, k=FAKE + 4096, v=FAKE + 8192, out=FAKE + 1 << 20, B=1, H=1, Nq=64, Nk=64,
@@ -106,7 +107,11 @@ def test_sam_argument_checks(lib):
     ok = sdpa._SamArgs(FAKE, FAKE, 8, 8, 8, 8)
     assert _call(lib, Nq=65, Nk=65, kind=2, args=ctypes.byref(ok)) == sdpa.ATTN_ERR_ARG
     diff = sdpa._SamArgs(FAKE, FAKE, 8, 8, 4, 4)
-    assert _call(lib, Nq=64, Nk=16, kind=2, args=ctypes.byref(diff)) == sdpa.ATTN_ERR_UNSUPPORTED
+    # unequal grids are valid; the key count must match the key grid
+    assert _call(lib, Nq=64, Nk=64, kind=2, args=ctypes.byref(diff)) == sdpa.ATTN_ERR_ARG
+    long_table = sdpa._SamArgs(FAKE, FAKE, 8, 8, 8, 8, 129, 0)
+    assert _call(lib, Nq=64, Nk=64, kind=2, args=ctypes.byref(long_table)) == sdpa.ATTN_ERR_UNSUPPORTED
+    assert b"longer than 128" in lib.attn_last_error()
     none = sdpa._SamArgs(None, FAKE, 8, 8, 8, 8)
     assert _call(lib, Nq=64, Nk=64, kind=2, args=ctypes.byref(none)) == sdpa.ATTN_ERR_ARG
     huge = sdpa._SamArgs(FAKE, FAKE, 100, 100, 100, 100)

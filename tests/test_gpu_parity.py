@@ -218,6 +218,76 @@ def _sam_bias_bit_exact(w, slices=None, rows=None):
         np.testing.assert_array_equal(got[s].numpy()[r], want[r])
 
 
+# ------------------------------------------- SAM on unequal grids, resampled --
+# Query grid != key grid (coordinate scalers) and tables of another length
+# than 2*max(q, k)-1 (linear resampling, which the kernel applies to G = Q.R).
+
+SAM_GENERAL_CASES = {
+    # name: (query grid, key grid, rel_h rows, rel_w rows)
+    "keys_coarser": ((12, 12), (6, 6), 23, 23),
+    "keys_finer": ((6, 8), (12, 16), 23, 31),
+    "aspect": ((20, 10), (5, 40), 39, 79),
+    "resample_down": ((14, 14), (14, 14), 40, 40),
+    "resample_up": ((16, 16), (16, 16), 9, 13),
+    "both": ((10, 12), (7, 9), 30, 11),
+}
+
+
+def _sam_general_inputs(qg, kg, lh, lw, H=2, d=80, seed=70):
+    g = torch.Generator().manual_seed(seed)
+    Nq, Nk = qg[0] * qg[1], kg[0] * kg[1]
+    q = torch.randn(1, H, Nq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, H, Nk, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, H, Nk, d, generator=g).to(torch.bfloat16)
+    rh = (torch.randn(lh, d, generator=g) * 0.05).to(torch.bfloat16)
+    rw = (torch.randn(lw, d, generator=g) * 0.05).to(torch.bfloat16)
+    return q, k, v, rh, rw
+
+
+@pytest.mark.parametrize("case", sorted(SAM_GENERAL_CASES))
+def test_sam_general_full(case):
+    require_gpu()
+    qg, kg, lh, lw = SAM_GENERAL_CASES[case]
+    q, k, v, rh, rw = _sam_general_inputs(qg, kg, lh, lw)
+    H, d = q.shape[1], q.shape[3]
+    scale = d ** -0.5
+    out = sdpa.attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale=scale,
+                        bias=sdpa.SamBias(rh.cuda(), rw.cuda(), qg[0], qg[1], kg[0], kg[1]))
+    torch.cuda.synchronize()
+    assert sdpa.attn_device_status() == sdpa.ATTN_OK
+    b = oracle.Bias("sam", rel_h=rh.double().numpy(), rel_w=rw.double().numpy(), s_h=qg[0], s_w=qg[1],
+                    k_h=kg[0], k_w=kg[1])
+    want, _ = oracle.attn_fwd(flat64(q), flat64(k), flat64(v), H, scale, b)
+    compare(flat64(out.cpu()), want, what=f"sam general {case}")
+
+
+@pytest.mark.parametrize("qg,kg", [((12, 12), (6, 6)), ((6, 8), (12, 16)), ((20, 10), (5, 40))])
+def test_sam_unequal_grids_bias_indexing_bit_exact(qg, kg):
+    """Integer tables (R_h[r,0] = r, R_w[r,1] = r) of the addressed length and
+    Q = 128*e0 + e1: the bias is 128*ih + iw exactly, so every float32
+    coordinate-scaler index must match the oracle's."""
+    require_gpu()
+    lh, lw = 2 * max(qg[0], kg[0]) - 1, 2 * max(qg[1], kg[1]) - 1
+    q, k, v, _, _ = _sam_general_inputs(qg, kg, lh, lw, seed=71)
+    d = q.shape[3]
+    rh = torch.zeros(lh, d)
+    rh[:, 0] = torch.arange(lh)
+    rw = torch.zeros(lw, d)
+    rw[:, 1] = torch.arange(lw)
+    rh, rw = rh.to(torch.bfloat16), rw.to(torch.bfloat16)
+    qq = torch.zeros_like(q, dtype=torch.float32)
+    qq[..., 0], qq[..., 1] = 128.0, 1.0
+    q = qq.to(torch.bfloat16)
+    got = sdpa.attn_debug_bias(q.cuda(), k.cuda(), v.cuda(), scale=d ** -0.5,
+                               bias=sdpa.SamBias(rh.cuda(), rw.cuda(), qg[0], qg[1], kg[0], kg[1]))
+    got = got.cpu().double().reshape(-1, qg[0] * qg[1], kg[0] * kg[1])
+    b = oracle.Bias("sam", rel_h=rh.double().numpy(), rel_w=rw.double().numpy(), s_h=qg[0], s_w=qg[1],
+                    k_h=kg[0], k_w=kg[1])
+    for s_ in range(got.shape[0]):
+        want = oracle.bias_matrix(flat64(q), q.shape[1], s_, kg[0] * kg[1], b)
+        np.testing.assert_array_equal(got[s_].numpy(), want)
+
+
 # ----------------------------------------------- Swin image token layout --
 # q/k/v/out as [images, grid_h, grid_w, H, d]: the kernel folds the cyclic
 # shift and the window partition into its loads (a box per window that does not
