@@ -481,7 +481,8 @@ def main(argv=None):
         del sets
         torch.cuda.empty_cache()
         suite = _suite(stream, dev, peaks, [n for n in ("swin_t_stage1@image", "sam_vith_window", "sam_vith_global",
-                                                        "sd_unet_self", "sd_unet_cross", "sd_unet_self_varlen")
+                                                        "sam_vith_global_768", "sd_unet_self", "sd_unet_cross",
+                                                        "sd_unet_self_varlen")
                                             if n != w.name])
     if rank == 0:
         line = {

@@ -128,6 +128,12 @@ struct AttnParams {
     int sam_general;
     float sam_qs_h, sam_ks_h, sam_off_h, sam_qs_w, sam_ks_w, sam_off_w;
     int sam_lin_h, sam_lout_h, sam_lin_w, sam_lout_w;
+    // Equal grids, tables of another length: each CTA resamples both tables
+    // once into shared memory at off_rtab (R_w' then R_h', one K-major tile
+    // each), and the G MMAs read them there instead of from the ring.
+    int sam_resample;
+    uint32_t off_rtab;
+    const void *rel_h, *rel_w;
 };
 
 // Variable-length batches (no bias, shared tiling): Q/O are the concatenation
@@ -549,26 +555,32 @@ __device__ __forceinline__ float sam_resampled(const float* g, int m, int lin, i
 }
 
 // General SAM bias rows of one query row (qh, qw): rel_h for every key row
-// and rel_w for every key column, from G_h (in tO) and G_w (in tS), stored
-// reversed like the generic grids' rows (entry k_h - 1 - kh).  The G rows go
+// and rel_w for every key column, from G_h (in tO) and G_w (in tS).  rel_h
+// goes to shared memory reversed like the generic grids' rows (entry
+// k_h - 1 - kh); rel_w likewise into sam_rw, or, when rw_local is set, into
+// rw_local[kw] for the square-grid kernels' registers.  The G rows go
 // through a local array because the rows they are read at vary per thread.
-static __device__ __noinline__ void sam_general_rows(uint32_t tS, uint32_t tO, const AttnParams& p, int qh, int qw,
-                                                     float f, float* sam_rh, float* sam_rw, int r) {
-    float g[kBlockN];
-    {
-        uint32_t v[kBlockN];
-        tmem_ld_cols<kBlockN>(tS, v);
-        for (int t = 0; t < kBlockN; ++t) g[t] = __uint_as_float(v[t]) * f;
+// Only the G columns of the table (its length rounded up to 16) are loaded:
+// the slot's S and O areas may be narrower than 128 columns.
+static __device__ __noinline__ void sam_g_row(uint32_t taddr, int cols, float f, float* g) {
+    for (int c0 = 0; c0 < cols; c0 += 16) {  // cols: the same on every lane (tcgen05.ld is warp-wide)
+        uint32_t v[16];
+        tmem_ld16(taddr + (uint32_t)c0, v);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) g[c0 + t] = __uint_as_float(v[t]) * f;
     }
+}
+static __device__ __noinline__ void sam_general_rows(uint32_t tS, uint32_t tO, const AttnParams& p, int qh, int qw,
+                                                     float f, float* sam_rh, float* sam_rw, float* rw_local, int r) {
+    float g[kBlockN];
+    sam_g_row(tS, p.n_rw, f, g);
     for (int kw = 0; kw < p.k_w; ++kw) {
         const int m = sam_rel_row(qw, kw, p.sam_qs_w, p.sam_ks_w, p.sam_off_w, p.sam_lout_w);
-        sam_rw[(p.k_w - 1 - kw) * kBlockM + r] = sam_resampled(g, m, p.sam_lin_w, p.sam_lout_w);
+        const float val = sam_resampled(g, m, p.sam_lin_w, p.sam_lout_w);
+        if (rw_local) rw_local[kw] = val;
+        else sam_rw[(p.k_w - 1 - kw) * kBlockM + r] = val;
     }
-    {
-        uint32_t v[kBlockN];
-        tmem_ld_cols<kBlockN>(tO, v);
-        for (int t = 0; t < kBlockN; ++t) g[t] = __uint_as_float(v[t]) * f;
-    }
+    sam_g_row(tO, p.n_rh, f, g);
     for (int kh = 0; kh < p.k_h; ++kh) {
         const int m = sam_rel_row(qh, kh, p.sam_qs_h, p.sam_ks_h, p.sam_off_h, p.sam_lout_h);
         sam_rh[(p.k_h - 1 - kh) * kBlockM + r] = sam_resampled(g, m, p.sam_lin_h, p.sam_lout_h);
@@ -807,6 +819,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     if constexpr (MODE == kModeSeparate) fence_proxy_async_smem();
+    if constexpr (BIAS == kBiasSam) {
+        if (p.sam_resample) {
+            // rel_pos_resized: each table linearly resampled to 2 * side - 1
+            // rows (half-pixel centres, clamped), rounded to the operand type
+            // as the model's resized table is, laid out as the MMA's K-major
+            // operand; rows past the table and columns past d are zero
+            constexpr int kChunks = DPAD / 8;
+            for (int i = tid; i < 2 * kBlockN * kChunks; i += kThreads) {
+                const int tb = i / (kBlockN * kChunks);  // 0: R_w, 1: R_h
+                const int m = (i / kChunks) % kBlockN;
+                const int c8 = i % kChunks;
+                const int lin = tb ? p.sam_lin_h : p.sam_lin_w, lout = tb ? p.sam_lout_h : p.sam_lout_w;
+                const uint16_t* src = static_cast<const uint16_t*>(tb ? p.rel_h : p.rel_w);
+                uint32_t pk[4] = {0u, 0u, 0u, 0u};
+                if (m < lout && c8 * 8 < p.d) {
+                    const float pos = fmaxf(__fmul_rn((float)lin / (float)lout, (float)m + 0.5f) - 0.5f, 0.f);
+                    const int i0 = min((int)pos, lin - 1), i1 = min(i0 + 1, lin - 1);
+                    const float w1 = pos - (float)i0;
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        float v[2];
+#pragma unroll
+                        for (int z = 0; z < 2; ++z) {
+                            const int col = c8 * 8 + e + z;
+                            const uint16_t a = src[(size_t)i0 * p.d + col], b = src[(size_t)i1 * p.d + col];
+                            const float fa = bf ? __bfloat162float(__ushort_as_bfloat16(a)) : __half2float(__ushort_as_half(a));
+                            const float fb = bf ? __bfloat162float(__ushort_as_bfloat16(b)) : __half2float(__ushort_as_half(b));
+                            v[z] = (1.f - w1) * fa + w1 * fb;
+                        }
+                        pk[e / 2] = (uint32_t)to_half_bits(v[0], bf) | ((uint32_t)to_half_bits(v[1], bf) << 16);
+                    }
+                }
+                *reinterpret_cast<uint4*>(smem + p.off_rtab + tb * T::kBytes + kmajor_offset(kBlockN, m, c8 * 8)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            fence_proxy_async_smem();  // read by the tensor core
+        }
+    }
     if constexpr (BIAS == kBiasSam && SW == 0) {
         // key table for generic grids: (k_h-1-kh) | (k_w-1-kw) << 16
         int* kt = reinterpret_cast<int*>(sExtra + 2 * (p.k_h + p.k_w) * kBlockM);
@@ -955,7 +1005,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_3d(dq + p.full_atoms * kBlockM * 32, &tm.qp, &bar_q_full[x][qb], 0, jr.q_row + x * kBlockM,
                                         jr.q_slice);
                     }
-                    const int n_uses = jr.n_kv + (BIAS == kBiasSam ? 1 : 0);
+                    // SAM: a first stage with the tables, unless the CTA resampled them
+                    const int t_use = (BIAS == kBiasSam && !p.sam_resample) ? 1 : 0;
+                    const int n_uses = jr.n_kv + t_use;
                     for (int u = 0; ok && u < n_uses; ++u) {
                         const int st = ring % nst;
                         if (ring >= nst &&
@@ -966,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++ring;
                         unsigned char* dk = sRing + st * p.ring_stage_bytes;
                         unsigned char* dv = dk + T::kBytes;
-                        if (BIAS == kBiasSam && u == 0) {
+                        if (BIAS == kBiasSam && u < t_use) {
                             // rel-pos tables: R_w in the K slot, R_h in the V slot
                             const uint32_t r_tx = (uint32_t)T::kAtoms * kBlockN * 32u;
                             mbar_arrive_expect_tx(&bar_full_k[st], r_tx);
@@ -976,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_3d(dv, &tm.rh, &bar_full_v[st], 0, 0, 0);
                             if (p.part) tma_load_2d(dv + p.full_atoms * kBlockN * 32, &tm.rhp, &bar_full_v[st], 0, 0);
                         } else {
-                            const int j = u - (BIAS == kBiasSam ? 1 : 0);
+                            const int j = u - t_use;
                             const int kr = jr.k_row + j * p.kv_w;
                             mbar_arrive_expect_tx(&bar_full_k[st], kv_tx);
                             tma_load_4d(dk, &tm.k, &bar_full_k[st], 0, kr, jr.k_slice, 0);
@@ -1122,21 +1174,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t qa = kdesc(smem_u32(sQ + (x * p.nq + qb) * T::kBytes));
                     if (!waitb(&bar_q_full[x][qb], (ju / p.nq) & 1, kStatusWaitQ)) { ok = false; break; }
                     if constexpr (BIAS == kBiasSam) {
+                        // the tables: a ring stage, or the CTA's resampled copies
                         const int st = ring % nst;
                         const uint32_t par = (ring / nst) & 1;
-                        if (!waitb(&bar_full_k[st], par, kStatusWaitK) || !waitb(&bar_full_v[st], par, kStatusWaitV)) {
+                        if (!p.sam_resample &&
+                            (!waitb(&bar_full_k[st], par, kStatusWaitK) || !waitb(&bar_full_v[st], par, kStatusWaitV))) {
                             ok = false;
                             break;
                         }
                         // G_h rewrites O_x: the previous job's epilogue must be done with it
                         if (ju > 0 && !waitb(&bar_oempty[x], (ju - 1) & 1, kStatusWaitO)) { ok = false; break; }
-                        issue_qk<DPAD>(tSx, qa, kdesc(smem_u32(sRing + st * p.ring_stage_bytes)),
-                                       make_idesc_f16(bf, kBlockM, p.n_rw, false));
-                        issue_qk<DPAD>(tOx, qa, kdesc(smem_u32(sRing + st * p.ring_stage_bytes + T::kBytes)),
-                                       make_idesc_f16(bf, kBlockM, p.n_rh, false));
+                        const uint32_t rw_a = p.sam_resample ? smem_u32(smem + p.off_rtab)
+                                                             : smem_u32(sRing + st * p.ring_stage_bytes);
+                        issue_qk<DPAD>(tSx, qa, kdesc(rw_a), make_idesc_f16(bf, kBlockM, p.n_rw, false));
+                        issue_qk<DPAD>(tOx, qa, kdesc(rw_a + T::kBytes), make_idesc_f16(bf, kBlockM, p.n_rh, false));
                         mma_commit(&bar_g[x]);
-                        mma_commit(&bar_empty[st]);
-                        ++ring;
+                        if (!p.sam_resample) {
+                            mma_commit(&bar_empty[st]);
+                            ++ring;
+                        }
                     }
                     const int n = shared_job<VL>(p, vt, job).n_kv;
                     {
@@ -1444,11 +1500,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!__all_sync(0xffffffffu, mbar_wait(&bar_g[x], ju & 1, abort_flag, kStatusWaitG))) { ok = false; break; }
                     tc_fence_after();
                     const float f = DBG ? 1.0f : kLog2e;
-                    if (SW == 0 && p.sam_general) {
+                    if (p.sam_general) {
                         // unequal grids or tables of another length: each key row /
                         // column reads its table row through the coordinate scalers,
                         // linearly resampled from G (resampling commutes with Q.R)
-                        sam_general_rows(tS, tO, p, min(qh, p.s_h - 1), min(qw, p.s_w - 1), f, sam_rh, sam_rw, r);
+                        if constexpr (SW > 0) {
+                            // the square-grid kernels hold rel_w as fp16 pairs (kw = 2u, 2u+1)
+                            float rw_loc[SW];
+                            sam_general_rows(tS, tO, p, min(qh, p.s_h - 1), min(qw, p.s_w - 1), f, sam_rh, nullptr,
+                                             rw_loc, r);
+#pragma unroll
+                            for (int u = 0; u < SW / 2; ++u)
+                                sam_rw_h2[u] = __floats2half2_rn(rw_loc[2 * u], rw_loc[2 * u + 1]);
+                        } else {
+                            sam_general_rows(tS, tO, p, min(qh, p.s_h - 1), min(qw, p.s_w - 1), f, sam_rh, sam_rw,
+                                             nullptr, r);
+                        }
                         tc_fence_before();
                         warp_arrive(&bar_gdone[x]);
                     } else {

@@ -93,6 +93,7 @@ cudaError_t launch_attn_sam(const LaunchArgs& a) {
     if (a.mode != kModeShared) return cudaErrorInvalidValue;
     switch (a.sw) {
         case 64: return launch_dbg<DPAD, kBiasSam, kModeShared, 64, 0>(a);
+        case 48: return launch_dbg<DPAD, kBiasSam, kModeShared, 48, 0>(a);
         case 14: return launch_dbg<DPAD, kBiasSam, kModeShared, 14, 0>(a);
         default: return launch_dbg<DPAD, kBiasSam, kModeShared, 0, 0>(a);
     }

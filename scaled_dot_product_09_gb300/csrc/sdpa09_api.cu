@@ -325,25 +325,39 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         p.s_w = a->q_w;
         p.k_h = a->k_h;
         p.k_w = a->k_w;
-        p.n_rh = (lin_h + 15) / 16 * 16;
-        p.n_rw = (lin_w + 15) / 16 * 16;
         p.sam_lin_h = lin_h;
         p.sam_lin_w = lin_w;
         p.sam_lout_h = lout_h;
         p.sam_lout_w = lout_w;
-        // unequal grids or resized tables: rows through the coordinate
-        // scalers, in float32 as the published code computes them
-        p.sam_general = (a->q_h != a->k_h || a->q_w != a->k_w || lin_h != lout_h || lin_w != lout_w) ? 1 : 0;
+        p.rel_h = a->rel_h;
+        p.rel_w = a->rel_w;
+        // Unequal grids: rows through the coordinate scalers (float32, as the
+        // published code computes them), resampled from G when the tables
+        // have another length.  Equal grids with such tables: each CTA
+        // resamples the tables once into shared memory (G then has the
+        // addressed length and the row is a plain shift).
+        p.sam_general = (a->q_h != a->k_h || a->q_w != a->k_w) ? 1 : 0;
+        p.sam_resample = (!p.sam_general && (lin_h != lout_h || lin_w != lout_w)) ? 1 : 0;
+        p.n_rh = ((p.sam_resample ? lout_h : lin_h) + 15) / 16 * 16;
+        p.n_rw = ((p.sam_resample ? lout_w : lin_w) + 15) / 16 * 16;
         p.sam_qs_h = (float)std::max((double)a->k_h / a->q_h, 1.0);
         p.sam_ks_h = (float)std::max((double)a->q_h / a->k_h, 1.0);
         p.sam_off_h = (float)((a->k_h - 1) * std::max((double)a->q_h / a->k_h, 1.0));
         p.sam_qs_w = (float)std::max((double)a->k_w / a->q_w, 1.0);
         p.sam_ks_w = (float)std::max((double)a->q_w / a->k_w, 1.0);
         p.sam_off_w = (float)((a->k_w - 1) * std::max((double)a->q_w / a->k_w, 1.0));
-        // square 14x14 and 64x64 grids have specialised kernels (the row of G
-        // that a query needs is then short and its shift has few bits)
-        sw_spec = (!p.sam_general && a->q_h == a->q_w && (a->q_w == 64 || a->q_w == 14)) ? a->q_w : 0;
+        // square 14x14, 48x48 and 64x64 grids have specialised kernels (the
+        // row of G that a query needs is then short and its shift has few
+        // bits; key tiles start on grid rows), also with resampled tables
+        const bool square = a->q_h == a->q_w && a->k_h == a->q_h && a->k_w == a->q_w;
+        sw_spec = (square && (a->q_w == 64 || a->q_w == 48 || a->q_w == 14)) ? a->q_w : 0;
         extra = (size_t)sam_extra_floats(sw_spec == 0, a->k_h, a->k_w, Nk) * 4;
+        if (p.sam_resample) {
+            // the resampled tables after the bias rows, 1 KB aligned (swizzled operands)
+            extra = (extra + 1023) / 1024 * 1024;
+            p.off_rtab = (uint32_t)extra;  // relative to the extra area until its offset is known
+            extra += 2 * tile_bytes;
+        }
         bias = kBiasSam;
     } else if (bias_kind != ATTN_BIAS_NONE) {
         return fail(ATTN_ERR_ARG, "unknown bias kind %d", (int)bias_kind);
@@ -426,6 +440,7 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         p.off_q = 0;
         p.off_ring = (uint32_t)(2 * nq * tile_bytes);
         p.off_extra = (uint32_t)(p.off_ring + nst * p.ring_stage_bytes);
+        if (p.sam_resample) p.off_rtab += p.off_extra;
     }
     const size_t smem = p.off_extra + extra + 1024;
     const int nsm = sm_count();

@@ -43,9 +43,10 @@ class Workload:
     grid_h: int = 0
     grid_w: int = 0
     shift: int = 0
-    # SAM grid (query grid == key grid)
+    # SAM grid (query grid == key grid) and table rows (0: 2*side-1)
     s_h: int = 0
     s_w: int = 0
+    rel_len: int = 0
     # variable-length batch: per-sequence query / key token counts (B of each)
     seqlens_q: tuple = ()
     seqlens_k: tuple = ()
@@ -92,7 +93,9 @@ class Workload:
         if self.bias == "swin":
             tab = (2 * self.win - 1) ** 2 * self.H * 4
         elif self.bias == "sam":
-            tab = ((2 * self.s_h - 1) + (2 * self.s_w - 1)) * self.d * e
+            lh = self.rel_len or 2 * self.s_h - 1
+            lw = self.rel_len or 2 * self.s_w - 1
+            tab = (lh + lw) * self.d * e
         return qo + kv + tab
 
     def with_(self, **kw) -> "Workload":
@@ -116,6 +119,11 @@ WORKLOADS = {
     "sam_vith_global": Workload(
         "sam_vith_global", B=8, H=16, Nq=4096, Nk=4096, d=80, dtype="bf16", bias="sam", seed=3,
         s_h=64, s_w=64, note="SAM ViT-H global encoder attention on the 64x64 grid"),
+    "sam_vith_global_768": Workload(
+        "sam_vith_global_768", B=8, H=16, Nq=48 * 48, Nk=48 * 48, d=80, dtype="bf16", bias="sam", seed=7,
+        s_h=48, s_w=48, rel_len=127,
+        note="SAM ViT-H global attention on a 768-pixel input (48x48 grid) with the 1024-pixel "
+             "model's 127-row tables, resampled to 95 rows"),
     "sd_unet_self": Workload(
         "sd_unet_self", B=16, H=8, Nq=4096, Nk=4096, d=40, dtype="fp16", bias="none", seed=4,
         note="Stable Diffusion UNet 64x64-latent self-attention"),
@@ -162,6 +170,6 @@ def make_inputs(w: Workload, seed: int | None = None) -> Inputs:
     if w.bias == "swin":
         out.table = normal(((2 * w.win - 1) ** 2, w.H), 0.02).contiguous()
     elif w.bias == "sam":
-        out.rel_h = normal((2 * w.s_h - 1, w.d), 0.02).to(dt)
-        out.rel_w = normal((2 * w.s_w - 1, w.d), 0.02).to(dt)
+        out.rel_h = normal((w.rel_len or 2 * w.s_h - 1, w.d), 0.02).to(dt)
+        out.rel_w = normal((w.rel_len or 2 * w.s_w - 1, w.d), 0.02).to(dt)
     return out

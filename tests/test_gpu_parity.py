@@ -80,7 +80,7 @@ def test_sd_cross_reduced():
 # ------------------------------------------------------ workloads, full size --
 
 @pytest.mark.parametrize("name", ["swin_t_stage1", "sam_vith_window", "sam_vith_global",
-                                  "sd_unet_self", "sd_unet_cross"])
+                                  "sam_vith_global_768", "sd_unet_self", "sd_unet_cross"])
 def test_full_size_sampled(name):
     sampled_parity(W[name])
 
@@ -195,6 +195,17 @@ def test_sam_window_bias_indexing_bit_exact():
 def test_sam_global_64x64_bias_indexing_bit_exact():
     # the kernel specialised for 64x64 grids (6-bit G-row shifts, 2-row key tiles)
     _sam_bias_bit_exact(W["sam_vith_global"].with_(B=1, H=2), slices=(0, 1), rows=range(0, 4096, 37))
+
+
+def test_sam_global_48x48_bias_indexing_bit_exact():
+    # the kernel specialised for 48x48 grids (96-key tiles of two grid rows)
+    _sam_bias_bit_exact(W["sam_vith_global_768"].with_(B=1, H=2, rel_len=0), slices=(0, 1),
+                        rows=range(0, 2304, 23))
+
+
+def test_sam_resampled_tables_48x48_full():
+    # 127-row tables resampled to 95 rows in the 48x48 kernel (768-pixel input)
+    full_parity(W["sam_vith_global_768"].with_(B=1, H=2, seed=72))
 
 
 def _sam_bias_bit_exact(w, slices=None, rows=None):
