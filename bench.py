@@ -60,16 +60,42 @@ def _peaks():
                 "source": "fallback"}
 
 
+def _code_tokens(text: str) -> str:
+    """C/C++/CUDA source without comments, whitespace runs collapsed: what
+    the compiler sees (string and character literals kept as written)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def _kernel_sources_hash() -> str:
-    """sha256 over the CUDA sources, to tell whether recorded ncu counters
-    still describe the kernel being run."""
+    """sha256 over the CUDA sources' code (comments and whitespace left out),
+    to tell whether recorded ncu counters still describe the kernel being
+    run."""
     import hashlib
     d = os.path.join(ROOT, "scaled_dot_product_09_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(d)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(d, name), encoding="utf-8") as f:
+                h.update(name.encode() + b"\0" + _code_tokens(f.read()).encode())
     return h.hexdigest()
 
 

@@ -121,10 +121,10 @@ struct AttnParams {
     // SAM
     int s_h, s_w, n_rh, n_rw;  // query grid; MMA widths of the R_h / R_w tables as given
     int k_h, k_w;              // key grid (the query grid unless general)
-    // General SAM (unequal grids or tables of another length, generic kernel
-    // only): per axis the float32 coordinate scalers of the query and key
-    // coordinates and the offset, the table length as given and the length
-    // the index addresses (2 * max(q, k) - 1)
+    // General SAM (unequal query and key grids, which the host sends to the
+    // generic kernel): per axis the float32 coordinate scalers of the query
+    // and key coordinates and the offset, the table length as given and the
+    // length the index addresses (2 * max(q, k) - 1)
     int sam_general;
     float sam_qs_h, sam_ks_h, sam_off_h, sam_qs_w, sam_ks_w, sam_off_w;
     int sam_lin_h, sam_lout_h, sam_lin_w, sam_lout_w;
@@ -1501,9 +1501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const float f = DBG ? 1.0f : kLog2e;
                     if (p.sam_general) {
-                        // unequal grids or tables of another length: each key row /
-                        // column reads its table row through the coordinate scalers,
-                        // linearly resampled from G (resampling commutes with Q.R)
+                        // unequal grids: each key row / column reads its table row
+                        // through the coordinate scalers, linearly resampled from G
+                        // when the tables have another length (resampling commutes
+                        // with Q.R); the square-grid branch is kept for kernels that
+                        // would be given unequal grids, which the host never does
                         if constexpr (SW > 0) {
                             // the square-grid kernels hold rel_w as fp16 pairs (kw = 2u, 2u+1)
                             float rw_loc[SW];

@@ -105,3 +105,12 @@ def test_bound_classification():
     assert bench._bound(WORKLOADS["sd_unet_cross"]) == "hbm"
     assert bench._bound(WORKLOADS["sd_unet_self"]) == "tensor"
     assert bench._bound(WORKLOADS["sam_vith_global"]) == "tensor"
+
+
+def test_sources_hash_ignores_comments_not_code():
+    a = 'int f(int x) {  // twice\n  return 2 * x; /* doubled */ }\nconst char* s = "//not a comment";'
+    b = 'int f(int x) {\n    return 2 * x; }\nconst char* s = "//not a comment"; // note'
+    c = 'int f(int x) { return 3 * x; }\nconst char* s = "//not a comment";'
+    assert bench._code_tokens(a) == bench._code_tokens(b)
+    assert bench._code_tokens(a) != bench._code_tokens(c)
+    assert '"//not a comment"' in bench._code_tokens(a)
