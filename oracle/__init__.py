@@ -301,3 +301,64 @@ def attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, H, scale, nthreads: int = 0
         o, _ = attn_fwd(qs, ks, vs, H, scale, None, nthreads)
         out[q0:q0 + H * lq] = o.reshape(H * lq, d)
     return out
+
+
+def attn_bwd(q, k, v, dout, H, scale, bias: Bias | None = None):
+    """Gradients of the forward pass for training (the Swin talk, "视觉大模型训练和
+    推理加速" section 二, treats the forward and the backward computation of its
+    custom operators alike).  Per slice, with P and O from the forward
+    definition and dO the gradient of the loss with respect to O:
+
+        dV = P^T dO,   dP = dO V^T,   D_i = sum_c dO[i,c] O[i,c]  (= sum_j P dP),
+        dS = P * (dP - D),   dQ = scale dS K,   dK = scale dS^T Q,
+
+    and dS is the gradient of every additive bias entry.  Swin: the table row
+    of each (query, key) pair of head h collects dS (the mask is constant).
+    SAM: bias[i,j] = Q_i . (R_h'[ih] + R_w'[iw]) adds sum_j dS[i,j] (R_h'[ih] +
+    R_w'[iw]) to dQ_i and dS[i,j] Q_i to rows ih / iw of the resampled
+    tables, which the transposed resampling returns to the tables as given.
+
+    q [BH, Nq, d], k/v [BH, Nk, d], dout [BH, Nq, d].  Returns a dict with
+    dq, dk, dv and, per bias kind, d_table [(2M-1)^2, H] or d_rel_h, d_rel_w
+    (fp64)."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    BH, Nq, Nk, d = _shape(q, k)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    kind = bias.kind if bias is not None else "none"
+    res = {}
+    if kind == "swin":
+        M = bias.win
+        t = np.arange(M * M)
+        idx = np.array([[swin_index(M, i // M, i % M, j // M, j % M) for j in t] for i in t])
+        d_table = np.zeros_like(bias.table)
+    elif kind == "sam":
+        i_q, i_k = np.arange(Nq), np.arange(Nk)
+        IH = bias._ih[(i_q // bias.s_w)[:, None], (i_k // bias.k_w)[None, :]]
+        IW = bias._iw[(i_q % bias.s_w)[:, None], (i_k % bias.k_w)[None, :]]
+        d_rh, d_rw = np.zeros_like(bias._rh), np.zeros_like(bias._rw)
+    for s in range(BH):
+        P, O = attn_probs(q, k, v, H, scale, s, bias)
+        dO = dout[s]
+        dv[s] = P.T @ dO
+        dP = dO @ v[s].T
+        D = np.sum(dO * O, axis=1, keepdims=True)
+        dS = P * (dP - D)
+        dq[s] = scale * (dS @ k[s])
+        dk[s] = scale * (dS.T @ q[s])
+        if kind == "swin":
+            np.add.at(d_table[:, s % H], idx.ravel(), dS.ravel())
+        elif kind == "sam":
+            dq[s] += np.einsum("ij,ijc->ic", dS, bias._rh[IH] + bias._rw[IW])
+            contrib = (dS[:, :, None] * q[s][:, None, :]).reshape(-1, d)
+            np.add.at(d_rh, IH.ravel(), contrib)
+            np.add.at(d_rw, IW.ravel(), contrib)
+    res.update(dq=dq, dk=dk, dv=dv)
+    if kind == "swin":
+        res["d_table"] = d_table
+    elif kind == "sam":
+        # the resampling is linear (R' = W R): its transpose carries the gradient back
+        W_h = sam_resize(np.eye(bias.rel_h.shape[0]), bias._rh.shape[0])
+        W_w = sam_resize(np.eye(bias.rel_w.shape[0]), bias._rw.shape[0])
+        res["d_rel_h"] = W_h.T @ d_rh
+        res["d_rel_w"] = W_w.T @ d_rw
+    return res

@@ -572,3 +572,109 @@ def test_sam_unequal_grids_attention_matches_torch_sdpa():
             torch.from_numpy(q[h])[None], torch.from_numpy(k[h])[None], torch.from_numpy(v[h])[None],
             attn_mask=bias[None], scale=0.4)[0].numpy()
         np.testing.assert_allclose(got[h], want, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------- backward pass --
+# attn_bwd against torch fp64 autograd of the forward definition (a separate
+# differentiation) and against central finite differences of the oracle's
+# own forward pass.
+
+def _torch_attn(q, k, v, scale, bias):
+    s = scale * q @ k.transpose(-1, -2) + bias
+    return torch.softmax(s, dim=-1) @ v
+
+
+def _grads(out, dout, *xs):
+    return torch.autograd.grad(out, xs, grad_outputs=dout)
+
+
+def test_bwd_no_bias_matches_autograd():
+    rng = np.random.default_rng(60)
+    BH, Nq, Nk, d, H = 4, 9, 13, 6, 2
+    q, k, v = (rng.standard_normal((BH, n, d)) for n in (Nq, Nk, Nk))
+    dout = rng.standard_normal((BH, Nq, d))
+    got = oracle.attn_bwd(q, k, v, dout, H, 0.3)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    want = _grads(_torch_attn(tq, tk, tv, 0.3, 0.0), torch.tensor(dout), tq, tk, tv)
+    for name, w in zip(("dq", "dk", "dv"), want):
+        np.testing.assert_allclose(got[name], w.numpy(), rtol=0, atol=1e-11)
+
+
+def test_bwd_swin_matches_autograd():
+    rng = np.random.default_rng(61)
+    M, G, s_, H, d = 3, 6, 1, 2, 5
+    nW = (G // M) ** 2
+    BH, N = nW * H, M * M
+    table = rng.standard_normal(((2 * M - 1) ** 2, H)) * 0.3
+    q, k, v, dout = (rng.standard_normal((BH, N, d)) for _ in range(4))
+    b = oracle.Bias("swin", table=table, win=M, grid_h=G, grid_w=G, shift=s_)
+    got = oracle.attn_bwd(q, k, v, dout, H, 0.4, b)
+    # torch: the table gathered by relative offset (requires grad), plus the
+    # constant mask taken from a zero table
+    r, c = np.arange(N) // M, np.arange(N) % M
+    idx = torch.tensor((r[:, None] - r[None, :] + M - 1) * (2 * M - 1) + (c[:, None] - c[None, :] + M - 1))
+    zero = oracle.Bias("swin", table=np.zeros_like(table), win=M, grid_h=G, grid_w=G, shift=s_)
+    mask = torch.tensor(np.stack([oracle.bias_matrix(q, H, i, N, zero) for i in range(BH)]))
+    tt = torch.tensor(table, requires_grad=True)
+    heads = torch.tensor([i % H for i in range(BH)])
+    bias = tt[idx][:, :, heads].permute(2, 0, 1) + mask
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    want = _grads(_torch_attn(tq, tk, tv, 0.4, bias), torch.tensor(dout), tq, tk, tv, tt)
+    for name, w in zip(("dq", "dk", "dv", "d_table"), want):
+        np.testing.assert_allclose(got[name], w.numpy(), rtol=0, atol=1e-11)
+
+
+def test_bwd_sam_unequal_resampled_matches_autograd():
+    rng = np.random.default_rng(62)
+    (qh, qw), (kh, kw), d, H = (3, 4), (2, 5), 6, 2
+    Nq, Nk = qh * qw, kh * kw
+    Rh = rng.standard_normal((4, d)) * 0.3    # 2*max(3,2)-1 = 5 rows addressed: upsampled
+    Rw = rng.standard_normal((12, d)) * 0.3   # 2*max(4,5)-1 = 9 rows addressed: downsampled
+    q, dout = (rng.standard_normal((H, Nq, d)) for _ in range(2))
+    k, v = (rng.standard_normal((H, Nk, d)) for _ in range(2))
+    b = oracle.Bias("sam", rel_h=Rh, rel_w=Rw, s_h=qh, s_w=qw, k_h=kh, k_w=kw)
+    got = oracle.attn_bwd(q, k, v, dout, H, 0.35, b)
+
+    def rows(R, a, bb):
+        L = 2 * max(a, bb) - 1
+        Rr = torch.nn.functional.interpolate(R.T[None], size=L, mode="linear", align_corners=False)[0].T
+        qc = torch.arange(a)[:, None] * max(bb / a, 1.0)
+        kc = torch.arange(bb)[None, :] * max(a / bb, 1.0)
+        return Rr, ((qc - kc) + (bb - 1) * max(a / bb, 1.0)).long()
+
+    tRh, tRw = torch.tensor(Rh, requires_grad=True), torch.tensor(Rw, requires_grad=True)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    Rh_r, ih = rows(tRh, qh, kh)
+    Rw_r, iw = rows(tRw, qw, kw)
+    i, j = torch.arange(Nq), torch.arange(Nk)
+    IH = ih[(i // qw)[:, None], (j // kw)[None, :]]
+    IW = iw[(i % qw)[:, None], (j % kw)[None, :]]
+    bias = torch.einsum("hic,ijc->hij", tq, Rh_r[IH] + Rw_r[IW])
+    want = _grads(_torch_attn(tq, tk, tv, 0.35, bias), torch.tensor(dout), tq, tk, tv, tRh, tRw)
+    for name, w in zip(("dq", "dk", "dv", "d_rel_h", "d_rel_w"), want):
+        np.testing.assert_allclose(got[name], w.numpy(), rtol=0, atol=1e-11)
+
+
+def test_bwd_finite_differences():
+    """Central differences of L = sum(dO * O) through the oracle's forward."""
+    rng = np.random.default_rng(63)
+    M, G, H, d = 2, 4, 1, 3
+    BH, N = (G // M) ** 2 * H, M * M
+    table = rng.standard_normal(((2 * M - 1) ** 2, H)) * 0.5
+    q, k, v, dout = (rng.standard_normal((BH, N, d)) for _ in range(4))
+
+    def loss(q_, k_, v_, t_):
+        b_ = oracle.Bias("swin", table=t_, win=M, grid_h=G, grid_w=G, shift=1)
+        o, _ = oracle.attn_fwd(q_, k_, v_, H, 0.6, b_)
+        return float(np.sum(o * dout))
+
+    got = oracle.attn_bwd(q, k, v, dout, H, 0.6, oracle.Bias("swin", table=table, win=M, grid_h=G, grid_w=G, shift=1))
+    eps = 1e-6
+    for name, x, pos in (("dq", q, (1, 2, 0)), ("dk", k, (3, 0, 2)), ("dv", v, (0, 3, 1)), ("d_table", table, (4, 0))):
+        xp, xm = x.copy(), x.copy()
+        xp[pos] += eps
+        xm[pos] -= eps
+        args_p = [xp if a is x else a for a in (q, k, v, table)]
+        args_m = [xm if a is x else a for a in (q, k, v, table)]
+        fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        assert abs(fd - got[name][pos]) < 1e-7, (name, fd, got[name][pos])
