@@ -225,6 +225,47 @@ class DeviceSets:
         self.bias = _gpu_bias(w, inp, dev, image)
 
 
+def _time_bwd(w: Workload, stream, dev, steps: int):
+    """Seconds per attn_bwd call (gradients of the whole workload) over
+    rotating input sets, CUDA-graph replays like the forward."""
+    import scaled_dot_product_09_gb300 as sdpa
+    inp = make_inputs(w)
+    n = max(2, math.ceil(3 * L2_BYTES / (2 * w.io_bytes)) + 1)
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    dout = torch.randn(inp.q.shape, generator=g).to(inp.q.dtype)
+    bias = _gpu_bias(w, inp, dev)
+    sets = []
+    for _ in range(n):
+        q, k, v, do = (x.to(dev) for x in (inp.q, inp.k, inp.v, dout))
+        o = sdpa.attn_fwd(q, k, v, scale=w.scale, bias=bias, stream=stream)
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                 torch.zeros_like(bias.table) if bias is not None else None)
+        sets.append((q, k, v, o, do, grads))
+    torch.cuda.synchronize()
+
+    def step(i):
+        q, k, v, o, do, grads = sets[i % n]
+        sdpa.attn_bwd(q, k, v, o, do, scale=w.scale, bias=bias, stream=stream, grads=grads)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(steps):
+            step(i)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        start.record(stream)
+        graph.replay()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3 / steps
+
+
 def _attn(w: Workload, q, k, v, out, bias, stream):
     """One step through the public API: attn_fwd, or attn_fwd_varlen for a
     nested batch."""
@@ -337,6 +378,13 @@ def _suite(stream, dev, peaks, names):
     for name in names:
         base, _, layout = name.partition("@")
         w = WORKLOADS[base]
+        if layout == "bwd":
+            # backward: 10*B*H*Nq*Nk*d (S recomputed, dV, dP, dQ, dK); CUDA-core fp32
+            t = _time_bwd(w, stream, dev, 50)
+            out[name] = {"us_per_step": round(t * 1e6, 2), "tflops": round(2.5 * w.flops / t / 1e12, 2),
+                         "bound": "alu"}
+            torch.cuda.empty_cache()
+            continue
         inp = make_inputs(w)
         sets = DeviceSets(w, inp, dev, image=layout == "image")
         steps = max(20, min(2000, int(0.3 / max(w.flops / 1e15, 1e-6))))
@@ -506,7 +554,8 @@ def main(argv=None):
     if rank == 0 and not args.no_suite:
         del sets
         torch.cuda.empty_cache()
-        suite = _suite(stream, dev, peaks, [n for n in ("swin_t_stage1@image", "sam_vith_window", "sam_vith_global",
+        suite = _suite(stream, dev, peaks, [n for n in ("swin_t_stage1@image", "swin_t_stage1@bwd",
+                                                        "sam_vith_window", "sam_vith_global",
                                                         "sam_vith_global_768", "sd_unet_self", "sd_unet_cross",
                                                         "sd_unet_self_varlen")
                                             if n != w.name])

@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define SDPA09_ABI_VERSION 4
+#define SDPA09_ABI_VERSION 5
 
 typedef enum {
     ATTN_BF16 = 0, /* bfloat16 Q/K/V/O ("model.to(torch.bfloat16)" in the SAM rewrite) */
@@ -174,6 +174,34 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int 
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, const int* cu_seqlens_q,
                     const int* cu_seqlens_k, int n_seq, int H, int d, float scale, attn_dtype dtype,
                     void* stream);
+
+/* attn_bwd -- gradients of attn_fwd for training, for short sequences
+ * (windows): the Swin talk ("视觉大模型训练和推理加速" section 二) builds the
+ * forward and backward computation of its window operators alike.  With
+ * P = softmax(scale*Q.K^T + bias), O = P.V and dO = dout:
+ *   dV = P^T dO,  dS = P * (dO V^T - rowsum(dO * O)),
+ *   dQ = scale dS K,  dK = scale dS^T Q,
+ * and for the Swin bias the table gradient: dS summed into the table row of
+ * each (query, key) pair of each head (the mask is constant).
+ *
+ *  q, k, v    device inputs of the forward call, layout [B][H][N][d];
+ *  out        device O of the forward call (for rowsum(dO * O));
+ *  dout       device gradient of the loss with respect to O, like out;
+ *  dq, dk, dv device outputs, like q, k, v; fully overwritten.
+ *  B, H, Nq, Nk, d, scale, dtype as for attn_fwd; Nq, Nk <= 128, d <= 64.
+ *  bias_kind  ATTN_BIAS_NONE or ATTN_BIAS_SWIN (windows layout, bias_args
+ *             as for attn_fwd).
+ *  d_table    device fp32 [(2*win-1)^2][H] for ATTN_BIAS_SWIN, ADDED to
+ *             (the caller zeroes it first); NULL otherwise.
+ *  stream     cudaStream_t to enqueue on.
+ * The probabilities are recomputed exactly in fp32 from the inputs (no
+ * saved statistics), products accumulate in fp32, outputs are rounded to
+ * nearest even.  Returns ATTN_OK, ATTN_ERR_ARG, ATTN_ERR_UNSUPPORTED
+ * (longer sequences, d > 64, SAM bias, image layout) or ATTN_ERR_CUDA.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, void* dq, void* dk,
+             void* dv, int B, int H, int Nq, int Nk, int d, float scale, attn_dtype dtype,
+             attn_bias_kind bias_kind, const void* bias_args, float* d_table, void* stream);
 
 /* attn_debug_bias -- test hook for the in-kernel bias builders.
  *

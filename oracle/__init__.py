@@ -303,7 +303,7 @@ def attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, H, scale, nthreads: int = 0
     return out
 
 
-def attn_bwd(q, k, v, dout, H, scale, bias: Bias | None = None):
+def attn_bwd(q, k, v, dout, H, scale, bias: Bias | None = None, out=None):
     """Gradients of the forward pass for training (the Swin talk, "视觉大模型训练和
     推理加速" section 二, treats the forward and the backward computation of its
     custom operators alike).  Per slice, with P and O from the forward
@@ -318,10 +318,13 @@ def attn_bwd(q, k, v, dout, H, scale, bias: Bias | None = None):
     R_w'[iw]) to dQ_i and dS[i,j] Q_i to rows ih / iw of the resampled
     tables, which the transposed resampling returns to the tables as given.
 
-    q [BH, Nq, d], k/v [BH, Nk, d], dout [BH, Nq, d].  Returns a dict with
+    q [BH, Nq, d], k/v [BH, Nk, d], dout [BH, Nq, d]; out, when given, is the
+    forward output the caller holds (e.g. rounded to 16 bits) and D is taken
+    from it, as a training step does; by default the exact O.  Returns a dict with
     dq, dk, dv and, per bias kind, d_table [(2M-1)^2, H] or d_rel_h, d_rel_w
     (fp64)."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    out = None if out is None else _f64(out)
     BH, Nq, Nk, d = _shape(q, k)
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     kind = bias.kind if bias is not None else "none"
@@ -338,6 +341,8 @@ def attn_bwd(q, k, v, dout, H, scale, bias: Bias | None = None):
         d_rh, d_rw = np.zeros_like(bias._rh), np.zeros_like(bias._rw)
     for s in range(BH):
         P, O = attn_probs(q, k, v, H, scale, s, bias)
+        if out is not None:
+            O = out[s]
         dO = dout[s]
         dv[s] = P.T @ dO
         dP = dO @ v[s].T

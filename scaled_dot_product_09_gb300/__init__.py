@@ -21,7 +21,7 @@ import math
 import os
 import threading
 
-__all__ = ["attn_fwd", "attn_fwd_varlen", "attn_debug_bias", "attn_device_status", "selftest_wait_timeout", "SwinBias", "SamBias",
+__all__ = ["attn_fwd", "attn_fwd_varlen", "attn_bwd", "attn_debug_bias", "attn_device_status", "selftest_wait_timeout", "SwinBias", "SamBias",
            "load_library", "AttnError", "ATTN_OK", "ATTN_ERR_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT", "HEADER_SYMBOLS"]
 
@@ -31,7 +31,7 @@ ATTN_BIAS_NONE, ATTN_BIAS_SWIN, ATTN_BIAS_SAM_RELPOS = 0, 1, 2
 ATTN_SWIN_WINDOWS, ATTN_SWIN_IMAGE = 0, 1
 
 # Every extern "C" function include/sdpa09.h declares.
-HEADER_SYMBOLS = ("attn_fwd", "attn_fwd_varlen", "attn_debug_bias", "attn_device_status",
+HEADER_SYMBOLS = ("attn_fwd", "attn_fwd_varlen", "attn_bwd", "attn_debug_bias", "attn_device_status",
                   "attn_selftest_wait_timeout", "attn_last_error", "attn_abi_version")
 ATTN_VARLEN_MAX_SEQ = 128
 
@@ -115,6 +115,8 @@ def load_library(build: bool = True):
         ip = ctypes.POINTER(ctypes.c_int)
         lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, ip, ip, i, i, i, f, i, vp]
         lib.attn_fwd_varlen.restype = i
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp]
+        lib.attn_bwd.restype = i
         lib.attn_debug_bias.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp]
         lib.attn_debug_bias.restype = i
         lib.attn_device_status.argtypes = [vp]
@@ -234,6 +236,33 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, H, out=None, scale=None
                              _dtype_code(q), _stream_ptr(stream))
     _check(lib, rc)
     return out
+
+
+def attn_bwd(q, k, v, out, dout, scale=None, bias=None, stream=None, grads=None):
+    """Gradients of attn_fwd for short sequences (Nq, Nk <= 128, d <= 64):
+    q/k/v/out/dout [B,H,N,d] contiguous bf16/fp16 CUDA tensors (out: the
+    forward's output, dout: the gradient with respect to it).  Returns
+    (dq, dk, dv, d_table) with d_table the fp32 gradient of a SwinBias table
+    (windows layout), else None.  grads: the four buffers to use instead
+    (d_table is added to)."""
+    import torch
+    lib = load_library()
+    B, H, Nq, Nk, d = _shape(q, k, v)
+    for t in (out, dout):
+        if t.shape != q.shape or not t.is_contiguous():
+            raise AttnError(ATTN_ERR_ARG, "out and dout must be contiguous and shaped like q")
+    if grads is not None:
+        dq, dk, dv, d_table = grads
+    else:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        d_table = torch.zeros_like(bias.table) if isinstance(bias, SwinBias) else None
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kind, _keep, args = _bias_args(bias)
+    rc = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                      B, H, Nq, Nk, d, scale, _dtype_code(q), kind, args,
+                      _ptr(d_table) if d_table is not None else None, _stream_ptr(stream))
+    _check(lib, rc)
+    return dq, dk, dv, d_table
 
 
 def attn_debug_bias(q, k, v, scale=None, bias=None, stream=None):

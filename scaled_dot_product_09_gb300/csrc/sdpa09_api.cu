@@ -19,6 +19,7 @@
 #include <string>
 
 #include "../../include/sdpa09.h"
+#include "attn_bwd_window.cuh"
 #include "attn_launch.cuh"
 
 namespace sdpa09 {
@@ -550,6 +551,64 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, cons
     if (jobs == 0) return ATTN_OK;  // no sequence has a query (the tensors may be empty)
     return sdpa09::run(q, k, v, out, nullptr, 1, H, cu_seqlens_q[n_seq], cu_seqlens_k[n_seq], d, scale, dtype,
                        ATTN_BIAS_NONE, nullptr, stream, &vt);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, void* dq, void* dk,
+             void* dv, int B, int H, int Nq, int Nk, int d, float scale, attn_dtype dtype,
+             attn_bias_kind bias_kind, const void* bias_args, float* d_table, void* stream) {
+    using sdpa09::fail;
+    sdpa09::g_last_error.clear();
+    const void* ptrs[8] = {q, k, v, out, dout, dq, dk, dv};
+    for (const void* x : ptrs) {
+        if (!x) return fail(ATTN_ERR_ARG, "null tensor pointer");
+        if (!sdpa09::aligned16(x)) return fail(ATTN_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    }
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return fail(ATTN_ERR_ARG, "B, H, Nq, Nk must be >= 1");
+    if (d < 8 || d % 8 != 0) return fail(ATTN_ERR_ARG, "d must be a positive multiple of 8 (got %d)", d);
+    if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return fail(ATTN_ERR_ARG, "unknown dtype %d", (int)dtype);
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return fail(ATTN_ERR_ARG, "scale must be finite");
+    if (Nq > 128 || Nk > 128 || d > 64)
+        return fail(ATTN_ERR_UNSUPPORTED, "backward is built for sequences of at most 128 tokens and d <= 64");
+    const int64_t BH = (int64_t)B * H;
+    if (BH >= (int64_t(1) << 31) / 128) return fail(ATTN_ERR_UNSUPPORTED, "too many slices");
+    sdpa09::BwdParams p;
+    memset(&p, 0, sizeof(p));
+    p.q = q; p.k = k; p.v = v; p.o = out; p.dout = dout;
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    p.BH = (int)BH; p.H = H; p.Nq = Nq; p.Nk = Nk; p.d = d;
+    p.scale = scale;
+    p.is_bf16 = dtype == ATTN_BF16;
+    if (bias_kind == ATTN_BIAS_SWIN) {
+        const attn_swin_args* a = static_cast<const attn_swin_args*>(bias_args);
+        if (!a || !a->table) return fail(ATTN_ERR_ARG, "SWIN bias needs attn_swin_args with a table");
+        if (!d_table) return fail(ATTN_ERR_ARG, "SWIN backward needs d_table");
+        const int M = a->win;
+        if (M < 1 || Nq != M * M || Nk != M * M) return fail(ATTN_ERR_ARG, "SWIN needs Nq == Nk == win*win");
+        if (a->grid_h < M || a->grid_w < M || a->grid_h % M || a->grid_w % M)
+            return fail(ATTN_ERR_ARG, "grid_h and grid_w must be positive multiples of win");
+        if (a->shift < 0 || a->shift >= M) return fail(ATTN_ERR_ARG, "shift must lie in [0, win)");
+        if (a->layout != ATTN_SWIN_WINDOWS)
+            return fail(ATTN_ERR_UNSUPPORTED, "the backward takes the windows token layout");
+        const int nW = (a->grid_h / M) * (a->grid_w / M);
+        if (B % nW) return fail(ATTN_ERR_ARG, "B (windows) must be a multiple of the windows per image");
+        p.swin = 1;
+        p.table = a->table;
+        p.d_table = d_table;
+        p.win = M; p.grid_h = a->grid_h; p.grid_w = a->grid_w; p.shift = a->shift;
+        p.n_w = nW; p.n_ww = a->grid_w / M;
+    } else if (bias_kind != ATTN_BIAS_NONE) {
+        return fail(ATTN_ERR_UNSUPPORTED, "the backward takes no bias or the Swin bias");
+    }
+    const size_t smem = sdpa09::bwd_window_smem_bytes(Nq, Nk, d, p.win, H, p.swin != 0);
+    if (smem > 227 * 1024) return fail(ATTN_ERR_UNSUPPORTED, "slice too large for shared memory (%zu bytes)", smem);
+    const int nsm = sdpa09::sm_count();
+    if (nsm <= 0) return fail(ATTN_ERR_CUDA, "no CUDA device");
+    int per_sm = (int)std::min<size_t>(8, (228 * 1024) / (smem + 1024));
+    if (per_sm < 1) per_sm = 1;
+    const int grid = (int)std::min<int64_t>(BH, (int64_t)nsm * per_sm);
+    cudaError_t e = sdpa09::launch_bwd_window(p, grid, smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    return ATTN_OK;
 }
 
 int attn_debug_bias(const void* q, const void* k, const void* v, float* bias_out, int B, int H,

@@ -1,0 +1,75 @@
+"""GPU parity of the backward pass (short sequences / windows) against the
+fp64 oracle's attn_bwd on the same seeded inputs, through the C ABI.
+
+Tolerance, derived from the arithmetic: dQ, dK and dV are rounded to the
+16-bit input type (relative 2^-8 for bf16, 2^-11 for fp16) after fp32
+accumulation from 16-bit operands, so |err| <= 2e-2 + 8e-3 |want| per
+element; the fp32 table gradient sums many dS terms, each off by fp32
+rounding only (the oracle takes D from the same 16-bit O): |err| <= 1e-3 +
+1e-3 |want|."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scaled_dot_product_09_gb300 as sdpa
+from scaled_dot_product_09_gb300.workloads import WORKLOADS, Workload, make_inputs
+
+from gpu_util import flat64, gpu_bias, oracle_bias, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+W = WORKLOADS
+
+
+def _check(got, want, what, atol=2e-2, rtol=8e-3):
+    got = np.asarray(got, dtype=np.float64)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    assert np.all(np.isfinite(got)), what
+    err = np.abs(got - want)
+    bad = err > atol + rtol * np.abs(want)
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements off, max |err| {err.max():.3e}"
+
+
+def _bwd_case(w: Workload, seed=None):
+    require_gpu()
+    inp = make_inputs(w, seed)
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    dout = torch.randn(inp.q.shape, generator=g).to(inp.q.dtype)
+    q, k, v, do = (x.cuda() for x in (inp.q, inp.k, inp.v, dout))
+    bias = gpu_bias(w, inp)
+    out = sdpa.attn_fwd(q, k, v, scale=w.scale, bias=bias)
+    dq, dk, dv, dtab = sdpa.attn_bwd(q, k, v, out, do, scale=w.scale, bias=bias)
+    torch.cuda.synchronize()
+    assert sdpa.attn_device_status() == sdpa.ATTN_OK
+    # D = rowsum(dO * O) from the 16-bit O the kernel was given
+    want = oracle.attn_bwd(flat64(inp.q), flat64(inp.k), flat64(inp.v), flat64(dout), w.H, w.scale,
+                           oracle_bias(w, inp), out=flat64(out.cpu()))
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check(flat64(t.cpu()), want[name], f"{w.name} {name}")
+    if w.bias == "swin":
+        _check(dtab.cpu().double().numpy(), want["d_table"], f"{w.name} d_table", atol=1e-3, rtol=1e-3)
+
+
+def test_bwd_no_bias_short():
+    _bwd_case(Workload("bwd_none", B=2, H=3, Nq=49, Nk=77, d=32, dtype="bf16", bias="none", seed=80))
+
+
+@pytest.mark.parametrize("nq,nk,d", [(1, 1, 8), (128, 128, 64), (100, 30, 40), (17, 128, 16)])
+def test_bwd_no_bias_shapes(nq, nk, d):
+    _bwd_case(Workload("bwd_shape", B=1, H=2, Nq=nq, Nk=nk, d=d, dtype="fp16", bias="none", seed=81 + nq))
+
+
+def test_bwd_swin_reduced():
+    # 2 images x 64 windows of 7x7, 3 heads, shift 3
+    _bwd_case(W["swin_t_stage1"].with_(B=2 * 64, seed=82))
+
+
+def test_bwd_swin_small_window_and_ragged_grid():
+    _bwd_case(W["swin_t_stage1"].with_(B=2 * 16, win=4, Nq=16, Nk=16, grid_h=16, grid_w=16, shift=2, seed=83))
+    _bwd_case(W["swin_t_stage1"].with_(B=9, grid_h=21, grid_w=21, dtype="bf16", seed=84))
+
+
+def test_bwd_swin_full_size():
+    """Swin-T stage 1, all 32 images: every gradient against the oracle."""
+    _bwd_case(W["swin_t_stage1"])
