@@ -25,11 +25,47 @@ namespace {
 
 constexpr int kBwdThreads = 256;
 
-__device__ __forceinline__ float ld16(const uint16_t* p, bool bf) {
-    return bf ? __bfloat162float(__ushort_as_bfloat16(*p)) : __half2float(__ushort_as_half(*p));
-}
 __device__ __forceinline__ uint16_t st16(float v, bool bf) {
     return bf ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
+}
+
+// Eight consecutive 16-bit values (16-byte aligned) as floats.
+__device__ __forceinline__ void ld8(const uint16_t* p, bool bf, float (&f)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        if (bf) {  // a bfloat16 is the high half of a float
+            f[2 * t] = __uint_as_float(w[t] << 16);
+            f[2 * t + 1] = __uint_as_float(w[t] & 0xffff0000u);
+        } else {
+            const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
+            f[2 * t] = x.x;
+            f[2 * t + 1] = x.y;
+        }
+    }
+}
+
+// Dot product of two rows of d 16-bit values (d % 8 == 0).
+__device__ __forceinline__ float dot_rows(const uint16_t* a, const uint16_t* b, int d, bool bf) {
+    float acc = 0.f;
+    for (int c = 0; c < d; c += 8) {
+        float x[8], y[8];
+        ld8(a + c, bf, x);
+        ld8(b + c, bf, y);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc = fmaf(x[t], y[t], acc);
+    }
+    return acc;
+}
+
+// Eight floats, scaled, rounded to 16 bits and stored as one 16-byte word.
+__device__ __forceinline__ void st8(uint16_t* p, const float (&a)[8], float scale, bool bf) {
+    uint32_t w[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+        w[t] = (uint32_t)st16(a[2 * t] * scale, bf) | ((uint32_t)st16(a[2 * t + 1] * scale, bf) << 16);
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Region of a coordinate along one axis of the shifted map: 0 inside, 1 in
@@ -89,9 +125,7 @@ __global__ void __launch_bounds__(kBwdThreads)
         // ---- S = scale Q.K^T + bias
         for (int e = tid; e < Nq * Nk; e += kBwdThreads) {
             const int i = e / Nk, j = e - (e / Nk) * Nk;
-            float acc = 0.f;
-            for (int c = 0; c < d; ++c) acc = fmaf(ld16(sQ + i * d + c, bf), ld16(sK + j * d + c, bf), acc);
-            float s = acc * p.scale;
+            float s = dot_rows(sQ + i * d, sK + j * d, d, bf) * p.scale;
             if (p.swin) {
                 const int ri = i / M, ci = i - ri * M, rj = j / M, cj = j - rj * M;
                 const int idx = (ri - rj + M - 1) * (2 * M - 1) + (ci - cj + M - 1);
@@ -125,29 +159,30 @@ __global__ void __launch_bounds__(kBwdThreads)
             }
         }
         // ---- D_i = dO_i . O_i
-        for (int i = tid; i < Nq; i += kBwdThreads) {
-            float acc = 0.f;
-            for (int c = 0; c < d; ++c) acc = fmaf(ld16(sdO + i * d + c, bf), ld16(sO + i * d + c, bf), acc);
-            sD[i] = acc;
-        }
+        for (int i = tid; i < Nq; i += kBwdThreads) sD[i] = dot_rows(sdO + i * d, sO + i * d, d, bf);
         __syncthreads();
-        // ---- dV = P^T dO
+        // ---- dV = P^T dO (each thread: eight adjacent columns of one row)
+        const int d8 = d / 8;
         {
             uint16_t* gdv = static_cast<uint16_t*>(p.dv) + (size_t)slice * Nk * d;
-            for (int e = tid; e < Nk * d; e += kBwdThreads) {
-                const int j = e / d, c = e - (e / d) * d;
-                float acc = 0.f;
-                for (int i = 0; i < Nq; ++i) acc = fmaf(sP[i * ld + j], ld16(sdO + i * d + c, bf), acc);
-                gdv[e] = st16(acc, bf);
+            for (int e = tid; e < Nk * d8; e += kBwdThreads) {
+                const int j = e / d8, c = (e - (e / d8) * d8) * 8;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int i = 0; i < Nq; ++i) {
+                    const float pij = sP[i * ld + j];
+                    float x[8];
+                    ld8(sdO + i * d + c, bf, x);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) acc[t] = fmaf(pij, x[t], acc[t]);
+                }
+                st8(gdv + j * d + c, acc, 1.f, bf);
             }
         }
         __syncthreads();  // P is read by dV before it becomes dS
         // ---- dS = P * (dO V^T - D), in place
         for (int e = tid; e < Nq * Nk; e += kBwdThreads) {
             const int i = e / Nk, j = e - (e / Nk) * Nk;
-            float acc = 0.f;
-            for (int c = 0; c < d; ++c) acc = fmaf(ld16(sdO + i * d + c, bf), ld16(sV + j * d + c, bf), acc);
-            const float ds = sP[i * ld + j] * (acc - sD[i]);
+            const float ds = sP[i * ld + j] * (dot_rows(sdO + i * d, sV + j * d, d, bf) - sD[i]);
             sP[i * ld + j] = ds;
             if (p.swin) {
                 const int ri = i / M, ci = i - ri * M, rj = j / M, cj = j - rj * M;
@@ -159,18 +194,30 @@ __global__ void __launch_bounds__(kBwdThreads)
         // ---- dQ = scale dS K,  dK = scale dS^T Q
         {
             uint16_t* gdq = static_cast<uint16_t*>(p.dq) + (size_t)slice * Nq * d;
-            for (int e = tid; e < Nq * d; e += kBwdThreads) {
-                const int i = e / d, c = e - (e / d) * d;
-                float acc = 0.f;
-                for (int j = 0; j < Nk; ++j) acc = fmaf(sP[i * ld + j], ld16(sK + j * d + c, bf), acc);
-                gdq[e] = st16(acc * p.scale, bf);
+            for (int e = tid; e < Nq * d8; e += kBwdThreads) {
+                const int i = e / d8, c = (e - (e / d8) * d8) * 8;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int j = 0; j < Nk; ++j) {
+                    const float sij = sP[i * ld + j];
+                    float x[8];
+                    ld8(sK + j * d + c, bf, x);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) acc[t] = fmaf(sij, x[t], acc[t]);
+                }
+                st8(gdq + i * d + c, acc, p.scale, bf);
             }
             uint16_t* gdk = static_cast<uint16_t*>(p.dk) + (size_t)slice * Nk * d;
-            for (int e = tid; e < Nk * d; e += kBwdThreads) {
-                const int j = e / d, c = e - (e / d) * d;
-                float acc = 0.f;
-                for (int i = 0; i < Nq; ++i) acc = fmaf(sP[i * ld + j], ld16(sQ + i * d + c, bf), acc);
-                gdk[e] = st16(acc * p.scale, bf);
+            for (int e = tid; e < Nk * d8; e += kBwdThreads) {
+                const int j = e / d8, c = (e - (e / d8) * d8) * 8;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int i = 0; i < Nq; ++i) {
+                    const float sij = sP[i * ld + j];
+                    float x[8];
+                    ld8(sQ + i * d + c, bf, x);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) acc[t] = fmaf(sij, x[t], acc[t]);
+                }
+                st8(gdk + j * d + c, acc, p.scale, bf);
             }
         }
     }
