@@ -1,6 +1,7 @@
 /*
  * sdpa09.h -- C ABI of the GB300 (sm_103a) fused scaled-dot-product
- * attention forward library, libsdpa09.so.
+ * attention library, libsdpa09.so: the forward pass (attn_fwd,
+ * attn_fwd_varlen) and its backward for windows (attn_bwd).
  *
  * The operation (per batch-head slice):
  *
@@ -14,16 +15,17 @@
  * (query, key, value) and every backend computes the same result.  The
  * bias kinds are described at attn_bias_kind.
  *
- * Conventions shared by every entry point:
+ * Conventions shared by the attention calls:
  *  - All tensors are device pointers owned by the caller.  The library
  *    never allocates per call, never copies host<->device and never
- *    synchronises the stream ("PyTorch团队重写「分割一切」模型，比原始实现快8倍",
+ *    synchronises the stream (attn_device_status, a status read, does) ("PyTorch团队重写「分割一切」模型，比原始实现快8倍",
  *    section on the bf16 baseline: an index operation whose host-side
  *    coordinates forced a copy and a blocking cudaStreamSynchronize was the
  *    first bottleneck removed).  Bias arguments are read from the host
  *    struct at call time and passed by value to the kernel.
  *  - Layout: Q and O are [B][H][Nq][d], K and V are [B][H][Nk][d], all
- *    contiguous with d innermost, in the dtype given (bf16 or fp16).  Each
+ *    contiguous with d innermost, in the dtype given (bf16 or fp16); the
+ *    Swin image layout and attn_fwd_varlen document their own.  Each
  *    pointer must be 16-byte aligned and d a multiple of 8 (the row pitch
  *    must be a multiple of 16 bytes for the tensor-memory-access engine).
  *  - Work runs on `stream` (a cudaStream_t; NULL = the legacy default
