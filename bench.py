@@ -446,6 +446,25 @@ def _oracle_sample(w: Workload, inp, budget_s: float, nthreads: int = 0):
     return flops / sec / 1e12, sec, rows_done, used
 
 
+def _torch_cpu_sample(w: Workload, inp, budget_s: float):
+    """Context for the no-bias workloads: torch's CPU scaled_dot_product_attention
+    in fp32 (the "native C++" backend of the Diffusers page, section 加速
+    Transformer 块) on whole slices until ~budget_s.  Returns (TFLOP/s,
+    seconds, slices, threads)."""
+    BH = w.B * w.H
+    q = inp.q.float().reshape(BH, w.Nq, w.d)
+    k = inp.k.float().reshape(BH, w.Nk, w.d)
+    v = inp.v.float().reshape(BH, w.Nk, w.d)
+    done, sec = 0, 0.0
+    while done < BH and sec < budget_s:
+        t0 = time.perf_counter()
+        torch.nn.functional.scaled_dot_product_attention(q[done:done + 1], k[done:done + 1], v[done:done + 1],
+                                                         scale=w.scale)
+        sec += time.perf_counter() - t0
+        done += 1
+    return 4.0 * done * w.Nq * w.Nk * w.d / sec / 1e12, sec, done, torch.get_num_threads()
+
+
 def run_reference(args, w: Workload, world, rank):
     if rank != 0:
         return 0
@@ -519,6 +538,10 @@ def main(argv=None):
             what += " of the first sequence"
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
                "sample": f"{what} ({sec:.1f} s, fp64, OpenMP over rows)"}
+        if w.bias == "none" and not w.varlen:
+            ttf, tsec, tsl, tth = _torch_cpu_sample(w, inp_cpu, 5.0)
+            cpu["torch_cpu_sdpa_fp32"] = {"value": ttf, "unit": "TFLOP/s", "threads": tth,
+                                          "sample": f"{tsl} of {w.B * w.H} slices ({tsec:.1f} s)"}
 
     inp = make_inputs(w)
     sets = DeviceSets(w, inp, dev)

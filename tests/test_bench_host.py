@@ -114,3 +114,9 @@ def test_sources_hash_ignores_comments_not_code():
     assert bench._code_tokens(a) == bench._code_tokens(b)
     assert bench._code_tokens(a) != bench._code_tokens(c)
     assert '"//not a comment"' in bench._code_tokens(a)
+
+
+def test_torch_cpu_context_sample():
+    w = WORKLOADS["toy"]
+    tf, sec, slices, threads = bench._torch_cpu_sample(w, make_inputs(w), budget_s=0.05)
+    assert tf > 0 and sec > 0 and 1 <= slices <= w.B * w.H and threads >= 1
