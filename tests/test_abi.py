@@ -66,6 +66,8 @@ def _call(lib, q=FAKE, k=FAKE + 4096, v=FAKE + 8192, out=FAKE + 1 << 20, B=1, H=
     (dict(kind=9), sdpa.ATTN_ERR_ARG),
     (dict(scale=float("nan")), sdpa.ATTN_ERR_ARG),
     (dict(out=FAKE), sdpa.ATTN_ERR_ARG),         # aliases q
+    (dict(B=1 << 16, H=1 << 8, Nq=1 << 8), sdpa.ATTN_ERR_UNSUPPORTED),  # 2^32 query rows
+    (dict(Nk=(1 << 20) + 1), sdpa.ATTN_ERR_UNSUPPORTED),                # over 2^20 keys
 ])
 def test_bad_arguments_rejected_before_cuda(lib, kw, code):
     assert _call(lib, **kw) == code
