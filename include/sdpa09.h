@@ -72,7 +72,10 @@ typedef enum {
  *   k_coords).  Tokens are row-major on a q_h x q_w grid; for query
  *   i = (qh,qw) and key j = (kh,kw)
  *       bias = Q_i . R_h[qh-kh+q_h-1] + Q_i . R_w[qw-kw+q_w-1]
- *   with the unscaled Q.  This version requires q_h == k_h, q_w == k_w.
+ *   with the unscaled Q, on equal query and key grids.  Unequal grids (keys
+ *   on a k_h x k_w grid) and tables of another length are accepted too: the
+ *   row index then goes through the coordinate scalers and the tables are
+ *   resampled, as attn_sam_args describes.
  */
 typedef enum {
     ATTN_BIAS_NONE = 0,
@@ -141,6 +144,13 @@ enum {
  *
  * Accumulation is fp32 (scores, softmax, P.V); P is rounded to the input
  * dtype before the second product; O is rounded to nearest even.
+ *
+ * Swin windows whose bias rows do not fit shared memory (more than 64
+ * tokens, or many heads) add the bias through the tensor core, as 16-bit
+ * operands holding table / scale and -100 / scale.  There a zero scale, or
+ * |scale| < 100 / 65504 for fp16 (100 / 3.3e38 for bf16), returns
+ * ATTN_ERR_UNSUPPORTED, and table entries must satisfy
+ * |table / scale| <= 65504 for fp16 (beyond it they saturate to infinity).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int H, int Nq,
              int Nk, int d, float scale, attn_dtype dtype, attn_bias_kind bias_kind,
@@ -169,8 +179,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int 
  * Returns ATTN_OK (also when no sequence has a query: then nothing is
  * launched and the tensor pointers may be null), ATTN_ERR_ARG,
  * ATTN_ERR_UNSUPPORTED (more than ATTN_VARLEN_MAX_SEQ sequences, d > 128)
- * or ATTN_ERR_CUDA.  Inputs must be finite: a tile's rows past its
- * sequence are read from the next one and weighted by zero.
+ * or ATTN_ERR_CUDA.  Sequences never interact: the rows of a neighbouring
+ * sequence that a tile holds are masked (keys) or cleared (values) before
+ * use, so even non-finite values there leave a sequence's output unchanged.
  */
 #define ATTN_VARLEN_MAX_SEQ 128
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, const int* cu_seqlens_q,

@@ -639,6 +639,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     __shared__ uint64_t bar_q_full[2][2], bar_q_empty[2][2];
     __shared__ uint64_t bar_full_k[kMaxStages], bar_full_v[kMaxStages], bar_empty[kMaxStages];
+    // variable-length batches: the V copy lands on bar_landed_v; the fix-up
+    // warp then clears the tile's rows past the sequence and arrives on
+    // bar_full_v
+    __shared__ uint64_t bar_landed_v[VL ? kMaxStages : 1];
     __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2], bar_g[2], bar_gdone[2], bar_oempty[2];
     __shared__ uint64_t bar_sfree[2], bar_pvd[2];
     __shared__ uint64_t bar_final;
@@ -681,6 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar_full_k[i], (MODE == kModeSeparate && BIAS == kBiasSwin && p.swin_image) ? 2 : 1);
             mbar_init(&bar_full_v[i], 1);
             mbar_init(&bar_empty[i], MODE == kModeShared ? 2 : 1);
+            if constexpr (VL) mbar_init(&bar_landed_v[i], 1);
         }
         mbar_init(&bar_final, 2);
         fence_mbar_init();
@@ -1033,9 +1038,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mbar_arrive_expect_tx(&bar_full_k[st], kv_tx);
                             tma_load_4d(dk, &tm.k, &bar_full_k[st], 0, kr, jr.k_slice, 0);
                             if (p.part) tma_load_3d(dk + p.full_atoms * kBlockN * 32, &tm.kp, &bar_full_k[st], 0, kr, jr.k_slice);
-                            mbar_arrive_expect_tx(&bar_full_v[st], kv_tx);
-                            tma_load_4d(dv, &tm.v, &bar_full_v[st], 0, kr, jr.k_slice, 0);
-                            if (p.part) tma_load_3d(dv + p.full_atoms * kBlockN * 32, &tm.vp, &bar_full_v[st], 0, kr, jr.k_slice);
+                            uint64_t* const bv = VL ? &bar_landed_v[st] : &bar_full_v[st];
+                            mbar_arrive_expect_tx(bv, kv_tx);
+                            tma_load_4d(dv, &tm.v, bv, 0, kr, jr.k_slice, 0);
+                            if (p.part) tma_load_3d(dv + p.full_atoms * kBlockN * 32, &tm.vp, bv, 0, kr, jr.k_slice);
                         }
                     }
                 } else {
@@ -1072,8 +1078,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int u = (ring > nst ? ring - nst : 0); u < ring; ++u) {
                     const int st = u % nst;
                     mbar_wait(&bar_full_k[st], (u / nst) & 1, nullptr, 0);
-                    if (MODE == kModeShared) mbar_wait(&bar_full_v[st], (u / nst) & 1, nullptr, 0);
+                    if (MODE == kModeShared) mbar_wait(VL ? &bar_landed_v[st] : &bar_full_v[st], (u / nst) & 1, nullptr, 0);
                 }
+            }
+        }
+      } else if (VL && warp == kGatherWarp) {
+        // ============================================ variable-length fix-up
+        // A key tile that runs past its sequence holds the next sequence's
+        // rows.  Their scores are masked to -inf, so they get P = 0, but a
+        // non-finite value there would still reach the output through
+        // 0 * inf = NaN in P.V: clear those V rows (whole 32-byte rows of
+        // every 16-column block, so the swizzle does not matter) before the
+        // tile is released to the MMA issuers.  Sequences then never
+        // interact, whatever the neighbouring data hold.
+        int ring = 0;
+        bool ok = true;
+        for (int job = job0; ok && job < p.n_jobs; job += job_step) {
+            const JobRows jr = shared_job<VL>(p, vt, job);
+            for (int u = 0; u < jr.n_kv; ++u, ++ring) {
+                const int st = ring % nst;
+                __syncwarp();
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_landed_v[st], (ring / nst) & 1, abort_flag, kStatusWaitV))) {
+                    ok = false;
+                    break;
+                }
+                const int hi = jr.nk - u * p.kv_w;  // rows of the sequence in this tile
+                if (hi < kBlockN) {
+                    unsigned char* dv = sRing + st * p.ring_stage_bytes + T::kBytes;
+                    const int n16 = 2 * (kBlockN - hi);  // 16-byte chunks per column block
+                    for (int c = lane; c < T::kAtoms * n16; c += 32) {
+                        const int blk = c / n16, rc = c - blk * n16;
+                        *reinterpret_cast<uint4*>(dv + blk * (kBlockN * 32) + (hi + (rc >> 1)) * 32 + (rc & 1) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();  // read by the tensor core next
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_full_v[st]);
             }
         }
       } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {

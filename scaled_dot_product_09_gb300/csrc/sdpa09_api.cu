@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -392,6 +393,15 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
             const size_t table = (size_t)(2 * p.win - 1) * (2 * p.win - 1) * H * 4;
             p.swin_rows = (sl <= 64 && rows <= kSwinRowsMax && table <= 2 * (size_t)p.ring_stage_bytes) ? 1 : 0;
             extra = p.swin_rows ? rows : swin_extra_bytes(sl, H);
+            // The bias-MMA variant holds table / scale and -100 / scale as
+            // 16-bit MMA operands: a zero scale, or one so small that the
+            // mask term leaves the operand type's range, cannot be
+            // represented there.
+            const double max16 = p.is_bf16 ? 3.3e38 : 65504.0;
+            if (!p.swin_rows && (scale == 0.0f || 100.0 / std::fabs((double)scale) > max16))
+                return fail(ATTN_ERR_UNSUPPORTED,
+                            "SWIN windows of this size fold the bias into 16-bit MMA operands as bias / scale; "
+                            "|scale| must be at least %g here (got %g)", 100.0 / max16, (double)scale);
         }
         const size_t avail = kSmemBudget > extra ? kSmemBudget - extra : 0;
         p.nst = (int)std::min<size_t>(kMaxStages, avail / p.ring_stage_bytes);

@@ -193,3 +193,15 @@ def test_bwd_argument_checks(lib):
     img = sdpa._SwinArgs(FAKE, 7, 56, 56, 3, 1)
     assert _bwd(lib, kind=1, args=ctypes.byref(img), d_table=FAKE) == sdpa.ATTN_ERR_UNSUPPORTED
     assert _bwd(lib, B=63, kind=1, args=ctypes.byref(swin), d_table=FAKE) == sdpa.ATTN_ERR_ARG
+
+
+def test_swin_bias_mma_variant_rejects_unrepresentable_scale(lib):
+    # 10x10 windows (100 tokens, 128-row slots) add the bias through 16-bit
+    # MMA operands holding table / scale and -100 / scale: scale = 0 (and,
+    # for fp16, a scale that overflows -100 / scale) is refused before any
+    # CUDA call instead of producing NaN or Inf
+    a = sdpa._SwinArgs(FAKE, 10, 20, 20, 5)
+    for dtype, scale in ((0, 0.0), (1, 0.0), (1, 1e-3), (1, -1e-3)):
+        assert _call(lib, B=4, Nq=100, Nk=100, kind=1, args=ctypes.byref(a), dtype=dtype,
+                     scale=scale) == sdpa.ATTN_ERR_UNSUPPORTED, (dtype, scale)
+        assert b"scale" in lib.attn_last_error()

@@ -107,3 +107,26 @@ def test_varlen_full_size_sampled():
         ids = np.unique(np.concatenate([[0, lq - 1, H * lq - 1], rng.integers(0, H * lq, 6)]))
         want, _ = oracle.attn_rows(qs, ks, vs, H, w.scale, ids)
         compare(got[H * cq[s] + ids], want, what=f"{w.name} sequence {s} (sampled)")
+
+
+def test_varlen_sequences_do_not_interact():
+    """Non-finite values in one sequence leave every other sequence's output
+    unchanged: a tile that runs past its sequence reads the next one's rows,
+    which must be masked (keys) and cleared (values), never weighted by zero
+    (0 * inf = NaN).  Sequence 1 is poisoned with inf in V and K and NaN in
+    Q; sequences 0 and 2 must still match the oracle on the clean data."""
+    lens = [200, 150, 130]
+    w = _varlen_workload(lens, lens, H=2, d=64, seed=44)
+    inp = make_inputs(w)
+    cq, H = w.cu_seqlens_q, w.H
+    poisoned = [x.clone() for x in (inp.q, inp.k, inp.v)]
+    rows = slice(H * cq[1], H * cq[2])
+    poisoned[0][rows] = float("nan")
+    poisoned[1][rows] = float("inf")
+    poisoned[2][rows] = float("inf")
+    got = _run(w, type(inp)(*poisoned)).double().numpy()
+    want = oracle.attn_varlen(inp.q.double().numpy(), inp.k.double().numpy(), inp.v.double().numpy(),
+                              w.cu_seqlens_q, w.cu_seqlens_k, w.H, w.scale)
+    for s in (0, 2):
+        r = slice(H * cq[s], H * cq[s + 1])
+        compare(got[r], want[r], what=f"sequence {s} next to a poisoned sequence")

@@ -678,3 +678,53 @@ def test_bwd_finite_differences():
         args_m = [xm if a is x else a for a in (q, k, v, table)]
         fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
         assert abs(fd - got[name][pos]) < 1e-7, (name, fd, got[name][pos])
+
+
+def test_bwd_out_given_as_exact_o_equals_default():
+    """attn_bwd(out=O) with O the forward's exact output reproduces the
+    default call, which takes O from the forward definition itself."""
+    rng = np.random.default_rng(64)
+    M, G, s_, H, d = 3, 6, 1, 2, 5
+    BH, N = (G // M) ** 2 * H, M * M
+    table = rng.standard_normal(((2 * M - 1) ** 2, H)) * 0.3
+    q, k, v, dout = (rng.standard_normal((BH, N, d)) for _ in range(4))
+    for b in (None, oracle.Bias("swin", table=table, win=M, grid_h=G, grid_w=G, shift=s_)):
+        o, _ = oracle.attn_fwd(q, k, v, H, 0.45, b)
+        base = oracle.attn_bwd(q, k, v, dout, H, 0.45, b)
+        given = oracle.attn_bwd(q, k, v, dout, H, 0.45, b, out=o)
+        for name in base:
+            np.testing.assert_allclose(given[name], base[name], rtol=0, atol=1e-14)
+
+
+def test_bwd_out_perturbed_follows_the_rowsum_formula():
+    """With out = O + E the oracle takes D' = rowsum(dO * (O + E)) in place of
+    the exact D.  dS then moves by P * (D - D'), which is the gradient of
+    sum_i (D_i - D'_i) * logsumexp_j S_ij: torch fp64 autograd of
+    L = sum(dO * O) + sum_i c_i logsumexp(S_i), c = D - D' held constant,
+    must give the same dQ, dK, dV (dV unchanged) and table gradient."""
+    rng = np.random.default_rng(65)
+    M, G, s_, H, d = 3, 6, 1, 2, 5
+    BH, N = (G // M) ** 2 * H, M * M
+    table = rng.standard_normal(((2 * M - 1) ** 2, H)) * 0.3
+    q, k, v, dout = (rng.standard_normal((BH, N, d)) for _ in range(4))
+    b = oracle.Bias("swin", table=table, win=M, grid_h=G, grid_w=G, shift=s_)
+    o, _ = oracle.attn_fwd(q, k, v, H, 0.45, b)
+    o_given = o + rng.standard_normal(o.shape) * 0.05
+    got = oracle.attn_bwd(q, k, v, dout, H, 0.45, b, out=o_given)
+    c = torch.tensor(np.sum(dout * o, axis=2) - np.sum(dout * o_given, axis=2))  # D - D'
+    r, cc = np.arange(N) // M, np.arange(N) % M
+    idx = torch.tensor((r[:, None] - r[None, :] + M - 1) * (2 * M - 1) + (cc[:, None] - cc[None, :] + M - 1))
+    zero = oracle.Bias("swin", table=np.zeros_like(table), win=M, grid_h=G, grid_w=G, shift=s_)
+    mask = torch.tensor(np.stack([oracle.bias_matrix(q, H, i, N, zero) for i in range(BH)]))
+    tt = torch.tensor(table, requires_grad=True)
+    heads = torch.tensor([i % H for i in range(BH)])
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    s = 0.45 * tq @ tk.transpose(-1, -2) + tt[idx][:, :, heads].permute(2, 0, 1) + mask
+    out = torch.softmax(s, dim=-1) @ tv
+    loss = torch.sum(torch.tensor(dout) * out) + torch.sum(c * torch.logsumexp(s, dim=-1))
+    want = torch.autograd.grad(loss, (tq, tk, tv, tt))
+    for name, w in zip(("dq", "dk", "dv", "d_table"), want):
+        np.testing.assert_allclose(got[name], w.numpy(), rtol=0, atol=1e-11)
+    # and the perturbation is not a no-op: dQ moved
+    base = oracle.attn_bwd(q, k, v, dout, H, 0.45, b)
+    assert np.abs(got["dq"] - base["dq"]).max() > 1e-3
