@@ -70,6 +70,9 @@ constexpr int kTmemCols = 512;
 constexpr int kMaxStages = 8;
 constexpr int kSamMaxSide = 64;  // rel-pos grids up to 64 x 64
 constexpr float kLog2e = 1.4426950408889634f;
+// SAM on the 64 x 64 grid: shared-memory extra area = rel_h rows (fp16,
+// [2 slots][64][128])
+constexpr uint32_t kSamDbsExtra = 2 * 64 * 128 * 2;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may reach 2^8 before O is rescaled
 
 enum BiasKind { kBiasNone = 0, kBiasSwin = 1, kBiasSam = 2 };
@@ -460,6 +463,37 @@ __device__ __forceinline__ float row_max(const float* x) {
     return fmaxf(fmaxf(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5])), fmaxf(m[6], m[7]));
 }
 
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Min of N floats, as row_max.
+template <int N>
+__device__ __forceinline__ float row_min(const float* x) {
+    static_assert(N >= 16, "row_min");
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = fminf(x[2 * i], x[2 * i + 1]);
+#pragma unroll
+    for (int c = 16; c + 16 <= N; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m[i] = min3f(m[i], x[c + 2 * i], x[c + 2 * i + 1]);
+#pragma unroll
+    for (int t = N / 16 * 16; t < N; ++t) m[t % 8] = fminf(m[t % 8], x[t]);
+    return fminf(fminf(min3f(m[0], m[1], m[2]), min3f(m[3], m[4], m[5])), fminf(m[6], m[7]));
+}
+
+// max over c of x[c] * sc: the largest x for sc >= 0, the smallest for a
+// negative multiplier (a negative scale flips the order of the scores).
+// Key columns masked with -inf must not be present when sc < 0; the callers
+// mask with -inf only after scaling, or with sc >= 0.
+template <int N>
+__device__ __forceinline__ float row_max_scaled(const float* x, float sc) {
+    return sc >= 0.f ? row_max<N>(x) * sc : row_min<N>(x) * sc;
+}
+
 // p = 2^(x*sc + off) for N columns (x = -inf gives 0), packed to 16-bit pairs;
 // returns the fp32 sum of the p values.
 template <int N>
@@ -502,6 +536,10 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
 __device__ __forceinline__ uint64_t kdesc(uint32_t addr) { return make_sdesc(addr, 16, 256, kSwizzle32B); }
 // MN-major (V): 16-column blocks kBlockN*32 bytes apart, 8-key groups 256 B apart.
 __device__ __forceinline__ uint64_t vdesc(uint32_t addr) { return make_sdesc(addr, kBlockN * 32, 256, kSwizzle32B); }
+// the same for a V tile of `rows` keys
+__device__ __forceinline__ uint64_t vdesc_rows(uint32_t addr, uint32_t rows) {
+    return make_sdesc(addr, rows * 32, 256, kSwizzle32B);
+}
 
 // S = Q.K^T for one 128-row tile: one MMA per 16-column block of d.
 template <int DPAD>
@@ -510,6 +548,16 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t 
     for (int ks = 0; ks < Tile<DPAD>::kAtoms; ++ks)
         mma_ss(d_tmem, qd + (uint64_t)(ks * (kBlockM * 32 / 16)), kd + (uint64_t)(ks * (kBlockN * 32 / 16)),
                idesc, ks > 0 ? 1u : 0u);
+}
+
+// The same against a key tile of ROWS rows (16-column blocks ROWS*32 bytes
+// apart), e.g. the 64-key tiles of one SAM grid row.
+template <int DPAD, int ROWS>
+__device__ __forceinline__ void issue_qk_rows(uint32_t d_tmem, uint64_t qd, uint64_t kd, uint32_t idesc) {
+#pragma unroll
+    for (int ks = 0; ks < Tile<DPAD>::kAtoms; ++ks)
+        mma_ss(d_tmem, qd + (uint64_t)(ks * (kBlockM * 32 / 16)), kd + (uint64_t)(ks * (ROWS * 32 / 16)), idesc,
+               ks > 0 ? 1u : 0u);
 }
 
 // D[:, 0:SL] (+)= Qone . E^T with Qone [128][SL] and E [SL][SL] K-major.
@@ -596,7 +644,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tiling when that lets separate P buffers fit tensor memory -- without
     // bias and every key in one tile (SW > 0, e.g. 80 for 77 text tokens), or
     // SAM on 14x14 grids (112 = eight grid rows).
-    constexpr int kCols = (MODE == kModeShared && BIAS == kBiasNone && SW > 0)  ? SW
+    //
+    // SAM on the 64 x 64 grid (kDbS) takes one grid row of 64 keys per score
+    // tile and keeps two score buffers per slot, so the tensor core computes
+    // the next two tiles' scores while the softmax works on this one:
+    //   slot x (256 columns from 256x): S0 [0,64) S1 [64,128) O [128,128+DPAD);
+    //   P of a tile lies over the first 32 columns of its own score buffer, so
+    //   P is double-buffered too: the tile that next uses that buffer has its
+    //   scores computed after this tile's P.V (in-order issue), and the
+    //   softmax never waits for a P.V before writing P.  At a job's start
+    //   G_w = Q.R_w^T lands over S0/S1 and G_h = Q.R_h^T over [128,256).
+    constexpr bool kDbS = MODE == kModeShared && BIAS == kBiasSam && SW == 64 && DPAD <= 96;
+    constexpr int kCols = kDbS ? 64
+                          : (MODE == kModeShared && BIAS == kBiasNone && SW > 0)  ? SW
                           : (MODE == kModeShared && BIAS == kBiasSam && SW == 14) ? 112
                                                                                   : 128;
     static_assert(kCols % 16 == 0 && kCols <= 128, "key columns");
@@ -617,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             kOffP + 128 + 4 * DPAD <= 512;
     constexpr int kOw = kShDbl ? 2 * DPAD : (DPAD <= 64 ? 64 : DPAD);
     constexpr int kOffO = kOffP + 128;
-    constexpr bool kSepP = kOffO + 2 * kOw <= 512 && (BIAS != kBiasSam || SW == 14);
+    constexpr bool kSepP = !kDbS && kOffO + 2 * kOw <= 512 && (BIAS != kBiasSam || SW == 14);
     // Packed tiling with head dims up to 32 and slots up to 64 rows: two O
     // buffers per slot (O_x holds 64 columns), so a tile's output is written
     // while the next tile's P.V runs.
@@ -645,6 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint64_t bar_landed_v[VL ? kMaxStages : 1];
     __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2], bar_g[2], bar_gdone[2], bar_oempty[2];
     __shared__ uint64_t bar_sfree[2], bar_pvd[2];
+    __shared__ uint64_t bar_sb[kDbS ? 2 : 1][2];  // kDbS: [slot][score buffer] scores ready
     __shared__ uint64_t bar_final;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -656,6 +717,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = &abort_sh;
     const int nst = p.nst;
     const bool bf = p.is_bf16 != 0;
+    // bytes of one K (or V) tile of a shared-tiling ring stage: box_kv rows
+    const uint32_t kv_tile_bytes = (uint32_t)T::kAtoms * (uint32_t)p.box_kv * 32u;
 
     // A kernel launched after this one on the stream may start its set-up
     // while this grid drains (programmatic dependent launch); it reads
@@ -679,6 +742,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar_oempty[x], 4);
             mbar_init(&bar_sfree[x], 4);
             mbar_init(&bar_pvd[x], 1);
+            if constexpr (kDbS) {
+                mbar_init(&bar_sb[x][0], 1);
+                mbar_init(&bar_sb[x][1], 1);
+            }
         }
         for (int i = 0; i < kMaxStages; ++i) {
             // the image-layout Swin stages are filled by two warps
@@ -1010,8 +1077,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_3d(dq + p.full_atoms * kBlockM * 32, &tm.qp, &bar_q_full[x][qb], 0, jr.q_row + x * kBlockM,
                                         jr.q_slice);
                     }
-                    // SAM: a first stage with the tables, unless the CTA resampled them
-                    const int t_use = (BIAS == kBiasSam && !p.sam_resample) ? 1 : 0;
+                    // SAM: a first stage with the tables, unless the CTA resampled them;
+                    // with 64-row tiles two stages: R_w rows [0,64) and [64,128) in
+                    // the K and V tiles of the first, R_h likewise in the second
+                    const int t_use = (BIAS == kBiasSam && !p.sam_resample) ? (kDbS ? 2 : 1) : 0;
                     const int n_uses = jr.n_kv + t_use;
                     for (int u = 0; ok && u < n_uses; ++u) {
                         const int st = ring % nst;
@@ -1022,8 +1091,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         ++ring;
                         unsigned char* dk = sRing + st * p.ring_stage_bytes;
-                        unsigned char* dv = dk + T::kBytes;
-                        if (BIAS == kBiasSam && u < t_use) {
+                        unsigned char* dv = dk + kv_tile_bytes;
+                        if (kDbS && u < t_use) {
+                            const CUtensorMap* tfull = u == 0 ? &tm.rw : &tm.rh;
+                            const CUtensorMap* tpart = u == 0 ? &tm.rwp : &tm.rhp;
+                            mbar_arrive_expect_tx(&bar_full_k[st], kv_tx);
+                            tma_load_3d(dk, tfull, &bar_full_k[st], 0, 0, 0);
+                            if (p.part) tma_load_2d(dk + p.full_atoms * p.box_kv * 32, tpart, &bar_full_k[st], 0, 0);
+                            mbar_arrive_expect_tx(&bar_full_v[st], kv_tx);
+                            tma_load_3d(dv, tfull, &bar_full_v[st], 0, 64, 0);
+                            if (p.part) tma_load_2d(dv + p.full_atoms * p.box_kv * 32, tpart, &bar_full_v[st], 0, 64);
+                        } else if (BIAS == kBiasSam && u < t_use) {
                             // rel-pos tables: R_w in the K slot, R_h in the V slot
                             const uint32_t r_tx = (uint32_t)T::kAtoms * kBlockN * 32u;
                             mbar_arrive_expect_tx(&bar_full_k[st], r_tx);
@@ -1037,11 +1115,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int kr = jr.k_row + j * p.kv_w;
                             mbar_arrive_expect_tx(&bar_full_k[st], kv_tx);
                             tma_load_4d(dk, &tm.k, &bar_full_k[st], 0, kr, jr.k_slice, 0);
-                            if (p.part) tma_load_3d(dk + p.full_atoms * kBlockN * 32, &tm.kp, &bar_full_k[st], 0, kr, jr.k_slice);
+                            if (p.part) tma_load_3d(dk + p.full_atoms * p.box_kv * 32, &tm.kp, &bar_full_k[st], 0, kr, jr.k_slice);
                             uint64_t* const bv = VL ? &bar_landed_v[st] : &bar_full_v[st];
                             mbar_arrive_expect_tx(bv, kv_tx);
                             tma_load_4d(dv, &tm.v, bv, 0, kr, jr.k_slice, 0);
-                            if (p.part) tma_load_3d(dv + p.full_atoms * kBlockN * 32, &tm.vp, bv, 0, kr, jr.k_slice);
+                            if (p.part) tma_load_3d(dv + p.full_atoms * p.box_kv * 32, &tm.vp, bv, 0, kr, jr.k_slice);
                         }
                     }
                 } else {
@@ -1104,7 +1182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int hi = jr.nk - u * p.kv_w;  // rows of the sequence in this tile
                 if (hi < kBlockN) {
-                    unsigned char* dv = sRing + st * p.ring_stage_bytes + T::kBytes;
+                    unsigned char* dv = sRing + st * p.ring_stage_bytes + kv_tile_bytes;
                     const int n16 = 2 * (kBlockN - hi);  // 16-byte chunks per column block
                     for (int c = lane; c < T::kAtoms * n16; c += 32) {
                         const int blk = c / n16, rc = c - blk * n16;
@@ -1128,9 +1206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, MODE == kModeShared ? kCols : kBlockN, false);
             const uint32_t idesc_o = make_idesc_f16(bf, kBlockM, DPAD, true);
             const uint32_t idesc_b = make_idesc_f16(bf, kBlockM, MODE == kModeSeparate ? SL : 16, false);
-            const uint32_t tSx = tmem + (uint32_t)((kSepP ? kCols : 128) * x);
-            const uint32_t tPx = kSepP ? tmem + (uint32_t)(kOffP + 64 * x) : tSx;
-            const uint32_t tOx = tmem + (uint32_t)(kSepP ? kOffO + kOw * x : 256 + 128 * x);
+            const uint32_t tSx = tmem + (uint32_t)(kDbS ? 256 * x : (kSepP ? kCols : 128) * x);
+            const uint32_t tPx = kSepP ? tmem + (uint32_t)(kOffP + 64 * x) : tSx;  // kDbS: + 64 * buffer
+            const uint32_t tOx = kDbS ? tSx + 128 : tmem + (uint32_t)(kSepP ? kOffO + kOw * x : 256 + 128 * x);
             uint64_t* const bs = &bar_s[x];
             uint64_t* const bp = &bar_p[x];
             uint64_t* const bo = &bar_o[x];
@@ -1171,7 +1249,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             for (int job = job0; ok && job < p.n_jobs; job += job_step, ++ju) {
-                if constexpr (kShDbl) {
+                if constexpr (kDbS) {
+                    // SAM, 64 x 64 grid: 64-key score tiles, two score buffers
+                    const int qb = ju % p.nq;
+                    const uint64_t qa = kdesc(smem_u32(sQ + (x * p.nq + qb) * T::kBytes));
+                    if (!waitb(&bar_q_full[x][qb], (ju / p.nq) & 1, kStatusWaitQ)) { ok = false; break; }
+                    // G_w = Q.R_w^T over the score buffers, G_h = Q.R_h^T over O and
+                    // P, from the tables the CTA staged once.  O must have been read by
+                    // the previous job's epilogue; P was read by this thread's last
+                    // P.V, which the tensor core finishes first (in-order issue).
+                    if (ju > 0 && !waitb(&bar_oempty[x], (ju - 1) & 1, kStatusWaitO)) { ok = false; break; }
+                    if (p.sam_resample) {
+                        const uint32_t rt = smem_u32(smem + p.off_rtab);
+                        issue_qk<DPAD>(tSx, qa, kdesc(rt), make_idesc_f16(bf, kBlockM, p.n_rw, false));
+                        issue_qk<DPAD>(tOx, qa, kdesc(rt + T::kBytes), make_idesc_f16(bf, kBlockM, p.n_rh, false));
+                        mma_commit(&bar_g[x]);
+                    } else {
+                        // two ring stages: R_w rows [0,64) | [64,128), then R_h's
+                        for (int t = 0; t < 2; ++t) {
+                            const int use = ring + t, st = use % nst;
+                            if (!waitb(&bar_full_k[st], (use / nst) & 1, kStatusWaitK) ||
+                                !waitb(&bar_full_v[st], (use / nst) & 1, kStatusWaitV)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t kt = smem_u32(sRing + st * p.ring_stage_bytes);
+                            const uint32_t dst = t == 0 ? tSx : tOx;
+                            issue_qk_rows<DPAD, 64>(dst, qa, kdesc(kt), idesc_s);
+                            issue_qk_rows<DPAD, 64>(dst + 64, qa, kdesc(kt + kv_tile_bytes), idesc_s);
+                        }
+                        if (!ok) break;
+                        mma_commit(&bar_g[x]);
+                        mma_commit(&bar_empty[ring % nst]);
+                        mma_commit(&bar_empty[(ring + 1) % nst]);
+                        ring += 2;
+                    }
+                    // the scores overwrite G_w: every row must have gathered its terms
+                    if (!waitb(&bar_gdone[x], ju & 1, kStatusWaitG)) { ok = false; break; }
+                    const int n = shared_job<VL>(p, vt, job).n_kv;
+                    const int sbase = s_cnt;
+                    // S of key tile j into score buffer (sbase + j) & 1
+                    auto issue_s = [&](int j) -> bool {
+                        const int use = ring + j, st = use % nst, b = (sbase + j) & 1;
+                        if (!waitb(&bar_full_k[st], (use / nst) & 1, kStatusWaitK)) return false;
+                        issue_qk_rows<DPAD, 64>(tSx + 64u * (uint32_t)b, qa,
+                                                kdesc(smem_u32(sRing + st * p.ring_stage_bytes)), idesc_s);
+                        mma_commit(&bar_sb[x][b]);
+                        return true;
+                    };
+                    for (int j = 0; ok && j < n && j < 2; ++j) ok = issue_s(j);
+                    for (int j = 0; ok && j < n; ++j) {
+                        const int use = ring + j, st = use % nst;
+                        if (!waitb(bp, ph_p, kStatusWaitP) || !waitb(&bar_full_v[st], (use / nst) & 1, kStatusWaitV)) {
+                            ok = false;
+                            break;
+                        }
+                        ph_p ^= 1;
+                        issue_pv<64>(tOx, tPx + 64u * (uint32_t)((sbase + j) & 1),
+                                     vdesc_rows(smem_u32(sRing + st * p.ring_stage_bytes) + kv_tile_bytes, 64u), idesc_o,
+                                     j > 0 ? 1u : 0u);
+                        if (j == n - 1) {
+                            mma_commit(bo);
+                            if (p.nq == 1) mma_commit(&bar_q_empty[x][qb]);
+                        } else {
+                            mma_commit(bpv);
+                        }
+                        mma_commit(&bar_empty[st]);
+                        // tile j + 2 reuses tile j's score buffer: the softmax read it
+                        // before it wrote P(j) there, and the P.V just issued reads
+                        // P(j) before these scores land (in-order issue)
+                        if (j + 2 < n) ok = issue_s(j + 2);
+                    }
+                    if (!ok) break;
+                    s_cnt += n;
+                    ring += n;
+                } else if constexpr (kShDbl) {
                     // one score tile per job: S of the next job as soon as the
                     // softmax has read this one, then this job's P.V into O
                     // buffer ju & 1; Q is released by the commit of its S
@@ -1324,9 +1476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int x = warp >> 2;                // slot A or B
         const int r = tid & 127;                // row in tile == TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_base + (uint32_t)((kSepP ? kCols : 128) * x);
-        const uint32_t tP = kSepP ? tmem + lane_base + (uint32_t)(kOffP + 64 * x) : tS;
-        const uint32_t tO = tmem + lane_base + (uint32_t)(kSepP ? kOffO + kOw * x : 256 + 128 * x);
+        const uint32_t tS = tmem + lane_base + (uint32_t)(kDbS ? 256 * x : (kSepP ? kCols : 128) * x);
+        const uint32_t tP = kSepP ? tmem + lane_base + (uint32_t)(kOffP + 64 * x) : tS;  // kDbS: + 64 * buffer
+        const uint32_t tO = kDbS ? tS + 128 : tmem + lane_base + (uint32_t)(kSepP ? kOffO + kOw * x : 256 + 128 * x);
         int pvd_cnt = 0;  // P.V completions of this slot awaited (separate P buffers)
         int cnt_s = 0, ju = 0;
         bool ok = true;
@@ -1472,6 +1624,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (c < nk) dst[c] = (BIAS == kBiasSwin) ? xs[c] : 0.f;
                     }
                 }
+                if (!(sc > 0.f)) {
+                    // a scale <= 0: the multiplier goes on first, so that the
+                    // -inf of the masked keys below stays -inf
+                    const float2 s2 = make_float2(sc, sc);
+#pragma unroll
+                    for (int c = 0; c < kNe; c += 2) {
+                        const float2 y = __fmul2_rn(make_float2(xs[c], xs[c + 1]), s2);
+                        xs[c] = y.x;
+                        xs[c + 1] = y.y;
+                    }
+                    sc = 1.0f;
+                }
                 if constexpr (kNc == SL) {
                     // keys past the slice length: -inf (16-column chunks, uniform branches)
 #pragma unroll
@@ -1529,6 +1693,125 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pv_ok = row_ok;
                     continue;
                 }
+            } else if constexpr (kDbS) {
+                // ------------------------- SAM, 64 x 64 grid: 64-key score tiles
+                // Key tile j is key row kh = j.  rel_w of the row (64 values,
+                // log2 units) stays in registers for the job as aligned pairs,
+                // one 64-bit operand of the packed FMA each; rel_h goes to shared
+                // memory as fp16, [slot][kh][row], one load per tile.
+                __half* const rh16 = reinterpret_cast<__half*>(sExtraB) + x * (64 * kBlockM);
+                const int qh = min(my_tok >> 6, 63), qw = my_tok & 63;
+                __syncwarp();
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_g[x], ju & 1, abort_flag, kStatusWaitG))) { ok = false; break; }
+                tc_fence_after();
+                const float f = DBG ? 1.0f : kLog2e;
+                float2 rw2[32];
+                {
+                    float gv[128];
+                    {
+                        uint32_t v[128];
+                        tmem_ld_cols<128>(tS, v);  // G_w row
+#pragma unroll
+                        for (int t = 0; t < 128; ++t) gv[t] = __uint_as_float(v[t]) * f;
+                    }
+                    // rel_w for key column kw is G_w[qw + 63 - kw]
+                    shift_down<128, 6>(gv, qw);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) rw2[u] = make_float2(gv[63 - 2 * u], gv[62 - 2 * u]);
+                    {
+                        uint32_t v[128];
+                        tmem_ld_cols<128>(tO, v);  // G_h row
+#pragma unroll
+                        for (int t = 0; t < 128; ++t) gv[t] = __uint_as_float(v[t]) * f;
+                    }
+                    // rel_h for key row kh is G_h[qh + 63 - kh]
+                    shift_down<128, 6>(gv, qh);
+#pragma unroll
+                    for (int u = 0; u < 64; ++u) rh16[u * kBlockM + r] = __float2half_rn(gv[63 - u]);
+                }
+                tc_fence_before();
+                warp_arrive(&bar_gdone[x]);
+
+                float m_run = -INFINITY;
+                for (int j = 0; j < jr.n_kv; ++j) {
+                    const int b = cnt_s & 1;
+                    __syncwarp();
+                    if (!__all_sync(0xffffffffu, mbar_wait(&bar_sb[x][b], (cnt_s >> 1) & 1, abort_flag, kStatusWaitS))) {
+                        ok = false;
+                        break;
+                    }
+                    ++cnt_s;
+                    tc_fence_after();
+                    float xs[64];
+                    {
+                        uint32_t v[64];
+                        tmem_ld_cols<64>(tS + 64u * (uint32_t)b, v);
+#pragma unroll
+                        for (int t = 0; t < 64; ++t) xs[t] = __uint_as_float(v[t]);
+                    }
+                    const float rh = __half2float(rh16[min(j, 63) * kBlockM + r]);
+                    if constexpr (DBG) {
+                        if (row_ok) {
+                            float* dst = p.dbg + ((size_t)my_slice * p.Nq + my_tok) * p.Nk + j * 64;
+#pragma unroll
+                            for (int c = 0; c < 64; c += 2) {
+                                dst[c] = rw2[c / 2].x + rh;
+                                dst[c + 1] = rw2[c / 2].y + rh;
+                            }
+                        }
+                    }
+                    // x = s * scale * log2(e) + rel_w; the row's rel_h is constant
+                    // over the tile and joins through the max and the exponent's
+                    // offset (the bias goes on first, so any sign of the scale works)
+#pragma unroll
+                    for (int c = 0; c < 64; c += 2) {
+                        const float2 y = __ffma2_rn(make_float2(xs[c], xs[c + 1]), scale2, rw2[c / 2]);
+                        xs[c] = y.x;
+                        xs[c + 1] = y.y;
+                    }
+                    const float m_tile = row_max<64>(xs) + rh;
+                    // the previous P.V must be done before O is rescaled; every tile
+                    // after the first consumes that completion, at the latest just
+                    // before its P is handed over
+                    bool pv_waited = j == 0;
+                    auto wait_pv = [&]() -> bool {
+                        if (pv_waited) return true;
+                        pv_waited = true;
+                        __syncwarp();
+                        if (!__all_sync(0xffffffffu, mbar_wait(&bar_pvd[x], pvd_cnt & 1, abort_flag, kStatusWaitO))) return false;
+                        ++pvd_cnt;
+                        tc_fence_after();
+                        return true;
+                    };
+                    const float m_new = fmaxf(m_run, m_tile);
+                    const bool need = m_new > m_run + kRescaleThreshold;
+                    const bool any_rescale = __any_sync(0xffffffffu, need && j > 0);
+                    if (any_rescale) {
+                        if (!wait_pv()) { ok = false; break; }
+                        const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+#pragma unroll
+                        for (int c0 = 0; c0 < DPAD; c0 += 16) {
+                            uint32_t w16[16];
+                            tmem_ld16(tO + c0, w16);
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) w16[t] = __float_as_uint(__uint_as_float(w16[t]) * alpha);
+                            tmem_st16(tO + c0, w16);
+                        }
+                    }
+                    if (need) {
+                        l_run *= ex2_approx(m_run - m_new);
+                        m_run = m_new;
+                    }
+                    const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                    uint32_t pk[32];
+                    l_run += exp_pack<64>(xs, 1.0f, rh - m_use, bf, pk);
+                    tmem_st_cols<32>(tP + 64u * (uint32_t)b, pk);
+                    tmem_st_wait();
+                    if (!wait_pv()) { ok = false; break; }
+                    tc_fence_before();
+                    warp_arrive(&bar_p[x]);
+                }
+                if (!ok) break;
             } else {
                 // ------------------------------------------------- bias row setup
                 // rel_w of the row for kw = 2u, 2u + 1, held as fp16 pairs (half the
@@ -1624,16 +1907,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float sc;      // multiplier applied to xs in the exponent
                     if (BIAS == kBiasNone && !DBG) {
                         // no bias: max on raw scores, p = 2^(s*scale*log2e - m)
-                        if (hi < kCols) {
+                        if (!(p.scale_log2 > 0.f)) {
+                            // a scale <= 0: scale first, then mask the keys past the
+                            // sequence with -inf (-inf times the scale would not stay -inf)
+                            const float2 s2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-                            for (int c0 = 0; c0 < kCols; c0 += 16)
-                                if (c0 + 16 > hi)
+                            for (int c = 0; c < kCols; c += 2) {
+                                const float2 y = __fmul2_rn(make_float2(xs[c], xs[c + 1]), s2);
+                                xs[c] = c < hi ? y.x : -INFINITY;
+                                xs[c + 1] = c + 1 < hi ? y.y : -INFINITY;
+                            }
+                            m_tile = row_max<kCols>(xs);
+                            sc = 1.0f;
+                        } else {
+                            if (hi < kCols) {
 #pragma unroll
-                                    for (int t = 0; t < 16; ++t)
-                                        if (c0 + t >= hi) xs[c0 + t] = -INFINITY;
+                                for (int c0 = 0; c0 < kCols; c0 += 16)
+                                    if (c0 + 16 > hi)
+#pragma unroll
+                                        for (int t = 0; t < 16; ++t)
+                                            if (c0 + t >= hi) xs[c0 + t] = -INFINITY;
+                            }
+                            m_tile = row_max<kCols>(xs) * p.scale_log2;
+                            sc = p.scale_log2;
                         }
-                        m_tile = row_max<kCols>(xs) * p.scale_log2;
-                        sc = p.scale_log2;
                     } else {
                         constexpr int kRows = (BIAS == kBiasSam && SW > 0) ? (128 + (SW > 0 ? SW : 1) - 1) / (SW > 0 ? SW : 1) : 1;
                         float rh_tile[kRows];

@@ -354,6 +354,13 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         const bool square = a->q_h == a->q_w && a->k_h == a->q_h && a->k_w == a->q_w;
         sw_spec = (square && (a->q_w == 64 || a->q_w == 48 || a->q_w == 14)) ? a->q_w : 0;
         extra = (size_t)sam_extra_floats(sw_spec == 0, a->k_h, a->k_w, Nk) * 4;
+        if (sw_spec == 64 && dpad <= 96) {
+            // 64-key score tiles (one grid row), two score buffers per slot;
+            // rel_h rows as fp16 [2 slots][64][128].  The tables pass through
+            // two ring stages per job (64 rows per K or V tile), or, resampled,
+            // are staged once per CTA.
+            extra = kSamDbsExtra;
+        }
         if (p.sam_resample) {
             // the resampled tables after the bias rows, 1 KB aligned (swizzled operands)
             extra = (extra + 1023) / 1024 * 1024;
@@ -421,7 +428,10 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         if (sw_spec == 80 && 2 * 80 + 128 + 4 * dpad <= 512 && !dbg) extra = 2 * (size_t)kBlockM * d * 2;
         // SAM key tiles start on grid rows: 112 keys (8 rows) on the 14-wide
         // grid, 128 (2 rows) on the 64-wide one
-        p.kv_w = (bias == kBiasSam && sw_spec) ? (sw_spec == 14 ? 112 : (kBlockN / sw_spec) * sw_spec) : kBlockN;
+        // (head dims up to 96: O and P then share 128 tensor-memory columns)
+        const bool tiles64 = bias == kBiasSam && sw_spec == 64 && dpad <= 96;
+        p.kv_w = tiles64 ? 64 : (bias == kBiasSam && sw_spec) ? (sw_spec == 14 ? 112 : (kBlockN / sw_spec) * sw_spec)
+                                                              : kBlockN;
         p.kv_cols = kBlockN;  // unused by the kernel: its key-tile width is a compile-time constant
         p.n_kv = (Nk + p.kv_w - 1) / p.kv_w;
         p.q_jobs = (Nq + 2 * kBlockM - 1) / (2 * kBlockM);
@@ -430,11 +440,13 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         if (nj > 0x7fffffff) return fail(ATTN_ERR_UNSUPPORTED, "too many jobs");
         p.n_jobs = (int)nj;
         p.box_q = kBlockM;
-        p.box_kv = kBlockN;
-        p.ring_stage_bytes = (uint32_t)(2 * tile_bytes);
-        // prefer >= 3 K/V stages, then double-buffered Q
+        // K/V tiles of 64 rows for SAM on the 64 x 64 grid, else 128
+        p.box_kv = tiles64 ? 64 : kBlockN;
+        p.ring_stage_bytes = (uint32_t)(2 * (size_t)(dpad / 16) * p.box_kv * 32);
+        // prefer >= 3 K/V stages, then double-buffered Q (the 64-key tiles
+        // of the 64 x 64 SAM grid want >= 5: their scores run two tiles ahead)
         int nq = 0, nst = 0;
-        const int tries[4][2] = {{2, 3}, {1, 3}, {2, 2}, {1, 2}};
+        const int tries[6][2] = {{2, tiles64 ? 5 : 3}, {1, tiles64 ? 5 : 3}, {2, 3}, {1, 3}, {2, 2}, {1, 2}};
         for (auto& t : tries) {
             const size_t fixed = 2 * (size_t)t[0] * tile_bytes + extra;
             if (fixed >= kSmemBudget) continue;
@@ -475,12 +487,14 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         if ((rc = encode_operand(&tm.v, &tm.vp, v, bf, d, BH * Nk, 1, atoms, kBlockN, 1))) return rc;
     } else {
         if ((rc = encode_operand(&tm.q, &tm.qp, q, bf, d, Nq, BH, atoms, kBlockM, 1))) return rc;
-        if ((rc = encode_operand(&tm.k, &tm.kp, k, bf, d, Nk, BH, atoms, kBlockN, 1))) return rc;
-        if ((rc = encode_operand(&tm.v, &tm.vp, v, bf, d, Nk, BH, atoms, kBlockN, 1))) return rc;
+        if ((rc = encode_operand(&tm.k, &tm.kp, k, bf, d, Nk, BH, atoms, p.box_kv, 1))) return rc;
+        if ((rc = encode_operand(&tm.v, &tm.vp, v, bf, d, Nk, BH, atoms, p.box_kv, 1))) return rc;
     }
     if (bias == kBiasSam) {
-        if ((rc = encode_operand(&tm.rh, &tm.rhp, rel_h, bf, d, p.sam_lin_h, 0, atoms, kBlockN, 1))) return rc;
-        if ((rc = encode_operand(&tm.rw, &tm.rwp, rel_w, bf, d, p.sam_lin_w, 0, atoms, kBlockN, 1))) return rc;
+        // table copies land in K/V ring tiles: box_kv rows at a time
+        const int tb = separate ? kBlockN : p.box_kv;
+        if ((rc = encode_operand(&tm.rh, &tm.rhp, rel_h, bf, d, p.sam_lin_h, 0, atoms, tb, 1))) return rc;
+        if ((rc = encode_operand(&tm.rw, &tm.rwp, rel_w, bf, d, p.sam_lin_w, 0, atoms, tb, 1))) return rc;
     } else {
         tm.rh = tm.rhp = tm.rw = tm.rwp = tm.q;
     }

@@ -128,6 +128,29 @@ def test_large_scores_stay_finite():
     compare(flat64(got), want, what="large scores")
 
 
+NONPOS_SCALE_CASES = {
+    "none_shared_ragged": Workload("np1", B=1, H=2, Nq=300, Nk=333, d=64, dtype="bf16", bias="none", seed=11),
+    "none_packed": Workload("np2", B=3, H=2, Nq=49, Nk=40, d=32, dtype="fp16", bias="none", seed=12),
+    "none_one_tile": Workload("np3", B=2, H=2, Nq=300, Nk=77, d=40, dtype="fp16", bias="none", seed=13),
+    "swin_rows": W["swin_t_stage1"].with_(B=64, seed=14),
+    "sam_64x64": W["sam_vith_global"].with_(B=1, H=2, seed=15),
+    "sam_14x14": W["sam_vith_window"].with_(B=2, H=2, seed=16),
+}
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.3])
+@pytest.mark.parametrize("case", sorted(NONPOS_SCALE_CASES))
+def test_nonpositive_scale(case, scale):
+    """scale = 0 (every key weighted by its bias alone: the mean of V without
+    bias) and a negative scale (the score order flips), against the oracle;
+    masked key padding must stay at weight zero either way."""
+    w = NONPOS_SCALE_CASES[case]
+    inp = make_inputs(w)
+    got = run_gpu(w, inp, scale=scale)
+    want, _ = oracle.attn_fwd(flat64(inp.q), flat64(inp.k), flat64(inp.v), w.H, scale, oracle_bias(w, inp))
+    compare(flat64(got), want, what=f"{case} scale {scale}")
+
+
 def test_output_not_aliasing_and_repeatable():
     w = W["toy"]
     inp = make_inputs(w)
