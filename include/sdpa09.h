@@ -37,11 +37,13 @@
 #ifndef SDPA09_H
 #define SDPA09_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
 
-#define SDPA09_ABI_VERSION 5
+#define SDPA09_ABI_VERSION 6
 
 typedef enum {
     ATTN_BF16 = 0, /* bfloat16 Q/K/V/O ("model.to(torch.bfloat16)" in the SAM rewrite) */
@@ -156,6 +158,25 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int 
              int Nk, int d, float scale, attn_dtype dtype, attn_bias_kind bias_kind,
              const void* bias_args, void* stream);
 
+/* attn_fwd_train -- attn_fwd that also writes each query row's log-sum-exp,
+ * the statistic the backward pass (attn_bwd) recomputes the probabilities
+ * from: the Swin talk ("视觉大模型训练和推理加速" section 二) builds the forward
+ * and the backward computation of its attention operators alike, for
+ * training.  For row i of slice b,
+ *     lse[b * Nq + i] = log sum_j exp(scale * Q_i . K_j + bias_ij)
+ * (natural logarithm, fp32), so that P_ij = exp(scale * Q_i . K_j + bias_ij
+ * - lse_i).  With the Swin image layout the rows are still counted in the
+ * windows order (b a window-head slice, i a token of the window).
+ *
+ *  lse        device fp32 [B][H][Nq], fully overwritten, 4-byte aligned; must
+ *             not alias the other tensors.
+ *  the rest   as for attn_fwd; out is written exactly as attn_fwd writes it.
+ * Returns as attn_fwd (ATTN_ERR_ARG also for a null lse).
+ */
+int attn_fwd_train(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+                   int Nq, int Nk, int d, float scale, attn_dtype dtype, attn_bias_kind bias_kind,
+                   const void* bias_args, void* stream);
+
 /* attn_fwd_varlen -- attention over a batch of sequences of different
  * lengths packed in one buffer, each sequence attending only to itself: a
  * nested tensor ("PyTorch团队重写「分割一切」模型" and its translations: Nested
@@ -188,9 +209,9 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, cons
                     const int* cu_seqlens_k, int n_seq, int H, int d, float scale, attn_dtype dtype,
                     void* stream);
 
-/* attn_bwd -- gradients of attn_fwd for training, for short sequences
- * (windows): the Swin talk ("视觉大模型训练和推理加速" section 二) builds the
- * forward and backward computation of its window operators alike.  With
+/* attn_bwd -- gradients of attn_fwd for training: the Swin talk
+ * ("视觉大模型训练和推理加速" section 二) builds the forward and the backward
+ * computation of its window operators alike.  With
  * P = softmax(scale*Q.K^T + bias), O = P.V and dO = dout:
  *   dV = P^T dO,  dS = P * (dO V^T - rowsum(dO * O)),
  *   dQ = scale dS K,  dK = scale dS^T Q,
@@ -198,23 +219,38 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, cons
  * each (query, key) pair of each head (the mask is constant).
  *
  *  q, k, v    device inputs of the forward call, layout [B][H][N][d];
- *  out        device O of the forward call (for rowsum(dO * O));
+ *  out        device O of the forward call (rowsum(dO * O) is taken from it);
  *  dout       device gradient of the loss with respect to O, like out;
+ *  lse        device fp32 [B][H][Nq], the row log-sum-exp attn_fwd_train
+ *             wrote; may be NULL when Nq <= 128 and Nk <= 128 (each row then
+ *             fits one key tile and its softmax is recomputed exactly);
  *  dq, dk, dv device outputs, like q, k, v; fully overwritten.
- *  B, H, Nq, Nk, d, scale, dtype as for attn_fwd; Nq, Nk <= 128, d <= 64.
+ *  B, H, Nq, Nk, d, scale, dtype as for attn_fwd.
  *  bias_kind  ATTN_BIAS_NONE or ATTN_BIAS_SWIN (windows layout, bias_args
  *             as for attn_fwd).
- *  d_table    device fp32 [(2*win-1)^2][H] for ATTN_BIAS_SWIN, ADDED to
- *             (the caller zeroes it first); NULL otherwise.
+ *  d_bias     device fp32 bias gradient, ADDED to (the caller zeroes it
+ *             first): ATTN_BIAS_SWIN: [(2*win-1)^2][H]; NULL otherwise.
+ *  workspace, workspace_bytes
+ *             device scratch of at least attn_bwd_workspace_size(...) bytes,
+ *             16-byte aligned, owned by the caller (NULL when that size is
+ *             0); its contents on entry do not matter.
  *  stream     cudaStream_t to enqueue on.
- * The probabilities are recomputed exactly in fp32 from the inputs (no
- * saved statistics), products accumulate in fp32, outputs are rounded to
- * nearest even.  Returns ATTN_OK, ATTN_ERR_ARG, ATTN_ERR_UNSUPPORTED
- * (longer sequences, d > 64, SAM bias, image layout) or ATTN_ERR_CUDA.
+ * Products run on the tensor cores with fp32 accumulation from 16-bit
+ * operands (P and dS rounded to the input type); outputs are rounded to
+ * nearest even.  Returns ATTN_OK, ATTN_ERR_ARG, ATTN_ERR_UNSUPPORTED (see
+ * the limits below) or ATTN_ERR_CUDA.  Limits: d <= 64 for sequences of at
+ * most 128 tokens.
  */
-int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, void* dq, void* dk,
-             void* dv, int B, int H, int Nq, int Nk, int d, float scale, attn_dtype dtype,
-             attn_bias_kind bias_kind, const void* bias_args, float* d_table, void* stream);
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale,
+             attn_dtype dtype, attn_bias_kind bias_kind, const void* bias_args, float* d_bias,
+             void* workspace, size_t workspace_bytes, void* stream);
+
+/* attn_bwd_workspace_size -- bytes of device scratch attn_bwd needs for these
+ * arguments (0 when none is needed).  Reads only its arguments (and the host
+ * struct bias_args points to). */
+size_t attn_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, attn_bias_kind bias_kind,
+                               const void* bias_args);
 
 /* attn_debug_bias -- test hook for the in-kernel bias builders.
  *

@@ -228,6 +228,25 @@ def attn_probs(q, k, v, H, scale, slice_index, bias: Bias | None = None):
     return probs, out
 
 
+def attn_lse(q, k, H, scale, bias: Bias | None = None):
+    """Row log-sum-exp of the scores, lse_i = log sum_j exp(scale Q_i.K_j +
+    bias_ij) (natural log, fp64), the statistic a training step keeps from
+    the forward pass so that P = exp(S - lse) (the Swin talk, section 二:
+    forward and backward computations of the attention operators).  Plain
+    definition: the explicit score matrix of each slice with the largest
+    score taken out.  q [BH, Nq, d], k [BH, Nk, d]; returns [BH, Nq]."""
+    q, k = _f64(q), _f64(k)
+    BH, Nq, Nk, d = _shape(q, k)
+    out = np.empty((BH, Nq), dtype=np.float64)
+    for s in range(BH):
+        S = scale * (q[s] @ k[s].T)
+        if bias is not None and bias.kind != "none":
+            S = S + bias_matrix(q, H, s, Nk, bias)
+        m = S.max(axis=1, keepdims=True)
+        out[s] = (m + np.log(np.exp(S - m).sum(axis=1, keepdims=True)))[:, 0]
+    return out
+
+
 def bias_matrix(q, H, slice_index, Nk, bias: Bias):
     """The bias of one slice as an explicit Nq x Nk matrix (fp64)."""
     lib = _load()

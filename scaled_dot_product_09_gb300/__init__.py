@@ -21,7 +21,7 @@ import math
 import os
 import threading
 
-__all__ = ["attn_fwd", "attn_fwd_varlen", "attn_bwd", "attn_debug_bias", "attn_device_status", "selftest_wait_timeout", "SwinBias", "SamBias",
+__all__ = ["attn_fwd", "attn_fwd_train", "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size", "attn_debug_bias", "attn_device_status", "selftest_wait_timeout", "SwinBias", "SamBias",
            "load_library", "AttnError", "ATTN_OK", "ATTN_ERR_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT", "HEADER_SYMBOLS"]
 
@@ -31,7 +31,8 @@ ATTN_BIAS_NONE, ATTN_BIAS_SWIN, ATTN_BIAS_SAM_RELPOS = 0, 1, 2
 ATTN_SWIN_WINDOWS, ATTN_SWIN_IMAGE = 0, 1
 
 # Every extern "C" function include/sdpa09.h declares.
-HEADER_SYMBOLS = ("attn_fwd", "attn_fwd_varlen", "attn_bwd", "attn_debug_bias", "attn_device_status",
+HEADER_SYMBOLS = ("attn_fwd", "attn_fwd_train", "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size",
+                  "attn_debug_bias", "attn_device_status",
                   "attn_selftest_wait_timeout", "attn_last_error", "attn_abi_version")
 ATTN_VARLEN_MAX_SEQ = 128
 
@@ -112,11 +113,16 @@ def load_library(build: bool = True):
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp]
         lib.attn_fwd.restype = i
+        lib.attn_fwd_train.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp]
+        lib.attn_fwd_train.restype = i
         ip = ctypes.POINTER(ctypes.c_int)
         lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, ip, ip, i, i, i, f, i, vp]
         lib.attn_fwd_varlen.restype = i
-        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp]
+        sz = ctypes.c_size_t
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, sz, vp]
         lib.attn_bwd.restype = i
+        lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i, vp]
+        lib.attn_bwd_workspace_size.restype = sz
         lib.attn_debug_bias.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp]
         lib.attn_debug_bias.restype = i
         lib.attn_device_status.argtypes = [vp]
@@ -207,6 +213,26 @@ def attn_fwd(q, k, v, out=None, scale=None, bias=None, stream=None):
     return out
 
 
+def attn_fwd_train(q, k, v, out=None, lse=None, scale=None, bias=None, stream=None):
+    """attn_fwd that also returns each query row's natural-log log-sum-exp,
+    fp32 [B, H, Nq] (the statistic attn_bwd needs): returns (out, lse)."""
+    import torch
+    lib = load_library()
+    B, H, Nq, Nk, d = _shape_image(q, k, v, bias) if _is_image(bias) else _shape(q, k, v)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * Nq:
+        raise AttnError(ATTN_ERR_ARG, "lse must be a contiguous fp32 tensor of B * H * Nq values")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kind, _keep, args = _bias_args(bias)
+    rc = lib.attn_fwd_train(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d, scale,
+                            _dtype_code(q), kind, args, _stream_ptr(stream))
+    _check(lib, rc)
+    return out, lse
+
+
 def _cu_array(cu):
     vals = [int(x) for x in (cu.tolist() if hasattr(cu, "tolist") else cu)]
     return (ctypes.c_int * len(vals))(*vals), vals
@@ -238,31 +264,46 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, H, out=None, scale=None
     return out
 
 
-def attn_bwd(q, k, v, out, dout, scale=None, bias=None, stream=None, grads=None):
-    """Gradients of attn_fwd for short sequences (Nq, Nk <= 128, d <= 64):
-    q/k/v/out/dout [B,H,N,d] contiguous bf16/fp16 CUDA tensors (out: the
-    forward's output, dout: the gradient with respect to it).  Returns
-    (dq, dk, dv, d_table) with d_table the fp32 gradient of a SwinBias table
-    (windows layout), else None.  grads: the four buffers to use instead
-    (d_table is added to)."""
+def attn_bwd_workspace_size(B, H, Nq, Nk, d, bias=None):
+    """Bytes of device scratch attn_bwd needs for these sizes (0: none)."""
+    lib = load_library()
+    kind, _keep, args = _bias_args(bias)
+    return int(lib.attn_bwd_workspace_size(B, H, Nq, Nk, d, kind, args))
+
+
+def attn_bwd(q, k, v, out, dout, lse=None, scale=None, bias=None, stream=None, grads=None, workspace=None):
+    """Gradients of attn_fwd: q/k/v/out/dout [B,H,N,d] contiguous bf16/fp16
+    CUDA tensors (out: the forward's output, dout: the gradient with respect
+    to it), lse: the fp32 [B,H,Nq] row log-sum-exp from attn_fwd_train (may
+    be None when Nq, Nk <= 128).  Returns (dq, dk, dv, d_bias) with d_bias the
+    fp32 gradient of a SwinBias table, else None.  grads: the four buffers to
+    use instead (d_bias is added to); workspace: a uint8 CUDA tensor of at
+    least attn_bwd_workspace_size bytes (allocated here when None)."""
     import torch
     lib = load_library()
     B, H, Nq, Nk, d = _shape(q, k, v)
     for t in (out, dout):
         if t.shape != q.shape or not t.is_contiguous():
             raise AttnError(ATTN_ERR_ARG, "out and dout must be contiguous and shaped like q")
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * Nq):
+        raise AttnError(ATTN_ERR_ARG, "lse must be a contiguous fp32 tensor of B * H * Nq values")
     if grads is not None:
-        dq, dk, dv, d_table = grads
+        dq, dk, dv, d_bias = grads
     else:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        d_table = torch.zeros_like(bias.table) if isinstance(bias, SwinBias) else None
-    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+        d_bias = torch.zeros_like(bias.table) if isinstance(bias, SwinBias) else None
     kind, _keep, args = _bias_args(bias)
-    rc = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+    need = int(lib.attn_bwd_workspace_size(B, H, Nq, Nk, d, kind, args))
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
                       B, H, Nq, Nk, d, scale, _dtype_code(q), kind, args,
-                      _ptr(d_table) if d_table is not None else None, _stream_ptr(stream))
+                      _ptr(d_bias) if d_bias is not None else None,
+                      _ptr(workspace) if workspace is not None else None, ws_bytes, _stream_ptr(stream))
     _check(lib, rc)
-    return dq, dk, dv, d_table
+    return dq, dk, dv, d_bias
 
 
 def attn_debug_bias(q, k, v, scale=None, bias=None, stream=None):

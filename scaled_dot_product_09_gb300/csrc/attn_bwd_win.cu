@@ -1,0 +1,53 @@
+// Instantiates and launches the packed-windows backward kernel
+// (attn_bwd_kernel.cuh) for head dims padded to 32, 48 and 64, no bias or the
+// Swin bias, and slots of 32, 64 or 128 rows.
+#include <cuda_runtime.h>
+#include "attn_bwd_kernel.cuh"
+
+namespace sdpa09 {
+
+template <int DPAD, int BIAS, int SL>
+static cudaError_t launch_win_one(const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem,
+                                  cudaStream_t stream) {
+    auto kern = attn_bwd_win_kernel<DPAD, BIAS, SL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)kBwdThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tm, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <int DPAD, int BIAS>
+static cudaError_t launch_win_sl(const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem, cudaStream_t stream) {
+    switch (p.sl) {
+        case 32: return launch_win_one<DPAD, BIAS, 32>(tm, p, grid, smem, stream);
+        case 64: return launch_win_one<DPAD, BIAS, 64>(tm, p, grid, smem, stream);
+        case 128: return launch_win_one<DPAD, BIAS, 128>(tm, p, grid, smem, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_bwd_win(int dpad, bool swin, const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem,
+                           cudaStream_t stream) {
+    switch (dpad) {
+        case 32: return swin ? launch_win_sl<32, kBiasSwin>(tm, p, grid, smem, stream)
+                             : launch_win_sl<32, kBiasNone>(tm, p, grid, smem, stream);
+        case 48: return swin ? launch_win_sl<48, kBiasSwin>(tm, p, grid, smem, stream)
+                             : launch_win_sl<48, kBiasNone>(tm, p, grid, smem, stream);
+        case 64: return swin ? launch_win_sl<64, kBiasSwin>(tm, p, grid, smem, stream)
+                             : launch_win_sl<64, kBiasNone>(tm, p, grid, smem, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace sdpa09

@@ -94,6 +94,7 @@ enum DevStatus {
 
 struct AttnParams {
     void* out;        // [BH][Nq][d]
+    float* lse;       // [BH][Nq] natural-log row log-sum-exp, or null (not written)
     float* dbg;       // debug bias [BH][Nq][Nk] or null
     int* status;      // device status word
     int BH, H, Nq, Nk, d;
@@ -1493,8 +1494,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // O / l rounded to the output type and stored (row-per-thread, 16 bytes at a time)
-        auto epilogue = [&](uint32_t tObuf, float l, int slice, int tok, bool rok, int qbuf) {
+        // m: the row's reference maximum in log2 units (P = 2^(x - m)), for the
+        // row's log-sum-exp (m + log2 l) ln 2 when the caller asked for it
+        auto epilogue = [&](uint32_t tObuf, float l, float m, int slice, int tok, bool rok, int qbuf) {
             const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+            if (p.lse != nullptr && rok && !DBG)
+                p.lse[(size_t)slice * p.Nq + tok] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             uint32_t o[DPAD / 2];
             {
                 uint32_t v[DPAD];
@@ -1559,7 +1564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         // the previous job's row (pipelined epilogue)
-        float pv_l = 0.f;
+        float pv_l = 0.f, pv_m = 0.f;
         int pv_slice = 0, pv_tok = 0;
         bool pv_ok = false;
 
@@ -1581,6 +1586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 row_ok = (my_tok < p.Nq) && (my_sl < p.g) && (my_slice < p.BH);
             }
             float l_run = 0.f;
+            float m_fin = 0.f;  // the row's reference maximum (log2 units) once its keys are done
 
             if constexpr (MODE == kModeSeparate) {
                 // ---------------------------- one key tile: own slot's SL columns
@@ -1651,6 +1657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float m = row_max<kNc>(xs) * sc;
                 const float m_use = (m == -INFINITY) ? 0.f : m;
+                m_fin = m_use;
                 uint32_t own[SL / 2];
 #pragma unroll
                 for (int t = kNe / 2; t < SL / 2; ++t) own[t] = 0u;  // keys past the window
@@ -1665,7 +1672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_slice, pv_tok, pv_ok, 0);
+                        epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_m, pv_slice, pv_tok, pv_ok, 0);
                     }
                 }
                 if (ju == 0) {
@@ -1688,6 +1695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 warp_arrive(&bar_p[x]);
                 if constexpr (kDblO) {
                     pv_l = l_run;
+                    pv_m = m_fin;
                     pv_slice = my_slice;
                     pv_tok = my_tok;
                     pv_ok = row_ok;
@@ -1812,6 +1820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     warp_arrive(&bar_p[x]);
                 }
                 if (!ok) break;
+                m_fin = (m_run == -INFINITY) ? 0.f : m_run;
             } else {
                 // ------------------------------------------------- bias row setup
                 // rel_w of the row for kw = 2u, 2u + 1, held as fp16 pairs (half the
@@ -2031,7 +2040,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 break;
                             }
                             tc_fence_after();
-                            epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_slice, pv_tok, pv_ok, 0);
+                            epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_m, pv_slice, pv_tok, pv_ok, 0);
                         }
                     }
                     tmem_st_cols<kCols / 2>(tP, pk);
@@ -2040,11 +2049,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     warp_arrive(&bar_p[x]);
                 }
                 if (!ok) break;
+                m_fin = (m_run == -INFINITY) ? 0.f : m_run;
             }
 
             // -------------------------------------------------------- epilogue
             if constexpr (kShDbl) {  // written during the next job (or after the last)
                 pv_l = l_run;
+                pv_m = m_fin;
                 pv_slice = my_slice;
                 pv_tok = my_tok;
                 pv_ok = row_ok;
@@ -2054,16 +2065,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_o[x], ju & 1, abort_flag, kStatusWaitO))) { ok = false; break; }
             tc_fence_after();
             if constexpr (VL)  // output rows counted from the buffer start
-                epilogue(tO, l_run, 0, jr.out_row0 + my_tok, row_ok, ju % p.nq);
+                epilogue(tO, l_run, m_fin, 0, jr.out_row0 + my_tok, row_ok, ju % p.nq);
             else
-                epilogue(tO, l_run, my_slice, my_tok, row_ok, MODE == kModeShared ? ju % p.nq : 0);
+                epilogue(tO, l_run, m_fin, my_slice, my_tok, row_ok, MODE == kModeShared ? ju % p.nq : 0);
         }
         if constexpr (kDblO || kShDbl) {
             if (ok && ju > 0) {
                 __syncwarp();
                 if (__all_sync(0xffffffffu, mbar_wait(&bar_o[x], (ju - 1) & 1, abort_flag, kStatusWaitO))) {
                     tc_fence_after();
-                    epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_slice, pv_tok, pv_ok, 0);
+                    epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_m, pv_slice, pv_tok, pv_ok, 0);
                 }
             }
         }

@@ -20,10 +20,14 @@
 #include <string>
 
 #include "../../include/sdpa09.h"
-#include "attn_bwd_window.cuh"
+#include "attn_bwd_kernel.cuh"
 #include "attn_launch.cuh"
 
 namespace sdpa09 {
+
+cudaError_t launch_bwd_win(int dpad, bool swin, const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem,
+                           cudaStream_t stream);
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -237,7 +241,7 @@ constexpr size_t kSwinRowsMax = 96 * 1024;
 // tokens of all sequences, the operands viewed as [H * total][d] rows.
 int run(const void* q, const void* k, const void* v, void* out, float* dbg, int B, int H, int Nq,
         int Nk, int d, float scale, attn_dtype dtype, attn_bias_kind bias_kind,
-        const void* bias_args, void* stream, const VarlenTable* vt = nullptr) {
+        const void* bias_args, void* stream, const VarlenTable* vt = nullptr, float* lse = nullptr) {
     g_last_error.clear();
     if (!q || !k || !v || !(out || dbg)) return fail(ATTN_ERR_ARG, "null tensor pointer");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out ? out : (void*)dbg))
@@ -260,6 +264,7 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
     memset(&p, 0, sizeof(p));
     p.out = out;
     p.dbg = dbg;
+    p.lse = lse;
     p.BH = (int)BH;
     p.H = H;
     p.Nq = Nq;
@@ -519,6 +524,141 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
     return ATTN_OK;
 }
 
+// ------------------------------------------------------------------ backward
+
+// Workspace of the backward pass for sequences longer than one 128-key tile
+// (none is needed for windows of up to 128 tokens).
+size_t bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d, attn_bias_kind bias_kind, const void* bias_args) {
+    (void)d; (void)bias_kind; (void)bias_args;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return 0;
+    if (Nq <= kBlockM && Nk <= kBlockN) return 0;
+    return 0;
+}
+
+int run_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+            void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, attn_dtype dtype,
+            attn_bias_kind bias_kind, const void* bias_args, float* d_bias, void* workspace, size_t workspace_bytes,
+            void* stream) {
+    g_last_error.clear();
+    (void)lse; (void)workspace; (void)workspace_bytes;
+    const void* ptrs[8] = {q, k, v, out, dout, dq, dk, dv};
+    for (const void* x : ptrs) {
+        if (!x) return fail(ATTN_ERR_ARG, "null tensor pointer");
+        if (!aligned16(x)) return fail(ATTN_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    }
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return fail(ATTN_ERR_ARG, "B, H, Nq, Nk must be >= 1");
+    if (d < 8 || d % 8 != 0) return fail(ATTN_ERR_ARG, "d must be a positive multiple of 8 (got %d)", d);
+    if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return fail(ATTN_ERR_ARG, "unknown dtype %d", (int)dtype);
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return fail(ATTN_ERR_ARG, "scale must be finite");
+    const int64_t BH = (int64_t)B * H;
+    if (BH * Nq >= (int64_t(1) << 31) || BH * Nk >= (int64_t(1) << 31))
+        return fail(ATTN_ERR_UNSUPPORTED, "B*H*N must stay below 2^31 rows");
+    const int dpad = dpad_for(d);
+    BwdTcParams p;
+    memset(&p, 0, sizeof(p));
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.o = out;
+    p.BH = (int)BH;
+    p.H = H;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.d = d;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.is_bf16 = dtype == ATTN_BF16;
+    bool swin = false;
+    if (bias_kind == ATTN_BIAS_SWIN) {
+        const attn_swin_args* a = static_cast<const attn_swin_args*>(bias_args);
+        if (!a || !a->table) return fail(ATTN_ERR_ARG, "SWIN bias needs attn_swin_args with a table");
+        if (!d_bias) return fail(ATTN_ERR_ARG, "SWIN backward needs d_bias (the table gradient)");
+        const int M = a->win;
+        if (M < 1 || Nq != M * M || Nk != M * M) return fail(ATTN_ERR_ARG, "SWIN needs Nq == Nk == win*win");
+        if (a->grid_h < M || a->grid_w < M || a->grid_h % M || a->grid_w % M)
+            return fail(ATTN_ERR_ARG, "grid_h and grid_w must be positive multiples of win");
+        if (a->shift < 0 || a->shift >= M) return fail(ATTN_ERR_ARG, "shift must lie in [0, win)");
+        if (a->layout != ATTN_SWIN_WINDOWS)
+            return fail(ATTN_ERR_UNSUPPORTED, "the backward takes the windows token layout");
+        const int nW = (a->grid_h / M) * (a->grid_w / M);
+        if (B % nW) return fail(ATTN_ERR_ARG, "B (windows) must be a multiple of the windows per image");
+        swin = true;
+        p.table = a->table;
+        p.d_table = d_bias;
+        p.win = M;
+        p.grid_h = a->grid_h;
+        p.grid_w = a->grid_w;
+        p.shift = a->shift;
+        p.n_w = nW;
+        p.n_ww = a->grid_w / M;
+        p.n_wh = a->grid_h / M;
+        fast_div_params((uint32_t)H, p.fd_h);
+        fast_div_params((uint32_t)nW, p.fd_w);
+        fast_div_params((uint32_t)p.n_ww, p.fd_ww);
+    } else if (bias_kind != ATTN_BIAS_NONE) {
+        return fail(ATTN_ERR_UNSUPPORTED, "this backward takes no bias or the Swin bias");
+    }
+    if (Nq > kBlockM || Nk > kBlockN || dpad > 64)
+        return fail(ATTN_ERR_UNSUPPORTED, "backward for sequences of at most 128 tokens and d <= 64");
+    // packed windows: g slices of up to SL tokens share a 128-row tile
+    const int nmax = std::max(Nq, Nk);
+    const int sl = nmax <= 32 ? 32 : (nmax <= 64 ? 64 : 128);
+    p.sl = sl;
+    p.g = kBlockM / sl;
+    p.n_jobs = (int)((BH + p.g - 1) / p.g);
+    const size_t tile_bytes = (size_t)(dpad / 16) * kBlockM * 32;
+    p.stage_bytes = (uint32_t)(4 * tile_bytes);
+    const size_t pds = 2 * (size_t)8 * kBlockM * 32;
+    size_t extra = swin ? (2 * (size_t)(2 * p.win - 1) * (2 * p.win - 1) * H * 4 + 1023) / 1024 * 1024 : 0;
+    if (pds + extra + 2 * p.stage_bytes > kSmemBudget)
+        return fail(ATTN_ERR_UNSUPPORTED, "shared memory too small for this backward (H=%d)", H);
+    // Swin: the table gradient sums dS per (head, key token, query token) in
+    // shared memory when that fits (else one shared-memory atomic per pair,
+    // by relative offset), and per-CTA fp16 bias rows are used when they fit
+    // next to >= 3 stages (2 for the widest tiles), else per-element gathers
+    // from the table
+    if (swin) {
+        const size_t acc = ((size_t)H * Nq * Nk * 4 + 1023) / 1024 * 1024;
+        const int want = p.stage_bytes > 40 * 1024 ? 2 : 3;
+        p.swin_acc = (pds + extra + acc + 2 * (size_t)p.stage_bytes <= kSmemBudget) ? 1 : 0;
+        p.swin_acc_atomic = p.g > H ? 1 : 0;
+        p.off_acc = (uint32_t)extra;  // relative to the extra area until its offset is known
+        if (p.swin_acc) extra += acc;
+        const size_t rows = ((size_t)H * sl * sl * 2 + 3 * (size_t)sl * (sl / 32) * 4 + 1023) / 1024 * 1024;
+        p.swin_rows = (sl <= 64 && pds + extra + rows + want * (size_t)p.stage_bytes <= kSmemBudget) ? 1 : 0;
+        p.off_rows = (uint32_t)extra;
+        if (p.swin_rows) extra += rows;
+    }
+    p.nst = (int)std::min<size_t>(kMaxStages, (kSmemBudget - pds - extra) / p.stage_bytes);
+    p.off_ring = 0;
+    p.off_p = (uint32_t)(p.nst * p.stage_bytes);
+    p.off_ds = p.off_p + (uint32_t)(pds / 2);
+    p.off_extra = p.off_ds + (uint32_t)(pds / 2);
+    p.off_rows += p.off_extra;
+    p.off_acc += p.off_extra;
+    const size_t smem = p.off_extra + extra + 1024;
+    p.full_atoms = d / 16;
+    p.part = (d / 16 > 0 && d % 16) ? 1 : 0;
+    const int atoms = dpad / 16;
+    const bool bf = p.is_bf16 != 0;
+    BwdMaps tm;
+    int rc;
+    if ((rc = encode_operand(&tm.q, &tm.qp, q, bf, d, Nq, BH, atoms, sl, p.g))) return rc;
+    if ((rc = encode_operand(&tm.k, &tm.kp, k, bf, d, Nk, BH, atoms, sl, p.g))) return rc;
+    if ((rc = encode_operand(&tm.v, &tm.vp, v, bf, d, Nk, BH, atoms, sl, p.g))) return rc;
+    if ((rc = encode_operand(&tm.dout, &tm.dop, dout, bf, d, Nq, BH, atoms, sl, p.g))) return rc;
+    const int nsm = sm_count();
+    if (nsm <= 0) return fail(ATTN_ERR_CUDA, "no CUDA device");
+    p.status = status_ptr();
+    if (!p.status) return fail(ATTN_ERR_CUDA, "no CUDA device / status word unavailable");
+    const int grid = std::min(p.n_jobs, nsm);
+    cudaError_t e = launch_bwd_win(dpad, swin, tm, p, grid, smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    static const bool debug_env = getenv("SDPA09_DEBUG") && getenv("SDPA09_DEBUG")[0] == '1';
+    if (debug_env) return attn_device_status(stream);
+    return ATTN_OK;
+}
+
 }  // namespace
 }  // namespace sdpa09
 
@@ -530,6 +670,16 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int 
     if (!out) return sdpa09::fail(ATTN_ERR_ARG, "null output pointer");
     return sdpa09::run(q, k, v, out, nullptr, B, H, Nq, Nk, d, scale, dtype, bias_kind, bias_args,
                        stream);
+}
+
+int attn_fwd_train(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int Nq,
+                   int Nk, int d, float scale, attn_dtype dtype, attn_bias_kind bias_kind, const void* bias_args,
+                   void* stream) {
+    if (!out) return sdpa09::fail(ATTN_ERR_ARG, "null output pointer");
+    if (!lse) return sdpa09::fail(ATTN_ERR_ARG, "null lse pointer");
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return sdpa09::fail(ATTN_ERR_ARG, "lse must be 4-byte aligned");
+    return sdpa09::run(q, k, v, out, nullptr, B, H, Nq, Nk, d, scale, dtype, bias_kind, bias_args, stream, nullptr,
+                       lse);
 }
 
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, const int* cu_seqlens_q,
@@ -577,62 +727,17 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, cons
                        ATTN_BIAS_NONE, nullptr, stream, &vt);
 }
 
-int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, void* dq, void* dk,
-             void* dv, int B, int H, int Nq, int Nk, int d, float scale, attn_dtype dtype,
-             attn_bias_kind bias_kind, const void* bias_args, float* d_table, void* stream) {
-    using sdpa09::fail;
-    sdpa09::g_last_error.clear();
-    const void* ptrs[8] = {q, k, v, out, dout, dq, dk, dv};
-    for (const void* x : ptrs) {
-        if (!x) return fail(ATTN_ERR_ARG, "null tensor pointer");
-        if (!sdpa09::aligned16(x)) return fail(ATTN_ERR_ARG, "tensor pointers must be 16-byte aligned");
-    }
-    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return fail(ATTN_ERR_ARG, "B, H, Nq, Nk must be >= 1");
-    if (d < 8 || d % 8 != 0) return fail(ATTN_ERR_ARG, "d must be a positive multiple of 8 (got %d)", d);
-    if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return fail(ATTN_ERR_ARG, "unknown dtype %d", (int)dtype);
-    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return fail(ATTN_ERR_ARG, "scale must be finite");
-    if (Nq > 128 || Nk > 128 || d > 64)
-        return fail(ATTN_ERR_UNSUPPORTED, "backward is built for sequences of at most 128 tokens and d <= 64");
-    const int64_t BH = (int64_t)B * H;
-    if (BH >= (int64_t(1) << 31) / 128) return fail(ATTN_ERR_UNSUPPORTED, "too many slices");
-    sdpa09::BwdParams p;
-    memset(&p, 0, sizeof(p));
-    p.q = q; p.k = k; p.v = v; p.o = out; p.dout = dout;
-    p.dq = dq; p.dk = dk; p.dv = dv;
-    p.BH = (int)BH; p.H = H; p.Nq = Nq; p.Nk = Nk; p.d = d;
-    p.scale = scale;
-    p.is_bf16 = dtype == ATTN_BF16;
-    if (bias_kind == ATTN_BIAS_SWIN) {
-        const attn_swin_args* a = static_cast<const attn_swin_args*>(bias_args);
-        if (!a || !a->table) return fail(ATTN_ERR_ARG, "SWIN bias needs attn_swin_args with a table");
-        if (!d_table) return fail(ATTN_ERR_ARG, "SWIN backward needs d_table");
-        const int M = a->win;
-        if (M < 1 || Nq != M * M || Nk != M * M) return fail(ATTN_ERR_ARG, "SWIN needs Nq == Nk == win*win");
-        if (a->grid_h < M || a->grid_w < M || a->grid_h % M || a->grid_w % M)
-            return fail(ATTN_ERR_ARG, "grid_h and grid_w must be positive multiples of win");
-        if (a->shift < 0 || a->shift >= M) return fail(ATTN_ERR_ARG, "shift must lie in [0, win)");
-        if (a->layout != ATTN_SWIN_WINDOWS)
-            return fail(ATTN_ERR_UNSUPPORTED, "the backward takes the windows token layout");
-        const int nW = (a->grid_h / M) * (a->grid_w / M);
-        if (B % nW) return fail(ATTN_ERR_ARG, "B (windows) must be a multiple of the windows per image");
-        p.swin = 1;
-        p.table = a->table;
-        p.d_table = d_table;
-        p.win = M; p.grid_h = a->grid_h; p.grid_w = a->grid_w; p.shift = a->shift;
-        p.n_w = nW; p.n_ww = a->grid_w / M;
-    } else if (bias_kind != ATTN_BIAS_NONE) {
-        return fail(ATTN_ERR_UNSUPPORTED, "the backward takes no bias or the Swin bias");
-    }
-    const size_t smem = sdpa09::bwd_window_smem_bytes(Nq, Nk, d, p.win, H, p.swin != 0);
-    if (smem > 227 * 1024) return fail(ATTN_ERR_UNSUPPORTED, "slice too large for shared memory (%zu bytes)", smem);
-    const int nsm = sdpa09::sm_count();
-    if (nsm <= 0) return fail(ATTN_ERR_CUDA, "no CUDA device");
-    int per_sm = (int)std::min<size_t>(8, (228 * 1024) / (smem + 1024));
-    if (per_sm < 1) per_sm = 1;
-    const int grid = (int)std::min<int64_t>(BH, (int64_t)nsm * per_sm);
-    cudaError_t e = sdpa09::launch_bwd_window(p, grid, smem, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
-    return ATTN_OK;
+size_t attn_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, attn_bias_kind bias_kind, const void* bias_args) {
+    (void)B; (void)H; (void)Nq; (void)Nk; (void)d; (void)bias_kind; (void)bias_args;
+    return sdpa09::bwd_workspace_bytes(B, H, Nq, Nk, d, bias_kind, bias_args);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, attn_dtype dtype,
+             attn_bias_kind bias_kind, const void* bias_args, float* d_bias, void* workspace, size_t workspace_bytes,
+             void* stream) {
+    return sdpa09::run_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, dtype, bias_kind, bias_args,
+                           d_bias, workspace, workspace_bytes, stream);
 }
 
 int attn_debug_bias(const void* q, const void* k, const void* v, float* bias_out, int B, int H,

@@ -318,6 +318,14 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(bool bf16, int M, int N, b
            | ((uint32_t)(M >> 4) << 24);            // M / 16
 }
 
+// The same with either operand's major-ness chosen: A or B MN-major (the
+// transpose bits 15 / 16), for products whose operand tile is stored with
+// its M (or N) dimension contiguous.
+__host__ __device__ constexpr uint32_t make_idesc_f16_mn(bool bf16, int M, int N, bool a_mn_major,
+                                                         bool b_mn_major) {
+    return make_idesc_f16(bf16, M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
+
 // Shared-memory matrix descriptor.  Layout codes for bits 61..63:
 // 0 none, 2 128B, 4 64B, 6 32B swizzle.
 constexpr uint64_t kSwizzle32B = 6;

@@ -43,8 +43,8 @@ def test_library_targets_sm103a_only():
 def test_abi_version(lib):
     # 2: attn_swin_args gained its token layout field; 3: attn_fwd_varlen;
     # 4: attn_sam_args gained the table lengths (unequal grids, resampling);
-    # 5: attn_bwd
-    assert lib.attn_abi_version() == 5
+    # 5: attn_bwd; 6: attn_fwd_train (row log-sum-exp for the backward)
+    assert lib.attn_abi_version() == 6
 
 
 def _call(lib, q=FAKE, k=FAKE + 4096, v=FAKE + 8192, out=FAKE + 1 << 20, B=1, H=1, Nq=64, Nk=64,
@@ -174,9 +174,9 @@ def test_varlen_binding_checks():
         sdpa.attn_fwd_varlen(q, q, q, [0, 5, 10], [0, 4, 9], H=2)        # q too short for the offsets
 
 
-def _bwd(lib, B=64, H=3, Nq=49, Nk=49, d=32, kind=0, args=None, d_table=None, q=FAKE):
-    return lib.attn_bwd(q, FAKE + 4096, FAKE + 8192, FAKE + 12288, FAKE + 16384, FAKE + 20480, FAKE + 24576,
-                        FAKE + 28672, B, H, Nq, Nk, d, 0.125, 0, kind, args, d_table, None)
+def _bwd(lib, B=64, H=3, Nq=49, Nk=49, d=32, kind=0, args=None, d_table=None, q=FAKE, lse=None):
+    return lib.attn_bwd(q, FAKE + 4096, FAKE + 8192, FAKE + 12288, FAKE + 16384, lse, FAKE + 20480, FAKE + 24576,
+                        FAKE + 28672, B, H, Nq, Nk, d, 0.125, 0, kind, args, d_table, None, 0, None)
 
 
 def test_bwd_argument_checks(lib):
@@ -189,7 +189,7 @@ def test_bwd_argument_checks(lib):
     assert _bwd(lib, kind=2, args=ctypes.byref(sam)) == sdpa.ATTN_ERR_UNSUPPORTED
     swin = sdpa._SwinArgs(FAKE, 7, 56, 56, 3)
     assert _bwd(lib, kind=1, args=ctypes.byref(swin)) == sdpa.ATTN_ERR_ARG    # no d_table
-    assert b"d_table" in lib.attn_last_error()
+    assert b"d_bias" in lib.attn_last_error()
     img = sdpa._SwinArgs(FAKE, 7, 56, 56, 3, 1)
     assert _bwd(lib, kind=1, args=ctypes.byref(img), d_table=FAKE) == sdpa.ATTN_ERR_UNSUPPORTED
     assert _bwd(lib, B=63, kind=1, args=ctypes.byref(swin), d_table=FAKE) == sdpa.ATTN_ERR_ARG

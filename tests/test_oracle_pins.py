@@ -728,3 +728,29 @@ def test_bwd_out_perturbed_follows_the_rowsum_formula():
     # and the perturbation is not a no-op: dQ moved
     base = oracle.attn_bwd(q, k, v, dout, H, 0.45, b)
     assert np.abs(got["dq"] - base["dq"]).max() > 1e-3
+
+
+# ------------------------------------------------------------ log-sum-exp --
+
+def test_lse_closed_form_uniform_scores():
+    """Q = 0 and no bias: every score is 0, so lse = log(Nk) exactly."""
+    rng = np.random.default_rng(66)
+    q = np.zeros((3, 5, 4))
+    k = rng.standard_normal((3, 7, 4))
+    np.testing.assert_allclose(oracle.attn_lse(q, k, 1, 0.7), np.log(7.0), rtol=0, atol=1e-15)
+
+
+def test_lse_gives_the_c_oracle_probabilities():
+    """exp(S - lse) equals the probabilities the C oracle computes (a
+    separate implementation of the softmax), with and without a bias."""
+    rng = np.random.default_rng(67)
+    M, G, H, d = 3, 6, 2, 5
+    BH, N = (G // M) ** 2 * H, M * M
+    table = rng.standard_normal(((2 * M - 1) ** 2, H)) * 0.3
+    q, k, v = (rng.standard_normal((BH, N, d)) for _ in range(3))
+    for b in (None, oracle.Bias("swin", table=table, win=M, grid_h=G, grid_w=G, shift=1)):
+        lse = oracle.attn_lse(q, k, H, 0.4, b)
+        for s in range(BH):
+            P, _ = oracle.attn_probs(q, k, v, H, 0.4, s, b)
+            S = 0.4 * q[s] @ k[s].T + (oracle.bias_matrix(q, H, s, N, b) if b is not None else 0.0)
+            np.testing.assert_allclose(np.exp(S - lse[s][:, None]), P, rtol=0, atol=1e-13)
