@@ -238,17 +238,19 @@ def _time_bwd(w: Workload, stream, dev, steps: int):
     dout = torch.randn(inp.q.shape, generator=g).to(inp.q.dtype)
     bias = _gpu_bias(w, inp, dev)
     sets = []
+    need = sdpa.attn_bwd_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d, bias)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     for _ in range(n):
         q, k, v, do = (x.to(dev) for x in (inp.q, inp.k, inp.v, dout))
-        o = sdpa.attn_fwd(q, k, v, scale=w.scale, bias=bias, stream=stream)
+        o, lse = sdpa.attn_fwd_train(q, k, v, scale=w.scale, bias=bias, stream=stream)
         grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
-                 torch.zeros_like(bias.table) if bias is not None else None)
-        sets.append((q, k, v, o, do, grads))
+                 torch.zeros_like(bias.table) if isinstance(bias, sdpa.SwinBias) else None)
+        sets.append((q, k, v, o, lse, do, grads))
     torch.cuda.synchronize()
 
     def step(i):
-        q, k, v, o, do, grads = sets[i % n]
-        sdpa.attn_bwd(q, k, v, o, do, scale=w.scale, bias=bias, stream=stream, grads=grads)
+        q, k, v, o, lse, do, grads = sets[i % n]
+        sdpa.attn_bwd(q, k, v, o, do, lse=lse, scale=w.scale, bias=bias, stream=stream, grads=grads, workspace=ws)
 
     with torch.cuda.stream(stream):
         for i in range(3):

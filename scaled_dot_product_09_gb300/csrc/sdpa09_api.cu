@@ -20,13 +20,25 @@
 #include <string>
 
 #include "../../include/sdpa09.h"
-#include "attn_bwd_kernel.cuh"
+#include "attn_bwd_long.cuh"
 #include "attn_launch.cuh"
 
 namespace sdpa09 {
 
 cudaError_t launch_bwd_win(int dpad, bool swin, const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem,
                            cudaStream_t stream);
+struct BwdPrepParams {
+    const void *q, *o, *dout;
+    float* Dws;
+    int rows, Nq, d, is_bf16;
+    const void *rel_h, *rel_w;
+    __half* rel;
+    float* d_relh;
+    int s_h, s_w, rel_stride, rw0;
+};
+cudaError_t launch_bwd_prep(const BwdPrepParams& p, bool sam, int nsm, cudaStream_t stream);
+cudaError_t launch_bwd_long(int dpad, int mode, int sw, const BwdMaps& tm, const BwdLongParams& p, int grid,
+                            size_t smem, cudaStream_t stream);
 
 namespace {
 
@@ -528,11 +540,141 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
 
 // Workspace of the backward pass for sequences longer than one 128-key tile
 // (none is needed for windows of up to 128 tokens).
+// Layout of the long-sequence backward's workspace (byte offsets, each
+// 256-byte aligned): D [rows] fp32; for SAM also the rel terms [rows][stride]
+// fp16, scale dS.K [rows][d] fp32, dRelH [rows][k_h] fp32, dRelW [rows][k_w]
+// fp32 (rows = B * H * Nq).
+struct BwdWs {
+    size_t d, rel, dq32, drh, drw, total;
+};
+static size_t al256(size_t x) { return (x + 255) / 256 * 256; }
+static BwdWs bwd_ws_layout(int64_t rows, int d, bool sam, int s_h, int s_w, int rel_stride) {
+    BwdWs w{};
+    size_t o = 0;
+    w.d = o;
+    o += al256((size_t)rows * 4);
+    if (sam) {
+        w.rel = o;
+        o += al256((size_t)rows * rel_stride * 2);
+        w.dq32 = o;
+        o += al256((size_t)rows * d * 4);
+        w.drh = o;
+        o += al256((size_t)rows * s_h * 4);
+        w.drw = o;
+        o += al256((size_t)rows * s_w * 4);
+    }
+    w.total = o;
+    return w;
+}
+static bool bwd_is_windows(int Nq, int Nk, int d) { return Nq <= kBlockM && Nk <= kBlockN && dpad_for(d) <= 64; }
+static int sam_rel_stride(int s_h, int s_w, int* rw0) {
+    *rw0 = (s_h + 7) / 8 * 8;
+    return *rw0 + (s_w + 7) / 8 * 8;
+}
+
 size_t bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d, attn_bias_kind bias_kind, const void* bias_args) {
-    (void)d; (void)bias_kind; (void)bias_args;
-    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return 0;
-    if (Nq <= kBlockM && Nk <= kBlockN) return 0;
-    return 0;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return 0;
+    if (bias_kind != ATTN_BIAS_SAM_RELPOS && bwd_is_windows(Nq, Nk, d)) return 0;
+    const int64_t rows = (int64_t)B * H * Nq;
+    bool sam = false;
+    int s_h = 0, s_w = 0, stride = 0, rw0 = 0;
+    if (bias_kind == ATTN_BIAS_SAM_RELPOS && bias_args) {
+        const attn_sam_args* a = static_cast<const attn_sam_args*>(bias_args);
+        sam = true;
+        s_h = a->q_h;
+        s_w = a->q_w;
+        stride = sam_rel_stride(s_h, s_w, &rw0);
+    }
+    return bwd_ws_layout(rows, d, sam, s_h, s_w, stride).total;
+}
+
+// Sequences longer than one 128-key tile (or d > 64): pre-pass for D, then
+// the key pass (dK, dV) and the query pass (dQ) on the tensor cores.
+int run_bwd_long(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, attn_dtype dtype,
+                 const attn_sam_args* sam, void* workspace, size_t workspace_bytes, void* stream) {
+    const int dpad = dpad_for(d);
+    if (dpad > 80) return fail(ATTN_ERR_UNSUPPORTED, "backward for sequences over 128 tokens needs d <= 80");
+    if (!lse)
+        return fail(ATTN_ERR_ARG, "sequences over 128 tokens (or d > 64) need the forward's lse (attn_fwd_train)");
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return fail(ATTN_ERR_ARG, "lse must be 4-byte aligned");
+    const int64_t BH = (int64_t)B * H, rows = BH * Nq;
+    int rw0 = 0, stride = 0;
+    if (sam) stride = sam_rel_stride(sam->q_h, sam->q_w, &rw0);
+    const BwdWs ws = bwd_ws_layout(rows, d, sam != nullptr, sam ? sam->q_h : 0, sam ? sam->q_w : 0, stride);
+    if (!workspace || workspace_bytes < ws.total)
+        return fail(ATTN_ERR_ARG, "workspace of %zu bytes needed (attn_bwd_workspace_size), %zu given", ws.total,
+                    workspace_bytes);
+    if (!aligned16(workspace)) return fail(ATTN_ERR_ARG, "workspace must be 16-byte aligned");
+    unsigned char* wsb = static_cast<unsigned char*>(workspace);
+    const int nsm = sm_count();
+    if (nsm <= 0) return fail(ATTN_ERR_CUDA, "no CUDA device");
+    int* status = status_ptr();
+    if (!status) return fail(ATTN_ERR_CUDA, "no CUDA device / status word unavailable");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool bf = dtype == ATTN_BF16;
+
+    BwdPrepParams pp;
+    memset(&pp, 0, sizeof(pp));
+    pp.q = q;
+    pp.o = out;
+    pp.dout = dout;
+    pp.Dws = reinterpret_cast<float*>(wsb + ws.d);
+    pp.rows = (int)rows;
+    pp.Nq = Nq;
+    pp.d = d;
+    pp.is_bf16 = bf;
+    cudaError_t e = launch_bwd_prep(pp, false, nsm, st);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+
+    BwdLongParams p;
+    memset(&p, 0, sizeof(p));
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.lse = lse;
+    p.Dws = pp.Dws;
+    p.status = status;
+    p.BH = (int)BH;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.d = d;
+    p.kv_w = kBlockN;
+    p.n_qb = (Nq + kBlockM - 1) / kBlockM;
+    p.n_kb = (Nk + p.kv_w - 1) / p.kv_w;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.is_bf16 = bf;
+    p.full_atoms = d / 16;
+    p.part = (d / 16 > 0 && d % 16) ? 1 : 0;
+    const size_t tile = (size_t)(dpad / 16) * kBlockM * 32;
+    p.stage_bytes = (uint32_t)(2 * tile);
+    const int atoms = dpad / 16;
+    BwdMaps tm;
+    int rc;
+    if ((rc = encode_operand(&tm.q, &tm.qp, q, bf, d, Nq, BH, atoms, kBlockM, 1))) return rc;
+    if ((rc = encode_operand(&tm.k, &tm.kp, k, bf, d, Nk, BH, atoms, kBlockN, 1))) return rc;
+    if ((rc = encode_operand(&tm.v, &tm.vp, v, bf, d, Nk, BH, atoms, kBlockN, 1))) return rc;
+    if ((rc = encode_operand(&tm.dout, &tm.dop, dout, bf, d, Nq, BH, atoms, kBlockM, 1))) return rc;
+    for (int mode = 0; mode < 2; ++mode) {
+        const size_t pds = mode == kBwdKeyPass ? 2 * (size_t)8 * kBlockM * 32 : (size_t)8 * kBlockM * 32;
+        const size_t fixed = 2 * tile + pds;
+        if (fixed + 2 * p.stage_bytes > kSmemBudget) return fail(ATTN_ERR_UNSUPPORTED, "shared memory too small (d=%d)", d);
+        p.nst = (int)std::min<size_t>(kMaxStages, (kSmemBudget - fixed) / p.stage_bytes);
+        p.off_res = 0;
+        p.off_ring = (uint32_t)(2 * tile);
+        p.off_p = p.off_ring + (uint32_t)(p.nst * p.stage_bytes);
+        p.off_ds = p.off_p + (mode == kBwdKeyPass ? (uint32_t)(8 * kBlockM * 32) : 0u);
+        p.off_e = p.off_ds + (uint32_t)(8 * kBlockM * 32);
+        const size_t smem = p.off_e + 1024;
+        p.n_jobs = (int)(BH * (mode == kBwdKeyPass ? p.n_kb : p.n_qb));
+        const int grid = std::min(p.n_jobs, nsm);
+        e = launch_bwd_long(dpad, mode, 0, tm, p, grid, smem, st);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    }
+    static const bool debug_env = getenv("SDPA09_DEBUG") && getenv("SDPA09_DEBUG")[0] == '1';
+    if (debug_env) return attn_device_status(stream);
+    return ATTN_OK;
 }
 
 int run_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
@@ -595,11 +737,16 @@ int run_bwd(const void* q, const void* k, const void* v, const void* out, const 
         fast_div_params((uint32_t)H, p.fd_h);
         fast_div_params((uint32_t)nW, p.fd_w);
         fast_div_params((uint32_t)p.n_ww, p.fd_ww);
+    } else if (bias_kind == ATTN_BIAS_SAM_RELPOS) {
+        return fail(ATTN_ERR_UNSUPPORTED, "SAM backward not built yet");
     } else if (bias_kind != ATTN_BIAS_NONE) {
-        return fail(ATTN_ERR_UNSUPPORTED, "this backward takes no bias or the Swin bias");
+        return fail(ATTN_ERR_ARG, "unknown bias kind %d", (int)bias_kind);
     }
-    if (Nq > kBlockM || Nk > kBlockN || dpad > 64)
-        return fail(ATTN_ERR_UNSUPPORTED, "backward for sequences of at most 128 tokens and d <= 64");
+    if (!bwd_is_windows(Nq, Nk, d)) {
+        if (swin) return fail(ATTN_ERR_UNSUPPORTED, "SWIN backward with d > 64");
+        return run_bwd_long(q, k, v, out, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, dtype, nullptr, workspace,
+                            workspace_bytes, stream);
+    }
     // packed windows: g slices of up to SL tokens share a 128-row tile
     const int nmax = std::max(Nq, Nk);
     const int sl = nmax <= 32 ? 32 : (nmax <= 64 ? 64 : 128);
@@ -728,7 +875,6 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, cons
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, attn_bias_kind bias_kind, const void* bias_args) {
-    (void)B; (void)H; (void)Nq; (void)Nk; (void)d; (void)bias_kind; (void)bias_args;
     return sdpa09::bwd_workspace_bytes(B, H, Nq, Nk, d, bias_kind, bias_args);
 }
 

@@ -183,8 +183,14 @@ def test_bwd_argument_checks(lib):
     assert _bwd(lib, q=None) == sdpa.ATTN_ERR_ARG
     assert _bwd(lib, q=FAKE + 8) == sdpa.ATTN_ERR_ARG                       # misaligned
     assert _bwd(lib, d=36) == sdpa.ATTN_ERR_ARG
-    assert _bwd(lib, Nq=129) == sdpa.ATTN_ERR_UNSUPPORTED                   # long sequences
-    assert _bwd(lib, d=72) == sdpa.ATTN_ERR_UNSUPPORTED
+    # long sequences (or d > 64) take the two-pass path: the forward's lse and a workspace are required
+    assert _bwd(lib, Nq=129) == sdpa.ATTN_ERR_ARG
+    assert b"lse" in lib.attn_last_error()
+    assert _bwd(lib, Nq=129, lse=FAKE + 32768) == sdpa.ATTN_ERR_ARG
+    assert b"workspace" in lib.attn_last_error()
+    assert lib.attn_bwd_workspace_size(64, 3, 129, 49, 32, 0, None) >= 64 * 3 * 129 * 4
+    assert lib.attn_bwd_workspace_size(64, 3, 49, 49, 32, 0, None) == 0     # windows need none
+    assert _bwd(lib, d=88) == sdpa.ATTN_ERR_UNSUPPORTED                     # d > 80
     sam = sdpa._SamArgs(FAKE, FAKE, 7, 7, 7, 7)
     assert _bwd(lib, kind=2, args=ctypes.byref(sam)) == sdpa.ATTN_ERR_UNSUPPORTED
     swin = sdpa._SwinArgs(FAKE, 7, 56, 56, 3)

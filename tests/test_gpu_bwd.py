@@ -30,15 +30,16 @@ def _check_table(got, want, what, atol=1e-3, rtol=1e-3):
     assert not bad.any(), f"{what}: {int(bad.sum())} elements off, max |err| {err.max():.3e}"
 
 
-def _bwd_case(w: Workload, seed=None):
+def _bwd_case(w: Workload, seed=None, use_lse=False):
     require_gpu()
     inp = make_inputs(w, seed)
     g = torch.Generator().manual_seed(w.seed + 1000)
     dout = torch.randn(inp.q.shape, generator=g).to(inp.q.dtype)
     q, k, v, do = (x.cuda() for x in (inp.q, inp.k, inp.v, dout))
     bias = gpu_bias(w, inp)
-    out = sdpa.attn_fwd(q, k, v, scale=w.scale, bias=bias)
-    dq, dk, dv, dtab = sdpa.attn_bwd(q, k, v, out, do, scale=w.scale, bias=bias)
+    out, lse = sdpa.attn_fwd_train(q, k, v, scale=w.scale, bias=bias)
+    dq, dk, dv, dtab = sdpa.attn_bwd(q, k, v, out, do, lse=lse if use_lse or w.Nq > 128 or w.Nk > 128 else None,
+                                     scale=w.scale, bias=bias)
     torch.cuda.synchronize()
     assert sdpa.attn_device_status() == sdpa.ATTN_OK
     # D = rowsum(dO * O) from the 16-bit O the kernel was given
@@ -72,3 +73,24 @@ def test_bwd_swin_small_window_and_ragged_grid():
 def test_bwd_swin_full_size():
     """Swin-T stage 1, all 32 images: every gradient against the oracle."""
     _bwd_case(W["swin_t_stage1"])
+
+
+# --------------------------------------------------------- long sequences --
+# Two tensor-core passes (key blocks: dK, dV; query blocks: dQ) from the
+# forward's row log-sum-exp.
+
+@pytest.mark.parametrize("nq,nk,d,dtype", [(300, 300, 64, "bf16"), (200, 513, 40, "fp16"), (257, 129, 80, "bf16"),
+                                           (129, 40, 32, "fp16"), (60, 700, 16, "bf16")])
+def test_bwd_long_no_bias(nq, nk, d, dtype):
+    _bwd_case(Workload("bwd_long", B=1, H=2, Nq=nq, Nk=nk, d=d, dtype=dtype, bias="none", seed=90 + nq + nk))
+
+
+def test_bwd_long_windows_path_with_lse():
+    # a short sequence with d > 64 takes the long path too
+    _bwd_case(Workload("bwd_d80", B=2, H=2, Nq=100, Nk=77, d=80, dtype="bf16", bias="none", seed=95), use_lse=True)
+
+
+def test_bwd_long_sd_self_4096():
+    """Stable Diffusion self-attention rows (4096 tokens, d = 40) on two
+    slices: every gradient against the oracle."""
+    _bwd_case(W["sd_unet_self"].with_(B=1, H=2, seed=96))
