@@ -252,6 +252,30 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
 size_t attn_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, attn_bias_kind bias_kind,
                                const void* bias_args);
 
+/* attn_bwd_noalloc -- attn_bwd without a bias and without a caller
+ * workspace: the same gradients, for callers that cannot allocate device
+ * memory at the point where they run the backward pass -- code whose device
+ * memory all belongs to a pool or fixed budget set up by someone else (an
+ * engine with a preallocated arena, a plugin whose host forbids allocation
+ * while it runs), or code with no allocator at hand.  It allocates nothing:
+ * its scratch (one fp32 value per query row) is a fixed array inside the
+ * library, 4 MiB on every GPU that loads the library, held until the process
+ * exits.  The reference pages have no counterpart to this call.
+ *
+ *  Arguments as for attn_bwd with bias_kind ATTN_BIAS_NONE, no d_bias and no
+ *  workspace.  B * H * Nq must not exceed 2^20 (1048576) query rows; larger
+ *  calls return ATTN_ERR_UNSUPPORTED before any CUDA call.
+ *  The first call on a device looks up the array's device address (with that
+ *  device current); make that first call before any stream capture.
+ *  Every call uses the same array and leaves its last contents there (nothing
+ *  in it needs to start at zero: each call writes what it reads).  Calls
+ *  whose kernels overlap on the GPU -- on different streams, or from several
+ *  threads -- race on the array; order them on one stream.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                     float scale, attn_dtype dtype, void* stream);
+
 /* attn_debug_bias -- test hook for the in-kernel bias builders.
  *
  * Runs the same kernel as attn_fwd with the same arguments but, instead

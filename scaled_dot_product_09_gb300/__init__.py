@@ -21,7 +21,7 @@ import math
 import os
 import threading
 
-__all__ = ["attn_fwd", "attn_fwd_train", "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size", "attn_debug_bias", "attn_device_status", "selftest_wait_timeout", "SwinBias", "SamBias",
+__all__ = ["attn_fwd", "attn_fwd_train", "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size", "attn_bwd_noalloc", "attn_debug_bias", "attn_device_status", "selftest_wait_timeout", "SwinBias", "SamBias",
            "load_library", "AttnError", "ATTN_OK", "ATTN_ERR_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT", "HEADER_SYMBOLS"]
 
@@ -32,6 +32,7 @@ ATTN_SWIN_WINDOWS, ATTN_SWIN_IMAGE = 0, 1
 
 # Every extern "C" function include/sdpa09.h declares.
 HEADER_SYMBOLS = ("attn_fwd", "attn_fwd_train", "attn_fwd_varlen", "attn_bwd", "attn_bwd_workspace_size",
+                  "attn_bwd_noalloc",
                   "attn_debug_bias", "attn_device_status",
                   "attn_selftest_wait_timeout", "attn_last_error", "attn_abi_version")
 ATTN_VARLEN_MAX_SEQ = 128
@@ -123,6 +124,8 @@ def load_library(build: bool = True):
         lib.attn_bwd.restype = i
         lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i, vp]
         lib.attn_bwd_workspace_size.restype = sz
+        lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.attn_bwd_noalloc.restype = i
         lib.attn_debug_bias.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp]
         lib.attn_debug_bias.restype = i
         lib.attn_device_status.argtypes = [vp]
@@ -304,6 +307,28 @@ def attn_bwd(q, k, v, out, dout, lse=None, scale=None, bias=None, stream=None, g
                       _ptr(workspace) if workspace is not None else None, ws_bytes, _stream_ptr(stream))
     _check(lib, rc)
     return dq, dk, dv, d_bias
+
+
+def attn_bwd_noalloc(q, k, v, out, dout, lse=None, scale=None, stream=None, grads=None):
+    """attn_bwd without a bias, for callers that may not allocate device memory
+    while they run it: the library's own fixed scratch (at most 2^20 query
+    rows B * H * Nq) stands in for the workspace.  grads: (dq, dk, dv) buffers
+    to write (allocated here when None).  Calls that overlap on the GPU race on
+    that scratch; returns (dq, dk, dv)."""
+    import torch
+    lib = load_library()
+    B, H, Nq, Nk, d = _shape(q, k, v)
+    for t in (out, dout):
+        if t.shape != q.shape or not t.is_contiguous():
+            raise AttnError(ATTN_ERR_ARG, "out and dout must be contiguous and shaped like q")
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * Nq):
+        raise AttnError(ATTN_ERR_ARG, "lse must be a contiguous fp32 tensor of B * H * Nq values")
+    dq, dk, dv = grads if grads is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib.attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                              _ptr(dv), B, H, Nq, Nk, d, scale, _dtype_code(q), _stream_ptr(stream))
+    _check(lib, rc)
+    return dq, dk, dv
 
 
 def attn_debug_bias(q, k, v, scale=None, bias=None, stream=None):

@@ -111,6 +111,29 @@ int* status_ptr() {
     return ptrs[dev];
 }
 
+// Scratch of attn_bwd_noalloc: the per-row D of the long-sequence backward
+// (4 MiB, rows B * H * Nq <= 2^20).  Every GPU that loads the library holds it
+// until the process exits; all calls share it.
+constexpr int kNoAllocRows = 1 << 20;
+static __device__ __align__(256) float g_bwd_scratch[kNoAllocRows];
+
+// Device address of g_bwd_scratch on the current device, looked up once per
+// device (the host-side name of the array is only a stand-in for it).
+float* noalloc_scratch_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    static float* ptrs[64] = {nullptr};
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= 64) return nullptr;
+    if (!ptrs[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_bwd_scratch) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<float*>(ptr);
+    }
+    return ptrs[dev];
+}
+
 // Generic tiled map with 32-byte swizzle over 16-bit elements.
 int encode(CUtensorMap* m, const void* base, bool bf16, int rank, const uint64_t* dims,
            const uint64_t* strides_bytes, const uint32_t* box) {
@@ -884,6 +907,26 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
              void* stream) {
     return sdpa09::run_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, dtype, bias_kind, bias_args,
                            d_bias, workspace, workspace_bytes, stream);
+}
+
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale,
+                     attn_dtype dtype, void* stream) {
+    using sdpa09::fail;
+    sdpa09::g_last_error.clear();
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return fail(ATTN_ERR_ARG, "B, H, Nq, Nk must be >= 1");
+    const size_t need = sdpa09::bwd_workspace_bytes(B, H, Nq, Nk, d, ATTN_BIAS_NONE, nullptr);
+    if ((int64_t)B * H * Nq > sdpa09::kNoAllocRows || need > sizeof(float) * (size_t)sdpa09::kNoAllocRows)
+        return fail(ATTN_ERR_UNSUPPORTED,
+                    "attn_bwd_noalloc holds scratch for at most %d query rows (B*H*Nq = %lld); use attn_bwd with a "
+                    "workspace", sdpa09::kNoAllocRows, (long long)B * H * Nq);
+    float* scratch = nullptr;
+    if (need > 0) {
+        scratch = sdpa09::noalloc_scratch_ptr();
+        if (!scratch) return fail(ATTN_ERR_CUDA, "no CUDA device / scratch address unavailable");
+    }
+    return sdpa09::run_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, dtype, ATTN_BIAS_NONE,
+                           nullptr, nullptr, scratch, need, stream);
 }
 
 int attn_debug_bias(const void* q, const void* k, const void* v, float* bias_out, int B, int H,
