@@ -243,8 +243,13 @@ def _time_bwd(w: Workload, stream, dev, steps: int):
     for _ in range(n):
         q, k, v, do = (x.to(dev) for x in (inp.q, inp.k, inp.v, dout))
         o, lse = sdpa.attn_fwd_train(q, k, v, scale=w.scale, bias=bias, stream=stream)
-        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
-                 torch.zeros_like(bias.table) if isinstance(bias, sdpa.SwinBias) else None)
+        if isinstance(bias, sdpa.SwinBias):
+            d_bias = torch.zeros_like(bias.table)
+        elif isinstance(bias, sdpa.SamBias):
+            d_bias = torch.zeros((bias.rel_h.shape[0] + bias.rel_w.shape[0], w.d), dtype=torch.float32, device=dev)
+        else:
+            d_bias = None
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), d_bias)
         sets.append((q, k, v, o, lse, do, grads))
     torch.cuda.synchronize()
 

@@ -372,10 +372,14 @@ def attn_bwd(q, k, v, dout, H, scale, bias: Bias | None = None, out=None):
         if kind == "swin":
             np.add.at(d_table[:, s % H], idx.ravel(), dS.ravel())
         elif kind == "sam":
-            dq[s] += np.einsum("ij,ijc->ic", dS, bias._rh[IH] + bias._rw[IW])
-            contrib = (dS[:, :, None] * q[s][:, None, :]).reshape(-1, d)
-            np.add.at(d_rh, IH.ravel(), contrib)
-            np.add.at(d_rw, IW.ravel(), contrib)
+            # the same sums a block of query rows at a time, so that the
+            # [rows, Nk, d] gathers stay small on long sequences
+            for i0 in range(0, Nq, 64):
+                i1 = min(Nq, i0 + 64)
+                dq[s, i0:i1] += np.einsum("ij,ijc->ic", dS[i0:i1], bias._rh[IH[i0:i1]] + bias._rw[IW[i0:i1]])
+                contrib = (dS[i0:i1, :, None] * q[s][i0:i1, None, :]).reshape(-1, d)
+                np.add.at(d_rh, IH[i0:i1].ravel(), contrib)
+                np.add.at(d_rw, IW[i0:i1].ravel(), contrib)
     res.update(dq=dq, dk=dk, dv=dv)
     if kind == "swin":
         res["d_table"] = d_table

@@ -278,10 +278,12 @@ def attn_bwd(q, k, v, out, dout, lse=None, scale=None, bias=None, stream=None, g
     """Gradients of attn_fwd: q/k/v/out/dout [B,H,N,d] contiguous bf16/fp16
     CUDA tensors (out: the forward's output, dout: the gradient with respect
     to it), lse: the fp32 [B,H,Nq] row log-sum-exp from attn_fwd_train (may
-    be None when Nq, Nk <= 128).  Returns (dq, dk, dv, d_bias) with d_bias the
-    fp32 gradient of a SwinBias table, else None.  grads: the four buffers to
-    use instead (d_bias is added to); workspace: a uint8 CUDA tensor of at
-    least attn_bwd_workspace_size bytes (allocated here when None)."""
+    be None when Nq, Nk <= 128 without SAM).  Returns (dq, dk, dv, d_bias) with
+    d_bias the fp32 gradient of a SwinBias table, the pair (d_rel_h, d_rel_w)
+    of a SamBias, else None.  grads: the four buffers to use instead (d_bias is
+    added to; for SAM one fp32 [L_h + L_w, d] tensor); workspace: a uint8 CUDA
+    tensor of at least attn_bwd_workspace_size bytes (allocated here when
+    None)."""
     import torch
     lib = load_library()
     B, H, Nq, Nk, d = _shape(q, k, v)
@@ -294,7 +296,12 @@ def attn_bwd(q, k, v, out, dout, lse=None, scale=None, bias=None, stream=None, g
         dq, dk, dv, d_bias = grads
     else:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        d_bias = torch.zeros_like(bias.table) if isinstance(bias, SwinBias) else None
+        if isinstance(bias, SwinBias):
+            d_bias = torch.zeros_like(bias.table)
+        elif isinstance(bias, SamBias):
+            d_bias = torch.zeros((bias.rel_h.shape[0] + bias.rel_w.shape[0], d), dtype=torch.float32, device=q.device)
+        else:
+            d_bias = None
     kind, _keep, args = _bias_args(bias)
     need = int(lib.attn_bwd_workspace_size(B, H, Nq, Nk, d, kind, args))
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
@@ -306,6 +313,9 @@ def attn_bwd(q, k, v, out, dout, lse=None, scale=None, bias=None, stream=None, g
                       _ptr(d_bias) if d_bias is not None else None,
                       _ptr(workspace) if workspace is not None else None, ws_bytes, _stream_ptr(stream))
     _check(lib, rc)
+    if isinstance(bias, SamBias) and d_bias is not None:
+        n_h = bias.rel_h.shape[0]
+        return dq, dk, dv, (d_bias[:n_h], d_bias[n_h:])
     return dq, dk, dv, d_bias
 
 

@@ -18,18 +18,19 @@
 //
 // SAM decomposed relative position: the bias of (q, k) is
 // rel_h[q][kh] + rel_w[q][kw] (log2 units), read from the pre-pass's table of
-// each query row.  Its gradient: dRelH[q][kh] = sum_kw dS[q][(kh,kw)] (the
-// softmax threads sum their columns of each key row) and dRelW[q][kw] =
-// sum_kh dS[q][(kh,kw)] = dS . E with E[key][kw] = [key mod SW == kw], an
-// MMA into tensor memory (key tiles start on grid rows).  A post-pass turns
-// them into dQ and table gradients.
+// each query row.  Its gradient: dRelH[q][kh] = sum_kw dS[q][(kh,kw)] and
+// dRelW[q][kw] = sum_kh dS[q][(kh,kw)], summed in fp32 by the softmax threads
+// of the query pass (key tiles start on grid rows, so a column's kw is fixed
+// at compile time); rows of dS sum to zero, so these partial sums cancel
+// heavily and are kept out of 16-bit operands.  A post-pass turns them into
+// dQ and table gradients.
 //
 // Warps: 0-7 softmax (thread = query row of lane (warp & 3) * 32 + lane;
 // warps 0-3 take key columns [0,64), warps 4-7 [64,128)), 8 TMA producer,
 // 9 MMA issue (+ TMEM allocation), 10-11 idle.
 //
 // Tensor memory: S [0,128) dP [128,256); key pass dV [256,256+DPAD) dK [..,
-// +DPAD); query pass dQ [256,256+DPAD) dRelW [.., +nE).
+// +DPAD); query pass dQ [256,256+DPAD).
 #pragma once
 #include "attn_bwd_kernel.cuh"
 
@@ -44,16 +45,16 @@ struct BwdLongParams {
     const float* Dws;       // [BH][Nq] rowsum(dO * O)
     const __half* rel;      // SAM: [BH][Nq][rel_stride] fp16 log2 units: rel_h at 0, rel_w at rw0
     float* d_relh;          // SAM query pass: [BH][Nq][k_h] (added to: zeroed by the pre-pass)
-    float* d_relw;          // SAM query pass: [BH][Nq][k_w] (written)
+    float* d_relw;          // SAM query pass: [BH][Nq][k_w] (added to: zeroed by the pre-pass)
     int* status;
     int BH, Nq, Nk, d;
     int n_qb, n_kb;         // query / key blocks per slice
     int n_jobs;
     int kv_w;               // keys per key block (128; 112 on 14-wide SAM grids)
-    int k_h, k_w, rel_stride, rw0, nE;
+    int k_h, k_w, rel_stride, rw0;
     int nst;
     int full_atoms, part;
-    uint32_t off_res, off_ring, off_p, off_ds, off_e, stage_bytes;
+    uint32_t off_res, off_ring, off_p, off_ds, stage_bytes;
     float scale, scale_log2;
     int is_bf16;
 };
@@ -84,7 +85,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     unsigned char* sRing = smem + p.off_ring;  // key pass: (Q_i, dO_i); query pass: (K_j, V_j)
     unsigned char* sP = smem + p.off_p;        // key pass only
     unsigned char* sDS = smem + p.off_ds;
-    unsigned char* sE = smem + p.off_e;        // SAM query pass: E [8 key blocks][nE rows][32 B]
 
     __shared__ uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
     __shared__ uint64_t bar_res_full, bar_res_empty;
@@ -122,28 +122,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         prefetch_tensormap(&tm.dout);
     }
     griddep_wait();
-    if constexpr (kSam && !kKey) {
-        // E: B operand of dRelW += dS.E, K-major (rows kw, 16 keys per block):
-        // a one at key column c of row kw when c mod SW == kw and c < kv_w
-        const uint32_t one = to_half_bits(1.0f, bf);
-        for (int c = tid; c < 8 * p.nE * 2; c += kBwdThreads) {  // 16-byte chunks: block, row, half
-            const int blk = c / (p.nE * 2), row = (c / 2) % p.nE, hh = c & 1;
-            uint32_t pk[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                uint32_t w = 0;
-#pragma unroll
-                for (int z = 0; z < 2; ++z) {
-                    const int key = blk * 16 + hh * 8 + 2 * u + z;
-                    if (key < p.kv_w && key % SW == row) w |= one << (16 * z);
-                }
-                pk[u] = w;
-            }
-            *reinterpret_cast<uint4*>(sE + blk * (p.nE * 32) + (uint32_t)(row * 32 + ((hh ^ ((row >> 2) & 1)) << 4))) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-        fence_proxy_async_smem();
-    }
     if (warp == kMmaWarp) {
         tmem_alloc(&tmem_base_sh, kTmemCols);
         tmem_relinquish();
@@ -204,8 +182,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, kBlockN, false);
             const uint32_t idesc_g = make_idesc_f16_mn(bf, kBlockM, DPAD, true, true);   // dV, dK: A MN-major
             const uint32_t idesc_q = make_idesc_f16_mn(bf, kBlockM, DPAD, false, true);  // dQ: A K-major
-            const uint32_t idesc_e = make_idesc_f16(bf, kBlockM, p.nE > 0 ? p.nE : 16, false);
-            const uint32_t aRes = smem_u32(sRes), aP = smem_u32(sP), aDS = smem_u32(sDS), aE = smem_u32(sE);
+            const uint32_t aRes = smem_u32(sRes), aP = smem_u32(sP), aDS = smem_u32(sDS);
             auto waitb = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
                 if (!mbar_wait(bar, parity, abort_flag, code)) return false;
                 tc_fence_after();
@@ -253,12 +230,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         for (int ks = 0; ks < 8; ++ks)  // dQ += dS.K over 16 keys per step
                             mma_ss(tA0, kdesc(aDS + ks * (kBlockM * 32)), vdesc(aK + ks * 512), idesc_q,
                                    (acc || ks > 0) ? 1u : 0u);
-                        if constexpr (kSam) {
-#pragma unroll
-                            for (int ks = 0; ks < 8; ++ks)  // dRelW += dS.E
-                                mma_ss(tA1, kdesc(aDS + ks * (kBlockM * 32)), kdesc(aE + ks * (p.nE * 32)), idesc_e,
-                                       (acc || ks > 0) ? 1u : 0u);
-                        }
                     }
                     mma_commit(&bar_pfree);
                     mma_commit(&bar_empty[st]);
@@ -295,33 +266,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 Dq = q_ok ? p.Dws[ri] : 0.f;
             };
             if (!kKey) row_stats(blk * kBlockM + r);
+            // SAM query pass: the row's dRelW partial sums (this thread's columns)
+            float dw[kSam && !kKey ? (SW > 0 ? SW : 1) : 1];
+#pragma unroll
+            for (int c = 0; c < (int)(sizeof(dw) / sizeof(float)); ++c) dw[c] = 0.f;
             for (int it = 0; it < n_inner; ++it, ++u) {
                 if (kKey) row_stats(it * kBlockM + r);
                 const int key0 = kKey ? blk * p.kv_w : it * p.kv_w;
                 const int nvalid = min(p.kv_w, p.Nk - key0);  // key columns of this tile
-                // SAM bias terms of the row for this tile's keys (log2 units)
-                float rw[SW > 0 ? (SW < 64 ? SW : 64) : 1];
+                // SAM bias terms of the row for this tile's keys (log2 units):
+                // rel_w of every key column as fp16 pairs, rel_h of the key rows
+                constexpr int kRW = SW > 0 ? (SW + 1) / 2 : 1;
+                __half2 rw2[kRW];
                 float rh[SW > 0 ? (SW < 64 ? 8 : 1) : 1];
                 if constexpr (kSam) {
                     const __half* rel = p.rel + ((size_t)slice * p.Nq + (q_ok ? q : 0)) * p.rel_stride;
                     const int kh0 = key0 / SW;
+#pragma unroll
+                    for (int j8 = 0; j8 < (SW + 7) / 8; ++j8) {
+                        const uint4 u4 = *reinterpret_cast<const uint4*>(rel + p.rw0 + 8 * j8);
+                        const uint32_t w4[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (4 * j8 + e < kRW) rw2[4 * j8 + e] = *reinterpret_cast<const __half2*>(&w4[e]);
+                    }
                     if constexpr (SW == 64) {
-#pragma unroll
-                        for (int j8 = 0; j8 < 8; ++j8) {
-                            float f[8];
-                            half8(rel + p.rw0 + 8 * j8, f);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) rw[8 * j8 + e] = f[e];
-                        }
                         rh[0] = __half2float(rel[min(kh0 + half, p.k_h - 1)]);
                     } else {
                         float f[8];
-                        half8(rel + p.rw0, f);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) rw[e] = f[e];
-                        half8(rel + p.rw0 + 8, f);
-#pragma unroll
-                        for (int e = 0; e < SW - 8; ++e) rw[8 + e] = f[e];
                         half8(rel + kh0, f);  // key rows kh0..kh0+7 (kh0 is a multiple of 8)
 #pragma unroll
                         for (int e = 0; e < 8; ++e) rh[e] = f[e];
@@ -330,19 +302,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 __syncwarp();
                 if (!__all_sync(0xffffffffu, mbar_wait(&bar_s, u & 1, abort_flag, kStatusWaitS))) { ok = false; break; }
                 tc_fence_after();
-                float xs[64], dp[64];
+                float xs[64];
                 {
                     uint32_t v[64];
                     tmem_ld64(tS + lane_base + c0, v);
 #pragma unroll
                     for (int c = 0; c < 64; ++c) xs[c] = __uint_as_float(v[c]);
-                    tmem_ld64(tDP + lane_base + c0, v);
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) dp[c] = __uint_as_float(v[c]);
                 }
-                tc_fence_before();
-                warp_arrive(&bar_sfree);
-                // P = 2^(s scale log2e + bias - lse), dS = P (dP - D); zero outside the tile
+                // P = 2^(s scale log2e + bias - lse), zero outside the tile; then
+                // dS = P (dP - D), with dP read once P is done
+                float dp[64];
                 auto body = [&](auto hc) {
                     constexpr int H0 = decltype(hc)::value;  // this thread's column half
 #pragma unroll
@@ -350,28 +319,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         const int col = 64 * H0 + c;
                         float b = 0.f;
                         if constexpr (kSam) {
-                            if constexpr (SW == 64) b = rh[0] + rw[c];
-                            else b = rh[col / SW < 8 ? col / SW : 7] + rw[col % SW];
+                            const float2 rwf = __half22float2(rw2[(col % SW) / 2]);
+                            const float rwv = ((col % SW) & 1) ? rwf.y : rwf.x;
+                            if constexpr (SW == 64) b = rh[0] + rwv;
+                            else b = rh[col / SW < 8 ? col / SW : 7] + rwv;
                         }
                         const bool valid = q_ok && col < nvalid;
-                        const float pv = valid ? ex2_approx(fmaf(xs[c], p.scale_log2, b - lse2)) : 0.f;
-                        xs[c] = pv;
-                        dp[c] = pv * (dp[c] - Dq);
+                        xs[c] = valid ? ex2_approx(fmaf(xs[c], p.scale_log2, b - lse2)) : 0.f;
                     }
+                    {
+                        uint32_t v[64];
+                        tmem_ld64(tDP + lane_base + c0, v);
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) dp[c] = xs[c] * (__uint_as_float(v[c]) - Dq);
+                    }
+                    tc_fence_before();
+                    warp_arrive(&bar_sfree);
                     if constexpr (kSam && !kKey) {
                         // dRelH: the row's dS summed over each key row of its columns
+                        // (a key row can straddle the two column halves: atomic adds);
+                        // dRelW: summed per key column over the job's key rows
                         if (q_ok) {
                             const int kh0 = key0 / SW;
                             float* dst = p.d_relh + ((size_t)slice * p.Nq + q) * p.k_h;
-                            if constexpr (SW == 64) {
-                                float a = 0.f;
+                            constexpr int kr0 = (64 * H0) / SW, kr1 = (64 * H0 + 63) / SW;
 #pragma unroll
-                                for (int c = 0; c < 64; ++c) a += dp[c];
-                                if (kh0 + H0 < p.k_h) atomicAdd(dst + kh0 + H0, a);
-                            } else {
-                                constexpr int kr0 = (64 * H0) / SW, kr1 = (64 * H0 + 63) / SW;
-#pragma unroll
-                                for (int kr = kr0; kr <= kr1 && kr < 8; ++kr) {
+                            for (int kr = kr0; kr <= kr1; ++kr) {
+                                if (kr < (SW == 64 ? 2 : 8)) {
                                     float a = 0.f;
 #pragma unroll
                                     for (int c = 0; c < 64; ++c)
@@ -380,6 +354,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 }
                             }
                         }
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) dw[(64 * H0 + c) % SW] += dp[c];
                     }
                 };
                 if (half == 0) body(std::integral_constant<int, 0>{});
@@ -466,16 +442,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             }
                         }
                     }
-                } else if constexpr (kSam) {
-                    // dRelW row: sum over key rows of dS per key column
-                    constexpr int kE = SW == 64 ? 64 : 16;
-                    uint32_t v[kE];
-                    tmem_ld_cols<kE>(tA1 + lane_base, v);
+                }
+                if constexpr (kSam) {
+                    // dRelW row: both column halves add their sums
                     if (q_ok) {
                         float* dst = p.d_relw + ((size_t)slice * p.Nq + q) * p.k_w;
 #pragma unroll
-                        for (int c = 0; c < kE; ++c)
-                            if (c < p.k_w) dst[c] = __uint_as_float(v[c]);
+                        for (int c = 0; c < SW; ++c)
+                            if (c < p.k_w) atomicAdd(dst + c, dw[c]);
                     }
                 }
             }

@@ -34,11 +34,22 @@ struct BwdPrepParams {
     const void *rel_h, *rel_w;
     __half* rel;
     float* d_relh;
+    float* d_relw;
     int s_h, s_w, rel_stride, rw0;
 };
 cudaError_t launch_bwd_prep(const BwdPrepParams& p, bool sam, int nsm, cudaStream_t stream);
 cudaError_t launch_bwd_long(int dpad, int mode, int sw, const BwdMaps& tm, const BwdLongParams& p, int grid,
                             size_t smem, cudaStream_t stream);
+struct BwdSamPostParams {
+    const float* dq32;
+    const float* d_relh;
+    const float* d_relw;
+    const void *q, *rel_h, *rel_w;
+    void* dq;
+    float* d_bias;
+    int rows, Nq, d, S, BH, groups, is_bf16;
+};
+cudaError_t launch_bwd_sam_post(const BwdSamPostParams& p, int nsm, cudaStream_t stream);
 
 namespace {
 
@@ -615,7 +626,7 @@ size_t bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d, attn_bias_kind b
 // the key pass (dK, dV) and the query pass (dQ) on the tensor cores.
 int run_bwd_long(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
                  void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, attn_dtype dtype,
-                 const attn_sam_args* sam, void* workspace, size_t workspace_bytes, void* stream) {
+                 const attn_sam_args* sam, float* d_bias, void* workspace, size_t workspace_bytes, void* stream) {
     const int dpad = dpad_for(d);
     if (dpad > 80) return fail(ATTN_ERR_UNSUPPORTED, "backward for sequences over 128 tokens needs d <= 80");
     if (!lse)
@@ -647,7 +658,18 @@ int run_bwd_long(const void* q, const void* k, const void* v, const void* out, c
     pp.Nq = Nq;
     pp.d = d;
     pp.is_bf16 = bf;
-    cudaError_t e = launch_bwd_prep(pp, false, nsm, st);
+    if (sam) {
+        pp.rel_h = sam->rel_h;
+        pp.rel_w = sam->rel_w;
+        pp.rel = reinterpret_cast<__half*>(wsb + ws.rel);
+        pp.d_relh = reinterpret_cast<float*>(wsb + ws.drh);
+        pp.d_relw = reinterpret_cast<float*>(wsb + ws.drw);
+        pp.s_h = sam->q_h;
+        pp.s_w = sam->q_w;
+        pp.rel_stride = stride;
+        pp.rw0 = rw0;
+    }
+    cudaError_t e = launch_bwd_prep(pp, sam != nullptr, nsm, st);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
 
     BwdLongParams p;
@@ -662,7 +684,19 @@ int run_bwd_long(const void* q, const void* k, const void* v, const void* out, c
     p.Nq = Nq;
     p.Nk = Nk;
     p.d = d;
-    p.kv_w = kBlockN;
+    const int sw = sam ? sam->q_w : 0;
+    // key tiles start on grid rows: 112 keys (8 rows) on the 14-wide grid
+    p.kv_w = sw == 14 ? 112 : kBlockN;
+    if (sam) {
+        p.rel = pp.rel;
+        p.rel_stride = stride;
+        p.rw0 = rw0;
+        p.k_h = sam->k_h;
+        p.k_w = sam->k_w;
+        p.dq32 = reinterpret_cast<float*>(wsb + ws.dq32);
+        p.d_relh = pp.d_relh;
+        p.d_relw = reinterpret_cast<float*>(wsb + ws.drw);
+    }
     p.n_qb = (Nq + kBlockM - 1) / kBlockM;
     p.n_kb = (Nk + p.kv_w - 1) / p.kv_w;
     p.scale = scale;
@@ -688,11 +722,31 @@ int run_bwd_long(const void* q, const void* k, const void* v, const void* out, c
         p.off_ring = (uint32_t)(2 * tile);
         p.off_p = p.off_ring + (uint32_t)(p.nst * p.stage_bytes);
         p.off_ds = p.off_p + (mode == kBwdKeyPass ? (uint32_t)(8 * kBlockM * 32) : 0u);
-        p.off_e = p.off_ds + (uint32_t)(8 * kBlockM * 32);
-        const size_t smem = p.off_e + 1024;
+        const size_t smem = p.off_ds + (size_t)8 * kBlockM * 32 + 1024;
         p.n_jobs = (int)(BH * (mode == kBwdKeyPass ? p.n_kb : p.n_qb));
         const int grid = std::min(p.n_jobs, nsm);
-        e = launch_bwd_long(dpad, mode, 0, tm, p, grid, smem, st);
+        e = launch_bwd_long(dpad, mode, sw, tm, p, grid, smem, st);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    }
+    if (sam) {
+        BwdSamPostParams sp;
+        memset(&sp, 0, sizeof(sp));
+        sp.dq32 = p.dq32;
+        sp.d_relh = p.d_relh;
+        sp.d_relw = p.d_relw;
+        sp.q = q;
+        sp.rel_h = sam->rel_h;
+        sp.rel_w = sam->rel_w;
+        sp.dq = dq;
+        sp.d_bias = d_bias;
+        sp.rows = (int)rows;
+        sp.Nq = Nq;
+        sp.d = d;
+        sp.S = sw;
+        sp.BH = (int)BH;
+        sp.groups = (int)std::min<int64_t>(BH, std::max(1, 4 * nsm / sw));
+        sp.is_bf16 = bf;
+        e = launch_bwd_sam_post(sp, nsm, st);
         if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     }
     static const bool debug_env = getenv("SDPA09_DEBUG") && getenv("SDPA09_DEBUG")[0] == '1';
@@ -761,14 +815,28 @@ int run_bwd(const void* q, const void* k, const void* v, const void* out, const 
         fast_div_params((uint32_t)nW, p.fd_w);
         fast_div_params((uint32_t)p.n_ww, p.fd_ww);
     } else if (bias_kind == ATTN_BIAS_SAM_RELPOS) {
-        return fail(ATTN_ERR_UNSUPPORTED, "SAM backward not built yet");
+        const attn_sam_args* a = static_cast<const attn_sam_args*>(bias_args);
+        if (!a || !a->rel_h || !a->rel_w) return fail(ATTN_ERR_ARG, "SAM bias needs attn_sam_args with rel_h, rel_w");
+        if (!d_bias) return fail(ATTN_ERR_ARG, "SAM backward needs d_bias (the rel_h and rel_w gradients)");
+        if (a->q_h * a->q_w != Nq || a->k_h * a->k_w != Nk)
+            return fail(ATTN_ERR_ARG, "SAM needs Nq == q_h*q_w and Nk == k_h*k_w");
+        const int S = a->q_w;
+        const int lh = a->rel_h_len ? a->rel_h_len : 2 * a->q_h - 1, lw = a->rel_w_len ? a->rel_w_len : 2 * a->q_w - 1;
+        if (a->q_h != S || a->k_h != S || a->k_w != S || (S != 14 && S != 64) || lh != 2 * S - 1 || lw != 2 * S - 1)
+            return fail(ATTN_ERR_UNSUPPORTED,
+                        "the SAM backward takes square 14 x 14 or 64 x 64 grids with tables of 2 * side - 1 rows");
+        if (dpad != 64 && dpad != 80) return fail(ATTN_ERR_UNSUPPORTED, "the SAM backward takes 48 < d <= 80");
+        if (!aligned16(a->rel_h) || !aligned16(a->rel_w)) return fail(ATTN_ERR_ARG, "rel_h/rel_w must be 16-byte aligned");
+        if ((reinterpret_cast<uintptr_t>(d_bias) & 3u) != 0) return fail(ATTN_ERR_ARG, "d_bias must be 4-byte aligned");
+        return run_bwd_long(q, k, v, out, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, dtype, a, d_bias, workspace,
+                            workspace_bytes, stream);
     } else if (bias_kind != ATTN_BIAS_NONE) {
         return fail(ATTN_ERR_ARG, "unknown bias kind %d", (int)bias_kind);
     }
     if (!bwd_is_windows(Nq, Nk, d)) {
         if (swin) return fail(ATTN_ERR_UNSUPPORTED, "SWIN backward with d > 64");
-        return run_bwd_long(q, k, v, out, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, dtype, nullptr, workspace,
-                            workspace_bytes, stream);
+        return run_bwd_long(q, k, v, out, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, dtype, nullptr, nullptr,
+                            workspace, workspace_bytes, stream);
     }
     // packed windows: g slices of up to SL tokens share a 128-row tile
     const int nmax = std::max(Nq, Nk);

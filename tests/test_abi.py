@@ -192,7 +192,9 @@ def test_bwd_argument_checks(lib):
     assert lib.attn_bwd_workspace_size(64, 3, 49, 49, 32, 0, None) == 0     # windows need none
     assert _bwd(lib, d=88) == sdpa.ATTN_ERR_UNSUPPORTED                     # d > 80
     sam = sdpa._SamArgs(FAKE, FAKE, 7, 7, 7, 7)
-    assert _bwd(lib, kind=2, args=ctypes.byref(sam)) == sdpa.ATTN_ERR_UNSUPPORTED
+    assert _bwd(lib, kind=2, args=ctypes.byref(sam)) == sdpa.ATTN_ERR_ARG          # no d_bias
+    assert _bwd(lib, kind=2, args=ctypes.byref(sam), d_table=FAKE) == sdpa.ATTN_ERR_UNSUPPORTED  # 7 x 7 grid
+    assert b"14 x 14 or 64 x 64" in lib.attn_last_error()
     swin = sdpa._SwinArgs(FAKE, 7, 56, 56, 3)
     assert _bwd(lib, kind=1, args=ctypes.byref(swin)) == sdpa.ATTN_ERR_ARG    # no d_table
     assert b"d_bias" in lib.attn_last_error()

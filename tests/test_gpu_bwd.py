@@ -49,6 +49,9 @@ def _bwd_case(w: Workload, seed=None, use_lse=False):
         compare(flat64(t.cpu()), want[name], what=f"{w.name} {name}")
     if w.bias == "swin":
         _check_table(dtab.cpu().double().numpy(), want["d_table"], f"{w.name} d_table")
+    if w.bias == "sam":
+        _check_table(dtab[0].cpu().double().numpy(), want["d_rel_h"], f"{w.name} d_rel_h")
+        _check_table(dtab[1].cpu().double().numpy(), want["d_rel_w"], f"{w.name} d_rel_w")
 
 
 def test_bwd_no_bias_short():
@@ -94,3 +97,16 @@ def test_bwd_long_sd_self_4096():
     """Stable Diffusion self-attention rows (4096 tokens, d = 40) on two
     slices: every gradient against the oracle."""
     _bwd_case(W["sd_unet_self"].with_(B=1, H=2, seed=96))
+
+
+# ------------------------------------------------------------- SAM rel-pos --
+# dQ, dK, dV and the gradients of both rel-pos tables (d_rel_h, d_rel_w).
+
+def test_bwd_sam_window_14x14():
+    """SAM windowed attention (14 x 14 windows, 196 tokens, d = 80)."""
+    _bwd_case(W["sam_vith_window"].with_(B=2, H=2, seed=97), use_lse=True)
+
+
+def test_bwd_sam_global_64x64():
+    """SAM global attention on the 64 x 64 grid (4096 tokens, d = 80), one slice."""
+    _bwd_case(W["sam_vith_global"].with_(B=1, H=1, seed=98), use_lse=True)
