@@ -38,14 +38,21 @@ namespace sdpa09 {
 
 enum BwdLongMode { kBwdKeyPass = 0, kBwdQueryPass = 1 };
 
+struct BwdPrepParams {
+    const void *o, *dout;  // [BH][Nq][d] 16-bit
+    float* Dws;            // [BH][Nq] rowsum(dO * O)
+    int rows, d, is_bf16;
+};
+cudaError_t launch_bwd_prep(const BwdPrepParams& p, int nsm, cudaStream_t stream);
+
 struct BwdLongParams {
     void *dq, *dk, *dv;     // 16-bit outputs [BH][N][d]
     float* dq32;            // SAM query pass: scale * dS.K in fp32 [BH][Nq][d] (the post-pass adds the rel terms)
     const float* lse;       // [BH][Nq] natural log
     const float* Dws;       // [BH][Nq] rowsum(dO * O)
     const __half* rel;      // SAM: [BH][Nq][rel_stride] fp16 log2 units: rel_h at 0, rel_w at rw0
-    float* d_relh;          // SAM query pass: [BH][Nq][k_h] (added to: zeroed by the pre-pass)
-    float* d_relw;          // SAM query pass: [BH][Nq][k_w] (added to: zeroed by the pre-pass)
+    float* d_relh;          // SAM query pass: [BH][Nq][k_h] (64-wide grids: stored; 14-wide: added to rows the pre-pass cleared)
+    float* d_relw;          // SAM query pass: [2][BH][Nq][k_w], one array per column half (stored)
     int* status;
     int BH, Nq, Nk, d;
     int n_qb, n_kb;         // query / key blocks per slice
@@ -337,7 +344,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     warp_arrive(&bar_sfree);
                     if constexpr (kSam && !kKey) {
                         // dRelH: the row's dS summed over each key row of its columns
-                        // (a key row can straddle the two column halves: atomic adds);
+                        // (64-wide grids: one key row per column half, stored; on 14-wide
+                        // grids a key row can straddle the halves: atomic adds);
                         // dRelW: summed per key column over the job's key rows
                         if (q_ok) {
                             const int kh0 = key0 / SW;
@@ -350,7 +358,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                                     for (int c = 0; c < 64; ++c)
                                         if ((64 * H0 + c) / SW == kr) a += dp[c];
-                                    if (kh0 + kr < p.k_h) atomicAdd(dst + kh0 + kr, a);
+                                    if constexpr (SW == 64) dst[kh0 + kr] = a;
+                                    else if (kh0 + kr < p.k_h) atomicAdd(dst + kh0 + kr, a);
                                 }
                             }
                         }
@@ -444,12 +453,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                 }
                 if constexpr (kSam) {
-                    // dRelW row: both column halves add their sums
+                    // dRelW row: each column half stores its sums in its own array
                     if (q_ok) {
-                        float* dst = p.d_relw + ((size_t)slice * p.Nq + q) * p.k_w;
+                        float* dst = p.d_relw + (((size_t)half * p.BH + slice) * p.Nq + q) * p.k_w;
+                        if constexpr (SW % 4 == 0) {
 #pragma unroll
-                        for (int c = 0; c < SW; ++c)
-                            if (c < p.k_w) atomicAdd(dst + c, dw[c]);
+                            for (int c = 0; c < SW; c += 4)
+                                *reinterpret_cast<float4*>(dst + c) = make_float4(dw[c], dw[c + 1], dw[c + 2], dw[c + 3]);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < SW; c += 2) *reinterpret_cast<float2*>(dst + c) = make_float2(dw[c], dw[c + 1]);
+                        }
                     }
                 }
             }

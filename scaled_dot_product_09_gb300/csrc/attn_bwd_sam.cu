@@ -1,0 +1,540 @@
+// attn_bwd_sam.cu -- the SAM decomposed rel-pos parts of the long-sequence
+// backward, on the CUDA cores in fp32 (every product has 16-bit inputs or
+// fp32 sums as operands and is accumulated in fp32; nothing is rounded to
+// 16 bits before the stored result):
+//
+//   rel pre-pass:  rel_h[q][kh] = Q_q . R_h[qh - kh + S - 1] and
+//                  rel_w[q][kw] = Q_q . R_w[qw - kw + S - 1], in log2 units,
+//                  stored fp16 for the two tensor-core passes to add to the
+//                  scores;
+//   dQ post-pass:  dQ_q = (scale dS.K)_q + sum_kh dRelH[q][kh] R_h[qh - kh + S - 1]
+//                                        + sum_kw dRelW[q][kw] R_w[qw - kw + S - 1];
+//   table pass:    dR_h[j] = sum of dRelH[q][kh] Q_q over the (q, kh) with
+//                  qh - kh + S - 1 = j, and dR_w[j] alike with qw - kw + S - 1 = j.
+//
+// (Segment Anything, image encoder: the decomposed relative position terms
+// added to the attention logits, and their gradients by the chain rule.)
+//
+// The grids are square: side S = 14 or 64, tables of 2 S - 1 rows.  Work is
+// cut in blocks of 64 query rows of one slice: one grid row when S = 64; four
+// grid rows, each padded from 14 to 16 columns, when S = 14 (block row r is
+// grid row bp * LPC + r / QWP, grid column r % QWP; padded rows are zero).
+// Every product is a small GEMM tiled in registers: a thread keeps an 8 x 4
+// (pre-pass, dQ) or 4 x 4 (tables) tile of outputs and reads both operands
+// as float4 (or four 16-bit values) from shared memory.  For the w terms the
+// index j = qw - kw + S - 1 turns the skew into a band that is dense in j:
+// the pre-pass forms Q_q . R_w[j] over the band of its rows and scatters each
+// value to its kw, and the post-passes spread dRelW[q][kw] to row j of a
+// zero-filled matrix before multiplying.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "attn_bwd_sam.cuh"
+
+namespace sdpa09 {
+
+namespace {
+
+constexpr float kLog2eSam = 1.4426950408889634f;
+
+template <int S>
+struct SamGeom {
+    static_assert(S == 14 || S == 64, "SAM backward grids are 14 x 14 or 64 x 64");
+    static constexpr int QWP = S > 16 ? 64 : 16;    // block rows per grid row
+    static constexpr int LPC = 64 / QWP;            // grid rows per block
+    static constexpr int NBP = (S + LPC - 1) / LPC; // blocks per slice
+    static constexpr int NT = 2 * S - 1;            // table rows
+    static constexpr int G8 = QWP / 8;              // groups of 8 block rows per grid row
+    // pre-pass: j-groups of 4 per (terms, row group); table columns staged
+    __host__ __device__ static constexpr int jw_last(int g) { return (8 * g + 7 + S - 1) / 4; }
+    __host__ __device__ static constexpr int jh_last(int qh) { return (qh + S - 1) / 4; }
+    __host__ __device__ static constexpr int cmax(int a, int b) { return a > b ? a : b; }
+    __host__ __device__ static constexpr int nj() {
+        int m = 0;
+        for (int g = 0; g < G8; ++g) m = cmax(m, jw_last(g) - 2 * g + 1);
+        for (int qh = 0; qh < S; ++qh) m = cmax(m, jh_last(qh) - qh / 4 + 1);
+        return m;
+    }
+    static constexpr int NJ = nj();
+    static constexpr int JP = 4 * (cmax(jw_last(G8 - 1), jh_last(S - 1)) + 1);
+    static constexpr int kRelThreads = LPC * 2 * G8 * NJ;
+    // dQ post-pass: rows j of the spread dRelW matrix
+    static constexpr int JW = QWP + S - 1;
+
+    // block row r of block (s, bp): global query row and whether it exists
+    __device__ static bool row(int s, int bp, int r, int Nq, int& grow) {
+        const int l = r / QWP, qw = r - l * QWP, qh = bp * LPC + l;
+        grow = s * Nq + qh * S + qw;
+        return qw < S && qh < S;
+    }
+};
+
+template <bool BF>
+__device__ __forceinline__ float4 ld4h(const uint16_t* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    if constexpr (BF) {
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                           __uint_as_float(u.y & 0xffff0000u));
+    } else {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+}
+
+template <bool BF>
+__device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        if constexpr (BF) {
+            f[2 * e] = __uint_as_float(w[e] << 16);
+            f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        } else {
+            const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+            f[2 * e] = t.x;
+            f[2 * e + 1] = t.y;
+        }
+    }
+}
+
+template <bool BF>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if constexpr (BF) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+__device__ __forceinline__ void fma8x4(float (&acc)[8][4], const float4 a0, const float4 a1, const float4 b) {
+    const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][e] = fmaf(a[i], bb[e], acc[i][e]);
+}
+
+__device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 a, const float4 b) {
+    const float aa[4] = {a.x, a.y, a.z, a.w};
+    const float bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][e] = fmaf(aa[i], bb[e], acc[i][e]);
+}
+
+// ------------------------------------------------------------ rel pre-pass
+// A thread owns one task of the block: (grid row l of the block, terms h or
+// w, group g of 8 block rows, j-group jg of 4 table rows).  Q is staged as
+// fp32 [c][64 block rows], the tables as 16-bit [terms][c][JP] (j fastest),
+// and the block's output rows as fp16 [64][rel_stride] before a coalesced
+// copy out.
+template <int S, bool BF>
+__global__ void __launch_bounds__(SamGeom<S>::kRelThreads, 2) bwd_sam_rel_kernel(const SamBwdParams p) {
+    using G = SamGeom<S>;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int d = p.d, stride = p.rel_stride;
+    uint16_t* sR = reinterpret_cast<uint16_t*>(smem);
+    float* sQ = reinterpret_cast<float*>(smem + (size_t)2 * d * G::JP * 2);
+    __half* sO = reinterpret_cast<__half*>(smem + (size_t)2 * d * G::JP * 2 + (size_t)d * 64 * 4);
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const uint16_t* tab_h = static_cast<const uint16_t*>(p.rel_h);
+    const uint16_t* tab_w = static_cast<const uint16_t*>(p.rel_w);
+    for (int i = tid; i < 2 * d * G::JP; i += nt) {
+        const int part = i / (d * G::JP), rem = i - part * (d * G::JP), c = rem / G::JP, j = rem - c * G::JP;
+        sR[i] = j < G::NT ? (part ? tab_w : tab_h)[j * d + c] : (uint16_t)0;
+    }
+    const int jj = tid % G::NJ;
+    int rest = tid / G::NJ;
+    const int g = rest % G::G8;
+    rest /= G::G8;
+    const int part = rest & 1, l = rest >> 1;  // part 0: h terms, 1: w terms
+    const uint16_t* q16 = static_cast<const uint16_t*>(p.q);
+    const int nblk = p.BH * G::NBP;
+    for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        const int s = blk / G::NBP, bp = blk - s * G::NBP;
+        __syncthreads();  // the previous block is done with sQ and sO
+        for (int i = tid; i < 64 * (d / 8); i += nt) {
+            const int r = i & 63, c8 = i >> 6;
+            int grow;
+            float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (G::row(s, bp, r, p.Nq, grow))
+                unpack8<BF>(*reinterpret_cast<const uint4*>(q16 + (size_t)grow * d + c8 * 8), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sQ[(c8 * 8 + e) * 64 + r] = f[e];
+        }
+        for (int i = tid; i < 64 * stride / 2; i += nt) reinterpret_cast<uint32_t*>(sO)[i] = 0u;
+        __syncthreads();
+        const int qh = bp * G::LPC + l;
+        int jg0, cnt;
+        if (part) {
+            jg0 = 2 * g;
+            cnt = G::jw_last(g) - jg0 + 1;
+        } else {
+            jg0 = qh / 4;
+            cnt = G::jh_last(qh) - jg0 + 1;
+        }
+        if (qh < S && jj < cnt) {
+            const int jg = jg0 + jj;
+            float acc[8][4];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+            const float* qa = sQ + l * G::QWP + 8 * g;
+            const uint16_t* rb = sR + (size_t)part * d * G::JP + 4 * jg;
+#pragma unroll 4
+            for (int c = 0; c < d; ++c) {
+                const float4 a0 = *reinterpret_cast<const float4*>(qa + c * 64);
+                const float4 a1 = *reinterpret_cast<const float4*>(qa + c * 64 + 4);
+                fma8x4(acc, a0, a1, ld4h<BF>(rb + c * G::JP));
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int qw = 8 * g + i;
+                if (qw < S) {
+                    __half* orow = sO + (l * G::QWP + qw) * stride + (part ? p.rw0 : 0);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 4 * jg + e;
+                        const int kk = (part ? qw : qh) + S - 1 - j;
+                        if (kk >= 0 && kk < S) orow[kk] = __float2half_rn(acc[i][e] * kLog2eSam);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        const int cpr = stride / 8;  // 16-byte chunks per row
+        for (int i = tid; i < 64 * cpr; i += nt) {
+            const int r = i / cpr, ch = i - r * cpr;
+            int grow;
+            if (G::row(s, bp, r, p.Nq, grow))
+                *reinterpret_cast<uint4*>(p.rel + (size_t)grow * stride + ch * 8) =
+                    *reinterpret_cast<const uint4*>(sO + r * stride + ch * 8);
+        }
+        if constexpr (S != 64) {
+            // on 14-wide grids a key row can straddle the query pass's two column
+            // halves, so it adds its dRelH sums into rows cleared here
+            for (int i = tid; i < 64 * S; i += nt) {
+                const int r = i / S, kh = i - r * S;
+                int grow;
+                if (G::row(s, bp, r, p.Nq, grow)) p.d_relh[(size_t)grow * S + kh] = 0.f;
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------------- dQ post-pass
+// 160 threads: group g of 8 block rows (tid / 20) x group cg of 4 columns of
+// d (tid % 20).  Staged per block: dRelH as [kh][block row] and the spread
+// dRelW as [j][block row] (row pitch kAP floats), both fp32; the tables as
+// 16-bit [terms][j][d] for the CTA's life.
+constexpr int kAP = 68;  // pitch: 16-byte rows, and the staging stores below hit distinct banks
+constexpr int kDqThreads = 160;
+
+template <int S, bool BF>
+__global__ void __launch_bounds__(kDqThreads, S == 64 ? 2 : 4) bwd_sam_dq_kernel(const SamBwdParams p) {
+    using G = SamGeom<S>;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int d = p.d;
+    uint16_t* sT = reinterpret_cast<uint16_t*>(smem);
+    float* sAh = reinterpret_cast<float*>(smem + (size_t)2 * G::NT * d * 2);
+    float* sAw = sAh + S * kAP;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    {
+        const uint16_t* tab_h = static_cast<const uint16_t*>(p.rel_h);
+        const uint16_t* tab_w = static_cast<const uint16_t*>(p.rel_w);
+        for (int i = tid; i < G::NT * d; i += nt) {
+            sT[i] = tab_h[i];
+            sT[G::NT * d + i] = tab_w[i];
+        }
+    }
+    const int g = tid / 20, cg = tid - g * 20;
+    const bool act = 4 * cg < d;
+    const int r0 = 8 * g, l = r0 / G::QWP, qw0 = r0 - l * G::QWP;
+    const size_t rows = (size_t)p.BH * p.Nq;
+    const float* drw1 = p.d_relw + rows * S;
+    const int nblk = p.BH * G::NBP;
+    for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        const int s = blk / G::NBP, bp = blk - s * G::NBP;
+        const int qh = bp * G::LPC + l;
+        __syncthreads();  // the previous block is done with sAh and sAw
+        for (int i = tid; i < G::JW * kAP / 4; i += nt) reinterpret_cast<float4*>(sAw)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (S == 64) {
+            // dRelH rows as float4: a warp takes 16 rows x 2 column groups
+            for (int i = tid; i < 64 * 16; i += nt) {
+                const int rr = i & 15, kb = (i >> 4) & 1, rest = i >> 5, kp = rest & 7, rb = rest >> 3;
+                const int r = 16 * rb + rr, k4 = 2 * kp + kb;
+                int grow;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (G::row(s, bp, r, p.Nq, grow)) v = *reinterpret_cast<const float4*>(p.d_relh + (size_t)grow * S + 4 * k4);
+                sAh[(4 * k4 + 0) * kAP + r] = v.x;
+                sAh[(4 * k4 + 1) * kAP + r] = v.y;
+                sAh[(4 * k4 + 2) * kAP + r] = v.z;
+                sAh[(4 * k4 + 3) * kAP + r] = v.w;
+            }
+        } else {
+            for (int i = tid; i < 64 * S; i += nt) {
+                const int r = i & 63, kh = i >> 6;
+                int grow;
+                sAh[kh * kAP + r] = G::row(s, bp, r, p.Nq, grow) ? p.d_relh[(size_t)grow * S + kh] : 0.f;
+            }
+        }
+        __syncthreads();
+        // dRelW (both halves) spread to row j = qw + S - 1 - kw
+        if constexpr (S == 64) {
+            for (int i = tid; i < 64 * 16; i += nt) {
+                const int rr = i & 15, kb = (i >> 4) & 1, rest = i >> 5, kp = rest & 7, rb = rest >> 3;
+                const int r = 16 * rb + rr, k4 = 2 * kp + kb;
+                int grow;
+                if (G::row(s, bp, r, p.Nq, grow)) {
+                    const float4 a = *reinterpret_cast<const float4*>(p.d_relw + (size_t)grow * S + 4 * k4);
+                    const float4 b = *reinterpret_cast<const float4*>(drw1 + (size_t)grow * S + 4 * k4);
+                    const int j0 = r + S - 1 - 4 * k4;  // qw = r on 64-wide grids
+                    sAw[(j0 - 0) * kAP + r] = a.x + b.x;
+                    sAw[(j0 - 1) * kAP + r] = a.y + b.y;
+                    sAw[(j0 - 2) * kAP + r] = a.z + b.z;
+                    sAw[(j0 - 3) * kAP + r] = a.w + b.w;
+                }
+            }
+        } else {
+            for (int i = tid; i < 64 * S; i += nt) {
+                const int r = i & 63, kw = i >> 6;
+                int grow;
+                if (G::row(s, bp, r, p.Nq, grow)) {
+                    const int qw = r % G::QWP;
+                    sAw[(qw + S - 1 - kw) * kAP + r] =
+                        p.d_relw[(size_t)grow * S + kw] + drw1[(size_t)grow * S + kw];
+                }
+            }
+        }
+        __syncthreads();
+        if (!act) continue;
+        float acc[8][4];
+        bool ok[8];
+        int grows[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            ok[i] = G::row(s, bp, r0 + i, p.Nq, grows[i]);
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ok[i]) v = *reinterpret_cast<const float4*>(p.dq32 + (size_t)grows[i] * d + 4 * cg);
+            acc[i][0] = v.x;
+            acc[i][1] = v.y;
+            acc[i][2] = v.z;
+            acc[i][3] = v.w;
+        }
+        if (qh < S) {
+            const uint16_t* th = sT + (size_t)(qh + S - 1) * d + 4 * cg;  // row qh + S - 1 - kh
+#pragma unroll 4
+            for (int kh = 0; kh < S; ++kh) {
+                const float4 a0 = *reinterpret_cast<const float4*>(sAh + kh * kAP + r0);
+                const float4 a1 = *reinterpret_cast<const float4*>(sAh + kh * kAP + r0 + 4);
+                fma8x4(acc, a0, a1, ld4h<BF>(th - (size_t)kh * d));
+            }
+            const uint16_t* tw = sT + (size_t)G::NT * d + 4 * cg;
+            const int j1 = min(qw0 + 7 + S - 1, G::NT - 1);
+#pragma unroll 4
+            for (int j = qw0; j <= j1; ++j) {
+                const float4 a0 = *reinterpret_cast<const float4*>(sAw + j * kAP + r0);
+                const float4 a1 = *reinterpret_cast<const float4*>(sAw + j * kAP + r0 + 4);
+                fma8x4(acc, a0, a1, ld4h<BF>(tw + (size_t)j * d));
+            }
+        }
+        uint16_t* dq16 = static_cast<uint16_t*>(p.dq);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (ok[i])
+                *reinterpret_cast<uint2*>(dq16 + (size_t)grows[i] * d + 4 * cg) =
+                    make_uint2(pack2<BF>(acc[i][0], acc[i][1]), pack2<BF>(acc[i][2], acc[i][3]));
+    }
+}
+
+// ----------------------------------------------------------------- table pass
+// A CTA takes one block position bp (fixed grid rows) and a group of slices,
+// and keeps in registers: Y_h[kh][c] = sum dRelH[q][kh] Q_q[c] over the q of
+// one grid row (4 x 4 tile; table row qh - kh + S - 1) and, for two j-groups,
+// Y_w[j][c] = sum over the block's rows of the spread dRelW[q][j] Q_q[c]
+// (table row j).  Threads: warp w = 5 wr + wc, lane = 4 lr + lc; tile row
+// group kg = 8 wr + lr (0..15), column group cg = 4 wc + lc (0..19).
+// Staged per slice: dRelH as [block row][KHP], the spread dRelW as
+// [block row][JWS] (zeros outside each row's band, written once), Q as fp32
+// [block row][d].
+constexpr int kTabThreads = 320;
+
+template <int S, bool BF>
+__global__ void __launch_bounds__(kTabThreads, 2) bwd_sam_dtab_kernel(const SamBwdParams p) {
+    using G = SamGeom<S>;
+    constexpr int KHP = S == 64 ? 64 : 16;   // dRelH row pitch
+    constexpr int JWS = S == 64 ? 128 : 32;  // spread dRelW row pitch (>= QWP + S - 1, multiple of 4)
+    constexpr int JG = (G::NT + 3) / 4;      // j-groups of the w table
+    static_assert(G::QWP + S - 1 <= JWS && 4 * JG <= JWS, "pitch");
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int d = p.d;
+    float* sAh = reinterpret_cast<float*>(smem);  // [64][KHP]
+    float* sAw = sAh + 64 * KHP;                  // [64][JWS]
+    float* sQ = sAw + 64 * JWS;                   // [64][d]
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int kg = 8 * (warp / 5) + (lane >> 2), cg = 4 * (warp % 5) + (lane & 3);
+    const bool act = 4 * cg < d;
+    const int bp = blockIdx.x % G::NBP, grp = blockIdx.x / G::NBP;
+    const int per = (p.BH + p.groups - 1) / p.groups;
+    const int s0 = grp * per, s1 = min(p.BH, s0 + per);
+    const size_t rows = (size_t)p.BH * p.Nq;
+    const float* drw1 = p.d_relw + rows * S;
+    const uint16_t* q16 = static_cast<const uint16_t*>(p.q);
+    // h tile: grid row lh of the block, kh group khg
+    const int lh = kg / (KHP / 4), khg = kg - lh * (KHP / 4);
+    const int qh = bp * G::LPC + lh;
+    float yh[4][4], yw[2][4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            yh[i][e] = 0.f;
+            yw[0][i][e] = 0.f;
+            yw[1][i][e] = 0.f;
+        }
+    for (int i = tid; i < 64 * (KHP + JWS + d); i += nt) sAh[i] = 0.f;
+    for (int s = s0; s < s1; ++s) {
+        __syncthreads();  // zeros written / the previous slice is done
+        for (int i = tid; i < 64 * S; i += nt) {
+            const int r = i / S, kk = i - r * S;
+            int grow;
+            if (G::row(s, bp, r, p.Nq, grow)) {
+                const size_t o = (size_t)grow * S + kk;
+                sAh[r * KHP + kk] = p.d_relh[o];
+                sAw[r * JWS + (r % G::QWP) + S - 1 - kk] = p.d_relw[o] + drw1[o];
+            }
+        }
+        for (int i = tid; i < 64 * (d / 8); i += nt) {
+            const int r = i / (d / 8), c8 = i - r * (d / 8);
+            int grow;
+            if (G::row(s, bp, r, p.Nq, grow)) {
+                float f[8];
+                unpack8<BF>(*reinterpret_cast<const uint4*>(q16 + (size_t)grow * d + c8 * 8), f);
+                float4* dst = reinterpret_cast<float4*>(sQ + r * d + c8 * 8);
+                dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+                dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+            }
+        }
+        __syncthreads();
+        if (!act) continue;
+        if (qh < S && 4 * khg < S) {
+            const float* a = sAh + lh * G::QWP * KHP + 4 * khg;
+            const float* b = sQ + lh * G::QWP * d + 4 * cg;
+#pragma unroll 4
+            for (int qw = 0; qw < S; ++qw)
+                fma4x4(yh, *reinterpret_cast<const float4*>(a + qw * KHP), *reinterpret_cast<const float4*>(b + qw * d));
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int jg = kg + 16 * t;
+            if (jg < JG) {
+                const int qa = max(0, 4 * jg - S + 1), qb = min(S - 1, 4 * jg + 3);
+                for (int ll = 0; ll < G::LPC; ++ll) {
+                    const float* a = sAw + ll * G::QWP * JWS + 4 * jg;
+                    const float* b = sQ + ll * G::QWP * d + 4 * cg;
+#pragma unroll 4
+                    for (int qw = qa; qw <= qb; ++qw)
+                        fma4x4(yw[t], *reinterpret_cast<const float4*>(a + qw * JWS),
+                               *reinterpret_cast<const float4*>(b + qw * d));
+                }
+            }
+        }
+    }
+    if (!act || s0 >= s1) return;
+    float* dRh = p.d_bias;
+    float* dRw = p.d_bias + (size_t)G::NT * d;
+    if (qh < S) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int kh = 4 * khg + i;
+            if (kh < S) {
+                float* row = dRh + (size_t)(qh + S - 1 - kh) * d + 4 * cg;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) atomicAdd(row + e, yh[i][e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int jg = kg + 16 * t;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = 4 * jg + i;
+            if (jg < JG && j < G::NT) {
+                float* row = dRw + (size_t)j * d + 4 * cg;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) atomicAdd(row + e, yw[t][i][e]);
+            }
+        }
+    }
+}
+
+// Grid-stride kernels: as many CTAs as fit on the SMs at once, at most one
+// per unit of work.
+template <typename K>
+cudaError_t launch_k(K kern, int work, int threads, size_t smem, int nsm, cudaStream_t st, const SamBwdParams& p) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = std::max(1, std::min(work, std::max(1, per_sm) * nsm));
+    kern<<<grid, threads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int S, bool BF>
+cudaError_t launch_pre(const SamBwdParams& p, int nsm, cudaStream_t st) {
+    using G = SamGeom<S>;
+    const size_t smem = (size_t)2 * p.d * G::JP * 2 + (size_t)p.d * 64 * 4 + (size_t)64 * p.rel_stride * 2;
+    const int nblk = p.BH * G::NBP;
+    return launch_k(bwd_sam_rel_kernel<S, BF>, nblk, G::kRelThreads, smem, nsm, st, p);
+}
+
+template <int S, bool BF>
+cudaError_t launch_post(const SamBwdParams& p, int nsm, cudaStream_t st) {
+    using G = SamGeom<S>;
+    const int nblk = p.BH * G::NBP;
+    const size_t smem_dq = (size_t)2 * G::NT * p.d * 2 + (size_t)(S + G::JW) * kAP * 4;
+    cudaError_t e = launch_k(bwd_sam_dq_kernel<S, BF>, nblk, kDqThreads, smem_dq, nsm, st, p);
+    if (e != cudaSuccess) return e;
+    constexpr int KHP = S == 64 ? 64 : 16, JWS = S == 64 ? 128 : 32;
+    const size_t smem_t = (size_t)64 * (KHP + JWS + p.d) * 4;
+    // one CTA per (block position, slice group): the grid is exactly that
+    cudaError_t e2 = cudaFuncSetAttribute(bwd_sam_dtab_kernel<S, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_t);
+    if (e2 != cudaSuccess) return e2;
+    bwd_sam_dtab_kernel<S, BF><<<G::NBP * p.groups, kTabThreads, smem_t, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int sam_bwd_groups(int S, int BH, int nsm) {
+    const int nbp = S == 64 ? SamGeom<64>::NBP : SamGeom<14>::NBP;
+    return std::max(1, std::min(BH, 2 * nsm / nbp));
+}
+
+cudaError_t launch_bwd_sam_rel(const SamBwdParams& p, int S, bool bf, int nsm, cudaStream_t st) {
+    if (S == 64) return bf ? launch_pre<64, true>(p, nsm, st) : launch_pre<64, false>(p, nsm, st);
+    if (S == 14) return bf ? launch_pre<14, true>(p, nsm, st) : launch_pre<14, false>(p, nsm, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_sam_post(const SamBwdParams& p, int S, bool bf, int nsm, cudaStream_t st) {
+    if (S == 64) return bf ? launch_post<64, true>(p, nsm, st) : launch_post<64, false>(p, nsm, st);
+    if (S == 14) return bf ? launch_post<14, true>(p, nsm, st) : launch_post<14, false>(p, nsm, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace sdpa09

@@ -21,36 +21,15 @@
 
 #include "../../include/sdpa09.h"
 #include "attn_bwd_long.cuh"
+#include "attn_bwd_sam.cuh"
 #include "attn_launch.cuh"
 
 namespace sdpa09 {
 
 cudaError_t launch_bwd_win(int dpad, bool swin, const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem,
                            cudaStream_t stream);
-struct BwdPrepParams {
-    const void *q, *o, *dout;
-    float* Dws;
-    int rows, Nq, d, is_bf16;
-    const void *rel_h, *rel_w;
-    __half* rel;
-    float* d_relh;
-    float* d_relw;
-    int s_h, s_w, rel_stride, rw0;
-};
-cudaError_t launch_bwd_prep(const BwdPrepParams& p, bool sam, int nsm, cudaStream_t stream);
 cudaError_t launch_bwd_long(int dpad, int mode, int sw, const BwdMaps& tm, const BwdLongParams& p, int grid,
                             size_t smem, cudaStream_t stream);
-struct BwdSamPostParams {
-    const float* dq32;
-    const float* d_relh;
-    const float* d_relw;
-    const void *q, *rel_h, *rel_w;
-    void* dq;
-    float* d_bias;
-    int rows, Nq, d, S, BH, groups, is_bf16;
-};
-cudaError_t launch_bwd_sam_post(const BwdSamPostParams& p, int nsm, cudaStream_t stream);
-
 namespace {
 
 thread_local std::string g_last_error;
@@ -576,8 +555,8 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
 // (none is needed for windows of up to 128 tokens).
 // Layout of the long-sequence backward's workspace (byte offsets, each
 // 256-byte aligned): D [rows] fp32; for SAM also the rel terms [rows][stride]
-// fp16, scale dS.K [rows][d] fp32, dRelH [rows][k_h] fp32, dRelW [rows][k_w]
-// fp32 (rows = B * H * Nq).
+// fp16, scale dS.K [rows][d] fp32, dRelH [rows][k_h] fp32 and dRelW
+// [2][rows][k_w] fp32, one array per column half (rows = B * H * Nq).
 struct BwdWs {
     size_t d, rel, dq32, drh, drw, total;
 };
@@ -595,7 +574,7 @@ static BwdWs bwd_ws_layout(int64_t rows, int d, bool sam, int s_h, int s_w, int 
         w.drh = o;
         o += al256((size_t)rows * s_h * 4);
         w.drw = o;
-        o += al256((size_t)rows * s_w * 4);
+        o += al256((size_t)2 * rows * s_w * 4);
     }
     w.total = o;
     return w;
@@ -650,27 +629,36 @@ int run_bwd_long(const void* q, const void* k, const void* v, const void* out, c
 
     BwdPrepParams pp;
     memset(&pp, 0, sizeof(pp));
-    pp.q = q;
     pp.o = out;
     pp.dout = dout;
     pp.Dws = reinterpret_cast<float*>(wsb + ws.d);
     pp.rows = (int)rows;
-    pp.Nq = Nq;
     pp.d = d;
     pp.is_bf16 = bf;
-    if (sam) {
-        pp.rel_h = sam->rel_h;
-        pp.rel_w = sam->rel_w;
-        pp.rel = reinterpret_cast<__half*>(wsb + ws.rel);
-        pp.d_relh = reinterpret_cast<float*>(wsb + ws.drh);
-        pp.d_relw = reinterpret_cast<float*>(wsb + ws.drw);
-        pp.s_h = sam->q_h;
-        pp.s_w = sam->q_w;
-        pp.rel_stride = stride;
-        pp.rw0 = rw0;
-    }
-    cudaError_t e = launch_bwd_prep(pp, sam != nullptr, nsm, st);
+    cudaError_t e = launch_bwd_prep(pp, nsm, st);
     if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    const int sw = sam ? sam->q_w : 0;
+    SamBwdParams sp;
+    memset(&sp, 0, sizeof(sp));
+    if (sam) {
+        sp.q = q;
+        sp.rel_h = sam->rel_h;
+        sp.rel_w = sam->rel_w;
+        sp.rel = reinterpret_cast<__half*>(wsb + ws.rel);
+        sp.dq32 = reinterpret_cast<float*>(wsb + ws.dq32);
+        sp.d_relh = reinterpret_cast<float*>(wsb + ws.drh);
+        sp.d_relw = reinterpret_cast<float*>(wsb + ws.drw);
+        sp.dq = dq;
+        sp.d_bias = d_bias;
+        sp.BH = (int)BH;
+        sp.Nq = Nq;
+        sp.d = d;
+        sp.rel_stride = stride;
+        sp.rw0 = rw0;
+        sp.groups = sam_bwd_groups(sw, (int)BH, nsm);
+        e = launch_bwd_sam_rel(sp, sw, bf, nsm, st);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    }
 
     BwdLongParams p;
     memset(&p, 0, sizeof(p));
@@ -684,18 +672,17 @@ int run_bwd_long(const void* q, const void* k, const void* v, const void* out, c
     p.Nq = Nq;
     p.Nk = Nk;
     p.d = d;
-    const int sw = sam ? sam->q_w : 0;
     // key tiles start on grid rows: 112 keys (8 rows) on the 14-wide grid
     p.kv_w = sw == 14 ? 112 : kBlockN;
     if (sam) {
-        p.rel = pp.rel;
+        p.rel = sp.rel;
         p.rel_stride = stride;
         p.rw0 = rw0;
         p.k_h = sam->k_h;
         p.k_w = sam->k_w;
-        p.dq32 = reinterpret_cast<float*>(wsb + ws.dq32);
-        p.d_relh = pp.d_relh;
-        p.d_relw = reinterpret_cast<float*>(wsb + ws.drw);
+        p.dq32 = const_cast<float*>(sp.dq32);
+        p.d_relh = sp.d_relh;
+        p.d_relw = const_cast<float*>(sp.d_relw);
     }
     p.n_qb = (Nq + kBlockM - 1) / kBlockM;
     p.n_kb = (Nk + p.kv_w - 1) / p.kv_w;
@@ -729,24 +716,7 @@ int run_bwd_long(const void* q, const void* k, const void* v, const void* out, c
         if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     }
     if (sam) {
-        BwdSamPostParams sp;
-        memset(&sp, 0, sizeof(sp));
-        sp.dq32 = p.dq32;
-        sp.d_relh = p.d_relh;
-        sp.d_relw = p.d_relw;
-        sp.q = q;
-        sp.rel_h = sam->rel_h;
-        sp.rel_w = sam->rel_w;
-        sp.dq = dq;
-        sp.d_bias = d_bias;
-        sp.rows = (int)rows;
-        sp.Nq = Nq;
-        sp.d = d;
-        sp.S = sw;
-        sp.BH = (int)BH;
-        sp.groups = (int)std::min<int64_t>(BH, std::max(1, 4 * nsm / sw));
-        sp.is_bf16 = bf;
-        e = launch_bwd_sam_post(sp, nsm, st);
+        e = launch_bwd_sam_post(sp, sw, bf, nsm, st);
         if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     }
     static const bool debug_env = getenv("SDPA09_DEBUG") && getenv("SDPA09_DEBUG")[0] == '1';
