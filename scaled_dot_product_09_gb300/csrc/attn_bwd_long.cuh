@@ -184,12 +184,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mbar_wait(&bar_full[w % nst], (w / nst) & 1, nullptr, 0);
                 if (jn > 0) mbar_wait(&bar_res_full, (jn - 1) & 1, nullptr, 0);
             }
-        } else if (warp == kMmaWarp && lane == 0) {
+        } else if (warp == kMmaWarp) {
             // ================================================================ MMA
+            // the whole warp runs the issue loop; lane 0 issues
             const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, kBlockN, false);
             const uint32_t idesc_g = make_idesc_f16_mn(bf, kBlockM, DPAD, true, true);   // dV, dK: A MN-major
             const uint32_t idesc_q = make_idesc_f16_mn(bf, kBlockM, DPAD, false, true);  // dQ: A K-major
             const uint32_t aRes = smem_u32(sRes), aP = smem_u32(sP), aDS = smem_u32(sDS);
+            // every lane waits (no warp vote: the lanes run in step)
             auto waitb = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
                 if (!mbar_wait(bar, parity, abort_flag, code)) return false;
                 tc_fence_after();

@@ -1198,11 +1198,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
         // ================================================================ MMA
-        // One issuing thread per slot (warp 9: slot A, warp 10: slot B):
-        // tcgen05.commit tracks the MMAs of the issuing thread, so each slot's
-        // products run on their own schedule; a shared K/V stage is released
-        // after both threads have committed their last use of it.
-        if (lane == 0) {
+        // One issuing warp per slot (warp 9: slot A, warp 10: slot B), all
+        // lanes converged, lane 0 issuing: tcgen05.commit tracks the MMAs of
+        // the issuing lane, so each slot's products run on their own
+        // schedule; a shared K/V stage is released after both warps have
+        // committed their last use of it.
+        {
             const int x = warp - kMmaWarp;
             const uint32_t idesc_s = make_idesc_f16(bf, kBlockM, MODE == kModeShared ? kCols : kBlockN, false);
             const uint32_t idesc_o = make_idesc_f16(bf, kBlockM, DPAD, true);
@@ -1222,6 +1223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             const uint64_t qone_d = kdesc(smem_u32(sExtraB));
             const uint32_t blocks = smem_u32(sExtraB) + kBlockM * SL * 2;
+            // every lane waits (no warp vote: the lanes run in step)
             auto waitb = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
                 if (!mbar_wait(bar, parity, abort_flag, code)) return false;
                 tc_fence_after();
