@@ -689,6 +689,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kNc = (MODE == kModeSeparate && BIAS == kBiasSwin && SW > 0) ? SW : (SL > 0 ? SL : 1);
     constexpr int kNe = (kNc + 1) & ~1;
     static_assert(MODE == kModeShared || kSepP, "the packed tiling uses separate P buffers");
+    // Shared tiling without the varlen fix-up: the K and V copies of a ring
+    // stage complete one barrier, so the MMA thread waits once per stage (its
+    // waits are costly while earlier MMAs are queued); a tile's P.V always
+    // follows its S, whose issue waited for the stage.
+    constexpr bool kMergeKV = MODE == kModeShared && !VL;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1 KB-aligned base, formed by offsetting the array itself so that the
     // compiler keeps every derived access in the shared state space
@@ -1093,32 +1098,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++ring;
                         unsigned char* dk = sRing + st * p.ring_stage_bytes;
                         unsigned char* dv = dk + kv_tile_bytes;
+                        // the V half lands on the stage's K barrier (kMergeKV) or its own
+                        uint64_t* const bk = &bar_full_k[st];
+                        uint64_t* const bv = kMergeKV ? bk : (VL ? &bar_landed_v[st] : &bar_full_v[st]);
                         if (kDbS && u < t_use) {
                             const CUtensorMap* tfull = u == 0 ? &tm.rw : &tm.rh;
                             const CUtensorMap* tpart = u == 0 ? &tm.rwp : &tm.rhp;
-                            mbar_arrive_expect_tx(&bar_full_k[st], kv_tx);
-                            tma_load_3d(dk, tfull, &bar_full_k[st], 0, 0, 0);
-                            if (p.part) tma_load_2d(dk + p.full_atoms * p.box_kv * 32, tpart, &bar_full_k[st], 0, 0);
-                            mbar_arrive_expect_tx(&bar_full_v[st], kv_tx);
-                            tma_load_3d(dv, tfull, &bar_full_v[st], 0, 64, 0);
-                            if (p.part) tma_load_2d(dv + p.full_atoms * p.box_kv * 32, tpart, &bar_full_v[st], 0, 64);
+                            mbar_arrive_expect_tx(bk, kMergeKV ? 2 * kv_tx : kv_tx);
+                            tma_load_3d(dk, tfull, bk, 0, 0, 0);
+                            if (p.part) tma_load_2d(dk + p.full_atoms * p.box_kv * 32, tpart, bk, 0, 0);
+                            if (!kMergeKV) mbar_arrive_expect_tx(bv, kv_tx);
+                            tma_load_3d(dv, tfull, bv, 0, 64, 0);
+                            if (p.part) tma_load_2d(dv + p.full_atoms * p.box_kv * 32, tpart, bv, 0, 64);
                         } else if (BIAS == kBiasSam && u < t_use) {
                             // rel-pos tables: R_w in the K slot, R_h in the V slot
                             const uint32_t r_tx = (uint32_t)T::kAtoms * kBlockN * 32u;
-                            mbar_arrive_expect_tx(&bar_full_k[st], r_tx);
-                            tma_load_3d(dk, &tm.rw, &bar_full_k[st], 0, 0, 0);
-                            if (p.part) tma_load_2d(dk + p.full_atoms * kBlockN * 32, &tm.rwp, &bar_full_k[st], 0, 0);
-                            mbar_arrive_expect_tx(&bar_full_v[st], r_tx);
-                            tma_load_3d(dv, &tm.rh, &bar_full_v[st], 0, 0, 0);
-                            if (p.part) tma_load_2d(dv + p.full_atoms * kBlockN * 32, &tm.rhp, &bar_full_v[st], 0, 0);
+                            mbar_arrive_expect_tx(bk, kMergeKV ? 2 * r_tx : r_tx);
+                            tma_load_3d(dk, &tm.rw, bk, 0, 0, 0);
+                            if (p.part) tma_load_2d(dk + p.full_atoms * kBlockN * 32, &tm.rwp, bk, 0, 0);
+                            if (!kMergeKV) mbar_arrive_expect_tx(bv, r_tx);
+                            tma_load_3d(dv, &tm.rh, bv, 0, 0, 0);
+                            if (p.part) tma_load_2d(dv + p.full_atoms * kBlockN * 32, &tm.rhp, bv, 0, 0);
                         } else {
                             const int j = u - t_use;
                             const int kr = jr.k_row + j * p.kv_w;
-                            mbar_arrive_expect_tx(&bar_full_k[st], kv_tx);
-                            tma_load_4d(dk, &tm.k, &bar_full_k[st], 0, kr, jr.k_slice, 0);
-                            if (p.part) tma_load_3d(dk + p.full_atoms * p.box_kv * 32, &tm.kp, &bar_full_k[st], 0, kr, jr.k_slice);
-                            uint64_t* const bv = VL ? &bar_landed_v[st] : &bar_full_v[st];
-                            mbar_arrive_expect_tx(bv, kv_tx);
+                            mbar_arrive_expect_tx(bk, kMergeKV ? 2 * kv_tx : kv_tx);
+                            tma_load_4d(dk, &tm.k, bk, 0, kr, jr.k_slice, 0);
+                            if (p.part) tma_load_3d(dk + p.full_atoms * p.box_kv * 32, &tm.kp, bk, 0, kr, jr.k_slice);
+                            if (!kMergeKV) mbar_arrive_expect_tx(bv, kv_tx);
                             tma_load_4d(dv, &tm.v, bv, 0, kr, jr.k_slice, 0);
                             if (p.part) tma_load_3d(dv + p.full_atoms * p.box_kv * 32, &tm.vp, bv, 0, kr, jr.k_slice);
                         }
@@ -1157,7 +1164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int u = (ring > nst ? ring - nst : 0); u < ring; ++u) {
                     const int st = u % nst;
                     mbar_wait(&bar_full_k[st], (u / nst) & 1, nullptr, 0);
-                    if (MODE == kModeShared) mbar_wait(VL ? &bar_landed_v[st] : &bar_full_v[st], (u / nst) & 1, nullptr, 0);
+                    if (MODE == kModeShared && !kMergeKV)
+                        mbar_wait(VL ? &bar_landed_v[st] : &bar_full_v[st], (u / nst) & 1, nullptr, 0);
                 }
             }
         }
@@ -1272,7 +1280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int t = 0; t < 2; ++t) {
                             const int use = ring + t, st = use % nst;
                             if (!waitb(&bar_full_k[st], (use / nst) & 1, kStatusWaitK) ||
-                                !waitb(&bar_full_v[st], (use / nst) & 1, kStatusWaitV)) {
+                                (!kMergeKV && !waitb(&bar_full_v[st], (use / nst) & 1, kStatusWaitV))) {
                                 ok = false;
                                 break;
                             }
@@ -1303,7 +1311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; ok && j < n && j < 2; ++j) ok = issue_s(j);
                     for (int j = 0; ok && j < n; ++j) {
                         const int use = ring + j, st = use % nst;
-                        if (!waitb(bp, ph_p, kStatusWaitP) || !waitb(&bar_full_v[st], (use / nst) & 1, kStatusWaitV)) {
+                        if (!waitb(bp, ph_p, kStatusWaitP) || (!kMergeKV && !waitb(&bar_full_v[st], (use / nst) & 1, kStatusWaitV))) {
                             ok = false;
                             break;
                         }
@@ -1355,7 +1363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_commit(&bar_q_empty[x][qb2]);
                         ++s_cnt;
                     }
-                    if (!waitb(bp, ph_p, kStatusWaitP) || !waitb(&bar_full_v[st], (ring / nst) & 1, kStatusWaitV)) {
+                    if (!waitb(bp, ph_p, kStatusWaitP) || (!kMergeKV && !waitb(&bar_full_v[st], (ring / nst) & 1, kStatusWaitV))) {
                         ok = false;
                         break;
                     }
@@ -1374,7 +1382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int st = ring % nst;
                         const uint32_t par = (ring / nst) & 1;
                         if (!p.sam_resample &&
-                            (!waitb(&bar_full_k[st], par, kStatusWaitK) || !waitb(&bar_full_v[st], par, kStatusWaitV))) {
+                            (!waitb(&bar_full_k[st], par, kStatusWaitK) || (!kMergeKV && !waitb(&bar_full_v[st], par, kStatusWaitV)))) {
                             ok = false;
                             break;
                         }
@@ -1414,7 +1422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_commit(bs);
                             ++s_cnt;
                         }
-                        if (!waitb(bp, ph_p, kStatusWaitP) || !waitb(&bar_full_v[st], (use / nst) & 1, kStatusWaitV)) {
+                        if (!waitb(bp, ph_p, kStatusWaitP) || (!kMergeKV && !waitb(&bar_full_v[st], (use / nst) & 1, kStatusWaitV))) {
                             ok = false;
                             break;
                         }
