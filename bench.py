@@ -390,10 +390,13 @@ def _suite(stream, dev, peaks, names):
         base, _, layout = name.partition("@")
         w = WORKLOADS[base]
         if layout == "bwd":
-            # backward: 10*B*H*Nq*Nk*d (S recomputed, dV, dP, dQ, dK); CUDA-core fp32
-            t = _time_bwd(w, stream, dev, 50)
-            out[name] = {"us_per_step": round(t * 1e6, 2), "tflops": round(2.5 * w.flops / t / 1e12, 2),
-                         "bound": "alu"}
+            # backward (attn_bwd, tensor cores): algorithmic work 10*B*H*Nq*Nk*d, the
+            # five products S, dP, dV, dK, dQ (the kernels recompute S and dP in
+            # both passes of the long-sequence path, which is not counted)
+            t = _time_bwd(w, stream, dev, 20 if w.flops > 1e11 else 50)
+            tf = 2.5 * w.flops / t / 1e12
+            out[name] = {"us_per_step": round(t * 1e6, 2), "tflops": round(tf, 2), "bound": "tensor",
+                         "frac": round(tf / peaks["bf16_tflops"], 4)}
             torch.cuda.empty_cache()
             continue
         inp = make_inputs(w)
@@ -520,10 +523,16 @@ def main(argv=None):
     ap.add_argument("--workload", default="sam_vith_global", choices=sorted(WORKLOADS))
     ap.add_argument("--no-suite", action="store_true", help="skip the other workloads' numbers")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling aid: run the workload with this B (a smaller case of the same kernels)")
+    ap.add_argument("--bwd-only", action="store_true",
+                    help="profiling aid: time only attn_bwd on the workload and print its numbers")
     args = ap.parse_args(argv)
     args.metric = "attention fwd TFLOP/s (4*B*H*Nq*Nk*d)"
     world, rank, local = _dist()
     w = WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
 
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
@@ -536,6 +545,12 @@ def main(argv=None):
     sdpa.load_library()
     peaks = _peaks()
     stream = torch.cuda.Stream(device=dev)
+    if args.bwd_only:
+        t = _time_bwd(w, stream, dev, max(1, args.steps))
+        if rank == 0:
+            print(json.dumps({"bwd_only": w.name, "B": w.B, "us_per_step": t * 1e6,
+                              "tflops": 2.5 * w.flops / t / 1e12}))
+        return 0
 
     # CPU baseline first (host only), before any GPU timing.
     cpu = None
@@ -589,9 +604,9 @@ def main(argv=None):
         del sets
         torch.cuda.empty_cache()
         suite = _suite(stream, dev, peaks, [n for n in ("swin_t_stage1", "swin_t_stage1@image", "swin_t_stage1@bwd",
-                                                        "sam_vith_window", "sam_vith_global",
-                                                        "sam_vith_global_768", "sd_unet_self", "sd_unet_cross",
-                                                        "sd_unet_self_varlen")
+                                                        "sam_vith_window", "sam_vith_window@bwd", "sam_vith_global",
+                                                        "sam_vith_global@bwd", "sam_vith_global_768", "sd_unet_self",
+                                                        "sd_unet_self@bwd", "sd_unet_cross", "sd_unet_self_varlen")
                                             if n != w.name])
     if rank == 0:
         line = {

@@ -1,7 +1,7 @@
 /*
  * sdpa09.h -- C ABI of the GB300 (sm_103a) fused scaled-dot-product
  * attention library, libsdpa09.so: the forward pass (attn_fwd,
- * attn_fwd_varlen) and its backward for windows (attn_bwd).
+ * attn_fwd_varlen, attn_fwd_train) and its backward (attn_bwd).
  *
  * The operation (per batch-head slice):
  *
@@ -215,8 +215,13 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, cons
  * P = softmax(scale*Q.K^T + bias), O = P.V and dO = dout:
  *   dV = P^T dO,  dS = P * (dO V^T - rowsum(dO * O)),
  *   dQ = scale dS K,  dK = scale dS^T Q,
- * and for the Swin bias the table gradient: dS summed into the table row of
- * each (query, key) pair of each head (the mask is constant).
+ * and the bias gradients: Swin, dS summed into the table row of each
+ * (query, key) pair of each head (the mask is constant); SAM
+ * ("Accelerating Generative AI (part 1), Segment Anything", Bfloat16
+ * section: the decomposed rel-pos terms rel_h[q][kh] = Q_q . R_h[qh-kh+S-1],
+ * rel_w alike), dRelH[q][kh] = sum over kw of dS[q][(kh,kw)] (dRelW alike),
+ * then dQ_q += sum_kh dRelH[q][kh] R_h[qh-kh+S-1] + the same over kw, and
+ * dR_h[j] = sum of dRelH[q][kh] Q_q over the (q, kh) with qh-kh+S-1 = j.
  *
  *  q, k, v    device inputs of the forward call, layout [B][H][N][d];
  *  out        device O of the forward call (rowsum(dO * O) is taken from it);
@@ -226,20 +231,29 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, cons
  *             fits one key tile and its softmax is recomputed exactly);
  *  dq, dk, dv device outputs, like q, k, v; fully overwritten.
  *  B, H, Nq, Nk, d, scale, dtype as for attn_fwd.
- *  bias_kind  ATTN_BIAS_NONE or ATTN_BIAS_SWIN (windows layout, bias_args
- *             as for attn_fwd).
+ *  bias_kind  ATTN_BIAS_NONE, ATTN_BIAS_SWIN (windows layout, bias_args as
+ *             for attn_fwd) or ATTN_BIAS_SAM_RELPOS (bias_args as for
+ *             attn_fwd, with equal square query and key grids of side
+ *             S = 14 or 64 and tables of 2*S-1 rows).
  *  d_bias     device fp32 bias gradient, ADDED to (the caller zeroes it
- *             first): ATTN_BIAS_SWIN: [(2*win-1)^2][H]; NULL otherwise.
+ *             first): ATTN_BIAS_SWIN: [(2*win-1)^2][H]; ATTN_BIAS_SAM_RELPOS:
+ *             [2*S-1][d] for R_h followed by [2*S-1][d] for R_w; NULL
+ *             otherwise.
  *  workspace, workspace_bytes
  *             device scratch of at least attn_bwd_workspace_size(...) bytes,
  *             16-byte aligned, owned by the caller (NULL when that size is
  *             0); its contents on entry do not matter.
  *  stream     cudaStream_t to enqueue on.
  * Products run on the tensor cores with fp32 accumulation from 16-bit
- * operands (P and dS rounded to the input type); outputs are rounded to
- * nearest even.  Returns ATTN_OK, ATTN_ERR_ARG, ATTN_ERR_UNSUPPORTED (see
- * the limits below) or ATTN_ERR_CUDA.  Limits: d <= 64 for sequences of at
- * most 128 tokens.
+ * operands (P and dS rounded to the input type); the SAM row sums of dS and
+ * their products with Q and the tables stay in fp32 (CUDA cores); outputs
+ * are rounded to nearest even.  Windows (Nq, Nk <= 128, d <= 64, no SAM
+ * bias) take one kernel and no workspace; longer sequences, d > 64 or the
+ * SAM bias take a pre-pass, a key pass (dK, dV), a query pass (dQ) and, for
+ * SAM, two post-passes, with lse and the workspace.  Returns ATTN_OK,
+ * ATTN_ERR_ARG, ATTN_ERR_UNSUPPORTED (see the limits) or ATTN_ERR_CUDA.
+ * Limits: d <= 80 (d <= 64 with the Swin bias, 48 < d <= 80 with the SAM
+ * bias); the Swin bias in the windows token layout only; B*H*N < 2^31.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
              void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale,

@@ -1,11 +1,13 @@
-"""GPU parity of the backward pass (short sequences / windows) against the
-fp64 oracle's attn_bwd on the same seeded inputs, through the C ABI.
+"""GPU parity of the backward pass (windows, long sequences, the Swin and SAM
+biases) against the fp64 oracle's attn_bwd on the same seeded inputs,
+through the C ABI.
 
 Tolerance: dQ, dK and dV are 16-bit outputs and are held to the bound
 stated for every 16-bit output against the fp64 oracle, max |err| <= 2e-2
 and mean |err| <= 2e-3 over each tensor.  The fp32 table gradient sums many
 dS terms, each off by fp32 rounding only (the oracle takes D from the same
-16-bit O): |err| <= 1e-3 + 1e-3 |want| per element."""
+16-bit O): |err| <= 1e-3 + 1e-3 |want| per element; the SAM table
+gradients (fp32 sums of fp32 row sums of dS) are held to the same bound."""
 import numpy as np
 import pytest
 import torch
