@@ -269,10 +269,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int st = t % nst;
                 const uint32_t b = smem_u32(sRing + st * p.stage_bytes);
                 const uint32_t aQ = b, aK = b + T::kBytes, aDO = b + 3 * T::kBytes;
-                if (!waitb(&bar_p, t & 1, kStatusWaitP)) break;
-                // the next tile's S and dP go first: the softmax works on them
-                // while the tensor core runs this tile's gradient products
+                // the next tile's S and dP go first, as soon as the softmax has
+                // read this tile's: they compute while it forms P and dS, and it
+                // works on them while the tensor core runs this tile's gradient
+                // products
                 if (t + 1 < n_tiles && !issue_sdp(t + 1)) break;
+                if (!waitb(&bar_p, t & 1, kStatusWaitP)) break;
                 // the accumulators are rewritten once the epilogue has read the last tile's
                 if (t > 0 && !waitb(&bar_accfree, (t - 1) & 1, kStatusWaitO)) break;
 #pragma unroll

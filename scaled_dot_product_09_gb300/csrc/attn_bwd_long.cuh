@@ -220,8 +220,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int it = 0; it < n_inner; ++it, ++u) {
                     const int st = u % nst;
                     const uint32_t b = smem_u32(sRing + st * p.stage_bytes);
-                    if (!waitb(&bar_p, u & 1, kStatusWaitP)) { ok = false; break; }
+                    // the next tile's S and dP as soon as the softmax has read this
+                    // tile's (they compute while it forms P and dS), then this
+                    // tile's gradient products once P and dS are in shared memory
                     if (it + 1 < n_inner && !issue_sdp(u + 1)) { ok = false; break; }
+                    if (!waitb(&bar_p, u & 1, kStatusWaitP)) { ok = false; break; }
                     // the accumulators are rewritten once the last job's epilogue read them
                     if (it == 0 && jn > 0 && !waitb(&bar_accfree, (jn - 1) & 1, kStatusWaitO)) { ok = false; break; }
                     const uint32_t acc = it > 0 ? 1u : 0u;
