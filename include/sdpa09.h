@@ -231,8 +231,11 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, cons
  *             fits one key tile and its softmax is recomputed exactly);
  *  dq, dk, dv device outputs, like q, k, v; fully overwritten.
  *  B, H, Nq, Nk, d, scale, dtype as for attn_fwd.
- *  bias_kind  ATTN_BIAS_NONE, ATTN_BIAS_SWIN (windows layout, bias_args as
- *             for attn_fwd) or ATTN_BIAS_SAM_RELPOS (bias_args as for
+ *  bias_kind  ATTN_BIAS_NONE, ATTN_BIAS_SWIN (bias_args as for attn_fwd,
+ *             either token layout: with ATTN_SWIN_IMAGE, q, k, v, out, dout
+ *             and dq, dk, dv are [images][grid_h][grid_w][H][d] and the
+ *             kernel folds the shift and the window partition into its loads
+ *             and their inverse into its stores) or ATTN_BIAS_SAM_RELPOS (bias_args as for
  *             attn_fwd, with equal square query and key grids of side
  *             S = 14 or 64 and tables of 2*S-1 rows).
  *  d_bias     device fp32 bias gradient, ADDED to (the caller zeroes it
@@ -253,7 +256,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, cons
  * SAM, two post-passes, with lse and the workspace.  Returns ATTN_OK,
  * ATTN_ERR_ARG, ATTN_ERR_UNSUPPORTED (see the limits) or ATTN_ERR_CUDA.
  * Limits: d <= 80 (d <= 64 with the Swin bias, 48 < d <= 80 with the SAM
- * bias); the Swin bias in the windows token layout only; B*H*N < 2^31.
+ * bias); B*H*N < 2^31.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
              void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale,

@@ -277,8 +277,10 @@ def attn_bwd_workspace_size(B, H, Nq, Nk, d, bias=None):
 def attn_bwd(q, k, v, out, dout, lse=None, scale=None, bias=None, stream=None, grads=None, workspace=None):
     """Gradients of attn_fwd: q/k/v/out/dout [B,H,N,d] contiguous bf16/fp16
     CUDA tensors (out: the forward's output, dout: the gradient with respect
-    to it), lse: the fp32 [B,H,Nq] row log-sum-exp from attn_fwd_train (may
-    be None when Nq, Nk <= 128 without SAM).  Returns (dq, dk, dv, d_bias) with
+    to it; with SwinBias(layout="image") all of them and the returned dq, dk,
+    dv are [images, grid_h, grid_w, H, d]), lse: the fp32 [B,H,Nq] row
+    log-sum-exp from attn_fwd_train (may be None when Nq, Nk <= 128 without
+    SAM).  Returns (dq, dk, dv, d_bias) with
     d_bias the fp32 gradient of a SwinBias table, the pair (d_rel_h, d_rel_w)
     of a SamBias, else None.  grads: the four buffers to use instead (d_bias is
     added to; for SAM one fp32 [L_h + L_w, d] tensor); workspace: a uint8 CUDA
@@ -286,7 +288,7 @@ def attn_bwd(q, k, v, out, dout, lse=None, scale=None, bias=None, stream=None, g
     None)."""
     import torch
     lib = load_library()
-    B, H, Nq, Nk, d = _shape(q, k, v)
+    B, H, Nq, Nk, d = _shape_image(q, k, v, bias) if _is_image(bias) else _shape(q, k, v)
     for t in (out, dout):
         if t.shape != q.shape or not t.is_contiguous():
             raise AttnError(ATTN_ERR_ARG, "out and dout must be contiguous and shaped like q")

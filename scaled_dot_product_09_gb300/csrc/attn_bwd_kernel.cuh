@@ -68,6 +68,12 @@ struct BwdTcParams {
     int swin_acc;       // 1: dS summed per (head, key token, query token) in shared memory
     int swin_acc_atomic;  // 1: two slots of a tile may share a head (g > H): atomic adds there
     uint32_t off_acc;   // that sum, fp32 [H][N keys][N queries]
+    // Swin image layout: q/k/v/out/dout/dq/dk/dv are [images][grid_h][grid_w][H][d];
+    // the producer warp gathers each window's rows (shift and partition folded
+    // into the addresses) and the epilogue writes the gradients back the same way
+    int swin_image;
+    uint32_t fd_m[2];
+    const void *q, *k, *v, *dout;
 };
 
 // Byte offset of the 16-byte half `hh` (columns 8hh..8hh+7) of row r in a
@@ -211,7 +217,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp >= 8) {
         regs_dec<kBwdCtlRegs>();
-        if (warp == kProducerWarp && lane == 0) {
+        if (BIAS == kBiasSwin && warp == kProducerWarp && p.swin_image) {
+            // ============================================ producer, image layout
+            // The whole warp copies each window's token rows of Q, K, V and dO
+            // with 16-byte cp.async copies into the same swizzled tiles the TMA
+            // path lands; token (r, c) of window (wr, wc) comes from image
+            // position ((wr*win + r + shift) mod grid_h, (wc*win + c + shift)
+            // mod grid_w) ("视觉大模型训练和推理加速" sections 一 and 二: the
+            // shift and the partition are index mappings).  Padding rows and
+            // columns are written as zeros.  The warp waits for its own copies
+            // before it signals the stage (the backward's tiles take long
+            // enough that one stage in flight per warp keeps up).
+            constexpr int kChunks = DPAD / 8;
+            constexpr int kLanesRow = kChunks <= 2 ? 2 : (kChunks <= 4 ? 4 : 8);
+            constexpr int kRowsIt = 32 / kLanesRow;
+            static_assert(SL % kRowsIt == 0, "a warp instruction stays inside one slice");
+            const int c = lane % kLanesRow, rsub = lane / kLanesRow;
+            const bool lane_on = c < kChunks, c_data = c * 8 < p.d;
+            const uint32_t dchunk = (uint32_t)((c >> 1) * (kBlockM * 32));
+            const size_t rowb = (size_t)p.d * 2;
+            int u = 0;
+            for (int job = job0; job < p.n_jobs; job += job_step, ++u) {
+                const int st = u % nst;
+                __syncwarp();
+                if (u >= nst &&
+                    !__all_sync(0xffffffffu, mbar_wait(&bar_empty[st], ((u / nst) + 1) & 1, abort_flag, kStatusWaitEmpty)))
+                    break;
+                unsigned char* b = sRing + st * p.stage_bytes;
+                if (lane_on) {
+#pragma unroll 1
+                    for (int g = 0; g < p.g; ++g) {
+                        const uint32_t slice = (uint32_t)(job * p.g + g);
+                        const bool sv = (int)slice < p.BH;
+#pragma unroll 4
+                        for (int it = 0; it < SL / kRowsIt; ++it) {
+                            const uint32_t t = (uint32_t)(it * kRowsIt + rsub);
+                            const int R = g * SL + (int)t;
+                            const bool on = c_data && sv && (int)t < p.Nq;
+                            const size_t row = on ? swin_image_row(slice, t, p.H, p.n_w, p.n_ww, p.win, p.grid_h, p.grid_w,
+                                                                   p.shift, p.fd_h, p.fd_w, p.fd_ww, p.fd_m)
+                                                  : 0;
+                            const size_t off = on ? row * rowb + (size_t)c * 16 : 0;
+                            const uint32_t dst = smem_u32(b + R * 32) + dchunk +
+                                                 ((((uint32_t)c & 1u) ^ (((uint32_t)R >> 2) & 1u)) << 4);
+                            const uint32_t nb = on ? 16u : 0u;
+                            cp_async16(dst, static_cast<const unsigned char*>(p.q) + off, nb);
+                            cp_async16(dst + T::kBytes, static_cast<const unsigned char*>(p.k) + off, nb);
+                            cp_async16(dst + 2 * T::kBytes, static_cast<const unsigned char*>(p.v) + off, nb);
+                            cp_async16(dst + 3 * T::kBytes, static_cast<const unsigned char*>(p.dout) + off, nb);
+                        }
+                    }
+                }
+                cp_async_commit();
+                cp_async_wait_n(0);
+                fence_proxy_async_smem();  // read by the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_full[st]);
+            }
+        } else if (warp == kProducerWarp && lane == 0) {
             // ============================================================ producer
             const uint32_t tx = 4u * (uint32_t)T::kBytes;
             int u = 0;
@@ -519,8 +582,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int slice = jb * p.g + slot;
             float D = 0.f;
             if (tok < p.Nq && slice < p.BH) {
+                const size_t orow_i = (BIAS == kBiasSwin && p.swin_image)
+                                          ? swin_image_row((uint32_t)slice, (uint32_t)tok, p.H, p.n_w, p.n_ww, p.win,
+                                                           p.grid_h, p.grid_w, p.shift, p.fd_h, p.fd_w, p.fd_ww, p.fd_m)
+                                          : (size_t)slice * p.Nq + tok;
                 const uint4* orow = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p.o) +
-                                                                   ((size_t)slice * p.Nq + tok) * (size_t)p.d * 2);
+                                                                   orow_i * (size_t)p.d * 2);
 #pragma unroll
                 for (int c8 = 0; c8 < DPAD / 8; ++c8) {
                     if (c8 * 8 < p.d) {
@@ -564,8 +631,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 void* base = which == 0 ? p.dv : which == 1 ? p.dk : p.dq;
                 const int n = which == 2 ? p.Nq : p.Nk;
                 if (ok_row) {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<unsigned char*>(base) +
-                                                          ((size_t)slice * n + tok) * (size_t)p.d * 2);
+                    const size_t grow = (BIAS == kBiasSwin && p.swin_image)
+                                            ? swin_image_row((uint32_t)slice, (uint32_t)tok, p.H, p.n_w, p.n_ww, p.win,
+                                                             p.grid_h, p.grid_w, p.shift, p.fd_h, p.fd_w, p.fd_ww, p.fd_m)
+                                            : (size_t)slice * n + tok;
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<unsigned char*>(base) + grow * (size_t)p.d * 2);
 #pragma unroll
                     for (int c8 = 0; c8 < DPAD / 8; ++c8) {
                         if (c8 * 8 < p.d) {

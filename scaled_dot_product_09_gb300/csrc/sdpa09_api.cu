@@ -767,11 +767,20 @@ int run_bwd(const void* q, const void* k, const void* v, const void* out, const 
         if (a->grid_h < M || a->grid_w < M || a->grid_h % M || a->grid_w % M)
             return fail(ATTN_ERR_ARG, "grid_h and grid_w must be positive multiples of win");
         if (a->shift < 0 || a->shift >= M) return fail(ATTN_ERR_ARG, "shift must lie in [0, win)");
-        if (a->layout != ATTN_SWIN_WINDOWS)
-            return fail(ATTN_ERR_UNSUPPORTED, "the backward takes the windows token layout");
+        if (a->layout != ATTN_SWIN_WINDOWS && a->layout != ATTN_SWIN_IMAGE)
+            return fail(ATTN_ERR_ARG, "unknown Swin token layout %d", (int)a->layout);
         const int nW = (a->grid_h / M) * (a->grid_w / M);
         if (B % nW) return fail(ATTN_ERR_ARG, "B (windows) must be a multiple of the windows per image");
         swin = true;
+        if (a->layout == ATTN_SWIN_IMAGE) {
+            // the kernel gathers the windows' rows and scatters the gradients
+            p.swin_image = 1;
+            fast_div_params((uint32_t)M, p.fd_m);
+            p.q = q;
+            p.k = k;
+            p.v = v;
+            p.dout = dout;
+        }
         p.table = a->table;
         p.d_table = d_bias;
         p.win = M;

@@ -198,8 +198,9 @@ def test_bwd_argument_checks(lib):
     swin = sdpa._SwinArgs(FAKE, 7, 56, 56, 3)
     assert _bwd(lib, kind=1, args=ctypes.byref(swin)) == sdpa.ATTN_ERR_ARG    # no d_table
     assert b"d_bias" in lib.attn_last_error()
-    img = sdpa._SwinArgs(FAKE, 7, 56, 56, 3, 1)
-    assert _bwd(lib, kind=1, args=ctypes.byref(img), d_table=FAKE) == sdpa.ATTN_ERR_UNSUPPORTED
+    lay = sdpa._SwinArgs(FAKE, 7, 56, 56, 3, 2)                             # unknown token layout
+    assert _bwd(lib, kind=1, args=ctypes.byref(lay), d_table=FAKE) == sdpa.ATTN_ERR_ARG
+    assert b"layout" in lib.attn_last_error()
     assert _bwd(lib, B=63, kind=1, args=ctypes.byref(swin), d_table=FAKE) == sdpa.ATTN_ERR_ARG
 
 

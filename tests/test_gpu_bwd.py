@@ -112,3 +112,44 @@ def test_bwd_sam_window_14x14():
 def test_bwd_sam_global_64x64():
     """SAM global attention on the 64 x 64 grid (4096 tokens, d = 80), one slice."""
     _bwd_case(W["sam_vith_global"].with_(B=1, H=1, seed=98), use_lse=True)
+
+
+# ------------------------------------------------- Swin image token layout --
+def _images(w):
+    return w.B // ((w.grid_h // w.win) * (w.grid_w // w.win))
+
+
+def _to_image(t, w):
+    """[B windows, H, win^2, d] -> [images, grid_h, grid_w, H, d], bit-exact."""
+    raw = t.reshape(w.B, w.H, w.Nq, w.d).view(torch.int16).numpy()
+    return torch.from_numpy(oracle.swin_unpartition(raw, _images(w), w.grid_h, w.grid_w, w.win, w.shift)).view(t.dtype)
+
+
+@pytest.mark.parametrize("case", ["swin_t_stage1_2img", "ragged_grid_21"])
+def test_bwd_swin_image_layout_matches_windows_layout(case):
+    """The image-layout backward (the kernel gathers each window's rows and
+    writes the gradients back to their image positions) returns, bit for
+    bit, the windows-layout backward's gradients mapped back to the image,
+    and the same table gradient (the windows layout is checked against the
+    oracle above)."""
+    require_gpu()
+    w = {"swin_t_stage1_2img": W["swin_t_stage1"].with_(B=2 * 64, seed=91),
+         "ragged_grid_21": W["swin_t_stage1"].with_(B=9, grid_h=21, grid_w=21, seed=92)}[case]
+    inp = make_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    dout = torch.randn(inp.q.shape, generator=g).to(inp.q.dtype)
+    qw, kw, vw, dow = (x.cuda() for x in (inp.q, inp.k, inp.v, dout))
+    bw = gpu_bias(w, inp)
+    ow, lse = sdpa.attn_fwd_train(qw, kw, vw, scale=w.scale, bias=bw)
+    want = sdpa.attn_bwd(qw, kw, vw, ow, dow, scale=w.scale, bias=bw)
+    bi = sdpa.SwinBias(inp.table.cuda(), w.win, w.grid_h, w.grid_w, w.shift, layout="image")
+    qi, ki, vi, oi, doi = (_to_image(x.cpu(), w).cuda() for x in (qw, kw, vw, ow, dow))
+    got = sdpa.attn_bwd(qi, ki, vi, oi, doi, scale=w.scale, bias=bi)
+    torch.cuda.synchronize()
+    assert sdpa.attn_device_status() == sdpa.ATTN_OK
+    for name, a, b in zip(("dq", "dk", "dv"), got[:3], want[:3]):
+        assert a.shape == (_images(w), w.grid_h, w.grid_w, w.H, w.d), name
+        assert torch.equal(a.cpu().view(torch.int16), _to_image(b.cpu(), w).view(torch.int16)), name
+    # the table gradient sums the same fp32 terms; the CTAs add their sums to
+    # the table with atomics, in an order that varies from call to call
+    np.testing.assert_allclose(got[3].cpu().numpy(), want[3].cpu().numpy(), rtol=1e-4, atol=1e-5)
