@@ -89,14 +89,18 @@ def _code_tokens(text: str) -> str:
 
 
 def _kernel_sources_hash() -> str:
-    """sha256 over the CUDA sources' code (comments and whitespace left out),
-    to tell whether recorded ncu counters still describe the kernel being
-    run."""
+    """sha256 over the code (comments and whitespace left out) of the sources
+    the forward kernel is compiled from -- its header, the PTX wrappers, the
+    launchers and the per-(head dim, bias) instantiation units -- to tell
+    whether recorded ncu counters of attn_fwd_kernel still describe the
+    kernel being run (the backward's files and the host code do not enter)."""
     import hashlib
     d = os.path.join(ROOT, "scaled_dot_product_09_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh")):
+        fwd = name in ("attn_fwd_kernel.cuh", "sm103_ptx.cuh", "attn_launch.cuh") or (
+            name.startswith("attn_d") and name.endswith(".cu"))
+        if fwd:
             with open(os.path.join(d, name), encoding="utf-8") as f:
                 h.update(name.encode() + b"\0" + _code_tokens(f.read()).encode())
     return h.hexdigest()
