@@ -655,8 +655,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     //   scores computed after this tile's P.V (in-order issue), and the
     //   softmax never waits for a P.V before writing P.  At a job's start
     //   G_w = Q.R_w^T lands over S0/S1 and G_h = Q.R_h^T over [128,256).
-    constexpr bool kDbS = MODE == kModeShared && BIAS == kBiasSam && SW == 64 && DPAD <= 96;
-    constexpr int kCols = kDbS ? 64
+    // The 48 x 48 grid (a 768-pixel input) runs the same way with 48-key
+    // tiles: S0 [0,48), S1 [48,96), O [128,128+DPAD); G_w (95 rows) over the
+    // score buffers, G_h over [128,224).
+    constexpr bool kDbS = MODE == kModeShared && BIAS == kBiasSam && (SW == 64 || SW == 48) && DPAD <= 96;
+    constexpr int kTw = SW == 48 ? 48 : 64;  // kDbS: keys per score tile (one grid row)
+    constexpr int kCols = kDbS ? kTw
                           : (MODE == kModeShared && BIAS == kBiasNone && SW > 0)  ? SW
                           : (MODE == kModeShared && BIAS == kBiasSam && SW == 14) ? 112
                                                                                   : 128;
@@ -1108,8 +1112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_3d(dk, tfull, bk, 0, 0, 0);
                             if (p.part) tma_load_2d(dk + p.full_atoms * p.box_kv * 32, tpart, bk, 0, 0);
                             if (!kMergeKV) mbar_arrive_expect_tx(bv, kv_tx);
-                            tma_load_3d(dv, tfull, bv, 0, 64, 0);
-                            if (p.part) tma_load_2d(dv + p.full_atoms * p.box_kv * 32, tpart, bv, 0, 64);
+                            tma_load_3d(dv, tfull, bv, 0, kTw, 0);
+                            if (p.part) tma_load_2d(dv + p.full_atoms * p.box_kv * 32, tpart, bv, 0, kTw);
                         } else if (BIAS == kBiasSam && u < t_use) {
                             // rel-pos tables: R_w in the K slot, R_h in the V slot
                             const uint32_t r_tx = (uint32_t)T::kAtoms * kBlockN * 32u;
@@ -1261,7 +1265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             for (int job = job0; ok && job < p.n_jobs; job += job_step, ++ju) {
                 if constexpr (kDbS) {
-                    // SAM, 64 x 64 grid: 64-key score tiles, two score buffers
+                    // SAM, 64 x 64 (48 x 48) grid: one grid row of keys per score tile,
+                    // two score buffers
                     const int qb = ju % p.nq;
                     const uint64_t qa = kdesc(smem_u32(sQ + (x * p.nq + qb) * T::kBytes));
                     if (!waitb(&bar_q_full[x][qb], (ju / p.nq) & 1, kStatusWaitQ)) { ok = false; break; }
@@ -1276,7 +1281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         issue_qk<DPAD>(tOx, qa, kdesc(rt + T::kBytes), make_idesc_f16(bf, kBlockM, p.n_rh, false));
                         mma_commit(&bar_g[x]);
                     } else {
-                        // two ring stages: R_w rows [0,64) | [64,128), then R_h's
+                        // two ring stages: R_w rows [0,kTw) | [kTw,2kTw), then R_h's
                         for (int t = 0; t < 2; ++t) {
                             const int use = ring + t, st = use % nst;
                             if (!waitb(&bar_full_k[st], (use / nst) & 1, kStatusWaitK) ||
@@ -1286,8 +1291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             const uint32_t kt = smem_u32(sRing + st * p.ring_stage_bytes);
                             const uint32_t dst = t == 0 ? tSx : tOx;
-                            issue_qk_rows<DPAD, 64>(dst, qa, kdesc(kt), idesc_s);
-                            issue_qk_rows<DPAD, 64>(dst + 64, qa, kdesc(kt + kv_tile_bytes), idesc_s);
+                            issue_qk_rows<DPAD, kTw>(dst, qa, kdesc(kt), idesc_s);
+                            issue_qk_rows<DPAD, kTw>(dst + kTw, qa, kdesc(kt + kv_tile_bytes), idesc_s);
                         }
                         if (!ok) break;
                         mma_commit(&bar_g[x]);
@@ -1303,7 +1308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     auto issue_s = [&](int j) -> bool {
                         const int use = ring + j, st = use % nst, b = (sbase + j) & 1;
                         if (!waitb(&bar_full_k[st], (use / nst) & 1, kStatusWaitK)) return false;
-                        issue_qk_rows<DPAD, 64>(tSx + 64u * (uint32_t)b, qa,
+                        issue_qk_rows<DPAD, kTw>(tSx + (uint32_t)kTw * (uint32_t)b, qa,
                                                 kdesc(smem_u32(sRing + st * p.ring_stage_bytes)), idesc_s);
                         mma_commit(&bar_sb[x][b]);
                         return true;
@@ -1316,8 +1321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         ph_p ^= 1;
-                        issue_pv<64>(tOx, tPx + 64u * (uint32_t)((sbase + j) & 1),
-                                     vdesc_rows(smem_u32(sRing + st * p.ring_stage_bytes) + kv_tile_bytes, 64u), idesc_o,
+                        issue_pv<kTw>(tOx, tPx + (uint32_t)kTw * (uint32_t)((sbase + j) & 1),
+                                     vdesc_rows(smem_u32(sRing + st * p.ring_stage_bytes) + kv_tile_bytes, (uint32_t)kTw), idesc_o,
                                      j > 0 ? 1u : 0u);
                         if (j == n - 1) {
                             mma_commit(bo);
@@ -1712,18 +1717,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
             } else if constexpr (kDbS) {
-                // ------------------------- SAM, 64 x 64 grid: 64-key score tiles
-                // Key tile j is key row kh = j.  rel_w of the row (64 values,
+                // -------------- SAM, 64 x 64 (48 x 48) grid: one grid row per score tile
+                // Key tile j is key row kh = j.  rel_w of the row (kTw values,
                 // log2 units) stays in registers for the job as aligned pairs,
                 // one 64-bit operand of the packed FMA each; rel_h goes to shared
                 // memory as fp16, [slot][kh][row], one load per tile.
                 __half* const rh16 = reinterpret_cast<__half*>(sExtraB) + x * (64 * kBlockM);
-                const int qh = min(my_tok >> 6, 63), qw = my_tok & 63;
+                const int qh = min(my_tok / kTw, kTw - 1), qw = my_tok % kTw;
                 __syncwarp();
                 if (!__all_sync(0xffffffffu, mbar_wait(&bar_g[x], ju & 1, abort_flag, kStatusWaitG))) { ok = false; break; }
                 tc_fence_after();
                 const float f = DBG ? 1.0f : kLog2e;
-                float2 rw2[32];
+                float2 rw2[kTw / 2];
                 {
                     float gv[128];
                     {
@@ -1732,20 +1737,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int t = 0; t < 128; ++t) gv[t] = __uint_as_float(v[t]) * f;
                     }
-                    // rel_w for key column kw is G_w[qw + 63 - kw]
+                    // rel_w for key column kw is G_w[qw + kTw - 1 - kw]
                     shift_down<128, 6>(gv, qw);
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) rw2[u] = make_float2(gv[63 - 2 * u], gv[62 - 2 * u]);
+                    for (int u = 0; u < kTw / 2; ++u) rw2[u] = make_float2(gv[kTw - 1 - 2 * u], gv[kTw - 2 - 2 * u]);
                     {
                         uint32_t v[128];
                         tmem_ld_cols<128>(tO, v);  // G_h row
 #pragma unroll
                         for (int t = 0; t < 128; ++t) gv[t] = __uint_as_float(v[t]) * f;
                     }
-                    // rel_h for key row kh is G_h[qh + 63 - kh]
+                    // rel_h for key row kh is G_h[qh + kTw - 1 - kh]
                     shift_down<128, 6>(gv, qh);
 #pragma unroll
-                    for (int u = 0; u < 64; ++u) rh16[u * kBlockM + r] = __float2half_rn(gv[63 - u]);
+                    for (int u = 0; u < kTw; ++u) rh16[u * kBlockM + r] = __float2half_rn(gv[kTw - 1 - u]);
                 }
                 tc_fence_before();
                 warp_arrive(&bar_gdone[x]);
@@ -1760,19 +1765,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ++cnt_s;
                     tc_fence_after();
-                    float xs[64];
+                    float xs[kTw];
                     {
-                        uint32_t v[64];
-                        tmem_ld_cols<64>(tS + 64u * (uint32_t)b, v);
+                        uint32_t v[kTw];
+                        tmem_ld_cols<kTw>(tS + (uint32_t)kTw * (uint32_t)b, v);
 #pragma unroll
-                        for (int t = 0; t < 64; ++t) xs[t] = __uint_as_float(v[t]);
+                        for (int t = 0; t < kTw; ++t) xs[t] = __uint_as_float(v[t]);
                     }
-                    const float rh = __half2float(rh16[min(j, 63) * kBlockM + r]);
+                    const float rh = __half2float(rh16[min(j, kTw - 1) * kBlockM + r]);
                     if constexpr (DBG) {
                         if (row_ok) {
-                            float* dst = p.dbg + ((size_t)my_slice * p.Nq + my_tok) * p.Nk + j * 64;
+                            float* dst = p.dbg + ((size_t)my_slice * p.Nq + my_tok) * p.Nk + j * kTw;
 #pragma unroll
-                            for (int c = 0; c < 64; c += 2) {
+                            for (int c = 0; c < kTw; c += 2) {
                                 dst[c] = rw2[c / 2].x + rh;
                                 dst[c + 1] = rw2[c / 2].y + rh;
                             }
@@ -1782,12 +1787,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // over the tile and joins through the max and the exponent's
                     // offset (the bias goes on first, so any sign of the scale works)
 #pragma unroll
-                    for (int c = 0; c < 64; c += 2) {
+                    for (int c = 0; c < kTw; c += 2) {
                         const float2 y = __ffma2_rn(make_float2(xs[c], xs[c + 1]), scale2, rw2[c / 2]);
                         xs[c] = y.x;
                         xs[c + 1] = y.y;
                     }
-                    const float m_tile = row_max<64>(xs) + rh;
+                    const float m_tile = row_max<kTw>(xs) + rh;
                     // the previous P.V must be done before O is rescaled; every tile
                     // after the first consumes that completion, at the latest just
                     // before its P is handed over
@@ -1821,9 +1826,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m_run = m_new;
                     }
                     const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-                    uint32_t pk[32];
-                    l_run += exp_pack<64>(xs, 1.0f, rh - m_use, bf, pk);
-                    tmem_st_cols<32>(tP + 64u * (uint32_t)b, pk);
+                    uint32_t pk[kTw / 2];
+                    l_run += exp_pack<kTw>(xs, 1.0f, rh - m_use, bf, pk);
+                    tmem_st_cols<kTw / 2>(tP + (uint32_t)kTw * (uint32_t)b, pk);
                     tmem_st_wait();
                     if (!wait_pv()) { ok = false; break; }
                     tc_fence_before();

@@ -384,8 +384,8 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         const bool square = a->q_h == a->q_w && a->k_h == a->q_h && a->k_w == a->q_w;
         sw_spec = (square && (a->q_w == 64 || a->q_w == 48 || a->q_w == 14)) ? a->q_w : 0;
         extra = (size_t)sam_extra_floats(sw_spec == 0, a->k_h, a->k_w, Nk) * 4;
-        if (sw_spec == 64 && dpad <= 96) {
-            // 64-key score tiles (one grid row), two score buffers per slot;
+        if ((sw_spec == 64 || sw_spec == 48) && dpad <= 96) {
+            // one grid row of keys per score tile, two score buffers per slot;
             // rel_h rows as fp16 [2 slots][64][128].  The tables pass through
             // two ring stages per job (64 rows per K or V tile), or, resampled,
             // are staged once per CTA.
@@ -459,9 +459,9 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         // SAM key tiles start on grid rows: 112 keys (8 rows) on the 14-wide
         // grid, 128 (2 rows) on the 64-wide one
         // (head dims up to 96: O and P then share 128 tensor-memory columns)
-        const bool tiles64 = bias == kBiasSam && sw_spec == 64 && dpad <= 96;
-        p.kv_w = tiles64 ? 64 : (bias == kBiasSam && sw_spec) ? (sw_spec == 14 ? 112 : (kBlockN / sw_spec) * sw_spec)
-                                                              : kBlockN;
+        const bool tiles64 = bias == kBiasSam && (sw_spec == 64 || sw_spec == 48) && dpad <= 96;
+        p.kv_w = tiles64 ? sw_spec : (bias == kBiasSam && sw_spec) ? (sw_spec == 14 ? 112 : (kBlockN / sw_spec) * sw_spec)
+                                                                   : kBlockN;
         p.kv_cols = kBlockN;  // unused by the kernel: its key-tile width is a compile-time constant
         p.n_kv = (Nk + p.kv_w - 1) / p.kv_w;
         p.q_jobs = (Nq + 2 * kBlockM - 1) / (2 * kBlockM);
@@ -470,8 +470,8 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         if (nj > 0x7fffffff) return fail(ATTN_ERR_UNSUPPORTED, "too many jobs");
         p.n_jobs = (int)nj;
         p.box_q = kBlockM;
-        // K/V tiles of 64 rows for SAM on the 64 x 64 grid, else 128
-        p.box_kv = tiles64 ? 64 : kBlockN;
+        // K/V tiles of one grid row for SAM on the 64 x 64 and 48 x 48 grids, else 128
+        p.box_kv = tiles64 ? sw_spec : kBlockN;
         p.ring_stage_bytes = (uint32_t)(2 * (size_t)(dpad / 16) * p.box_kv * 32);
         // prefer >= 3 K/V stages, then double-buffered Q (the 64-key tiles
         // of the 64 x 64 SAM grid want >= 5: their scores run two tiles ahead)

@@ -221,7 +221,7 @@ def test_sam_global_64x64_bias_indexing_bit_exact():
 
 
 def test_sam_global_48x48_bias_indexing_bit_exact():
-    # the kernel specialised for 48x48 grids (96-key tiles of two grid rows)
+    # the kernel specialised for 48x48 grids (48-key tiles of one grid row, two score buffers)
     _sam_bias_bit_exact(W["sam_vith_global_768"].with_(B=1, H=2, rel_len=0), slices=(0, 1),
                         rows=range(0, 2304, 23))
 
