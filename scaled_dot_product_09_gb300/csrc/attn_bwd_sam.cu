@@ -518,6 +518,99 @@ cudaError_t launch_post(const SamBwdParams& p, int nsm, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// ------------------------------------------ table pass, 14 x 14 windows
+// On the 14-wide grid a slice (196 query rows) is small, so the table pass
+// takes whole slices and forms a dense GEMM against a "spread" matrix: with
+// j the table row that a (query, key row / column) pair addresses --
+// j = qh - kh + 13 for R_h (j in [0, 27)) and 28 + qw - kw + 13 for R_w
+// (j in [28, 55)) -- the row sums dRelH, dRelW are spread to A[q][j] (zero
+// where no key row / column addresses j) and dR[j] = sum over slices and q
+// of A[q][j] Q_q.  (Per-slice versions of the pre-pass and the dQ pass on
+// the same plan measured slower than the block-wise ones: 351 vs 209 us and
+// 267 vs 200 us on the SAM window workload; this one 192 vs 307 us.)
+constexpr int k14 = 14, k14N = 196, k14J = 56, k14W = 28;  // side, rows per slice, stacked tables, R_w offset
+
+// dR[j] += sum_q A[q][j] Q_q over the CTA's slices; 288 threads: 14 table-row
+// groups of 4 x 20 column groups of 4; one atomic add per output at the end.
+template <bool BF>
+__global__ void __launch_bounds__(288, 2) bwd_sam14_dtab_kernel(const SamBwdParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int d = p.d;
+    float* sA = reinterpret_cast<float*>(smem);  // [196][56] spread row sums
+    float* sQ = sA + k14N * k14J;                // [196][d]
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int jg = tid / 20, cg = tid - jg * 20;
+    const bool act = jg < k14J / 4 && 4 * cg < d;
+    const size_t rows = (size_t)p.BH * p.Nq;
+    const float* drw1 = p.d_relw + rows * k14;
+    const uint16_t* q16 = static_cast<const uint16_t*>(p.q);
+    float y[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[i][e] = 0.f;
+    bool any = false;
+    for (int s = blockIdx.x; s < p.BH; s += gridDim.x) {
+        any = true;
+        const size_t row0 = (size_t)s * k14N;
+        __syncthreads();
+        for (int i = tid; i < k14N * k14J / 4; i += nt) reinterpret_cast<float4*>(sA)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = tid; i < k14N * (d / 8); i += nt) {
+            const int r = i / (d / 8), c8 = i - r * (d / 8);
+            float f[8];
+            unpack8<BF>(*reinterpret_cast<const uint4*>(q16 + (row0 + r) * d + c8 * 8), f);
+            float4* dst = reinterpret_cast<float4*>(sQ + r * d + c8 * 8);
+            dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+            dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
+        __syncthreads();
+        for (int i = tid; i < k14N * k14; i += nt) {
+            const int q = i / k14, k = i - q * k14, qh = q / k14, qw = q - qh * k14;
+            const size_t o = (row0 + q) * k14 + k;
+            sA[q * k14J + qh + k14 - 1 - k] = p.d_relh[o];
+            sA[q * k14J + k14W + qw + k14 - 1 - k] = p.d_relw[o] + drw1[o];
+        }
+        __syncthreads();
+        if (!act) continue;
+        // rows whose spread can reach this thread's table rows: R_h rows need
+        // qh in [4jg - 13, 4jg + 3]; R_w rows can be reached from every grid row
+        int q0 = 0, q1 = k14N;
+        if (4 * jg < 2 * k14 - 1) {
+            q0 = k14 * max(0, 4 * jg - (k14 - 1));
+            q1 = k14 * min(k14, 4 * jg + 4);
+        }
+#pragma unroll 4
+        for (int q = q0; q < q1; ++q) {
+            const float4 a = *reinterpret_cast<const float4*>(sA + q * k14J + 4 * jg);
+            const float4 b = *reinterpret_cast<const float4*>(sQ + q * d + 4 * cg);
+            fma4x4(y, a, b);
+        }
+    }
+    if (!act || !any) return;
+    const int nt_rows = 2 * k14 - 1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j = 4 * jg + i;
+        float* row = nullptr;
+        if (j < nt_rows) row = p.d_bias + (size_t)j * d;
+        else if (j >= k14W && j < k14W + nt_rows) row = p.d_bias + (size_t)(nt_rows + j - k14W) * d;
+        if (row)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) atomicAdd(row + 4 * cg + e, y[i][e]);
+    }
+}
+
+// 14-wide grids: the block-wise dQ pass, then the per-slice table pass
+template <bool BF>
+cudaError_t launch_post14(const SamBwdParams& p, int nsm, cudaStream_t st) {
+    using G = SamGeom<14>;
+    const size_t smem_dq = (size_t)2 * G::NT * p.d * 2 + (size_t)(14 + G::JW) * kAP * 4;
+    cudaError_t e = launch_k(bwd_sam_dq_kernel<14, BF>, p.BH * G::NBP, kDqThreads, smem_dq, nsm, st, p);
+    if (e != cudaSuccess) return e;
+    const size_t smem_t = (size_t)k14N * k14J * 4 + (size_t)k14N * p.d * 4;
+    return launch_k(bwd_sam14_dtab_kernel<BF>, p.BH, 288, smem_t, nsm, st, p);
+}
+
 }  // namespace
 
 int sam_bwd_groups(int S, int BH, int nsm) {
@@ -533,7 +626,7 @@ cudaError_t launch_bwd_sam_rel(const SamBwdParams& p, int S, bool bf, int nsm, c
 
 cudaError_t launch_bwd_sam_post(const SamBwdParams& p, int S, bool bf, int nsm, cudaStream_t st) {
     if (S == 64) return bf ? launch_post<64, true>(p, nsm, st) : launch_post<64, false>(p, nsm, st);
-    if (S == 14) return bf ? launch_post<14, true>(p, nsm, st) : launch_post<14, false>(p, nsm, st);
+    if (S == 14) return bf ? launch_post14<true>(p, nsm, st) : launch_post14<false>(p, nsm, st);
     return cudaErrorInvalidValue;
 }
 
