@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (tid == 0) {
         abort_sh = 0;
         for (int i = 0; i < kMaxStages; ++i) {
-            mbar_init(&bar_full[i], 1);
+            mbar_init(&bar_full[i], (BIAS == kBiasSwin && p.swin_image) ? 32 : 1);  // image layout: one per gathering lane
             mbar_init(&bar_empty[i], 1);
         }
         mbar_init(&bar_s, 1);
@@ -225,9 +225,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // position ((wr*win + r + shift) mod grid_h, (wc*win + c + shift)
             // mod grid_w) ("视觉大模型训练和推理加速" sections 一 and 二: the
             // shift and the partition are index mappings).  Padding rows and
-            // columns are written as zeros.  The warp waits for its own copies
-            // before it signals the stage (the backward's tiles take long
-            // enough that one stage in flight per warp keeps up).
+            // columns are written as zeros.  Each lane's arrival on the stage
+            // barrier is made by the copy hardware once that lane's copies
+            // have landed, so the warp runs ahead to the next stage; the MMA
+            // warp fences the proxies after its wait.
             constexpr int kChunks = DPAD / 8;
             constexpr int kLanesRow = kChunks <= 2 ? 2 : (kChunks <= 4 ? 4 : 8);
             constexpr int kRowsIt = 32 / kLanesRow;
@@ -268,12 +269,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                     }
                 }
-                cp_async_commit();
-                cp_async_wait_n(0);
-                fence_proxy_async_smem();  // read by the tensor core
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_full[st]);
+                cp_async_arrive_noinc(&bar_full[st]);
             }
+            cp_async_wait<0>();
         } else if (warp == kProducerWarp && lane == 0) {
             // ============================================================ producer
             const uint32_t tx = 4u * (uint32_t)T::kBytes;
@@ -320,6 +318,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int st = u % nst;
                 const uint32_t b = smem_u32(sRing + st * p.stage_bytes);
                 if (!waitb(&bar_full[st], (u / nst) & 1, kStatusWaitK)) return false;
+                // image layout: the tiles were written by cp.async (generic proxy)
+                if (BIAS == kBiasSwin && p.swin_image) fence_proxy_async_smem();
                 if (u > 0 && !waitb(&bar_sfree, (u - 1) & 1, kStatusWaitS)) return false;
                 issue_qk<DPAD>(tS, kdesc(b), kdesc(b + T::kBytes), idesc_s);
                 issue_qk<DPAD>(tDP, kdesc(b + 3 * T::kBytes), kdesc(b + 2 * T::kBytes), idesc_s);

@@ -759,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kMaxStages; ++i) {
             // the image-layout Swin stages are filled by two warps
-            mbar_init(&bar_full_k[i], (MODE == kModeSeparate && BIAS == kBiasSwin && p.swin_image) ? 2 : 1);
+            mbar_init(&bar_full_k[i], (MODE == kModeSeparate && BIAS == kBiasSwin && p.swin_image) ? 64 : 1);
             mbar_init(&bar_full_v[i], 1);
             mbar_init(&bar_empty[i], MODE == kModeShared ? 2 : 1);
             if constexpr (VL) mbar_init(&bar_landed_v[i], 1);
@@ -970,8 +970,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // take alternate slices of a tile, or alternate row groups when a
             // tile holds one slice.  (Rows of one head are 2d bytes out of
             // every 2Hd, too short for box copies to pay.)  A stage's barrier
-            // takes one arrival per warp, made once that warp's copies into
-            // the stage have landed.
+            // counts one arrival per lane of the two warps, each made by the
+            // copy hardware once that lane's copies have landed; the MMA
+            // warps fence the proxies after their wait.
             constexpr int kChunks = DPAD / 8;  // 16-byte chunks of a padded row
             constexpr int kLanesRow = kChunks <= 2 ? 2 : (kChunks <= 4 ? 4 : 8);
             constexpr int kRowsIt = 32 / kLanesRow;      // rows per warp instruction
@@ -985,29 +986,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool c_data = c * 8 < p.d;   // else the chunk is zero padding
             const uint32_t dchunk = (uint32_t)((c >> 1) * (kBlockM * 32));
             const size_t rowb = (size_t)p.d * 2;
-            // Ring uses whose copies are in flight, oldest first.  The MMA
-            // slot holding use u releases it only after the tile it looks
-            // ahead to, u + 2, has landed, so before waiting for use n - nst to
-            // be released this warp signals every use up to n - nst + 2.
-            int pend0 = 0, pend1 = 0, pend2 = 0, pend3 = 0;  // (scalars: no local-memory array)
-            int npend = 0;
-            auto pop_oldest = [&](int keep) {
-                cp_async_wait_n(keep);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_full_k[pend0 % nst]);
-                pend0 = pend1;
-                pend1 = pend2;
-                pend2 = pend3;
-                --npend;
-            };
             int ring = 0;
             bool ok = true;
             for (int job = job0; ok && job < p.n_jobs; job += job_step) {
                 for (int x = 0; x < 2; ++x) {
                     const int st = ring % nst;
                     if (ring >= nst) {
-                        while (npend > 0 && pend0 <= ring - nst + 2) pop_oldest(npend - 1);
                         __syncwarp();
                         if (!__all_sync(0xffffffffu, mbar_wait(&bar_empty[st], ((ring / nst) + 1) & 1, abort_flag,
                                                                kStatusWaitEmpty))) {
@@ -1055,15 +1039,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-                    cp_async_commit();
-                    if (npend == 0) pend0 = use;
-                    else if (npend == 1) pend1 = use;
-                    else if (npend == 2) pend2 = use;
-                    else pend3 = use;
-                    if (++npend > 3) pop_oldest(3);
+                    // every lane's arrival lands with its copies: the warp
+                    // never waits for them and runs ahead to the next stage
+                    cp_async_arrive_noinc(&bar_full_k[st]);
                 }
             }
-            while (npend > 0) pop_oldest(npend - 1);
+            cp_async_wait<0>();
         } else if (lane == 0) {
             const uint32_t q_tx = (uint32_t)T::kAtoms * (uint32_t)p.box_q * 32u;
             const uint32_t kv_tx = (uint32_t)T::kAtoms * (uint32_t)p.box_kv * 32u;
@@ -1458,8 +1439,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // slots doing so that needs three stages, else a slot would
                     // wait for the stage it holds.
                     const bool ahead = nst >= 3;
+                    // image-layout tiles are written by cp.async copies (generic
+                    // proxy) that signal the barrier themselves: the reader's
+                    // proxy fence orders them before its MMAs
+                    const bool gathered = BIAS == kBiasSwin && p.swin_image;
                     if (ju == 0 || !ahead) {
                         if (!waitb(&bar_full_k[u % nst], (u / nst) & 1, kStatusWaitK) || !s_free()) { ok = false; break; }
+                        if (gathered) fence_proxy_async_smem();
                         sep_scores(2 * job + x, qa);
                         mma_commit(bs);
                         ++s_cnt;
@@ -1469,6 +1455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // next tile's scores first: they overlap this tile's softmax
                         const int u2 = u + 2;
                         if (!waitb(&bar_full_k[u2 % nst], (u2 / nst) & 1, kStatusWaitK) || !s_free()) { ok = false; break; }
+                        if (gathered) fence_proxy_async_smem();
                         sep_scores(2 * next + x, smem_u32(sRing + (u2 % nst) * p.ring_stage_bytes));
                         mma_commit(bs);
                         ++s_cnt;

@@ -110,6 +110,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src, u
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// One arrival on the mbarrier once all of this thread's earlier cp.async
+// copies have landed (the barrier's count includes it: .noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 // wait until at most N of this thread's committed groups are still pending
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
