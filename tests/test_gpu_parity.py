@@ -324,10 +324,10 @@ def test_sam_unequal_grids_bias_indexing_bit_exact(qg, kg):
 
 # ----------------------------------------------- Swin image token layout --
 # q/k/v/out as [images, grid_h, grid_w, H, d]: the kernel folds the cyclic
-# shift and the window partition into its loads (a box per window that does not
-# wrap, a gather for one that does) and their inverse into its stores.  Image inputs are the windows-layout inputs mapped back through the
-# oracle's inverse partition (an exact index permutation); the expected output
-# is the oracle's window attention mapped the same way.
+# shift and the window partition into its row gathers and their inverse into
+# its stores.  Image inputs are the windows-layout inputs mapped back through
+# the oracle's inverse partition (an exact index permutation); the expected
+# output is the oracle's window attention mapped the same way.
 
 SWIN_IMAGE_CASES = {
     "stage1": dict(B=2 * 64),
@@ -347,7 +347,7 @@ SWIN_IMAGE_CASES = {
     # 6 heads, bias MMAs: 5 stages, 384 jobs
     "ring5_mma_many_heads": dict(B=16 * 16, H=6, grid_h=28, grid_w=28, seed=20),
     "bf16": dict(B=64, dtype="bf16", seed=17),
-    # d not a multiple of 16: no boxes, every window gathered (zero column padding)
+    # d not a multiple of 16: zero column padding written by the gathers
     "d40_gathered": dict(B=2 * 64, d=40, seed=21),
 }
 
