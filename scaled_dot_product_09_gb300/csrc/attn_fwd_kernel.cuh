@@ -683,6 +683,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kOw = kShDbl ? 2 * DPAD : (DPAD <= 64 ? 64 : DPAD);
     constexpr int kOffO = kOffP + 128;
     constexpr bool kSepP = !kDbS && kOffO + 2 * kOw <= 512 && (BIAS != kBiasSam || SW == 14);
+    // SAM on the 14 x 14 grid: G_w and G_h (32 columns each) land in the
+    // slot's P buffer, columns [0,32) and [32,64), so a job's G and first S
+    // need neither the previous job's epilogue (O) nor the gather (S): both
+    // are issued as soon as the previous job's last S was read and its last
+    // P.V issued, and overlap that job's epilogue.  The first P.V of the job
+    // (which overwrites O) waits for that epilogue.
+    constexpr bool kGinP = MODE == kModeShared && BIAS == kBiasSam && SW == 14 && kSepP;
     // Packed tiling with head dims up to 32 and slots up to 64 rows: two O
     // buffers per slot (O_x holds 64 columns), so a tile's output is written
     // while the next tile's P.V runs.
@@ -1372,12 +1379,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
-                        // G_h rewrites O_x: the previous job's epilogue must be done with it
-                        if (ju > 0 && !waitb(&bar_oempty[x], (ju - 1) & 1, kStatusWaitO)) { ok = false; break; }
+                        // G_h rewrites O_x: the previous job's epilogue must be done with
+                        // it.  (G in P_x: P_x was last read by this thread's P.V, which
+                        // the tensor core finishes first, and written before that P.V;
+                        // O_x is next written by this job's first P.V, which waits for
+                        // P, which the softmax writes after its epilogue read O_x.)
+                        if (!kGinP && ju > 0 && !waitb(&bar_oempty[x], (ju - 1) & 1, kStatusWaitO)) { ok = false; break; }
                         const uint32_t rw_a = p.sam_resample ? smem_u32(smem + p.off_rtab)
                                                              : smem_u32(sRing + st * p.ring_stage_bytes);
-                        issue_qk<DPAD>(tSx, qa, kdesc(rw_a), make_idesc_f16(bf, kBlockM, p.n_rw, false));
-                        issue_qk<DPAD>(tOx, qa, kdesc(rw_a + T::kBytes), make_idesc_f16(bf, kBlockM, p.n_rh, false));
+                        issue_qk<DPAD>(kGinP ? tPx : tSx, qa, kdesc(rw_a), make_idesc_f16(bf, kBlockM, p.n_rw, false));
+                        issue_qk<DPAD>(kGinP ? tPx + 32 : tOx, qa, kdesc(rw_a + T::kBytes),
+                                       make_idesc_f16(bf, kBlockM, p.n_rh, false));
                         mma_commit(&bar_g[x]);
                         if (!p.sam_resample) {
                             mma_commit(&bar_empty[st]);
@@ -1389,7 +1401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int st = ring % nst;
                         if (!waitb(&bar_full_k[st], (ring / nst) & 1, kStatusWaitK)) { ok = false; break; }
                         // with the SAM bias S_x rewrites the G_w values the slot is still gathering
-                        if (BIAS == kBiasSam && !waitb(&bar_gdone[x], ju & 1, kStatusWaitG)) { ok = false; break; }
+                        if (BIAS == kBiasSam && !kGinP && !waitb(&bar_gdone[x], ju & 1, kStatusWaitG)) { ok = false; break; }
                         if (!s_free()) { ok = false; break; }
                         issue_qk<DPAD>(tSx, qa, kdesc(smem_u32(sRing + st * p.ring_stage_bytes)), idesc_s);
                         mma_commit(bs);
@@ -1864,7 +1876,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // G_w row: rel_w for key column kw is G_w[qw + s_w - 1 - kw]
                     {
                         uint32_t v[kGW];
-                        tmem_ld_cols<kGW>(tS, v);
+                        tmem_ld_cols<kGW>(kGinP ? tP : tS, v);
 #pragma unroll
                         for (int t = 0; t < kGW; ++t) gv[t] = __uint_as_float(v[t]) * f;
                     }
@@ -1880,7 +1892,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // G_h row: rel_h for key row kh is G_h[qh + s_h - 1 - kh]
                     {
                         uint32_t v[kGW];
-                        tmem_ld_cols<kGW>(tO, v);
+                        tmem_ld_cols<kGW>(kGinP ? tP + 32 : tO, v);
 #pragma unroll
                         for (int t = 0; t < kGW; ++t) gv[t] = __uint_as_float(v[t]) * f;
                     }
