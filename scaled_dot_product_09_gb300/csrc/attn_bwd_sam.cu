@@ -1,12 +1,9 @@
-// attn_bwd_sam.cu -- the SAM decomposed rel-pos parts of the long-sequence
-// backward, on the CUDA cores in fp32 (every product has 16-bit inputs or
-// fp32 sums as operands and is accumulated in fp32; nothing is rounded to
-// 16 bits before the stored result):
+// attn_bwd_sam.cu -- the SAM decomposed rel-pos gradients of the
+// long-sequence backward, on the CUDA cores in fp32 (every product has
+// 16-bit inputs or fp32 sums as operands and is accumulated in fp32; nothing
+// is rounded to 16 bits before the stored result; the rel terms the two
+// tensor-core passes add to their scores come from attn_bwd_sam_rel.cu):
 //
-//   rel pre-pass:  rel_h[q][kh] = Q_q . R_h[qh - kh + S - 1] and
-//                  rel_w[q][kw] = Q_q . R_w[qw - kw + S - 1], in log2 units,
-//                  stored fp16 for the two tensor-core passes to add to the
-//                  scores;
 //   dQ post-pass:  dQ_q = (scale dS.K)_q + sum_kh dRelH[q][kh] R_h[qh - kh + S - 1]
 //                                        + sum_kw dRelW[q][kw] R_w[qw - kw + S - 1];
 //   table pass:    dR_h[j] = sum of dRelH[q][kh] Q_q over the (q, kh) with
@@ -20,12 +17,11 @@
 // grid rows, each padded from 14 to 16 columns, when S = 14 (block row r is
 // grid row bp * LPC + r / QWP, grid column r % QWP; padded rows are zero).
 // Every product is a small GEMM tiled in registers: a thread keeps an 8 x 4
-// (pre-pass, dQ) or 4 x 4 (tables) tile of outputs and reads both operands
-// as float4 (or four 16-bit values) from shared memory.  For the w terms the
-// index j = qw - kw + S - 1 turns the skew into a band that is dense in j:
-// the pre-pass forms Q_q . R_w[j] over the band of its rows and scatters each
-// value to its kw, and the post-passes spread dRelW[q][kw] to row j of a
-// zero-filled matrix before multiplying.
+// (dQ) or 4 x 4 (tables) tile of outputs and reads both operands as float4
+// (or four 16-bit values) from shared memory.  For the w terms the index
+// j = qw - kw + S - 1 turns the skew into a band that is dense in j: the
+// passes spread dRelW[q][kw] to row j of a zero-filled matrix before
+// multiplying.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -39,7 +35,6 @@ namespace sdpa09 {
 
 namespace {
 
-constexpr float kLog2eSam = 1.4426950408889634f;
 
 template <int S>
 struct SamGeom {
@@ -48,20 +43,6 @@ struct SamGeom {
     static constexpr int LPC = 64 / QWP;            // grid rows per block
     static constexpr int NBP = (S + LPC - 1) / LPC; // blocks per slice
     static constexpr int NT = 2 * S - 1;            // table rows
-    static constexpr int G8 = QWP / 8;              // groups of 8 block rows per grid row
-    // pre-pass: j-groups of 4 per (terms, row group); table columns staged
-    __host__ __device__ static constexpr int jw_last(int g) { return (8 * g + 7 + S - 1) / 4; }
-    __host__ __device__ static constexpr int jh_last(int qh) { return (qh + S - 1) / 4; }
-    __host__ __device__ static constexpr int cmax(int a, int b) { return a > b ? a : b; }
-    __host__ __device__ static constexpr int nj() {
-        int m = 0;
-        for (int g = 0; g < G8; ++g) m = cmax(m, jw_last(g) - 2 * g + 1);
-        for (int qh = 0; qh < S; ++qh) m = cmax(m, jh_last(qh) - qh / 4 + 1);
-        return m;
-    }
-    static constexpr int NJ = nj();
-    static constexpr int JP = 4 * (cmax(jw_last(G8 - 1), jh_last(S - 1)) + 1);
-    static constexpr int kRelThreads = LPC * 2 * G8 * NJ;
     // dQ post-pass: rows j of the spread dRelW matrix
     static constexpr int JW = QWP + S - 1;
 
@@ -129,107 +110,6 @@ __device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 a, const
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[i][e] = fmaf(aa[i], bb[e], acc[i][e]);
-}
-
-// ------------------------------------------------------------ rel pre-pass
-// A thread owns one task of the block: (grid row l of the block, terms h or
-// w, group g of 8 block rows, j-group jg of 4 table rows).  Q is staged as
-// fp32 [c][64 block rows], the tables as 16-bit [terms][c][JP] (j fastest),
-// and the block's output rows as fp16 [64][rel_stride] before a coalesced
-// copy out.
-template <int S, bool BF>
-__global__ void __launch_bounds__(SamGeom<S>::kRelThreads, 2) bwd_sam_rel_kernel(const SamBwdParams p) {
-    using G = SamGeom<S>;
-    extern __shared__ __align__(16) unsigned char smem[];
-    const int d = p.d, stride = p.rel_stride;
-    uint16_t* sR = reinterpret_cast<uint16_t*>(smem);
-    float* sQ = reinterpret_cast<float*>(smem + (size_t)2 * d * G::JP * 2);
-    __half* sO = reinterpret_cast<__half*>(smem + (size_t)2 * d * G::JP * 2 + (size_t)d * 64 * 4);
-    const int tid = threadIdx.x, nt = blockDim.x;
-    const uint16_t* tab_h = static_cast<const uint16_t*>(p.rel_h);
-    const uint16_t* tab_w = static_cast<const uint16_t*>(p.rel_w);
-    for (int i = tid; i < 2 * d * G::JP; i += nt) {
-        const int part = i / (d * G::JP), rem = i - part * (d * G::JP), c = rem / G::JP, j = rem - c * G::JP;
-        sR[i] = j < G::NT ? (part ? tab_w : tab_h)[j * d + c] : (uint16_t)0;
-    }
-    const int jj = tid % G::NJ;
-    int rest = tid / G::NJ;
-    const int g = rest % G::G8;
-    rest /= G::G8;
-    const int part = rest & 1, l = rest >> 1;  // part 0: h terms, 1: w terms
-    const uint16_t* q16 = static_cast<const uint16_t*>(p.q);
-    const int nblk = p.BH * G::NBP;
-    for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
-        const int s = blk / G::NBP, bp = blk - s * G::NBP;
-        __syncthreads();  // the previous block is done with sQ and sO
-        for (int i = tid; i < 64 * (d / 8); i += nt) {
-            const int r = i & 63, c8 = i >> 6;
-            int grow;
-            float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (G::row(s, bp, r, p.Nq, grow))
-                unpack8<BF>(*reinterpret_cast<const uint4*>(q16 + (size_t)grow * d + c8 * 8), f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) sQ[(c8 * 8 + e) * 64 + r] = f[e];
-        }
-        for (int i = tid; i < 64 * stride / 2; i += nt) reinterpret_cast<uint32_t*>(sO)[i] = 0u;
-        __syncthreads();
-        const int qh = bp * G::LPC + l;
-        int jg0, cnt;
-        if (part) {
-            jg0 = 2 * g;
-            cnt = G::jw_last(g) - jg0 + 1;
-        } else {
-            jg0 = qh / 4;
-            cnt = G::jh_last(qh) - jg0 + 1;
-        }
-        if (qh < S && jj < cnt) {
-            const int jg = jg0 + jj;
-            float acc[8][4];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
-            const float* qa = sQ + l * G::QWP + 8 * g;
-            const uint16_t* rb = sR + (size_t)part * d * G::JP + 4 * jg;
-#pragma unroll 4
-            for (int c = 0; c < d; ++c) {
-                const float4 a0 = *reinterpret_cast<const float4*>(qa + c * 64);
-                const float4 a1 = *reinterpret_cast<const float4*>(qa + c * 64 + 4);
-                fma8x4(acc, a0, a1, ld4h<BF>(rb + c * G::JP));
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int qw = 8 * g + i;
-                if (qw < S) {
-                    __half* orow = sO + (l * G::QWP + qw) * stride + (part ? p.rw0 : 0);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = 4 * jg + e;
-                        const int kk = (part ? qw : qh) + S - 1 - j;
-                        if (kk >= 0 && kk < S) orow[kk] = __float2half_rn(acc[i][e] * kLog2eSam);
-                    }
-                }
-            }
-        }
-        __syncthreads();
-        const int cpr = stride / 8;  // 16-byte chunks per row
-        for (int i = tid; i < 64 * cpr; i += nt) {
-            const int r = i / cpr, ch = i - r * cpr;
-            int grow;
-            if (G::row(s, bp, r, p.Nq, grow))
-                *reinterpret_cast<uint4*>(p.rel + (size_t)grow * stride + ch * 8) =
-                    *reinterpret_cast<const uint4*>(sO + r * stride + ch * 8);
-        }
-        if constexpr (S != 64) {
-            // on 14-wide grids a key row can straddle the query pass's two column
-            // halves, so it adds its dRelH sums into rows cleared here
-            for (int i = tid; i < 64 * S; i += nt) {
-                const int r = i / S, kh = i - r * S;
-                int grow;
-                if (G::row(s, bp, r, p.Nq, grow)) p.d_relh[(size_t)grow * S + kh] = 0.f;
-            }
-        }
-    }
 }
 
 // --------------------------------------------------------------- dQ post-pass
@@ -495,14 +375,6 @@ cudaError_t launch_k(K kern, int work, int threads, size_t smem, int nsm, cudaSt
 }
 
 template <int S, bool BF>
-cudaError_t launch_pre(const SamBwdParams& p, int nsm, cudaStream_t st) {
-    using G = SamGeom<S>;
-    const size_t smem = (size_t)2 * p.d * G::JP * 2 + (size_t)p.d * 64 * 4 + (size_t)64 * p.rel_stride * 2;
-    const int nblk = p.BH * G::NBP;
-    return launch_k(bwd_sam_rel_kernel<S, BF>, nblk, G::kRelThreads, smem, nsm, st, p);
-}
-
-template <int S, bool BF>
 cudaError_t launch_post(const SamBwdParams& p, int nsm, cudaStream_t st) {
     using G = SamGeom<S>;
     const int nblk = p.BH * G::NBP;
@@ -616,12 +488,6 @@ cudaError_t launch_post14(const SamBwdParams& p, int nsm, cudaStream_t st) {
 int sam_bwd_groups(int S, int BH, int nsm) {
     const int nbp = S == 64 ? SamGeom<64>::NBP : SamGeom<14>::NBP;
     return std::max(1, std::min(BH, 2 * nsm / nbp));
-}
-
-cudaError_t launch_bwd_sam_rel(const SamBwdParams& p, int S, bool bf, int nsm, cudaStream_t st) {
-    if (S == 64) return bf ? launch_pre<64, true>(p, nsm, st) : launch_pre<64, false>(p, nsm, st);
-    if (S == 14) return bf ? launch_pre<14, true>(p, nsm, st) : launch_pre<14, false>(p, nsm, st);
-    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_sam_post(const SamBwdParams& p, int S, bool bf, int nsm, cudaStream_t st) {

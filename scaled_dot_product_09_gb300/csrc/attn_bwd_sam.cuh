@@ -1,5 +1,5 @@
 // attn_bwd_sam.cuh -- parameters and launchers of the SAM rel-pos parts of the
-// long-sequence backward (attn_bwd_sam.cu).
+// long-sequence backward (attn_bwd_sam_rel.cu, attn_bwd_sam.cu).
 #pragma once
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -17,10 +17,21 @@ struct SamBwdParams {
     float* d_bias;              // [2S-1][d] gradient of R_h, then [2S-1][d] of R_w (added to)
     int BH, Nq, d, rel_stride, rw0;
     int groups;                 // slice groups of the table pass (sam_bwd_groups)
+    int* status;                // device status word (a bounded wait that gave up)
+};
+
+// Row layout of the pre-pass output for a grid of side S: rel_h at
+// [0, S), rel_w at [kRw0, kRw0 + S), each part padded to a multiple of 8.
+template <int S>
+struct RelLayout {
+    static constexpr int kRw0 = (S + 7) / 8 * 8;
+    static constexpr int kStride = 2 * kRw0;
 };
 
 int sam_bwd_groups(int S, int BH, int nsm);
-cudaError_t launch_bwd_sam_rel(const SamBwdParams& p, int S, bool bf, int nsm, cudaStream_t st);
+// rel pre-pass on the tensor cores (attn_bwd_sam_rel.cu): rel_h, rel_w per
+// query row into p.rel; on 14-wide grids also clears p.d_relh
+cudaError_t launch_bwd_sam_rel_tc(const SamBwdParams& p, int S, bool bf, int nsm, cudaStream_t st);
 cudaError_t launch_bwd_sam_post(const SamBwdParams& p, int S, bool bf, int nsm, cudaStream_t st);
 
 }  // namespace sdpa09

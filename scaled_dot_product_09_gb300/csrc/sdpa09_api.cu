@@ -656,7 +656,8 @@ int run_bwd_long(const void* q, const void* k, const void* v, const void* out, c
         sp.rel_stride = stride;
         sp.rw0 = rw0;
         sp.groups = sam_bwd_groups(sw, (int)BH, nsm);
-        e = launch_bwd_sam_rel(sp, sw, bf, nsm, st);
+        sp.status = status;
+        e = launch_bwd_sam_rel_tc(sp, sw, bf, nsm, st);
         if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     }
 
