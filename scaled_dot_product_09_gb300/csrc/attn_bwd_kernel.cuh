@@ -340,15 +340,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!waitb(&bar_p, t & 1, kStatusWaitP)) break;
                 // the accumulators are rewritten once the epilogue has read the last tile's
                 if (t > 0 && !waitb(&bar_accfree, (t - 1) & 1, kStatusWaitO)) break;
+                // descriptors built once; a step only moves the start-address
+                // field (16-byte units): 512 B per 16 rows, kBlockM * 32 B per
+                // 16-column block
+                const uint64_t dP = vdesc(aP), dSm = vdesc(aDS), dSk = kdesc(aDS);
+                const uint64_t dDO = vdesc(aDO), dQm = vdesc(aQ), dKm = vdesc(aK);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)  // dV = P^T.dO over 16 query rows per step
-                    mma_ss(tDV, vdesc(aP + ks * 512), vdesc(aDO + ks * 512), idesc_g, ks > 0 ? 1u : 0u);
+                    mma_ss(tDV, dP + (uint64_t)(ks * 32), dDO + (uint64_t)(ks * 32), idesc_g, ks > 0 ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)  // dK = dS^T.Q
-                    mma_ss(tDK, vdesc(aDS + ks * 512), vdesc(aQ + ks * 512), idesc_g, ks > 0 ? 1u : 0u);
+                    mma_ss(tDK, dSm + (uint64_t)(ks * 32), dQm + (uint64_t)(ks * 32), idesc_g, ks > 0 ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)  // dQ = dS.K over 16 keys per step
-                    mma_ss(tDQ, kdesc(aDS + ks * (kBlockM * 32)), vdesc(aK + ks * 512), idesc_q, ks > 0 ? 1u : 0u);
+                    mma_ss(tDQ, dSk + (uint64_t)(ks * (kBlockM * 32 / 16)), dKm + (uint64_t)(ks * 32), idesc_q,
+                           ks > 0 ? 1u : 0u);
                 mma_commit(&bar_pfree);
                 mma_commit(&bar_acc);
                 mma_commit(&bar_empty[st]);

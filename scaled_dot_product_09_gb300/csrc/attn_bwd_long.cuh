@@ -228,19 +228,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     // the accumulators are rewritten once the last job's epilogue read them
                     if (it == 0 && jn > 0 && !waitb(&bar_accfree, (jn - 1) & 1, kStatusWaitO)) { ok = false; break; }
                     const uint32_t acc = it > 0 ? 1u : 0u;
+                    // descriptors built once; a step only moves the start-address
+                    // field (16-byte units): 512 B per 16 rows, kBlockM * 32 B per
+                    // 16-column block
                     if constexpr (kKey) {
-                        const uint32_t aQ = b, aDO = b + T::kBytes;
+                        const uint64_t dP = vdesc(aP), dS = vdesc(aDS), dQ = vdesc(b), dDO = vdesc(b + T::kBytes);
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)  // dV += P^T.dO over 16 query rows per step
-                            mma_ss(tA0, vdesc(aP + ks * 512), vdesc(aDO + ks * 512), idesc_g, (acc || ks > 0) ? 1u : 0u);
+                            mma_ss(tA0, dP + (uint64_t)(ks * 32), dDO + (uint64_t)(ks * 32), idesc_g, (acc || ks > 0) ? 1u : 0u);
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)  // dK += dS^T.Q
-                            mma_ss(tA1, vdesc(aDS + ks * 512), vdesc(aQ + ks * 512), idesc_g, (acc || ks > 0) ? 1u : 0u);
+                            mma_ss(tA1, dS + (uint64_t)(ks * 32), dQ + (uint64_t)(ks * 32), idesc_g, (acc || ks > 0) ? 1u : 0u);
                     } else {
-                        const uint32_t aK = b;
+                        const uint64_t dS = kdesc(aDS), dK = vdesc(b);
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)  // dQ += dS.K over 16 keys per step
-                            mma_ss(tA0, kdesc(aDS + ks * (kBlockM * 32)), vdesc(aK + ks * 512), idesc_q,
+                            mma_ss(tA0, dS + (uint64_t)(ks * (kBlockM * 32 / 16)), dK + (uint64_t)(ks * 32), idesc_q,
                                    (acc || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(&bar_pfree);
