@@ -114,6 +114,16 @@ def test_bwd_sam_global_64x64():
     _bwd_case(W["sam_vith_global"].with_(B=1, H=1, seed=98), use_lse=True)
 
 
+@pytest.mark.parametrize("case", ["14x14_d56_fp16", "64x64_d64_bf16"])
+def test_bwd_sam_narrow_heads(case):
+    """Head dims padded to 64 (d = 56: a partial 16-column block; d = 64),
+    fp16 and bf16: the rel pre-pass and both passes in their 64-column
+    instantiations."""
+    w = {"14x14_d56_fp16": W["sam_vith_window"].with_(B=1, H=3, d=56, dtype="fp16", seed=101),
+         "64x64_d64_bf16": W["sam_vith_global"].with_(B=1, H=1, d=64, seed=102)}[case]
+    _bwd_case(w, use_lse=True)
+
+
 # ------------------------------------------------- Swin image token layout --
 def _images(w):
     return w.B // ((w.grid_h // w.win) * (w.grid_w // w.win))
