@@ -1535,34 +1535,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (MODE == kModeShared && (kShDbl || p.nq == 2)) {
                 // The warp's 32 output rows, consecutive tokens of one slice,
-                // are staged so that each store writes 512 contiguous bytes: in
-                // the slot's finished Q tile (every P.V of the job is done),
-                // which then goes back to the producer, or in the one-tile
-                // pipeline's own staging area.
-                const int rb = p.d * 2;  // bytes per output row
+                // are staged so that they leave as 512 contiguous bytes per
+                // store: in the slot's finished Q tile (every P.V of the job
+                // is done), which then goes back to the producer, stored by
+                // the warp; or, in the one-tile pipeline, in its own staging
+                // area, written again one job later, from where lane 0 sends
+                // them in one bulk copy (async proxy), so the warp issues no
+                // stores.  (A bulk copy out of the Q tile measured slower: the
+                // tile goes back to the producer only once the copy has read
+                // it.)
+                const int rb = p.d * 2;  // bytes per output row (a multiple of 16)
                 unsigned char* stg = (kShDbl ? sExtraB + x * (kBlockM * rb) : sQ + (x * p.nq + qbuf) * T::kBytes) +
                                      (warp & 3) * (32 * rb);
                 if (!DBG) {
+                    if constexpr (kShDbl) {
+                        // the copy of this warp's previous rows has read them
+                        if (lane == 0) bulk_wait_read0();
+                        __syncwarp();
+                    }
 #pragma unroll
                     for (int c = 0; c < DPAD / 8; ++c)
                         if (c * 8 < p.d)
                             *reinterpret_cast<uint4*>(stg + lane * rb + c * 16) =
                                 make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                    if constexpr (kShDbl) fence_proxy_async_smem();  // read through the async proxy
                     __syncwarp();
                     const int nvalid = __popc(__ballot_sync(0xffffffffu, rok));  // a prefix of the lanes
                     unsigned char* dst = reinterpret_cast<unsigned char*>(p.out) +
                                          ((size_t)__shfl_sync(0xffffffffu, slice, 0) * p.Nq +
                                           __shfl_sync(0xffffffffu, tok, 0)) * (size_t)rb;
-                    const int nch = nvalid * rb / 16;
-                    for (int q = lane; q < nch; q += 32)
-                        *reinterpret_cast<uint4*>(dst + (size_t)q * 16) = *reinterpret_cast<const uint4*>(stg + q * 16);
+                    if constexpr (kShDbl) {
+                        if (lane == 0 && nvalid > 0) {
+                            bulk_s2g(dst, stg, (uint32_t)(nvalid * rb));
+                            bulk_commit();
+                        }
+                    } else {
+                        const int nch = nvalid * rb / 16;
+                        for (int q = lane; q < nch; q += 32)
+                            *reinterpret_cast<uint4*>(dst + (size_t)q * 16) = *reinterpret_cast<const uint4*>(stg + q * 16);
+                    }
                 }
                 if constexpr (!kShDbl) {
                     // generic accesses before the producer's next TMA write here
                     fence_proxy_async_smem();
                     warp_arrive(&bar_q_empty[x][qbuf]);
                 } else {
-                    __syncwarp();  // staged rows read before the next job writes them
+                    __syncwarp();
                 }
             } else if (rok && !DBG) {
                 // windows layout: [slice][token]; image layout: the token's
@@ -2091,6 +2109,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     epilogue(tO + ((ju - 1) & 1) * DPAD, pv_l, pv_m, pv_slice, pv_tok, pv_ok, 0);
                 }
             }
+        }
+        if constexpr (kShDbl) {
+            // the output copies have completed before the CTA retires
+            if (lane == 0) bulk_wait0();
+            __syncwarp();
         }
     }
 

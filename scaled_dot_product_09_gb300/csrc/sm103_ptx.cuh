@@ -132,6 +132,20 @@ __device__ __forceinline__ void cp_async_wait_n(int n) {
     }
 }
 
+// ------------------------------------------------ bulk copy shared -> global --
+// An async-proxy copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from shared to global memory, in this thread's bulk groups.
+__device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// until this thread's bulk copies have read their shared-memory sources
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// until they have completed
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ------------------------------------------- programmatic dependent launch --
 // Let the next kernel on the stream launch its CTAs as this grid's CTAs exit.
 __device__ __forceinline__ void griddep_launch_dependents() {
