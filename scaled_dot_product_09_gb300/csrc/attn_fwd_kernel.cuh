@@ -690,6 +690,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // P.V issued, and overlap that job's epilogue.  The first P.V of the job
     // (which overwrites O) waits for that epilogue.
     constexpr bool kGinP = MODE == kModeShared && BIAS == kBiasSam && SW == 14 && kSepP;
+    // Output rows staged per warp leave in one bulk copy (short jobs: the
+    // one-tile pipeline and the SAM 14 x 14 windows), else as the warp's
+    // own coalesced stores (long jobs, where the copy measured slower)
+    constexpr bool kBulkOut = kShDbl || kGinP;
     // Packed tiling with head dims up to 32 and slots up to 64 rows: two O
     // buffers per slot (O_x holds 64 columns), so a tile's output is written
     // while the next tile's P.V runs.
@@ -1495,6 +1499,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tP = kSepP ? tmem + lane_base + (uint32_t)(kOffP + 64 * x) : tS;  // kDbS: + 64 * buffer
         const uint32_t tO = kDbS ? tS + 128 : tmem + lane_base + (uint32_t)(kSepP ? kOffO + kOw * x : 256 + 128 * x);
         int pvd_cnt = 0;  // P.V completions of this slot awaited (separate P buffers)
+        // Q buffer whose staged output rows a bulk copy is still reading (-1:
+        // none); it goes back to the producer during the next job
+        int q_pending = -1;
+        auto release_q = [&]() {
+            if (q_pending < 0) return;
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+            warp_arrive(&bar_q_empty[x][q_pending]);
+            q_pending = -1;
+        };
         int cnt_s = 0, ju = 0;
         bool ok = true;
         const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
@@ -1535,15 +1549,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (MODE == kModeShared && (kShDbl || p.nq == 2)) {
                 // The warp's 32 output rows, consecutive tokens of one slice,
-                // are staged so that they leave as 512 contiguous bytes per
-                // store: in the slot's finished Q tile (every P.V of the job
-                // is done), which then goes back to the producer, stored by
-                // the warp; or, in the one-tile pipeline, in its own staging
-                // area, written again one job later, from where lane 0 sends
-                // them in one bulk copy (async proxy), so the warp issues no
-                // stores.  (A bulk copy out of the Q tile measured slower: the
-                // tile goes back to the producer only once the copy has read
-                // it.)
+                // are staged: in the slot's finished Q tile (every P.V of the
+                // job is done), which then goes back to the producer, or, in
+                // the one-tile pipeline, in its own staging area, written
+                // again one job later.  With kBulkOut they leave in one bulk
+                // copy (async proxy) of their contiguous bytes, issued by lane
+                // 0, so the warp issues no stores; a Q tile then goes back
+                // once the copy has read it -- during the next job, after its
+                // first scores, so that the copy is not waited for here.
+                // Otherwise the warp stores them, 512 contiguous bytes per
+                // instruction.
                 const int rb = p.d * 2;  // bytes per output row (a multiple of 16)
                 unsigned char* stg = (kShDbl ? sExtraB + x * (kBlockM * rb) : sQ + (x * p.nq + qbuf) * T::kBytes) +
                                      (warp & 3) * (32 * rb);
@@ -1558,13 +1573,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (c * 8 < p.d)
                             *reinterpret_cast<uint4*>(stg + lane * rb + c * 16) =
                                 make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-                    if constexpr (kShDbl) fence_proxy_async_smem();  // read through the async proxy
+                    if constexpr (kBulkOut) fence_proxy_async_smem();  // read through the async proxy
                     __syncwarp();
                     const int nvalid = __popc(__ballot_sync(0xffffffffu, rok));  // a prefix of the lanes
                     unsigned char* dst = reinterpret_cast<unsigned char*>(p.out) +
                                          ((size_t)__shfl_sync(0xffffffffu, slice, 0) * p.Nq +
                                           __shfl_sync(0xffffffffu, tok, 0)) * (size_t)rb;
-                    if constexpr (kShDbl) {
+                    if constexpr (kBulkOut) {
                         if (lane == 0 && nvalid > 0) {
                             bulk_s2g(dst, stg, (uint32_t)(nvalid * rb));
                             bulk_commit();
@@ -1576,9 +1591,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if constexpr (!kShDbl) {
-                    // generic accesses before the producer's next TMA write here
-                    fence_proxy_async_smem();
-                    warp_arrive(&bar_q_empty[x][qbuf]);
+                    if (!kBulkOut || DBG) {
+                        // generic accesses before the producer's next TMA write here
+                        fence_proxy_async_smem();
+                        warp_arrive(&bar_q_empty[x][qbuf]);
+                    } else {
+                        q_pending = qbuf;
+                    }
                 } else {
                     __syncwarp();
                 }
@@ -1930,6 +1949,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[x], cnt_s & 1, abort_flag, kStatusWaitS))) { ok = false; break; }
                     ++cnt_s;
                     tc_fence_after();
+                    if (kBulkOut && j == 0) release_q();  // the last job's Q tile, once its output copy has read it
                     float xs[kCols];
                     {
                         uint32_t v[kCols];
@@ -2110,7 +2130,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if constexpr (kShDbl) {
+        if constexpr (kBulkOut) {
+            release_q();
             // the output copies have completed before the CTA retires
             if (lane == 0) bulk_wait0();
             __syncwarp();
