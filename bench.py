@@ -609,7 +609,7 @@ def main(argv=None):
         torch.cuda.empty_cache()
         suite = _suite(stream, dev, peaks, [n for n in ("swin_t_stage1", "swin_t_stage1@image", "swin_t_stage1@bwd",
                                                         "sam_vith_window", "sam_vith_window@bwd", "sam_vith_global",
-                                                        "sam_vith_global@bwd", "sam_vith_global_768", "sd_unet_self",
+                                                        "sam_vith_global@bwd", "sam_vith_global_768", "sam_vith_global_768@bwd", "sd_unet_self",
                                                         "sd_unet_self@bwd", "sd_unet_cross", "sd_unet_self_varlen")
                                             if n != w.name])
     if rank == 0:

@@ -237,11 +237,14 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, cons
  *             kernel folds the shift and the window partition into its loads
  *             and their inverse into its stores) or ATTN_BIAS_SAM_RELPOS (bias_args as for
  *             attn_fwd, with equal square query and key grids of side
- *             S = 14 or 64 and tables of 2*S-1 rows).
+ *             S = 14, 48 or 64 and tables of 1 to 128 rows; tables of another
+ *             length than 2*S-1 are resampled to 2*S-1 rows as the forward
+ *             resamples them, and their gradients returned through the
+ *             transposed resampling).
  *  d_bias     device fp32 bias gradient, ADDED to (the caller zeroes it
  *             first): ATTN_BIAS_SWIN: [(2*win-1)^2][H]; ATTN_BIAS_SAM_RELPOS:
- *             [2*S-1][d] for R_h followed by [2*S-1][d] for R_w; NULL
- *             otherwise.
+ *             [rel_h rows][d] for R_h followed by [rel_w rows][d] for R_w
+ *             (the tables' lengths as given); NULL otherwise.
  *  workspace, workspace_bytes
  *             device scratch of at least attn_bwd_workspace_size(...) bytes,
  *             16-byte aligned, owned by the caller (NULL when that size is

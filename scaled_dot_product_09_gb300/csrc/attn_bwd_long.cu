@@ -73,6 +73,9 @@ static cudaError_t launch_long_d(int mode, int sw, const BwdMaps& tm, const BwdL
         if (sw == 14)
             return mode == kBwdKeyPass ? launch_long_one<DPAD, kBiasSam, kBwdKeyPass, 14>(tm, p, grid, smem, st)
                                        : launch_long_one<DPAD, kBiasSam, kBwdQueryPass, 14>(tm, p, grid, smem, st);
+        if (sw == 48)
+            return mode == kBwdKeyPass ? launch_long_one<DPAD, kBiasSam, kBwdKeyPass, 48>(tm, p, grid, smem, st)
+                                       : launch_long_one<DPAD, kBiasSam, kBwdQueryPass, 48>(tm, p, grid, smem, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -57,7 +57,7 @@ struct BwdLongParams {
     int BH, Nq, Nk, d;
     int n_qb, n_kb;         // query / key blocks per slice
     int n_jobs;
-    int kv_w;               // keys per key block (128; 112 on 14-wide SAM grids)
+    int kv_w;               // keys per key block (128; 112 on 14-wide SAM grids, 96 on 48-wide ones)
     int k_h, k_w, rel_stride, rw0;
     int nst;
     int full_atoms, part;
@@ -82,7 +82,7 @@ template <int DPAD, int BIAS, int MODE, int SW>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_long_kernel(const __grid_constant__ BwdMaps tm, const BwdLongParams p) {
     using T = Tile<DPAD>;
-    static_assert(BIAS == kBiasNone || (BIAS == kBiasSam && (SW == 14 || SW == 64)), "bias kinds");
+    static_assert(BIAS == kBiasNone || (BIAS == kBiasSam && (SW == 14 || SW == 48 || SW == 64)), "bias kinds");
     static_assert(256 + 2 * DPAD <= 512 && 256 + DPAD + 64 <= 512, "tensor memory");
     constexpr bool kSam = BIAS == kBiasSam;
     constexpr bool kKey = MODE == kBwdKeyPass;
@@ -293,7 +293,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // rel_w of every key column as fp16 pairs, rel_h of the key rows
                 constexpr int kRW = SW > 0 ? (SW + 1) / 2 : 1;
                 __half2 rw2[kRW];
-                float rh[SW > 0 ? (SW < 64 ? 8 : 1) : 1];
+                // key rows per key tile: 2 on 64- and 48-wide grids, 8 on 14-wide ones
+                constexpr int kKR = SW == 14 ? 8 : 2;
+                float rh[SW > 0 ? (SW == 64 ? 1 : kKR) : 1];
                 if constexpr (kSam) {
                     const __half* rel = p.rel + ((size_t)slice * p.Nq + (q_ok ? q : 0)) * p.rel_stride;
                     const int kh0 = key0 / SW;
@@ -307,6 +309,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                     if constexpr (SW == 64) {
                         rh[0] = __half2float(rel[min(kh0 + half, p.k_h - 1)]);
+                    } else if constexpr (SW == 48) {
+                        // key rows kh0, kh0 + 1 (kh0 is even)
+                        const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(rel + kh0));
+                        rh[0] = f2.x;
+                        rh[1] = f2.y;
                     } else {
                         float f[8];
                         half8(rel + kh0, f);  // key rows kh0..kh0+7 (kh0 is a multiple of 8)
@@ -337,7 +344,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             const float2 rwf = __half22float2(rw2[(col % SW) / 2]);
                             const float rwv = ((col % SW) & 1) ? rwf.y : rwf.x;
                             if constexpr (SW == 64) b = rh[0] + rwv;
-                            else b = rh[col / SW < 8 ? col / SW : 7] + rwv;
+                            else b = rh[col / SW < kKR ? col / SW : kKR - 1] + rwv;
                         }
                         const bool valid = q_ok && col < nvalid;
                         xs[c] = valid ? ex2_approx(fmaf(xs[c], p.scale_log2, b - lse2)) : 0.f;
@@ -352,8 +359,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     warp_arrive(&bar_sfree);
                     if constexpr (kSam && !kKey) {
                         // dRelH: the row's dS summed over each key row of its columns
-                        // (64-wide grids: one key row per column half, stored; on 14-wide
-                        // grids a key row can straddle the halves: atomic adds);
+                        // (64-wide grids: one key row per column half, stored; on 14- and
+                        // 48-wide grids a key row can straddle the halves: atomic adds);
                         // dRelW: summed per key column over the job's key rows
                         if (q_ok) {
                             const int kh0 = key0 / SW;
@@ -361,7 +368,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             constexpr int kr0 = (64 * H0) / SW, kr1 = (64 * H0 + 63) / SW;
 #pragma unroll
                             for (int kr = kr0; kr <= kr1; ++kr) {
-                                if (kr < (SW == 64 ? 2 : 8)) {
+                                if (kr < kKR) {
                                     float a = 0.f;
 #pragma unroll
                                     for (int c = 0; c < 64; ++c)

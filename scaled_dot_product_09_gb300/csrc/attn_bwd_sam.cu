@@ -12,10 +12,13 @@
 // (Segment Anything, image encoder: the decomposed relative position terms
 // added to the attention logits, and their gradients by the chain rule.)
 //
-// The grids are square: side S = 14 or 64, tables of 2 S - 1 rows.  Work is
-// cut in blocks of 64 query rows of one slice: one grid row when S = 64; four
-// grid rows, each padded from 14 to 16 columns, when S = 14 (block row r is
-// grid row bp * LPC + r / QWP, grid column r % QWP; padded rows are zero).
+// The grids are square: side S = 14, 48 or 64, tables of 2 S - 1 rows (tables
+// of another length are resampled to that first, and their gradients
+// resampled back; see the end of this file).  Work is cut in blocks of 64
+// query rows of one slice: one grid row when S = 64 (S = 48: one grid row
+// padded to 64); four grid rows, each padded from 14 to 16 columns, when
+// S = 14 (block row r is grid row bp * LPC + r / QWP, grid column r % QWP;
+// padded rows are zero).
 // Every product is a small GEMM tiled in registers: a thread keeps an 8 x 4
 // (dQ) or 4 x 4 (tables) tile of outputs and reads both operands as float4
 // (or four 16-bit values) from shared memory.  For the w terms the index
@@ -38,7 +41,7 @@ namespace {
 
 template <int S>
 struct SamGeom {
-    static_assert(S == 14 || S == 64, "SAM backward grids are 14 x 14 or 64 x 64");
+    static_assert(S == 14 || S == 48 || S == 64, "SAM backward grids are 14 x 14, 48 x 48 or 64 x 64");
     static constexpr int QWP = S > 16 ? 64 : 16;    // block rows per grid row
     static constexpr int LPC = 64 / QWP;            // grid rows per block
     static constexpr int NBP = (S + LPC - 1) / LPC; // blocks per slice
@@ -252,8 +255,8 @@ constexpr int kTabThreads = 320;
 template <int S, bool BF>
 __global__ void __launch_bounds__(kTabThreads, 2) bwd_sam_dtab_kernel(const SamBwdParams p) {
     using G = SamGeom<S>;
-    constexpr int KHP = S == 64 ? 64 : 16;   // dRelH row pitch
-    constexpr int JWS = S == 64 ? 128 : 32;  // spread dRelW row pitch (>= QWP + S - 1, multiple of 4)
+    constexpr int KHP = S > 16 ? 64 : 16;   // dRelH row pitch
+    constexpr int JWS = S > 16 ? 128 : 32;  // spread dRelW row pitch (>= QWP + S - 1, multiple of 4)
     constexpr int JG = (G::NT + 3) / 4;      // j-groups of the w table
     static_assert(G::QWP + S - 1 <= JWS && 4 * JG <= JWS, "pitch");
     extern __shared__ __align__(16) unsigned char smem[];
@@ -381,7 +384,7 @@ cudaError_t launch_post(const SamBwdParams& p, int nsm, cudaStream_t st) {
     const size_t smem_dq = (size_t)2 * G::NT * p.d * 2 + (size_t)(S + G::JW) * kAP * 4;
     cudaError_t e = launch_k(bwd_sam_dq_kernel<S, BF>, nblk, kDqThreads, smem_dq, nsm, st, p);
     if (e != cudaSuccess) return e;
-    constexpr int KHP = S == 64 ? 64 : 16, JWS = S == 64 ? 128 : 32;
+    constexpr int KHP = S > 16 ? 64 : 16, JWS = S > 16 ? 128 : 32;
     const size_t smem_t = (size_t)64 * (KHP + JWS + p.d) * 4;
     // one CTA per (block position, slice group): the grid is exactly that
     cudaError_t e2 = cudaFuncSetAttribute(bwd_sam_dtab_kernel<S, BF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_t);
@@ -486,14 +489,88 @@ cudaError_t launch_post14(const SamBwdParams& p, int nsm, cudaStream_t st) {
 }  // namespace
 
 int sam_bwd_groups(int S, int BH, int nsm) {
-    const int nbp = S == 64 ? SamGeom<64>::NBP : SamGeom<14>::NBP;
+    const int nbp = S == 64 ? SamGeom<64>::NBP : (S == 48 ? SamGeom<48>::NBP : SamGeom<14>::NBP);
     return std::max(1, std::min(BH, 2 * nsm / nbp));
 }
 
 cudaError_t launch_bwd_sam_post(const SamBwdParams& p, int S, bool bf, int nsm, cudaStream_t st) {
     if (S == 64) return bf ? launch_post<64, true>(p, nsm, st) : launch_post<64, false>(p, nsm, st);
+    if (S == 48) return bf ? launch_post<48, true>(p, nsm, st) : launch_post<48, false>(p, nsm, st);
     if (S == 14) return bf ? launch_post14<true>(p, nsm, st) : launch_post14<false>(p, nsm, st);
     return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------- resampled tables (rel_pos_resized)
+// A table of lin rows used at lout = 2 S - 1 rows: row m is the linear
+// interpolation, at half-pixel centres clamped to the table, of rows i0(m)
+// and i1(m) with weights 1 - w(m) and w(m) -- the forward's resampling,
+// rounded to the operand type as there.  The backward runs on the resampled
+// rows and returns their fp32 gradients through the transposed map:
+// dR[i] += sum over m with i0(m) = i of (1 - w(m)) dR'[m] + sum over m with
+// i1(m) = i of w(m) dR'[m].
+namespace {
+
+__device__ __forceinline__ void resample_pos(int m, int lin, int lout, int& i0, int& i1, float& w1) {
+    const float pos = fmaxf(__fmul_rn((float)lin / (float)lout, (float)m + 0.5f) - 0.5f, 0.f);
+    i0 = min((int)pos, lin - 1);
+    i1 = min(i0 + 1, lin - 1);
+    w1 = pos - (float)i0;
+}
+
+// dst [lout][d] 16-bit from src [lin][d]; also clears dz (n floats)
+template <bool BF>
+__global__ void bwd_sam_resample_kernel(const uint16_t* src, uint16_t* dst, int lin, int lout, int d, float* dz, int n) {
+    const int stride = gridDim.x * blockDim.x;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < lout * d; i += stride) {
+        const int m = i / d, c = i - m * d;
+        int i0, i1;
+        float w1;
+        resample_pos(m, lin, lout, i0, i1, w1);
+        const uint16_t a = src[(size_t)i0 * d + c], b = src[(size_t)i1 * d + c];
+        const float fa = BF ? __bfloat162float(__ushort_as_bfloat16(a)) : __half2float(__ushort_as_half(a));
+        const float fb = BF ? __bfloat162float(__ushort_as_bfloat16(b)) : __half2float(__ushort_as_half(b));
+        const float v = (1.f - w1) * fa + w1 * fb;
+        dst[i] = BF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
+    }
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) dz[i] = 0.f;
+}
+
+// dR [lin][d] += the transposed resampling of dRr [lout][d]
+__global__ void bwd_sam_unresample_kernel(const float* dRr, float* dR, int lin, int lout, int d) {
+    const int stride = gridDim.x * blockDim.x;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < lin * d; i += stride) {
+        const int r = i / d, c = i - r * d;
+        float acc = 0.f;
+        for (int m = 0; m < lout; ++m) {
+            int i0, i1;
+            float w1;
+            resample_pos(m, lin, lout, i0, i1, w1);
+            if (i0 == r) acc += (1.f - w1) * dRr[(size_t)m * d + c];
+            if (i1 == r) acc += w1 * dRr[(size_t)m * d + c];
+        }
+        dR[i] += acc;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_sam_resample(const void* src, void* dst, int lin, int lout, int d, bool bf, float* dz, int n,
+                                    cudaStream_t st) {
+    const int work = std::max(lout * d, n);
+    const int blocks = std::max(1, std::min((work + 255) / 256, 1024));
+    if (bf)
+        bwd_sam_resample_kernel<true><<<blocks, 256, 0, st>>>(static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst),
+                                                              lin, lout, d, dz, n);
+    else
+        bwd_sam_resample_kernel<false><<<blocks, 256, 0, st>>>(static_cast<const uint16_t*>(src),
+                                                               static_cast<uint16_t*>(dst), lin, lout, d, dz, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_sam_unresample(const float* dRr, float* dR, int lin, int lout, int d, cudaStream_t st) {
+    const int blocks = std::max(1, std::min((lin * d + 255) / 256, 1024));
+    bwd_sam_unresample_kernel<<<blocks, 256, 0, st>>>(dRr, dR, lin, lout, d);
+    return cudaGetLastError();
 }
 
 }  // namespace sdpa09

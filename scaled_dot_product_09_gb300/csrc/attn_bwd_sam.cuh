@@ -33,5 +33,11 @@ int sam_bwd_groups(int S, int BH, int nsm);
 // query row into p.rel; on 14-wide grids also clears p.d_relh
 cudaError_t launch_bwd_sam_rel_tc(const SamBwdParams& p, int S, bool bf, int nsm, cudaStream_t st);
 cudaError_t launch_bwd_sam_post(const SamBwdParams& p, int S, bool bf, int nsm, cudaStream_t st);
+// tables of another length: the resampled 16-bit copy [lout][d] of a table
+// [lin][d] (also clears n floats at dz), and the transposed resampling of the
+// gradient of that copy added to the table's gradient
+cudaError_t launch_bwd_sam_resample(const void* src, void* dst, int lin, int lout, int d, bool bf, float* dz, int n,
+                                    cudaStream_t st);
+cudaError_t launch_bwd_sam_unresample(const float* dRr, float* dR, int lin, int lout, int d, cudaStream_t st);
 
 }  // namespace sdpa09

@@ -228,12 +228,16 @@ cudaError_t launch_rel_tc_d(const SamBwdParams& p, int nsm, cudaStream_t st) {
 
 }  // namespace
 
+template <int S>
+cudaError_t launch_rel_tc_s(const SamBwdParams& p, bool bf, int nsm, cudaStream_t st) {
+    if (p.rel_stride != RelLayout<S>::kStride || p.rw0 != RelLayout<S>::kRw0) return cudaErrorInvalidValue;
+    return bf ? launch_rel_tc_d<S, true>(p, nsm, st) : launch_rel_tc_d<S, false>(p, nsm, st);
+}
+
 cudaError_t launch_bwd_sam_rel_tc(const SamBwdParams& p, int S, bool bf, int nsm, cudaStream_t st) {
-    if (p.rel_stride != (S == 64 ? RelLayout<64>::kStride : RelLayout<14>::kStride) ||
-        p.rw0 != (S == 64 ? RelLayout<64>::kRw0 : RelLayout<14>::kRw0))
-        return cudaErrorInvalidValue;
-    if (S == 64) return bf ? launch_rel_tc_d<64, true>(p, nsm, st) : launch_rel_tc_d<64, false>(p, nsm, st);
-    if (S == 14) return bf ? launch_rel_tc_d<14, true>(p, nsm, st) : launch_rel_tc_d<14, false>(p, nsm, st);
+    if (S == 64) return launch_rel_tc_s<64>(p, bf, nsm, st);
+    if (S == 48) return launch_rel_tc_s<48>(p, bf, nsm, st);
+    if (S == 14) return launch_rel_tc_s<14>(p, bf, nsm, st);
     return cudaErrorInvalidValue;
 }
 

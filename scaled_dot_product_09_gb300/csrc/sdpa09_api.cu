@@ -556,12 +556,14 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
 // Layout of the long-sequence backward's workspace (byte offsets, each
 // 256-byte aligned): D [rows] fp32; for SAM also the rel terms [rows][stride]
 // fp16, scale dS.K [rows][d] fp32, dRelH [rows][k_h] fp32 and dRelW
-// [2][rows][k_w] fp32, one array per column half (rows = B * H * Nq).
+// [2][rows][k_w] fp32, one array per column half (rows = B * H * Nq); with
+// tables of another length than 2 S - 1 rows also their resampled 16-bit
+// copies [2][2S-1][d] and the fp32 gradients of those [2][2S-1][d].
 struct BwdWs {
-    size_t d, rel, dq32, drh, drw, total;
+    size_t d, rel, dq32, drh, drw, rtab, drr, total;
 };
 static size_t al256(size_t x) { return (x + 255) / 256 * 256; }
-static BwdWs bwd_ws_layout(int64_t rows, int d, bool sam, int s_h, int s_w, int rel_stride) {
+static BwdWs bwd_ws_layout(int64_t rows, int d, bool sam, int s_h, int s_w, int rel_stride, bool resample) {
     BwdWs w{};
     size_t o = 0;
     w.d = o;
@@ -575,9 +577,23 @@ static BwdWs bwd_ws_layout(int64_t rows, int d, bool sam, int s_h, int s_w, int 
         o += al256((size_t)rows * s_h * 4);
         w.drw = o;
         o += al256((size_t)2 * rows * s_w * 4);
+        if (resample) {
+            const size_t nt = (size_t)(2 * s_w - 1);
+            w.rtab = o;
+            o += al256(2 * nt * d * 2);
+            w.drr = o;
+            o += al256(2 * nt * d * 4);
+        }
     }
     w.total = o;
     return w;
+}
+// table lengths of a SAM bias as given (0: 2 * side - 1) and whether the
+// backward resamples them
+static bool sam_bwd_resample(const attn_sam_args* a, int* lh, int* lw) {
+    *lh = a->rel_h_len ? a->rel_h_len : 2 * a->q_h - 1;
+    *lw = a->rel_w_len ? a->rel_w_len : 2 * a->q_w - 1;
+    return *lh != 2 * a->q_h - 1 || *lw != 2 * a->q_w - 1;
 }
 static bool bwd_is_windows(int Nq, int Nk, int d) { return Nq <= kBlockM && Nk <= kBlockN && dpad_for(d) <= 64; }
 static int sam_rel_stride(int s_h, int s_w, int* rw0) {
@@ -589,7 +605,7 @@ size_t bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d, attn_bias_kind b
     if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return 0;
     if (bias_kind != ATTN_BIAS_SAM_RELPOS && bwd_is_windows(Nq, Nk, d)) return 0;
     const int64_t rows = (int64_t)B * H * Nq;
-    bool sam = false;
+    bool sam = false, resample = false;
     int s_h = 0, s_w = 0, stride = 0, rw0 = 0;
     if (bias_kind == ATTN_BIAS_SAM_RELPOS && bias_args) {
         const attn_sam_args* a = static_cast<const attn_sam_args*>(bias_args);
@@ -597,8 +613,10 @@ size_t bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d, attn_bias_kind b
         s_h = a->q_h;
         s_w = a->q_w;
         stride = sam_rel_stride(s_h, s_w, &rw0);
+        int lh = 0, lw = 0;
+        resample = sam_bwd_resample(a, &lh, &lw);
     }
-    return bwd_ws_layout(rows, d, sam, s_h, s_w, stride).total;
+    return bwd_ws_layout(rows, d, sam, s_h, s_w, stride, resample).total;
 }
 
 // Sequences longer than one 128-key tile (or d > 64): pre-pass for D, then
@@ -612,9 +630,13 @@ int run_bwd_long(const void* q, const void* k, const void* v, const void* out, c
         return fail(ATTN_ERR_ARG, "sequences over 128 tokens (or d > 64) need the forward's lse (attn_fwd_train)");
     if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return fail(ATTN_ERR_ARG, "lse must be 4-byte aligned");
     const int64_t BH = (int64_t)B * H, rows = BH * Nq;
-    int rw0 = 0, stride = 0;
-    if (sam) stride = sam_rel_stride(sam->q_h, sam->q_w, &rw0);
-    const BwdWs ws = bwd_ws_layout(rows, d, sam != nullptr, sam ? sam->q_h : 0, sam ? sam->q_w : 0, stride);
+    int rw0 = 0, stride = 0, lin_h = 0, lin_w = 0;
+    bool resample = false;
+    if (sam) {
+        stride = sam_rel_stride(sam->q_h, sam->q_w, &rw0);
+        resample = sam_bwd_resample(sam, &lin_h, &lin_w);
+    }
+    const BwdWs ws = bwd_ws_layout(rows, d, sam != nullptr, sam ? sam->q_h : 0, sam ? sam->q_w : 0, stride, resample);
     if (!workspace || workspace_bytes < ws.total)
         return fail(ATTN_ERR_ARG, "workspace of %zu bytes needed (attn_bwd_workspace_size), %zu given", ws.total,
                     workspace_bytes);
@@ -657,6 +679,20 @@ int run_bwd_long(const void* q, const void* k, const void* v, const void* out, c
         sp.rw0 = rw0;
         sp.groups = sam_bwd_groups(sw, (int)BH, nsm);
         sp.status = status;
+        if (resample) {
+            // the tables resampled to 2 S - 1 rows as the forward does; the post
+            // passes add the gradients of those rows to a cleared area, which
+            // the transposed resampling returns to d_bias at the end
+            const int nt = 2 * sw - 1;
+            uint16_t* rt = reinterpret_cast<uint16_t*>(wsb + ws.rtab);
+            float* drr = reinterpret_cast<float*>(wsb + ws.drr);
+            e = launch_bwd_sam_resample(sam->rel_h, rt, lin_h, nt, d, bf, drr, 2 * nt * d, st);
+            if (e == cudaSuccess) e = launch_bwd_sam_resample(sam->rel_w, rt + (size_t)nt * d, lin_w, nt, d, bf, nullptr, 0, st);
+            if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+            sp.rel_h = rt;
+            sp.rel_w = rt + (size_t)nt * d;
+            sp.d_bias = drr;
+        }
         e = launch_bwd_sam_rel_tc(sp, sw, bf, nsm, st);
         if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     }
@@ -673,8 +709,9 @@ int run_bwd_long(const void* q, const void* k, const void* v, const void* out, c
     p.Nq = Nq;
     p.Nk = Nk;
     p.d = d;
-    // key tiles start on grid rows: 112 keys (8 rows) on the 14-wide grid
-    p.kv_w = sw == 14 ? 112 : kBlockN;
+    // key tiles start on grid rows: 112 keys (8 rows) on the 14-wide grid, 96
+    // (2 rows) on the 48-wide one
+    p.kv_w = sw == 14 ? 112 : (sw == 48 ? 96 : kBlockN);
     if (sam) {
         p.rel = sp.rel;
         p.rel_stride = stride;
@@ -718,6 +755,12 @@ int run_bwd_long(const void* q, const void* k, const void* v, const void* out, c
     }
     if (sam) {
         e = launch_bwd_sam_post(sp, sw, bf, nsm, st);
+        if (e == cudaSuccess && resample) {
+            const int nt = 2 * sw - 1;
+            e = launch_bwd_sam_unresample(sp.d_bias, d_bias, lin_h, nt, d, st);
+            if (e == cudaSuccess)
+                e = launch_bwd_sam_unresample(sp.d_bias + (size_t)nt * d, d_bias + (size_t)lin_h * d, lin_w, nt, d, st);
+        }
         if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     }
     static const bool debug_env = getenv("SDPA09_DEBUG") && getenv("SDPA09_DEBUG")[0] == '1';
@@ -801,10 +844,12 @@ int run_bwd(const void* q, const void* k, const void* v, const void* out, const 
         if (a->q_h * a->q_w != Nq || a->k_h * a->k_w != Nk)
             return fail(ATTN_ERR_ARG, "SAM needs Nq == q_h*q_w and Nk == k_h*k_w");
         const int S = a->q_w;
-        const int lh = a->rel_h_len ? a->rel_h_len : 2 * a->q_h - 1, lw = a->rel_w_len ? a->rel_w_len : 2 * a->q_w - 1;
-        if (a->q_h != S || a->k_h != S || a->k_w != S || (S != 14 && S != 64) || lh != 2 * S - 1 || lw != 2 * S - 1)
-            return fail(ATTN_ERR_UNSUPPORTED,
-                        "the SAM backward takes square 14 x 14 or 64 x 64 grids with tables of 2 * side - 1 rows");
+        int lh = 0, lw = 0;
+        sam_bwd_resample(a, &lh, &lw);
+        if (a->q_h != S || a->k_h != S || a->k_w != S || (S != 14 && S != 48 && S != 64))
+            return fail(ATTN_ERR_UNSUPPORTED, "the SAM backward takes square 14 x 14, 48 x 48 or 64 x 64 grids");
+        if (lh < 1 || lw < 1 || lh > kBlockN || lw > kBlockN)
+            return fail(ATTN_ERR_UNSUPPORTED, "SAM tables of 1 to %d rows", kBlockN);
         if (dpad != 64 && dpad != 80) return fail(ATTN_ERR_UNSUPPORTED, "the SAM backward takes 48 < d <= 80");
         if (!aligned16(a->rel_h) || !aligned16(a->rel_w)) return fail(ATTN_ERR_ARG, "rel_h/rel_w must be 16-byte aligned");
         if ((reinterpret_cast<uintptr_t>(d_bias) & 3u) != 0) return fail(ATTN_ERR_ARG, "d_bias must be 4-byte aligned");

@@ -194,7 +194,15 @@ def test_bwd_argument_checks(lib):
     sam = sdpa._SamArgs(FAKE, FAKE, 7, 7, 7, 7)
     assert _bwd(lib, kind=2, args=ctypes.byref(sam)) == sdpa.ATTN_ERR_ARG          # no d_bias
     assert _bwd(lib, kind=2, args=ctypes.byref(sam), d_table=FAKE) == sdpa.ATTN_ERR_UNSUPPORTED  # 7 x 7 grid
-    assert b"14 x 14 or 64 x 64" in lib.attn_last_error()
+    assert b"14 x 14, 48 x 48 or 64 x 64" in lib.attn_last_error()
+    long_tab = sdpa._SamArgs(FAKE, FAKE, 14, 14, 14, 14, 129, 27)               # a table over 128 rows
+    assert _bwd(lib, Nq=196, Nk=196, d=80, kind=2, args=ctypes.byref(long_tab), d_table=FAKE) == sdpa.ATTN_ERR_UNSUPPORTED
+    assert b"128 rows" in lib.attn_last_error()
+    # tables of another length than 2 * side - 1: the workspace holds their resampled copies
+    plain = sdpa._SamArgs(FAKE, FAKE, 48, 48, 48, 48)
+    resized = sdpa._SamArgs(FAKE, FAKE, 48, 48, 48, 48, 127, 127)
+    assert (lib.attn_bwd_workspace_size(1, 1, 2304, 2304, 80, 2, ctypes.byref(resized))
+            > lib.attn_bwd_workspace_size(1, 1, 2304, 2304, 80, 2, ctypes.byref(plain)) > 0)
     swin = sdpa._SwinArgs(FAKE, 7, 56, 56, 3)
     assert _bwd(lib, kind=1, args=ctypes.byref(swin)) == sdpa.ATTN_ERR_ARG    # no d_table
     assert b"d_bias" in lib.attn_last_error()

@@ -24,12 +24,30 @@ W = WORKLOADS
 
 
 def _check_table(got, want, what, atol=1e-3, rtol=1e-3):
+    """fp32 bias gradients: |err| <= atol * max(1, max |want|) + rtol * |want|
+    per element.  Each entry is a sum over every query row of a slice batch;
+    the rounding of its terms (fp32 sums, the 16-bit P in dS, the fp16 bias
+    terms) follows the size of the summands, i.e. the gradient's overall
+    scale, so the absolute floor scales with the largest entry."""
     got = np.asarray(got, dtype=np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)
     assert np.all(np.isfinite(got)), what
     err = np.abs(got - want)
-    bad = err > atol + rtol * np.abs(want)
+    bad = err > atol * max(1.0, float(np.abs(want).max())) + rtol * np.abs(want)
     assert not bad.any(), f"{what}: {int(bad.sum())} elements off, max |err| {err.max():.3e}"
+
+
+def _sam_resized_rounded(w: Workload, inp):
+    """SAM tables of another length than 2 * side - 1, read as the kernels
+    read them: resampled (the oracle's rel_pos_resized) and rounded to the
+    model dtype, as the model's resized tensor is.  Returns the oracle bias on
+    those tables and, per table, the resampling matrix A [2S-1][L] (A applied
+    to the unit rows), whose transpose returns a gradient to the table."""
+    L = 2 * w.s_h - 1
+    rz = [torch.from_numpy(oracle.sam_resize(t.double().numpy(), L)).to(t.dtype).double().numpy()
+          for t in (inp.rel_h, inp.rel_w)]
+    A = [oracle.sam_resize(np.eye(t.shape[0]), L) for t in (inp.rel_h, inp.rel_w)]
+    return oracle.Bias("sam", rel_h=rz[0], rel_w=rz[1], s_h=w.s_h, s_w=w.s_w), A
 
 
 def _bwd_case(w: Workload, seed=None, use_lse=False):
@@ -44,9 +62,13 @@ def _bwd_case(w: Workload, seed=None, use_lse=False):
                                      scale=w.scale, bias=bias)
     torch.cuda.synchronize()
     assert sdpa.attn_device_status() == sdpa.ATTN_OK
+    resized = w.bias == "sam" and w.rel_len and w.rel_len != 2 * w.s_h - 1
+    ob, A = _sam_resized_rounded(w, inp) if resized else (oracle_bias(w, inp), None)
     # D = rowsum(dO * O) from the 16-bit O the kernel was given
     want = oracle.attn_bwd(flat64(inp.q), flat64(inp.k), flat64(inp.v), flat64(dout), w.H, w.scale,
-                           oracle_bias(w, inp), out=flat64(out.cpu()))
+                           ob, out=flat64(out.cpu()))
+    if resized:
+        want["d_rel_h"], want["d_rel_w"] = A[0].T @ want["d_rel_h"], A[1].T @ want["d_rel_w"]
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         compare(flat64(t.cpu()), want[name], what=f"{w.name} {name}")
     if w.bias == "swin":
@@ -112,6 +134,19 @@ def test_bwd_sam_window_14x14():
 def test_bwd_sam_global_64x64():
     """SAM global attention on the 64 x 64 grid (4096 tokens, d = 80), one slice."""
     _bwd_case(W["sam_vith_global"].with_(B=1, H=1, seed=98), use_lse=True)
+
+
+@pytest.mark.parametrize("case", ["48x48_tables127", "14x14_tables31_fp16", "64x64_tables95"])
+def test_bwd_sam_48_and_resampled_tables(case):
+    """The 48 x 48 grid (a 768-pixel input) with the 1024-pixel model's
+    127-row tables, and 14 x 14 / 64 x 64 grids with tables of another length:
+    the backward runs on the tables resampled to 2 * side - 1 rows as the
+    forward does, and returns their gradients through the transposed
+    resampling; every gradient against the oracle."""
+    w = {"48x48_tables127": W["sam_vith_global_768"].with_(B=1, H=1, seed=103),
+         "14x14_tables31_fp16": W["sam_vith_window"].with_(B=1, H=2, rel_len=31, dtype="fp16", seed=104),
+         "64x64_tables95": W["sam_vith_global"].with_(B=1, H=1, rel_len=95, seed=105)}[case]
+    _bwd_case(w, use_lse=True)
 
 
 @pytest.mark.parametrize("case", ["14x14_d56_fp16", "64x64_d64_bf16"])
