@@ -20,9 +20,9 @@ struct LaunchArgs {
     const VarlenTable* vt;  // variable-length batch table, or null
 };
 
-template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL = false>
+template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL = false, bool IMG = false>
 cudaError_t launch_one(const LaunchArgs& a) {
-    auto kern = attn_fwd_kernel<DPAD, BIAS, MODE, SW, SL, DBG, VL>;
+    auto kern = attn_fwd_kernel<DPAD, BIAS, MODE, SW, SL, DBG, VL, IMG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a.smem);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the CTAs may become resident while the
@@ -45,10 +45,10 @@ cudaError_t launch_one(const LaunchArgs& a) {
     return cudaGetLastError();
 }
 
-template <int DPAD, int BIAS, int MODE, int SW, int SL>
+template <int DPAD, int BIAS, int MODE, int SW, int SL, bool IMG = false>
 cudaError_t launch_dbg(const LaunchArgs& a) {
-    return a.dbg ? launch_one<DPAD, BIAS, MODE, SW, SL, true>(a)
-                 : launch_one<DPAD, BIAS, MODE, SW, SL, false>(a);
+    return a.dbg ? launch_one<DPAD, BIAS, MODE, SW, SL, true, false, IMG>(a)
+                 : launch_one<DPAD, BIAS, MODE, SW, SL, false, false, IMG>(a);
 }
 
 // Defined in the per-(DPAD, bias) translation units.
@@ -78,7 +78,13 @@ cudaError_t launch_attn_none(const LaunchArgs& a) {
 template <int DPAD>
 cudaError_t launch_attn_swin(const LaunchArgs& a) {
     if constexpr (DPAD <= 64) {
-        if (a.mode == kModeSeparate) {
+        // the windows and the image token layout are separate instantiations
+        if (a.mode == kModeSeparate && a.p->swin_image) {
+            if (a.sl == 32) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 32, true>(a);
+            if (a.sl == 64 && a.sw == 49) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 49, 64, true>(a);
+            if (a.sl == 64) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 64, true>(a);
+            if (a.sl == 128) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 128, true>(a);
+        } else if (a.mode == kModeSeparate) {
             if (a.sl == 32) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 32>(a);
             if (a.sl == 64 && a.sw == 49) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 49, 64>(a);
             if (a.sl == 64) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 64>(a);
