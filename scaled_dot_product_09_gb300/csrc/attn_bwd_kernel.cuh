@@ -82,10 +82,13 @@ __device__ __forceinline__ uint32_t half_off(int r, int hh) {
     return (uint32_t)(r * 32 + ((hh ^ ((r >> 2) & 1)) << 4));
 }
 
-template <int DPAD, int BIAS, int SL>
+template <int DPAD, int BIAS, int SL, bool IMG>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_win_kernel(const __grid_constant__ BwdMaps tm, const BwdTcParams p) {
     using T = Tile<DPAD>;
+    // Swin image token layout (p.swin_image) as a compile-time choice: the
+    // windows-layout kernel carries none of its gather and scatter code
+    constexpr bool kImg = IMG && BIAS == kBiasSwin;
     static_assert(SL == 32 || SL == 64 || SL == 128, "slot rows");
     static_assert(256 + 3 * DPAD <= 512, "tensor memory: S, dP and three accumulators");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (tid == 0) {
         abort_sh = 0;
         for (int i = 0; i < kMaxStages; ++i) {
-            mbar_init(&bar_full[i], (BIAS == kBiasSwin && p.swin_image) ? 32 : 1);  // image layout: one per gathering lane
+            mbar_init(&bar_full[i], kImg ? 32 : 1);  // image layout: one per gathering lane
             mbar_init(&bar_empty[i], 1);
         }
         mbar_init(&bar_s, 1);
@@ -217,7 +220,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp >= 8) {
         regs_dec<kBwdCtlRegs>();
-        if (BIAS == kBiasSwin && warp == kProducerWarp && p.swin_image) {
+        if (kImg && warp == kProducerWarp) {
             // ============================================ producer, image layout
             // The whole warp copies each window's token rows of Q, K, V and dO
             // with 16-byte cp.async copies into the same swizzled tiles the TMA
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint32_t b = smem_u32(sRing + st * p.stage_bytes);
                 if (!waitb(&bar_full[st], (u / nst) & 1, kStatusWaitK)) return false;
                 // image layout: the tiles were written by cp.async (generic proxy)
-                if (BIAS == kBiasSwin && p.swin_image) fence_proxy_async_smem();
+                if constexpr (kImg) fence_proxy_async_smem();
                 if (u > 0 && !waitb(&bar_sfree, (u - 1) & 1, kStatusWaitS)) return false;
                 issue_qk<DPAD>(tS, kdesc(b), kdesc(b + T::kBytes), idesc_s);
                 issue_qk<DPAD>(tDP, kdesc(b + 3 * T::kBytes), kdesc(b + 2 * T::kBytes), idesc_s);
@@ -588,7 +591,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int slice = jb * p.g + slot;
             float D = 0.f;
             if (tok < p.Nq && slice < p.BH) {
-                const size_t orow_i = (BIAS == kBiasSwin && p.swin_image)
+                const size_t orow_i = kImg
                                           ? swin_image_row((uint32_t)slice, (uint32_t)tok, p.H, p.n_w, p.n_ww, p.win,
                                                            p.grid_h, p.grid_w, p.shift, p.fd_h, p.fd_w, p.fd_ww, p.fd_m)
                                           : (size_t)slice * p.Nq + tok;
@@ -637,7 +640,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 void* base = which == 0 ? p.dv : which == 1 ? p.dk : p.dq;
                 const int n = which == 2 ? p.Nq : p.Nk;
                 if (ok_row) {
-                    const size_t grow = (BIAS == kBiasSwin && p.swin_image)
+                    const size_t grow = kImg
                                             ? swin_image_row((uint32_t)slice, (uint32_t)tok, p.H, p.n_w, p.n_ww, p.win,
                                                              p.grid_h, p.grid_w, p.shift, p.fd_h, p.fd_w, p.fd_ww, p.fd_m)
                                             : (size_t)slice * n + tok;

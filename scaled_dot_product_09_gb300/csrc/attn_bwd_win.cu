@@ -6,10 +6,10 @@
 
 namespace sdpa09 {
 
-template <int DPAD, int BIAS, int SL>
+template <int DPAD, int BIAS, int SL, bool IMG>
 static cudaError_t launch_win_one(const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem,
                                   cudaStream_t stream) {
-    auto kern = attn_bwd_win_kernel<DPAD, BIAS, SL>;
+    auto kern = attn_bwd_win_kernel<DPAD, BIAS, SL, IMG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
@@ -27,14 +27,22 @@ static cudaError_t launch_win_one(const BwdMaps& tm, const BwdTcParams& p, int g
     return cudaGetLastError();
 }
 
-template <int DPAD, int BIAS>
-static cudaError_t launch_win_sl(const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem, cudaStream_t stream) {
+template <int DPAD, int BIAS, bool IMG>
+static cudaError_t launch_win_img(const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem, cudaStream_t stream) {
     switch (p.sl) {
-        case 32: return launch_win_one<DPAD, BIAS, 32>(tm, p, grid, smem, stream);
-        case 64: return launch_win_one<DPAD, BIAS, 64>(tm, p, grid, smem, stream);
-        case 128: return launch_win_one<DPAD, BIAS, 128>(tm, p, grid, smem, stream);
+        case 32: return launch_win_one<DPAD, BIAS, 32, IMG>(tm, p, grid, smem, stream);
+        case 64: return launch_win_one<DPAD, BIAS, 64, IMG>(tm, p, grid, smem, stream);
+        case 128: return launch_win_one<DPAD, BIAS, 128, IMG>(tm, p, grid, smem, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// the Swin image token layout is a separate instantiation
+template <int DPAD, int BIAS>
+static cudaError_t launch_win_sl(const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem, cudaStream_t stream) {
+    if constexpr (BIAS == kBiasSwin)
+        if (p.swin_image) return launch_win_img<DPAD, BIAS, true>(tm, p, grid, smem, stream);
+    return launch_win_img<DPAD, BIAS, false>(tm, p, grid, smem, stream);
 }
 
 cudaError_t launch_bwd_win(int dpad, bool swin, const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem,
