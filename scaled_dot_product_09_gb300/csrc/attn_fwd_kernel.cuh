@@ -606,9 +606,8 @@ __device__ __forceinline__ float sam_resampled(const float* g, int m, int lin, i
 // General SAM bias rows of one query row (qh, qw): rel_h for every key row
 // and rel_w for every key column, from G_h (in tO) and G_w (in tS).  rel_h
 // goes to shared memory reversed like the generic grids' rows (entry
-// k_h - 1 - kh); rel_w likewise into sam_rw, or, when rw_local is set, into
-// rw_local[kw] for the square-grid kernels' registers.  The G rows go
-// through a local array because the rows they are read at vary per thread.
+// k_h - 1 - kh); rel_w likewise into sam_rw.  The G rows go through a local
+// array because the rows they are read at vary per thread.
 // Only the G columns of the table (its length rounded up to 16) are loaded:
 // the slot's S and O areas may be narrower than 128 columns.
 static __device__ __noinline__ void sam_g_row(uint32_t taddr, int cols, float f, float* g) {
@@ -620,14 +619,13 @@ static __device__ __noinline__ void sam_g_row(uint32_t taddr, int cols, float f,
     }
 }
 static __device__ __noinline__ void sam_general_rows(uint32_t tS, uint32_t tO, const AttnParams& p, int qh, int qw,
-                                                     float f, float* sam_rh, float* sam_rw, float* rw_local, int r) {
+                                                     float f, float* sam_rh, float* sam_rw, int r) {
     float g[kBlockN];
     sam_g_row(tS, p.n_rw, f, g);
     for (int kw = 0; kw < p.k_w; ++kw) {
         const int m = sam_rel_row(qw, kw, p.sam_qs_w, p.sam_ks_w, p.sam_off_w, p.sam_lout_w);
         const float val = sam_resampled(g, m, p.sam_lin_w, p.sam_lout_w);
-        if (rw_local) rw_local[kw] = val;
-        else sam_rw[(p.k_w - 1 - kw) * kBlockM + r] = val;
+        sam_rw[(p.k_w - 1 - kw) * kBlockM + r] = val;
     }
     sam_g_row(tO, p.n_rh, f, g);
     for (int kh = 0; kh < p.k_h; ++kh) {
@@ -1887,24 +1885,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!__all_sync(0xffffffffu, mbar_wait(&bar_g[x], ju & 1, abort_flag, kStatusWaitG))) { ok = false; break; }
                     tc_fence_after();
                     const float f = DBG ? 1.0f : kLog2e;
-                    if (p.sam_general) {
-                        // unequal grids: each key row / column reads its table row
-                        // through the coordinate scalers, linearly resampled from G
-                        // when the tables have another length (resampling commutes
-                        // with Q.R); the square-grid branch is kept for kernels that
-                        // would be given unequal grids, which the host never does
-                        if constexpr (SW > 0) {
-                            // the square-grid kernels hold rel_w as fp16 pairs (kw = 2u, 2u+1)
-                            float rw_loc[SW];
-                            sam_general_rows(tS, tO, p, min(qh, p.s_h - 1), min(qw, p.s_w - 1), f, sam_rh, nullptr,
-                                             rw_loc, r);
-#pragma unroll
-                            for (int u = 0; u < SW / 2; ++u)
-                                sam_rw_h2[u] = __floats2half2_rn(rw_loc[2 * u], rw_loc[2 * u + 1]);
-                        } else {
-                            sam_general_rows(tS, tO, p, min(qh, p.s_h - 1), min(qw, p.s_w - 1), f, sam_rh, sam_rw,
-                                             nullptr, r);
-                        }
+                    if (SW == 0 && p.sam_general) {
+                        // unequal grids (the generic kernel only: the host sends
+                        // square grids alone to the kernels specialised for a side):
+                        // each key row / column reads its table row through the
+                        // coordinate scalers, linearly resampled from G when the
+                        // tables have another length (resampling commutes with Q.R)
+                        sam_general_rows(tS, tO, p, min(qh, p.s_h - 1), min(qw, p.s_w - 1), f, sam_rh, sam_rw, r);
                         tc_fence_before();
                         warp_arrive(&bar_gdone[x]);
                     } else {
