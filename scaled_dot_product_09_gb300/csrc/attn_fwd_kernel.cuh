@@ -638,9 +638,9 @@ template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL, bool 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ TmaMaps tm, const AttnParams p, const __grid_constant__ VarlenArg<VL> vt) {
     using T = Tile<DPAD>;
-    // Swin image token layout (p.swin_image), a compile-time choice so that
-    // the windows-layout kernel carries none of its gather and scatter code
-    constexpr bool kImg = IMG && MODE == kModeSeparate && BIAS == kBiasSwin;
+    // IMG: the Swin image token layout (p.swin_image) is a separate
+    // instantiation, so that the windows-layout kernel carries none of its
+    // gather and scatter code (the tests below are written out in full)
     static_assert(MODE == kModeShared || (SL == 32 || SL == 64 || SL == 128), "slot size");
     // Key columns of a score tile (S MMA N, P.V K): 128, or narrower in shared
     // tiling when that lets separate P buffers fit tensor memory -- without
@@ -771,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kMaxStages; ++i) {
             // the image-layout Swin stages are filled by two warps
-            mbar_init(&bar_full_k[i], kImg ? 64 : 1);
+            mbar_init(&bar_full_k[i], (MODE == kModeSeparate && BIAS == kBiasSwin && IMG && p.swin_image) ? 64 : 1);
             mbar_init(&bar_full_v[i], 1);
             mbar_init(&bar_empty[i], MODE == kModeShared ? 2 : 1);
             if constexpr (VL) mbar_init(&bar_landed_v[i], 1);
@@ -971,9 +971,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= 8) {
       regs_dec<kControlRegs>();
-      if (warp == kProducerWarp || (kImg && warp == kGatherWarp)) {
+      if (warp == kProducerWarp || (warp == kGatherWarp && MODE == kModeSeparate && BIAS == kBiasSwin && IMG && p.swin_image)) {
         // =========================================================== producer
-        if constexpr (kImg) {
+        if (MODE == kModeSeparate && BIAS == kBiasSwin && IMG && p.swin_image) {
             // Image layout: this warp and the gather warp copy each window's
             // token rows with 16-byte cp.async copies, the cyclic shift and
             // the window partition folded into the source addresses,
@@ -1459,7 +1459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // image-layout tiles are written by cp.async copies (generic
                     // proxy) that signal the barrier themselves: the reader's
                     // proxy fence orders them before its MMAs
-                    constexpr bool gathered = kImg;
+                    const bool gathered = BIAS == kBiasSwin && IMG && p.swin_image;
                     if (ju == 0 || !ahead) {
                         if (!waitb(&bar_full_k[u % nst], (u / nst) & 1, kStatusWaitK) || !s_free()) { ok = false; break; }
                         if (gathered) fence_proxy_async_smem();
@@ -1605,7 +1605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (rok && !DBG) {
                 // windows layout: [slice][token]; image layout: the token's
                 // place in the image (shift and partition undone)
-                const size_t orow = kImg
+                const size_t orow = (MODE == kModeSeparate && BIAS == kBiasSwin && IMG && p.swin_image)
                                         ? swin_image_row((uint32_t)slice, (uint32_t)tok, p.H, p.n_w, p.n_ww, p.win,
                                                          p.grid_h, p.grid_w, p.shift, p.fd_h, p.fd_w, p.fd_ww, p.fd_m)
                                         : (size_t)slice * p.Nq + tok;
