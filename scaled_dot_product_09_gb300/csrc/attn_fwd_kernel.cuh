@@ -634,13 +634,15 @@ static __device__ __noinline__ void sam_general_rows(uint32_t tS, uint32_t tO, c
     }
 }
 
-template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL, bool IMG>
+template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL, bool IMG, bool SWR>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ TmaMaps tm, const AttnParams p, const __grid_constant__ VarlenArg<VL> vt) {
     using T = Tile<DPAD>;
     // IMG: the Swin image token layout (p.swin_image) is a separate
     // instantiation, so that the windows-layout kernel carries none of its
-    // gather and scatter code (the tests below are written out in full)
+    // gather and scatter code (the tests below are written out in full).
+    // SWR: the Swin bias added from per-CTA rows (the host's swin_rows), not
+    // by MMAs, likewise a separate instantiation
     static_assert(MODE == kModeShared || (SL == 32 || SL == 64 || SL == 128), "slot size");
     // Key columns of a score tile (S MMA N, P.V K): 128, or narrower in shared
     // tiling when that lets separate P buffers fit tensor memory -- without
@@ -791,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Global memory is touched only after the grids this launch depends on
     // have completed and their writes are visible.
     griddep_wait();
-    if (BIAS == kBiasSwin && SL <= 64 && p.swin_rows) {
+    if (BIAS == kBiasSwin && SL <= 64 && SWR) {
         // Per head h: row i (query token), column j (key token) holds
         // table[idx(i, j), h] in log2 units (natural units when debugging);
         // idx is the relative-position index ("视觉大模型训练和推理加速"
@@ -1242,9 +1244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // S of packed tile `tile` (separate mode), with the Swin bias
             auto sep_scores = [&](int tile, uint32_t qa) {
-                if (!DBG || BIAS != kBiasSwin || (SL <= 64 && p.swin_rows))
+                if (!DBG || BIAS != kBiasSwin || (SL <= 64 && SWR))
                     issue_qk<DPAD>(tSx, kdesc(qa), kdesc(qa + T::kBytes), idesc_s);
-                if (BIAS == kBiasSwin && !(SL <= 64 && p.swin_rows)) {
+                if (BIAS == kBiasSwin && !(SL <= 64 && SWR)) {
                     for (int sl = 0; sl < p.g; ++sl) {
                         const uint32_t slice = (uint32_t)(tile * p.g + sl);
                         if ((int)slice >= p.BH) break;
@@ -1658,7 +1660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 warp_arrive(&bar_sfree[x]);
                 const int nk = p.Nk;
                 float sc = p.scale_log2;  // multiplier of xs in the exponent
-                if (BIAS == kBiasSwin && SL <= 64 && p.swin_rows) {
+                if (BIAS == kBiasSwin && SL <= 64 && SWR) {
                     // xs = s * scale * log2(e) + bias row (+ region mask), log2 units
                     int h, kind;
                     swin_slice_info((uint32_t)min(my_slice, p.BH - 1), p.H, p.n_w, p.n_ww, p.n_wh, p.shift, p.fd_h,

@@ -20,9 +20,9 @@ struct LaunchArgs {
     const VarlenTable* vt;  // variable-length batch table, or null
 };
 
-template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL = false, bool IMG = false>
+template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL = false, bool IMG = false, bool SWR = false>
 cudaError_t launch_one(const LaunchArgs& a) {
-    auto kern = attn_fwd_kernel<DPAD, BIAS, MODE, SW, SL, DBG, VL, IMG>;
+    auto kern = attn_fwd_kernel<DPAD, BIAS, MODE, SW, SL, DBG, VL, IMG, SWR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a.smem);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the CTAs may become resident while the
@@ -45,10 +45,10 @@ cudaError_t launch_one(const LaunchArgs& a) {
     return cudaGetLastError();
 }
 
-template <int DPAD, int BIAS, int MODE, int SW, int SL, bool IMG = false>
+template <int DPAD, int BIAS, int MODE, int SW, int SL, bool IMG = false, bool SWR = false>
 cudaError_t launch_dbg(const LaunchArgs& a) {
-    return a.dbg ? launch_one<DPAD, BIAS, MODE, SW, SL, true, false, IMG>(a)
-                 : launch_one<DPAD, BIAS, MODE, SW, SL, false, false, IMG>(a);
+    return a.dbg ? launch_one<DPAD, BIAS, MODE, SW, SL, true, false, IMG, SWR>(a)
+                 : launch_one<DPAD, BIAS, MODE, SW, SL, false, false, IMG, SWR>(a);
 }
 
 // Defined in the per-(DPAD, bias) translation units.
@@ -75,20 +75,30 @@ cudaError_t launch_attn_none(const LaunchArgs& a) {
     return cudaErrorInvalidValue;
 }
 
+// packed Swin with slots of 32 or 64 rows (64: also the 49-key softmax)
+template <int DPAD, bool IMG, bool SWR>
+cudaError_t launch_swin_sl(const LaunchArgs& a) {
+    if (a.sl == 32) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 32, IMG, SWR>(a);
+    if (a.sl == 64 && a.sw == 49) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 49, 64, IMG, SWR>(a);
+    if (a.sl == 64) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 64, IMG, SWR>(a);
+    return cudaErrorInvalidValue;
+}
+
 template <int DPAD>
 cudaError_t launch_attn_swin(const LaunchArgs& a) {
     if constexpr (DPAD <= 64) {
-        // the windows and the image token layout are separate instantiations
-        if (a.mode == kModeSeparate && a.p->swin_image) {
-            if (a.sl == 32) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 32, true>(a);
-            if (a.sl == 64 && a.sw == 49) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 49, 64, true>(a);
-            if (a.sl == 64) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 64, true>(a);
-            if (a.sl == 128) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 128, true>(a);
-        } else if (a.mode == kModeSeparate) {
-            if (a.sl == 32) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 32>(a);
-            if (a.sl == 64 && a.sw == 49) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 49, 64>(a);
-            if (a.sl == 64) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 64>(a);
-            if (a.sl == 128) return launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 128>(a);
+        // the windows and the image token layout, and the bias rows and the
+        // bias MMAs (slots of 128 rows take the MMAs only), are separate
+        // instantiations
+        if (a.mode == kModeSeparate) {
+            if (a.sl == 128) {
+                if (a.p->swin_rows) return cudaErrorInvalidValue;
+                return a.p->swin_image ? launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 128, true>(a)
+                                       : launch_dbg<DPAD, kBiasSwin, kModeSeparate, 0, 128, false>(a);
+            }
+            if (a.p->swin_image)
+                return a.p->swin_rows ? launch_swin_sl<DPAD, true, true>(a) : launch_swin_sl<DPAD, true, false>(a);
+            return a.p->swin_rows ? launch_swin_sl<DPAD, false, true>(a) : launch_swin_sl<DPAD, false, false>(a);
         }
     }
     return cudaErrorInvalidValue;
