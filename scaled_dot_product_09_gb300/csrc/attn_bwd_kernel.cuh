@@ -82,12 +82,15 @@ __device__ __forceinline__ uint32_t half_off(int r, int hh) {
     return (uint32_t)(r * 32 + ((hh ^ ((r >> 2) & 1)) << 4));
 }
 
-template <int DPAD, int BIAS, int SL, bool IMG>
+template <int DPAD, int BIAS, int SL, bool IMG, bool FAST>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_win_kernel(const __grid_constant__ BwdMaps tm, const BwdTcParams p) {
     using T = Tile<DPAD>;
     // Swin image token layout (p.swin_image) as a compile-time choice: the
-    // windows-layout kernel carries none of its gather and scatter code
+    // windows-layout kernel carries none of its gather and scatter code.
+    // FAST: the Swin case of bias rows and a shared, non-atomic table-gradient
+    // area (p.swin_rows, p.swin_acc, !p.swin_acc_atomic), fixed at compile
+    // time so that the kernel carries only that path
     constexpr bool kImg = IMG && BIAS == kBiasSwin;
     static_assert(SL == 32 || SL == 64 || SL == 128, "slot rows");
     static_assert(256 + 3 * DPAD <= 512, "tensor memory: S, dP and three accumulators");
@@ -165,9 +168,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             sTab[i] = p.table[i];
             sDTab[i] = 0.f;
         }
-        if (p.swin_acc)
+        if ((FAST || p.swin_acc))
             for (int i = tid; i < p.H * p.Nq * p.Nk; i += kBwdThreads) sAcc[i] = 0.f;
-        if (p.swin_rows) {
+        if ((FAST || p.swin_rows)) {
             __syncthreads();
             const int N = p.Nk, c0 = 2 * M * (M - 1);
             for (int w = tid; w < p.H * SL * (SL / 8); w += kBwdThreads) {
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 sel = ((kind & 1) ? 0x3 : 0) | ((kind & 2) ? 0xC : 0);
             }
             float m = -INFINITY;
-            if (BIAS == kBiasSwin && p.swin_rows) {
+            if (BIAS == kBiasSwin && (FAST || p.swin_rows)) {
                 // x = s * scale * log2(e) + bias row (-inf past the window; and
                 // -100 log2(e) across regions in edge windows)
                 const unsigned char* rowp = sRows + (h * SL + tok) * SL * 2;
@@ -488,7 +491,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 ok = false;
                 break;
             }
-            if (BIAS == kBiasSwin && p.swin_acc && t > 0 &&
+            if (BIAS == kBiasSwin && (FAST || p.swin_acc) && t > 0 &&
                 !__all_sync(0xffffffffu, mbar_wait(&bar_accsync, (t - 1) & 1, abort_flag, kStatusWaitP))) {
                 ok = false;
                 break;
@@ -502,12 +505,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int c = 0; c < kCh; ++c) dq[c] = xs[ch + c] * (dq[c] - D);
                 if constexpr (BIAS == kBiasSwin) {
-                    if (p.swin_acc) {
+                    if ((FAST || p.swin_acc)) {
                         // dS summed per (head, key token, query token): the query
                         // token's own entries, consecutive across the warp's lanes
                         if (row_ok) {
                             float* a = sAcc + (size_t)h * p.Nk * p.Nq + tok;
-                            if (!p.swin_acc_atomic) {
+                            if (!(!FAST && p.swin_acc_atomic)) {
                                 // 16 loads, then 16 stores: the entries are distinct
 #pragma unroll
                                 for (int c0 = 0; c0 < kCh; c0 += 16) {
@@ -569,7 +572,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             warp_arrive(&bar_p);
             // the next tile may add to the same (head, token) sums from another
             // warp: every warp's additions of this tile come first
-            if (BIAS == kBiasSwin && p.swin_acc) warp_arrive(&bar_accsync);
+            if (BIAS == kBiasSwin && (FAST || p.swin_acc)) warp_arrive(&bar_accsync);
         }
     } else {
         regs_inc<kBwdEpiRegs>();
@@ -671,7 +674,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     if constexpr (BIAS == kBiasSwin) {
         if (abort_sh == 0) {
-            if (p.swin_acc) {
+            if ((FAST || p.swin_acc)) {
                 // each table entry (head, offset (dr, dc)) sums the (key, query)
                 // sums of its pairs q = (rq, cq), k = (rq - dr, cq - dc)
                 const int M = p.win, N = p.Nq, TT = 2 * M - 1;

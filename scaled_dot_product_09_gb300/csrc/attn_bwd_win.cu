@@ -6,10 +6,10 @@
 
 namespace sdpa09 {
 
-template <int DPAD, int BIAS, int SL, bool IMG>
+template <int DPAD, int BIAS, int SL, bool IMG, bool FAST = false>
 static cudaError_t launch_win_one(const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem,
                                   cudaStream_t stream) {
-    auto kern = attn_bwd_win_kernel<DPAD, BIAS, SL, IMG>;
+    auto kern = attn_bwd_win_kernel<DPAD, BIAS, SL, IMG, FAST>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
@@ -29,9 +29,16 @@ static cudaError_t launch_win_one(const BwdMaps& tm, const BwdTcParams& p, int g
 
 template <int DPAD, int BIAS, bool IMG>
 static cudaError_t launch_win_img(const BwdMaps& tm, const BwdTcParams& p, int grid, size_t smem, cudaStream_t stream) {
+    // Swin with bias rows and a shared, non-atomic table-gradient area (slots
+    // of at most 64 rows) has an instantiation of its own
+    const bool fast = BIAS == kBiasSwin && p.swin_rows && p.swin_acc && !p.swin_acc_atomic;
     switch (p.sl) {
-        case 32: return launch_win_one<DPAD, BIAS, 32, IMG>(tm, p, grid, smem, stream);
-        case 64: return launch_win_one<DPAD, BIAS, 64, IMG>(tm, p, grid, smem, stream);
+        case 32:
+            return fast ? launch_win_one<DPAD, BIAS, 32, IMG, true>(tm, p, grid, smem, stream)
+                        : launch_win_one<DPAD, BIAS, 32, IMG>(tm, p, grid, smem, stream);
+        case 64:
+            return fast ? launch_win_one<DPAD, BIAS, 64, IMG, true>(tm, p, grid, smem, stream)
+                        : launch_win_one<DPAD, BIAS, 64, IMG>(tm, p, grid, smem, stream);
         case 128: return launch_win_one<DPAD, BIAS, 128, IMG>(tm, p, grid, smem, stream);
         default: return cudaErrorInvalidValue;
     }
