@@ -634,7 +634,7 @@ static __device__ __noinline__ void sam_general_rows(uint32_t tS, uint32_t tO, c
     }
 }
 
-template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL, bool IMG, bool SWR>
+template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL, bool IMG, bool SWR, bool NS>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ TmaMaps tm, const AttnParams p, const __grid_constant__ VarlenArg<VL> vt) {
     using T = Tile<DPAD>;
@@ -642,7 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // instantiation, so that the windows-layout kernel carries none of its
     // gather and scatter code (the tests below are written out in full).
     // SWR: the Swin bias added from per-CTA rows (the host's swin_rows), not
-    // by MMAs, likewise a separate instantiation
+    // by MMAs, likewise a separate instantiation.  NS: a scale <= 0 without
+    // bias in shared tiling (its softmax scales before the max), likewise
     static_assert(MODE == kModeShared || (SL == 32 || SL == 64 || SL == 128), "slot size");
     // Key columns of a score tile (S MMA N, P.V K): 128, or narrower in shared
     // tiling when that lets separate P buffers fit tensor memory -- without
@@ -1960,7 +1961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float sc;      // multiplier applied to xs in the exponent
                     if (BIAS == kBiasNone && !DBG) {
                         // no bias: max on raw scores, p = 2^(s*scale*log2e - m)
-                        if (!(p.scale_log2 > 0.f)) {
+                        if (NS && !(p.scale_log2 > 0.f)) {
                             // a scale <= 0: scale first, then mask the keys past the
                             // sequence with -inf (-inf times the scale would not stay -inf)
                             const float2 s2 = make_float2(p.scale_log2, p.scale_log2);

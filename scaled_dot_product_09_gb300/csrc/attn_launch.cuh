@@ -20,9 +20,10 @@ struct LaunchArgs {
     const VarlenTable* vt;  // variable-length batch table, or null
 };
 
-template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL = false, bool IMG = false, bool SWR = false>
+template <int DPAD, int BIAS, int MODE, int SW, int SL, bool DBG, bool VL = false, bool IMG = false, bool SWR = false,
+          bool NS = false>
 cudaError_t launch_one(const LaunchArgs& a) {
-    auto kern = attn_fwd_kernel<DPAD, BIAS, MODE, SW, SL, DBG, VL, IMG, SWR>;
+    auto kern = attn_fwd_kernel<DPAD, BIAS, MODE, SW, SL, DBG, VL, IMG, SWR, NS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a.smem);
     if (e != cudaSuccess) return e;
     // Programmatic dependent launch: the CTAs may become resident while the
@@ -57,16 +58,29 @@ cudaError_t launch_attn(const LaunchArgs& a);
 
 // The packed (separate) tiling keeps three tiles per ring stage; it is built
 // for head dims up to 64 only.
+// Shared tiling without bias: a scale <= 0 (scaled before the max) is an
+// instantiation of its own
+template <int DPAD, int SW>
+cudaError_t launch_none_shared(const LaunchArgs& a) {
+    const bool ns = !(a.p->scale_log2 > 0.f);
+    if (a.dbg)
+        return ns ? launch_one<DPAD, kBiasNone, kModeShared, SW, 0, true, false, false, false, true>(a)
+                  : launch_one<DPAD, kBiasNone, kModeShared, SW, 0, true>(a);
+    return ns ? launch_one<DPAD, kBiasNone, kModeShared, SW, 0, false, false, false, false, true>(a)
+              : launch_one<DPAD, kBiasNone, kModeShared, SW, 0, false>(a);
+}
+
 template <int DPAD>
 cudaError_t launch_attn_none(const LaunchArgs& a) {
     if (a.vt) {
         if (a.mode != kModeShared || a.sw != 0 || a.dbg) return cudaErrorInvalidValue;
-        return launch_one<DPAD, kBiasNone, kModeShared, 0, 0, false, true>(a);
+        return !(a.p->scale_log2 > 0.f) ? launch_one<DPAD, kBiasNone, kModeShared, 0, 0, false, true, false, false, true>(a)
+                                        : launch_one<DPAD, kBiasNone, kModeShared, 0, 0, false, true>(a);
     }
     if (a.mode == kModeShared) {
         if constexpr (DPAD <= 64)
-            if (a.sw == 80) return launch_dbg<DPAD, kBiasNone, kModeShared, 80, 0>(a);
-        return launch_dbg<DPAD, kBiasNone, kModeShared, 0, 0>(a);
+            if (a.sw == 80) return launch_none_shared<DPAD, 80>(a);
+        return launch_none_shared<DPAD, 0>(a);
     }
     if constexpr (DPAD <= 64) {
         if (a.sl == 32) return launch_dbg<DPAD, kBiasNone, kModeSeparate, 0, 32>(a);
