@@ -203,6 +203,13 @@ int attn_fwd_train(const void* q, const void* k, const void* v, void* out, float
  * or ATTN_ERR_CUDA.  Sequences never interact: the rows of a neighbouring
  * sequence that a tile holds are masked (keys) or cleared (values) before
  * use, so even non-finite values there leave a sequence's output unchanged.
+ *
+ * With d <= 64, sequences of at most 32 (64) query and key tokens are
+ * packed: four (two) (sequence, head) slices share one 128-row tile, the way
+ * the Swin windows of attn_fwd do, but each slice's P.V reads only its own
+ * values, so packed sequences stay apart in the same sense.  The call then
+ * makes up to three launches on the stream (longer sequences, slices of 32,
+ * slices of 64 rows); an error stops at the first failing one.
  */
 #define ATTN_VARLEN_MAX_SEQ 128
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, const int* cu_seqlens_q,

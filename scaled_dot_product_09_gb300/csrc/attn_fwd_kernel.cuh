@@ -701,7 +701,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Packed tiling with head dims up to 32 and slots up to 64 rows: two O
     // buffers per slot (O_x holds 64 columns), so a tile's output is written
     // while the next tile's P.V runs.
-    constexpr bool kDblO = MODE == kModeSeparate && DPAD <= 32 && SL <= 64;
+    constexpr bool kDblO = MODE == kModeSeparate && DPAD <= 32 && SL <= 64 && !VL;
+    // Packed variable-length batch: each slice of a tile is one (sequence,
+    // head) of at most SL query and SL key tokens, its rows gathered with
+    // zero fill past the sequence.  P.V runs one slice at a time (K = SL, its
+    // own keys and values only) into the slot's O, which the slice's rows
+    // read before the next slice's products overwrite it: a row never meets
+    // another sequence's values, so the sequences stay apart whatever those
+    // hold (block-diagonal P alone would still form 0 * inf there).
+    constexpr bool kVP = MODE == kModeSeparate && VL;
+    static_assert(!kVP || (BIAS == kBiasNone && SL <= 64), "packed variable-length batches: no bias, slots <= 64");
     // Packed Swin with the key count fixed at compile time (SW > 0, e.g. 49 for
     // 7x7 windows): the softmax touches only those columns (kNe: rounded up to
     // a pair), not the whole slot.
@@ -731,6 +740,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2], bar_g[2], bar_gdone[2], bar_oempty[2];
     __shared__ uint64_t bar_sfree[2], bar_pvd[2];
     __shared__ uint64_t bar_sb[kDbS ? 2 : 1][2];  // kDbS: [slot][score buffer] scores ready
+    // kVP: [slot][slice] that slice's P.V done; [slot] a slice's rows have read O
+    __shared__ uint64_t bar_og[kVP ? 2 : 1][kVP ? kBlockM / SL : 1], bar_ohand[kVP ? 2 : 1];
     __shared__ uint64_t bar_final;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -771,10 +782,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_init(&bar_sb[x][0], 1);
                 mbar_init(&bar_sb[x][1], 1);
             }
+            if constexpr (kVP) {
+                for (int g = 0; g < kBlockM / SL; ++g) mbar_init(&bar_og[x][g], 1);
+                mbar_init(&bar_ohand[x], SL / 32);  // the warps of one slice
+            }
         }
         for (int i = 0; i < kMaxStages; ++i) {
             // the image-layout Swin stages are filled by two warps
-            mbar_init(&bar_full_k[i], (MODE == kModeSeparate && BIAS == kBiasSwin && IMG && p.swin_image) ? 64 : 1);
+            mbar_init(&bar_full_k[i], (kVP || (MODE == kModeSeparate && BIAS == kBiasSwin && IMG && p.swin_image)) ? 64 : 1);
             mbar_init(&bar_full_v[i], 1);
             mbar_init(&bar_empty[i], MODE == kModeShared ? 2 : 1);
             if constexpr (VL) mbar_init(&bar_landed_v[i], 1);
@@ -974,9 +989,79 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= 8) {
       regs_dec<kControlRegs>();
-      if (warp == kProducerWarp || (warp == kGatherWarp && MODE == kModeSeparate && BIAS == kBiasSwin && IMG && p.swin_image)) {
+      if (warp == kProducerWarp ||
+          (warp == kGatherWarp && (kVP || (MODE == kModeSeparate && BIAS == kBiasSwin && IMG && p.swin_image)))) {
         // =========================================================== producer
-        if (MODE == kModeSeparate && BIAS == kBiasSwin && IMG && p.swin_image) {
+        if constexpr (kVP) {
+            // Packed variable-length batch: this warp and the gather warp
+            // copy alternate slices of each tile with 16-byte cp.async copies,
+            // kLanesRow lanes per row, into the swizzled tiles the TMA path
+            // lands.  A slice is one (sequence, head): query rows from its
+            // [H][Lq][d] block, key and value rows from its [H][Lk][d] block;
+            // rows past the sequence, padding columns and slices past the last
+            // are written as zeros.  Arrivals as in the image-layout gather.
+            constexpr int kChunks = DPAD / 8;
+            constexpr int kLanesRow = kChunks <= 2 ? 2 : (kChunks <= 4 ? 4 : 8);
+            constexpr int kRowsIt = 32 / kLanesRow;
+            constexpr int kG = kBlockM / SL;
+            static_assert(SL % kRowsIt == 0 && kG >= 2, "a warp instruction stays inside one slice");
+            const int half = warp == kProducerWarp ? 0 : 1;
+            const int c = lane % kLanesRow;
+            const int rsub = lane / kLanesRow;
+            const bool lane_on = c < kChunks;
+            const bool c_data = c * 8 < p.d;
+            const uint32_t dchunk = (uint32_t)((c >> 1) * (kBlockM * 32));
+            const size_t rowb = (size_t)p.d * 2;
+            int ring = 0;
+            bool ok = true;
+            for (int job = job0; ok && job < p.n_jobs; job += job_step) {
+                for (int x = 0; x < 2; ++x) {
+                    const int st = ring % nst;
+                    if (ring >= nst) {
+                        __syncwarp();
+                        if (!__all_sync(0xffffffffu, mbar_wait(&bar_empty[st], ((ring / nst) + 1) & 1, abort_flag,
+                                                               kStatusWaitEmpty))) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    ++ring;
+                    const int tile = 2 * job + x;
+                    unsigned char* base = sRing + st * p.ring_stage_bytes;
+                    if (lane_on) {
+#pragma unroll 1
+                        for (int g = half; g < kG; g += 2) {
+                            const int slice = tile * kG + g;
+                            int lq = 0, lk = 0;
+                            size_t qrow = 0, krow = 0;
+                            if (slice < p.BH) {
+                                const int e = slice / p.H, h = slice - e * p.H;
+                                lq = vt.q_len[e];
+                                lk = vt.k_len[e];
+                                qrow = (size_t)p.H * (size_t)vt.q_off[e] + (size_t)h * (size_t)lq;
+                                krow = (size_t)p.H * (size_t)vt.k_off[e] + (size_t)h * (size_t)lk;
+                            }
+#pragma unroll 4
+                            for (int it = 0; it < SL / kRowsIt; ++it) {
+                                const int t = it * kRowsIt + rsub;
+                                const int R = g * SL + t;
+                                const bool onq = c_data && t < lq, onk = c_data && t < lk;
+                                const size_t offq = onq ? (qrow + t) * rowb + (size_t)c * 16 : 0;
+                                const size_t offk = onk ? (krow + t) * rowb + (size_t)c * 16 : 0;
+                                const uint32_t dst = smem_u32(base + R * 32) + dchunk +
+                                                     ((((uint32_t)c & 1u) ^ (((uint32_t)R >> 2) & 1u)) << 4);
+                                cp_async16(dst, static_cast<const unsigned char*>(p.q) + offq, onq ? 16u : 0u);
+                                cp_async16(dst + T::kBytes, static_cast<const unsigned char*>(p.k) + offk, onk ? 16u : 0u);
+                                cp_async16(dst + 2 * T::kBytes, static_cast<const unsigned char*>(p.v) + offk,
+                                           onk ? 16u : 0u);
+                            }
+                        }
+                    }
+                    cp_async_arrive_noinc(&bar_full_k[st]);
+                }
+            }
+            cp_async_wait<0>();
+        } else if (MODE == kModeSeparate && BIAS == kBiasSwin && IMG && p.swin_image) {
             // Image layout: this warp and the gather warp copy each window's
             // token rows with 16-byte cp.async copies, the cyclic shift and
             // the window partition folded into the source addresses,
@@ -1169,7 +1254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-      } else if (VL && warp == kGatherWarp) {
+      } else if (VL && MODE == kModeShared && warp == kGatherWarp) {
         // ============================================ variable-length fix-up
         // A key tile that runs past its sequence holds the next sequence's
         // rows.  Their scores are masked to -inf, so they get P = 0, but a
@@ -1227,6 +1312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int ring = 0;  // stage uses consumed
             uint32_t ph_p = 0;
             int s_cnt = 0;  // score tiles issued
+            int hand_cnt = 0;  // kVP: slice hand-overs of O awaited
             int ju = 0;
             bool ok = true;
             const uint64_t qone_d = kdesc(smem_u32(sExtraB));
@@ -1462,7 +1548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // image-layout tiles are written by cp.async copies (generic
                     // proxy) that signal the barrier themselves: the reader's
                     // proxy fence orders them before its MMAs
-                    const bool gathered = BIAS == kBiasSwin && IMG && p.swin_image;
+                    const bool gathered = kVP || (BIAS == kBiasSwin && IMG && p.swin_image);
                     if (ju == 0 || !ahead) {
                         if (!waitb(&bar_full_k[u % nst], (u / nst) & 1, kStatusWaitK) || !s_free()) { ok = false; break; }
                         if (gathered) fence_proxy_async_smem();
@@ -1482,9 +1568,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (!waitb(bp, ph_p, kStatusWaitP)) { ok = false; break; }
                     ph_p ^= 1;
-                    issue_pv(tOx + (kDblO ? (uint32_t)((ju & 1) * DPAD) : 0u), tPx, vdesc(qa + 2 * T::kBytes), idesc_o, 0u);
-                    mma_commit(&bar_empty[u % nst]);
-                    mma_commit(bo);
+                    if constexpr (kVP) {
+                        // one slice at a time: its P columns against its own
+                        // value rows, after the previous slice's rows have read O
+                        const uint64_t vd = vdesc(qa + 2 * T::kBytes);
+                        for (int g = 0; g < kBlockM / SL; ++g) {
+                            if (g > 0) {
+                                if (!waitb(&bar_ohand[x], hand_cnt & 1, kStatusWaitO)) { ok = false; break; }
+                                ++hand_cnt;
+                            }
+                            issue_pv<SL>(tOx, tPx + (uint32_t)(g * (SL / 2)), vd + (uint64_t)(g * (SL / 16) * 32), idesc_o,
+                                         0u);
+                            mma_commit(&bar_og[x][g]);
+                        }
+                        if (!ok) break;
+                        mma_commit(&bar_empty[u % nst]);
+                    } else {
+                        issue_pv(tOx + (kDblO ? (uint32_t)((ju & 1) * DPAD) : 0u), tPx, vdesc(qa + 2 * T::kBytes),
+                                 idesc_o, 0u);
+                        mma_commit(&bar_empty[u % nst]);
+                        mma_commit(bo);
+                    }
                     ring += 2;
                 }
             }
@@ -1525,6 +1629,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             sam_kt = reinterpret_cast<const int*>(sExtra + 2 * (p.k_h + p.k_w) * kBlockM);
         }
 
+        // kVP: this warp's slice is not the tile's last, so its reading of O
+        // hands O over to the next slice's P.V
+        bool vp_hand = false;
         // O / l rounded to the output type and stored (row-per-thread, 16 bytes at a time)
         // m: the row's reference maximum in log2 units (P = 2^(x - m)), for the
         // row's log-sum-exp (m + log2 l) ln 2 when the caller asked for it
@@ -1550,6 +1657,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // O_x is free for the next job's G_h
                 tc_fence_before();
                 warp_arrive(&bar_oempty[x]);
+            }
+            if constexpr (kVP) {
+                if (vp_hand) {
+                    tc_fence_before();
+                    warp_arrive(&bar_ohand[x]);
+                }
             }
             if (MODE == kModeShared && (kShDbl || p.nq == 2)) {
                 // The warp's 32 output rows, consecutive tokens of one slice,
@@ -1626,6 +1739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int job = job0; ok && job < p.n_jobs; job += job_step, ++ju) {
             // ------------------------------------------------- row of this job
             int my_slice, my_tok, my_sl = 0;
+            int vp_nk = 0, vp_orow = 0;  // kVP: the slice's key count, the row's output row
             bool row_ok;
             JobRows jr{};
             if constexpr (MODE == kModeShared) {
@@ -1639,6 +1753,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 my_slice = tile * p.g + my_sl;
                 my_tok = r - my_sl * SL;
                 row_ok = (my_tok < p.Nq) && (my_sl < p.g) && (my_slice < p.BH);
+                if constexpr (kVP) {
+                    // the slice's sequence and head (a slice past the last has
+                    // no rows and no keys)
+                    int lq = 0;
+                    if (my_slice < p.BH) {
+                        const int e = my_slice / p.H, h = my_slice - e * p.H;
+                        lq = vt.q_len[e];
+                        vp_nk = vt.k_len[e];
+                        vp_orow = p.H * vt.q_off[e] + h * lq + my_tok;
+                    }
+                    row_ok = my_tok < lq;
+                }
             }
             float l_run = 0.f;
             float m_fin = 0.f;  // the row's reference maximum (log2 units) once its keys are done
@@ -1659,7 +1785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // S_x may now be overwritten by the next tile's scores
                 tc_fence_before();
                 warp_arrive(&bar_sfree[x]);
-                const int nk = p.Nk;
+                const int nk = kVP ? vp_nk : p.Nk;
                 float sc = p.scale_log2;  // multiplier of xs in the exponent
                 if (BIAS == kBiasSwin && SL <= 64 && SWR) {
                     // xs = s * scale * log2(e) + bias row (+ region mask), log2 units
@@ -2107,9 +2233,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             __syncwarp();
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_o[x], ju & 1, abort_flag, kStatusWaitO))) { ok = false; break; }
+            uint64_t* ob = &bar_o[x];
+            if constexpr (kVP) ob = &bar_og[x][my_sl];  // the P.V of this row's slice
+            if (!__all_sync(0xffffffffu, mbar_wait(ob, ju & 1, abort_flag, kStatusWaitO))) { ok = false; break; }
             tc_fence_after();
-            if constexpr (VL)  // output rows counted from the buffer start
+            if constexpr (kVP) {
+                vp_hand = my_sl < kBlockM / SL - 1;
+                epilogue(tO, l_run, m_fin, 0, vp_orow, row_ok, 0);
+            } else if constexpr (VL)  // output rows counted from the buffer start
                 epilogue(tO, l_run, m_fin, 0, jr.out_row0 + my_tok, row_ok, ju % p.nq);
             else
                 epilogue(tO, l_run, m_fin, my_slice, my_tok, row_ok, MODE == kModeShared ? ju % p.nq : 0);

@@ -73,7 +73,15 @@ cudaError_t launch_none_shared(const LaunchArgs& a) {
 template <int DPAD>
 cudaError_t launch_attn_none(const LaunchArgs& a) {
     if (a.vt) {
-        if (a.mode != kModeShared || a.sw != 0 || a.dbg) return cudaErrorInvalidValue;
+        if (a.sw != 0 || a.dbg) return cudaErrorInvalidValue;
+        if (a.mode == kModeSeparate) {
+            // short sequences packed SL rows per slice
+            if constexpr (DPAD <= 64) {
+                if (a.sl == 32) return launch_one<DPAD, kBiasNone, kModeSeparate, 0, 32, false, true>(a);
+                if (a.sl == 64) return launch_one<DPAD, kBiasNone, kModeSeparate, 0, 64, false, true>(a);
+            }
+            return cudaErrorInvalidValue;
+        }
         return !(a.p->scale_log2 > 0.f) ? launch_one<DPAD, kBiasNone, kModeShared, 0, 0, false, true, false, false, true>(a)
                                         : launch_one<DPAD, kBiasNone, kModeShared, 0, 0, false, true>(a);
     }

@@ -264,9 +264,12 @@ constexpr size_t kSwinRowsMax = 96 * 1024;
 
 // vt: a variable-length batch (no bias): B = 1, Nq / Nk = total query / key
 // tokens of all sequences, the operands viewed as [H * total][d] rows.
+// vp_sl: with vt, its sequences (each at most vp_sl query and key tokens)
+// packed vp_sl rows per (sequence, head) slice; 0: shared tiling.
 int run(const void* q, const void* k, const void* v, void* out, float* dbg, int B, int H, int Nq,
         int Nk, int d, float scale, attn_dtype dtype, attn_bias_kind bias_kind,
-        const void* bias_args, void* stream, const VarlenTable* vt = nullptr, float* lse = nullptr) {
+        const void* bias_args, void* stream, const VarlenTable* vt = nullptr, float* lse = nullptr,
+        int vp_sl = 0) {
     g_last_error.clear();
     if (!q || !k || !v || !(out || dbg)) return fail(ATTN_ERR_ARG, "null tensor pointer");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out ? out : (void*)dbg))
@@ -404,8 +407,10 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
 
     // ---- job layout
     const int nmax = std::max(Nq, Nk);
-    const int sl = nmax <= 32 ? 32 : (nmax <= 64 ? 64 : 128);
-    const bool separate = !vt && (bias == kBiasSwin || (bias == kBiasNone && sl <= 64 && dpad <= 64));
+    const int sl = vp_sl ? vp_sl : (nmax <= 32 ? 32 : (nmax <= 64 ? 64 : 128));
+    const bool separate = vt ? (vp_sl != 0) : (bias == kBiasSwin || (bias == kBiasNone && sl <= 64 && dpad <= 64));
+    if (vt && vp_sl && (bias != kBiasNone || dpad > 64 || (vp_sl != 32 && vp_sl != 64)))
+        return fail(ATTN_ERR_UNSUPPORTED, "packed variable-length tiling: no bias, d <= 64, 32- or 64-row slices");
     int mode;
     if (separate) {
         mode = kModeSeparate;
@@ -413,7 +418,9 @@ int run(const void* q, const void* k, const void* v, void* out, float* dbg, int 
         // for that key count
         if (bias == kBiasSwin && Nk == 49 && sl == 64) sw_spec = 49;
         p.g = kBlockM / sl;
-        const int64_t n_tiles = (BH + p.g - 1) / p.g;
+        // packed variable-length batch: one slice per (sequence, head)
+        if (vt) p.BH = H * vt->n_seq;
+        const int64_t n_tiles = ((int64_t)p.BH + p.g - 1) / p.g;
         p.n_jobs = (int)((n_tiles + 1) / 2);
         p.n_kv = 1;
         p.kv_w = kBlockN;
@@ -957,17 +964,32 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, cons
         return fail(ATTN_ERR_UNSUPPORTED, "more than %d sequences", sdpa09::kVarlenMaxSeq);
     if (H < 1) return fail(ATTN_ERR_ARG, "H must be >= 1");
     if (cu_seqlens_q[0] != 0 || cu_seqlens_k[0] != 0) return fail(ATTN_ERR_ARG, "cu_seqlens must start at 0");
+    // Sequences of at most 32 (64) query and key tokens, with d <= 64, are
+    // packed four (two) (sequence, head) slices per 128-row tile; the others
+    // take the shared tiling, longest key range first (the CTAs take jobs
+    // round-robin, and this order evens out their totals).
     int order[sdpa09::kVarlenMaxSeq];
-    int n_q = 0;  // sequences with queries
+    int n_q = 0;  // sequences with queries in the shared tiling
+    sdpa09::VarlenTable packed[2];  // slices of 32 and of 64 rows
+    memset(packed, 0, sizeof(packed));
     for (int s = 0; s < n_seq; ++s) {
         const int lq = cu_seqlens_q[s + 1] - cu_seqlens_q[s], lk = cu_seqlens_k[s + 1] - cu_seqlens_k[s];
         if (lq < 0 || lk < 0) return fail(ATTN_ERR_ARG, "cu_seqlens must be nondecreasing (sequence %d)", s);
         if (lq > 0 && lk == 0) return fail(ATTN_ERR_ARG, "sequence %d has queries but no keys", s);
         if (lk > (1 << 20)) return fail(ATTN_ERR_UNSUPPORTED, "sequence %d has more than 2^20 keys", s);
-        if (lq > 0) order[n_q++] = s;
+        if (lq == 0) continue;
+        const int n = std::max(lq, lk);
+        if (d <= 64 && n <= 64) {
+            sdpa09::VarlenTable& t = packed[n <= 32 ? 0 : 1];
+            t.q_off[t.n_seq] = cu_seqlens_q[s];
+            t.q_len[t.n_seq] = lq;
+            t.k_off[t.n_seq] = cu_seqlens_k[s];
+            t.k_len[t.n_seq] = lk;
+            ++t.n_seq;
+        } else {
+            order[n_q++] = s;
+        }
     }
-    // longest key range first: the CTAs take jobs round-robin, and this
-    // order evens out their totals
     std::stable_sort(order, order + n_q, [&](int a, int b) {
         return cu_seqlens_k[a + 1] - cu_seqlens_k[a] > cu_seqlens_k[b + 1] - cu_seqlens_k[b];
     });
@@ -985,9 +1007,15 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, cons
         if (jobs > 0x7fffffff) return fail(ATTN_ERR_UNSUPPORTED, "too many jobs");
         vt.jobs_end[e] = (int)jobs;
     }
-    if (jobs == 0) return ATTN_OK;  // no sequence has a query (the tensors may be empty)
-    return sdpa09::run(q, k, v, out, nullptr, 1, H, cu_seqlens_q[n_seq], cu_seqlens_k[n_seq], d, scale, dtype,
-                       ATTN_BIAS_NONE, nullptr, stream, &vt);
+    const int tq = cu_seqlens_q[n_seq], tk = cu_seqlens_k[n_seq];
+    int rc = ATTN_OK;
+    if (jobs > 0)
+        rc = sdpa09::run(q, k, v, out, nullptr, 1, H, tq, tk, d, scale, dtype, ATTN_BIAS_NONE, nullptr, stream, &vt);
+    for (int i = 0; i < 2 && rc == ATTN_OK; ++i)
+        if (packed[i].n_seq > 0)
+            rc = sdpa09::run(q, k, v, out, nullptr, 1, H, tq, tk, d, scale, dtype, ATTN_BIAS_NONE, nullptr, stream,
+                             &packed[i], nullptr, i == 0 ? 32 : 64);
+    return rc;  // (no sequence with a query: nothing to do, the tensors may be empty)
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int Nq, int Nk, int d, attn_bias_kind bias_kind, const void* bias_args) {

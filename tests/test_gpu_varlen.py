@@ -130,3 +130,59 @@ def test_varlen_sequences_do_not_interact():
     for s in (0, 2):
         r = slice(H * cq[s], H * cq[s + 1])
         compare(got[r], want[r], what=f"sequence {s} next to a poisoned sequence")
+
+
+# ------------------------------------------------ packed short sequences
+# Sequences of at most 32 (64) query and key tokens with d <= 64 share
+# 128-row tiles, four (two) (sequence, head) slices per tile.
+
+@pytest.mark.parametrize("lq,lk,H,d,dtype", [
+    # slices of 32 rows: one token, tile-edge lengths, an odd slice count
+    ([1, 7, 32, 20, 31, 16, 2], None, 3, 32, "fp16"),
+    # slices of 64 rows, d = 40 (a partial 16-column block), bf16
+    ([33, 64, 50, 40, 63], None, 4, 40, "bf16"),
+    # queries and keys of different lengths (the longer decides the slice)
+    ([3, 60, 10, 32, 1], [64, 2, 33, 1, 32], 2, 64, "fp16"),
+    # d = 48 and d = 16 (one data chunk of a 32-column block), one head
+    ([5, 17, 29, 64, 45, 12], None, 1, 48, "bf16"),
+    ([9, 30, 57, 3], None, 5, 16, "fp16"),
+])
+def test_varlen_packed_short(lq, lk, H, d, dtype):
+    lk = lq if lk is None else lk
+    _full(_varlen_workload(lq, lk, H=H, d=d, dtype=dtype, seed=50 + H + d))
+
+
+def test_varlen_packed_mixed_with_long():
+    # three launches: the shared tiling (300, 129) and both packed slice sizes
+    lens = [5, 300, 64, 33, 1, 129, 17, 0, 65]
+    _full(_varlen_workload(lens, lens, H=2, d=64, seed=60))
+
+
+def test_varlen_packed_many_sequences():
+    rng = np.random.default_rng(61)
+    lens = [int(x) for x in rng.integers(1, 65, sdpa.ATTN_VARLEN_MAX_SEQ)]
+    _full(_varlen_workload(lens, lens, H=3, d=32, dtype="bf16", seed=62))
+
+
+@pytest.mark.parametrize("lens", [[20, 30, 25, 10], [40, 50, 60]])
+def test_varlen_packed_sequences_do_not_interact(lens):
+    """With one head, consecutive sequences share a packed tile (four slices
+    of 32 rows, or two of 64).  Sequence 1 is poisoned with NaN in Q and inf
+    in K and V; every other sequence must still match the oracle on the clean
+    data, although its tile's P.V also holds sequence 1's values."""
+    w = _varlen_workload(lens, lens, H=1, d=32, seed=63)
+    inp = make_inputs(w)
+    cq, H = w.cu_seqlens_q, w.H
+    poisoned = [x.clone() for x in (inp.q, inp.k, inp.v)]
+    rows = slice(H * cq[1], H * cq[2])
+    poisoned[0][rows] = float("nan")
+    poisoned[1][rows] = float("inf")
+    poisoned[2][rows] = float("inf")
+    got = _run(w, type(inp)(*poisoned)).double().numpy()
+    want = oracle.attn_varlen(inp.q.double().numpy(), inp.k.double().numpy(), inp.v.double().numpy(),
+                              w.cu_seqlens_q, w.cu_seqlens_k, w.H, w.scale)
+    for s in range(len(lens)):
+        if s == 1:
+            continue
+        r = slice(H * cq[s], H * cq[s + 1])
+        compare(got[r], want[r], what=f"packed sequence {s} next to a poisoned sequence")
