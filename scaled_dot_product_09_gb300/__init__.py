@@ -16,6 +16,7 @@ section Bfloat16 半精度).
 """
 from __future__ import annotations
 
+import array
 import ctypes
 import math
 import os
@@ -237,8 +238,17 @@ def attn_fwd_train(q, k, v, out=None, lse=None, scale=None, bias=None, stream=No
 
 
 def _cu_array(cu):
-    vals = [int(x) for x in (cu.tolist() if hasattr(cu, "tolist") else cu)]
-    return (ctypes.c_int * len(vals))(*vals), vals
+    """Host token offsets (list, tuple, numpy array or tensor) as an int32
+    array and a ctypes view of it (built without a Python int per element:
+    this runs on every call)."""
+    if hasattr(cu, "detach"):  # a tensor
+        cu = cu.detach().cpu()
+    if hasattr(cu, "numpy") or hasattr(cu, "dtype"):
+        import numpy as np
+        vals = array.array("i", np.ascontiguousarray(cu, dtype=np.int32).tobytes())
+    else:
+        vals = array.array("i", cu)
+    return (ctypes.c_int * len(vals)).from_buffer(vals), vals
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, H, out=None, scale=None, stream=None):
