@@ -186,3 +186,21 @@ def test_varlen_packed_sequences_do_not_interact(lens):
             continue
         r = slice(H * cq[s], H * cq[s + 1])
         compare(got[r], want[r], what=f"packed sequence {s} next to a poisoned sequence")
+
+
+@pytest.mark.parametrize("scale,d", [(-0.3, 8), (0.0, 64), (2.5, 24)])
+def test_varlen_packed_scales_and_narrow_heads(scale, d):
+    """Packed slices with a negative, a zero and a large scale (the softmax
+    scales before its maximum when scale <= 0), and head dims 8 and 24 (one
+    and three data chunks of a 32-column block)."""
+    lens = [3, 40, 17, 64, 1, 32]
+    w = _varlen_workload(lens, lens, H=3, d=d, dtype="bf16", seed=70 + d)
+    inp = make_inputs(w)
+    require_gpu()
+    q, k, v = (x.cuda() for x in (inp.q, inp.k, inp.v))
+    got = sdpa.attn_fwd_varlen(q, k, v, w.cu_seqlens_q, w.cu_seqlens_k, w.H, scale=scale)
+    torch.cuda.synchronize()
+    assert sdpa.attn_device_status() == sdpa.ATTN_OK
+    want = oracle.attn_varlen(inp.q.double().numpy(), inp.k.double().numpy(), inp.v.double().numpy(),
+                              w.cu_seqlens_q, w.cu_seqlens_k, w.H, scale)
+    compare(got.double().cpu().numpy(), want, what=f"packed, scale {scale}, d {d}")
