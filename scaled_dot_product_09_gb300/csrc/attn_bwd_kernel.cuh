@@ -536,20 +536,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             if (ch + c < nk) atomicAdd(&sDTab[(pq - (s_tok[ch + c] & 0xFFFF)) * p.H + h], dq[c]);
                     }
                 }
+                // one loop per operand type, chosen once per chunk (not per pair)
+                auto pack_rows = [&](auto b16) {
 #pragma unroll
-                for (int c0 = 0; c0 < kCh; c0 += 8) {
-                    uint32_t wp[4], wd[4];
+                    for (int c0 = 0; c0 < kCh; c0 += 8) {
+                        uint32_t wp[4], wd[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float p0 = xs[ch + c0 + 2 * e], p1 = xs[ch + c0 + 2 * e + 1];
-                        wp[e] = bf ? pack_bf16(p0, p1) : pack_f16(p0, p1);
-                        wd[e] = bf ? pack_bf16(dq[c0 + 2 * e], dq[c0 + 2 * e + 1]) : pack_f16(dq[c0 + 2 * e], dq[c0 + 2 * e + 1]);
+                        for (int e = 0; e < 4; ++e) {
+                            const float p0 = xs[ch + c0 + 2 * e], p1 = xs[ch + c0 + 2 * e + 1];
+                            const float d0 = dq[c0 + 2 * e], d1 = dq[c0 + 2 * e + 1];
+                            wp[e] = decltype(b16)::value ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+                            wd[e] = decltype(b16)::value ? pack_bf16(d0, d1) : pack_f16(d0, d1);
+                        }
+                        const int col = (int)col0 + ch + c0;
+                        const uint32_t off = (uint32_t)((col >> 4) * (kBlockM * 32)) + half_off(r, (col >> 3) & 1);
+                        *reinterpret_cast<uint4*>(sP + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+                        *reinterpret_cast<uint4*>(sDS + off) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
                     }
-                    const int col = (int)col0 + ch + c0;
-                    const uint32_t off = (uint32_t)((col >> 4) * (kBlockM * 32)) + half_off(r, (col >> 3) & 1);
-                    *reinterpret_cast<uint4*>(sP + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
-                    *reinterpret_cast<uint4*>(sDS + off) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-                }
+                };
+                if (bf) pack_rows(std::true_type{});
+                else pack_rows(std::false_type{});
             };
             if constexpr (SL <= 64) {
                 do_chunk(dp, 0);
@@ -593,13 +599,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const unsigned char* sDO = sRing + st * p.stage_bytes + 3 * T::kBytes;
             const int slice = jb * p.g + slot;
             float D = 0.f;
-            if (tok < p.Nq && slice < p.BH) {
-                const size_t orow_i = kImg
-                                          ? swin_image_row((uint32_t)slice, (uint32_t)tok, p.H, p.n_w, p.n_ww, p.win,
-                                                           p.grid_h, p.grid_w, p.shift, p.fd_h, p.fd_w, p.fd_ww, p.fd_m)
-                                          : (size_t)slice * p.Nq + tok;
-                const uint4* orow = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p.o) +
-                                                                   orow_i * (size_t)p.d * 2);
+            // one loop per input type
+            auto dot_row = [&](auto b16, const uint4* orow) {
 #pragma unroll
                 for (int c8 = 0; c8 < DPAD / 8; ++c8) {
                     if (c8 * 8 < p.d) {
@@ -609,7 +610,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             float2 a, c;
-                            if (bf) {
+                            if constexpr (decltype(b16)::value) {
                                 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
                                 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[e]));
                             } else {
@@ -620,6 +621,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                     }
                 }
+            };
+            if (tok < p.Nq && slice < p.BH) {
+                const size_t orow_i = kImg
+                                          ? swin_image_row((uint32_t)slice, (uint32_t)tok, p.H, p.n_w, p.n_ww, p.win,
+                                                           p.grid_h, p.grid_w, p.shift, p.fd_h, p.fd_w, p.fd_ww, p.fd_m)
+                                          : (size_t)slice * p.Nq + tok;
+                const uint4* orow = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p.o) +
+                                                                   orow_i * (size_t)p.d * 2);
+                if (bf) dot_row(std::true_type{}, orow);
+                else dot_row(std::false_type{}, orow);
             }
             sD[u & 1][r] = D;
             warp_arrive(&bar_d[u & 1]);
@@ -648,19 +659,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                                              p.grid_h, p.grid_w, p.shift, p.fd_h, p.fd_w, p.fd_ww, p.fd_m)
                                             : (size_t)slice * n + tok;
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<unsigned char*>(base) + grow * (size_t)p.d * 2);
+                    auto store_row = [&](auto b16) {
 #pragma unroll
-                    for (int c8 = 0; c8 < DPAD / 8; ++c8) {
-                        if (c8 * 8 < p.d) {
-                            uint32_t w[4];
+                        for (int c8 = 0; c8 < DPAD / 8; ++c8) {
+                            if (c8 * 8 < p.d) {
+                                uint32_t w[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float a = __uint_as_float(v[c8 * 8 + 2 * e]) * f;
-                                const float b = __uint_as_float(v[c8 * 8 + 2 * e + 1]) * f;
-                                w[e] = bf ? pack_bf16(a, b) : pack_f16(a, b);
+                                for (int e = 0; e < 4; ++e) {
+                                    const float a = __uint_as_float(v[c8 * 8 + 2 * e]) * f;
+                                    const float b = __uint_as_float(v[c8 * 8 + 2 * e + 1]) * f;
+                                    w[e] = decltype(b16)::value ? pack_bf16(a, b) : pack_f16(a, b);
+                                }
+                                dst[c8] = make_uint4(w[0], w[1], w[2], w[3]);
                             }
-                            dst[c8] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
-                    }
+                    };
+                    if (bf) store_row(std::true_type{});
+                    else store_row(std::false_type{});
                 }
             }
             tc_fence_before();
