@@ -391,19 +391,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     break;
                 }
                 tc_fence_after();
+                // one packing loop per operand type, chosen once per tile
+                auto pack_rows = [&](auto b16) {
 #pragma unroll
-                for (int cc = 0; cc < 64; cc += 8) {
-                    uint32_t wp[4], wd[4];
+                    for (int cc = 0; cc < 64; cc += 8) {
+                        uint32_t wp[4], wd[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        wp[e] = bf ? pack_bf16(xs[cc + 2 * e], xs[cc + 2 * e + 1]) : pack_f16(xs[cc + 2 * e], xs[cc + 2 * e + 1]);
-                        wd[e] = bf ? pack_bf16(dp[cc + 2 * e], dp[cc + 2 * e + 1]) : pack_f16(dp[cc + 2 * e], dp[cc + 2 * e + 1]);
+                        for (int e = 0; e < 4; ++e) {
+                            const float p0 = xs[cc + 2 * e], p1 = xs[cc + 2 * e + 1];
+                            const float d0 = dp[cc + 2 * e], d1 = dp[cc + 2 * e + 1];
+                            wp[e] = decltype(b16)::value ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+                            wd[e] = decltype(b16)::value ? pack_bf16(d0, d1) : pack_f16(d0, d1);
+                        }
+                        const int col = (int)c0 + cc;
+                        const uint32_t off = (uint32_t)((col >> 4) * (kBlockM * 32)) + half_off(r, (col >> 3) & 1);
+                        if constexpr (kKey) *reinterpret_cast<uint4*>(sP + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+                        *reinterpret_cast<uint4*>(sDS + off) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
                     }
-                    const int col = (int)c0 + cc;
-                    const uint32_t off = (uint32_t)((col >> 4) * (kBlockM * 32)) + half_off(r, (col >> 3) & 1);
-                    if constexpr (kKey) *reinterpret_cast<uint4*>(sP + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
-                    *reinterpret_cast<uint4*>(sDS + off) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-                }
+                };
+                if (bf) pack_rows(std::true_type{});
+                else pack_rows(std::false_type{});
                 fence_proxy_async_smem();  // read by the tensor core
                 warp_arrive(&bar_p);
             }
