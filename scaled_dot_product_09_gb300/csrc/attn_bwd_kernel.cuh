@@ -465,16 +465,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             }
             const float m_use = m == -INFINITY ? 0.f : m;
+            // column pairs through the packed FP32 ops, the row sum in four
+            // independent partial sums (128-token slots: one column at a time,
+            // which needs fewer registers)
             float l = 0.f;
+            if constexpr (SL <= 64) {
+                float2 l2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                const float2 nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
-            for (int c = 0; c < SL; ++c) {
-                xs[c] = ex2_approx(xs[c] - m_use);
-                l += xs[c];
+                for (int c = 0; c < SL; c += 2) {
+                    const float2 a = __fadd2_rn(make_float2(xs[c], xs[c + 1]), nm2);
+                    xs[c] = ex2_approx(a.x);
+                    xs[c + 1] = ex2_approx(a.y);
+                    l2[(c >> 1) & 3] = __fadd2_rn(l2[(c >> 1) & 3], make_float2(xs[c], xs[c + 1]));
+                }
+                const float2 l2s = __fadd2_rn(__fadd2_rn(l2[0], l2[1]), __fadd2_rn(l2[2], l2[3]));
+                l = l2s.x + l2s.y;
+            } else {
+#pragma unroll
+                for (int c = 0; c < SL; ++c) {
+                    xs[c] = ex2_approx(xs[c] - m_use);
+                    l += xs[c];
+                }
             }
             // P of the row (zero for rows past the slice or missing slices)
             const float inv_l = (row_ok && l > 0.f) ? 1.0f / l : 0.f;
+            if constexpr (SL <= 64) {
+                const float2 il2 = make_float2(inv_l, inv_l);
 #pragma unroll
-            for (int c = 0; c < SL; ++c) xs[c] *= inv_l;
+                for (int c = 0; c < SL; c += 2) {
+                    const float2 y = __fmul2_rn(make_float2(xs[c], xs[c + 1]), il2);
+                    xs[c] = y.x;
+                    xs[c + 1] = y.y;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < SL; ++c) xs[c] *= inv_l;
+            }
             constexpr int kDp = SL <= 64 ? SL : 1;
             float dp[kDp];
             if constexpr (SL <= 64) {
@@ -502,8 +529,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr int kCh = SL <= 64 ? SL : 64;
             // one chunk of kCh columns from column ch: dq holds dP on entry
             auto do_chunk = [&](float (&dq)[kCh], int ch) {
+                if constexpr (SL <= 64) {
+                    const float2 nd2 = make_float2(-D, -D);
 #pragma unroll
-                for (int c = 0; c < kCh; ++c) dq[c] = xs[ch + c] * (dq[c] - D);
+                    for (int c = 0; c < kCh; c += 2) {
+                        const float2 t = __fadd2_rn(make_float2(dq[c], dq[c + 1]), nd2);
+                        const float2 y = __fmul2_rn(make_float2(xs[ch + c], xs[ch + c + 1]), t);
+                        dq[c] = y.x;
+                        dq[c + 1] = y.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kCh; ++c) dq[c] = xs[ch + c] * (dq[c] - D);
+                }
                 if constexpr (BIAS == kBiasSwin) {
                     if ((FAST || p.swin_acc)) {
                         // dS summed per (head, key token, query token): the query

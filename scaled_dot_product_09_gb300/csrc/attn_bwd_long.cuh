@@ -336,24 +336,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 float dp[64];
                 auto body = [&](auto hc) {
                     constexpr int H0 = decltype(hc)::value;  // this thread's column half
+                    // column pairs through the packed FP32 ops (the same roundings
+                    // as one column at a time)
+                    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                    const float2 nl2 = make_float2(-lse2, -lse2);
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
+                    for (int c = 0; c < 64; c += 2) {
                         const int col = 64 * H0 + c;
-                        float b = 0.f;
+                        float2 b2 = make_float2(0.f, 0.f);
                         if constexpr (kSam) {
+                            // grid widths are even: both columns share a key row
                             const float2 rwf = __half22float2(rw2[(col % SW) / 2]);
-                            const float rwv = ((col % SW) & 1) ? rwf.y : rwf.x;
-                            if constexpr (SW == 64) b = rh[0] + rwv;
-                            else b = rh[col / SW < kKR ? col / SW : kKR - 1] + rwv;
+                            const float rhv = SW == 64 ? rh[0] : rh[col / SW < kKR ? col / SW : kKR - 1];
+                            b2 = make_float2(rhv + rwf.x, rhv + rwf.y);
                         }
-                        const bool valid = q_ok && col < nvalid;
-                        xs[c] = valid ? ex2_approx(fmaf(xs[c], p.scale_log2, b - lse2)) : 0.f;
+                        const float2 a = __ffma2_rn(make_float2(xs[c], xs[c + 1]), sc2, __fadd2_rn(b2, nl2));
+                        xs[c] = (q_ok && col < nvalid) ? ex2_approx(a.x) : 0.f;
+                        xs[c + 1] = (q_ok && col + 1 < nvalid) ? ex2_approx(a.y) : 0.f;
                     }
                     {
                         uint32_t v[64];
                         tmem_ld64(tDP + lane_base + c0, v);
+                        const float2 nd2 = make_float2(-Dq, -Dq);
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) dp[c] = xs[c] * (__uint_as_float(v[c]) - Dq);
+                        for (int c = 0; c < 64; c += 2) {
+                            const float2 t = __fadd2_rn(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), nd2);
+                            const float2 y = __fmul2_rn(make_float2(xs[c], xs[c + 1]), t);
+                            dp[c] = y.x;
+                            dp[c + 1] = y.y;
+                        }
                     }
                     tc_fence_before();
                     warp_arrive(&bar_sfree);
