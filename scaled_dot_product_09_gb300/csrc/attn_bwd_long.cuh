@@ -380,17 +380,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                             for (int kr = kr0; kr <= kr1; ++kr) {
                                 if (kr < kKR) {
-                                    float a = 0.f;
+                                    // column pairs (grid widths are even: a pair never
+                                    // straddles two key rows), four partial sums
+                                    float2 a2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-                                    for (int c = 0; c < 64; ++c)
-                                        if ((64 * H0 + c) / SW == kr) a += dp[c];
+                                    for (int c = 0; c < 64; c += 2)
+                                        if ((64 * H0 + c) / SW == kr)
+                                            a2[(c >> 1) & 1] = __fadd2_rn(a2[(c >> 1) & 1], make_float2(dp[c], dp[c + 1]));
+                                    const float2 s2 = __fadd2_rn(a2[0], a2[1]);
+                                    const float a = s2.x + s2.y;
                                     if constexpr (SW == 64) dst[kh0 + kr] = a;
                                     else if (kh0 + kr < p.k_h) atomicAdd(dst + kh0 + kr, a);
                                 }
                             }
                         }
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) dw[(64 * H0 + c) % SW] += dp[c];
+                        for (int c = 0; c < 64; c += 2) {
+                            const int i = (64 * H0 + c) % SW;
+                            const float2 y = __fadd2_rn(make_float2(dw[i], dw[i + 1]), make_float2(dp[c], dp[c + 1]));
+                            dw[i] = y.x;
+                            dw[i + 1] = y.y;
+                        }
                     }
                 };
                 if (half == 0) body(std::integral_constant<int, 0>{});
