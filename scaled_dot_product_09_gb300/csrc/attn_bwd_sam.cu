@@ -100,10 +100,16 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 __device__ __forceinline__ void fma8x4(float (&acc)[8][4], const float4 a0, const float4 a1, const float4 b) {
     const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
     const float bb[4] = {b.x, b.y, b.z, b.w};
+    // column pairs through the packed FMA (the same rounding per element)
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[i][e] = fmaf(a[i], bb[e], acc[i][e]);
+        for (int e = 0; e < 4; e += 2) {
+            const float2 y = __ffma2_rn(make_float2(a[i], a[i]), make_float2(bb[e], bb[e + 1]),
+                                        make_float2(acc[i][e], acc[i][e + 1]));
+            acc[i][e] = y.x;
+            acc[i][e + 1] = y.y;
+        }
 }
 
 __device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 a, const float4 b) {
@@ -112,7 +118,12 @@ __device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 a, const
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[i][e] = fmaf(aa[i], bb[e], acc[i][e]);
+        for (int e = 0; e < 4; e += 2) {
+            const float2 y = __ffma2_rn(make_float2(aa[i], aa[i]), make_float2(bb[e], bb[e + 1]),
+                                        make_float2(acc[i][e], acc[i][e + 1]));
+            acc[i][e] = y.x;
+            acc[i][e + 1] = y.y;
+        }
 }
 
 // --------------------------------------------------------------- dQ post-pass
