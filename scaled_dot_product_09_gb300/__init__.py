@@ -245,7 +245,10 @@ def _cu_array(cu):
         cu = cu.detach().cpu()
     if hasattr(cu, "numpy") or hasattr(cu, "dtype"):
         import numpy as np
-        vals = array.array("i", np.ascontiguousarray(cu, dtype=np.int32).tobytes())
+        a = np.asarray(cu)
+        if a.size and (int(a.max()) > 0x7FFFFFFF or int(a.min()) < -0x80000000):
+            raise OverflowError("token offsets must fit in int32")
+        vals = array.array("i", np.ascontiguousarray(a, dtype=np.int32).tobytes())
     else:
         vals = array.array("i", cu)
     return (ctypes.c_int * len(vals)).from_buffer(vals), vals

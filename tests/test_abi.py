@@ -222,3 +222,19 @@ def test_swin_bias_mma_variant_rejects_unrepresentable_scale(lib):
         assert _call(lib, B=4, Nq=100, Nk=100, kind=1, args=ctypes.byref(a), dtype=dtype,
                      scale=scale) == sdpa.ATTN_ERR_UNSUPPORTED, (dtype, scale)
         assert b"scale" in lib.attn_last_error()
+
+
+def test_varlen_offsets_marshalling():
+    """The token offsets reach the C ABI as int32 arrays whatever host type
+    holds them (list, tuple, numpy of any integer width, CPU tensor)."""
+    import numpy as np
+    import torch
+    from scaled_dot_product_09_gb300 import _cu_array
+    want = [0, 3, 9, 70]
+    for cu in (want, tuple(want), np.array(want, dtype=np.int64), np.array(want, dtype=np.int32),
+               torch.tensor(want), torch.tensor(want, dtype=torch.int32)):
+        arr, vals = _cu_array(cu)
+        assert list(arr) == want and list(vals) == want and vals[-1] == 70, type(cu)
+    for big in ([0, 1 << 40], np.array([0, 1 << 40]), torch.tensor([0, 1 << 40])):
+        with pytest.raises(OverflowError):
+            _cu_array(big)
